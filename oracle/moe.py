@@ -1,0 +1,319 @@
+"""Dropless-MoE layer on the CPU in float64: the definition the CUDA path is checked against.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this module;
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+use it.  It shares no code with the CUDA library and imports nothing from it.
+
+Sources (cited by short name below):
+[1] "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer Engine"
+    (zhiding.cn rewrite of the NVIDIA technical blog).  Sections used: the
+    opening (learnable router picks the top-K experts per token), "How dropless
+    MoE differs from capacity-based MoE" (every token is processed by every
+    expert it chose; nothing is dropped or padded), "What dropless MoE needs"
+    (kernels with data-dependent per-expert sizes the CPU never sees; Figure 3:
+    router -> dispatch -> two grouped GEMMs over variable-length groups ->
+    combine back into the original token order), "Optimisation 1: grouped GEMM"
+    (one launch over all experts, computing only the valid token rows),
+    "Optimisation 2: dispatch and combine" (dispatch = local rearrangement;
+    combine = route results back and accumulate per token).
+[3] Deep reading of arXiv 2603.07685 (paper-daily.com), "Method overview"
+    (Route -> Dispatch -> Compute -> Combine).
+
+The pages give no formulas.  Every step below is the plainest definition that
+matches them; the readings (softmax scoring with renormalised top-k weights,
+lower expert id wins ties, (expert, token) ordering of the permuted rows,
+SwiGLU experts with gate rows first, routing weight applied in combine) are
+listed in the design doc.
+
+Arrays are numpy; floating-point inputs are the exact stored values (bf16 or
+fp32) widened to float64, and all arithmetic is float64.
+
+Parity pins (tests/test_oracle_*.py): brute-force sorting for top-k and ties,
+a counting-loop construction of the permutation, the dense masked-MoE formula,
+E=1/k=1 reducing to a dense SwiGLU FFN in torch, equal counts against
+torch.bmm, the permute/combine identities, torch float64 autograd and
+gradcheck for the backward.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import mxfp8
+
+
+# ----------------------------------------------------------------------------- route
+
+def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
+    """Top-k expert selection and routing weights ([1] opening paragraph: a learnable
+    router activates the top-K experts of each token).
+
+    Selection orders the experts of a token by (logit descending, expert id
+    ascending) and keeps the first k, so slot j holds the j-th best expert.
+    Weights are the softmax of the selected logits (``renormalize``), which is
+    the full softmax restricted to the selection and rescaled to sum to one, or
+    the full-softmax probabilities of the selected experts.
+
+    Returns idx int32 [T,k], w float64 [T,k], counts int64 [E].
+    """
+    lg = np.asarray(logits)
+    if lg.dtype != np.float32:
+        raise TypeError("router logits are float32")
+    if np.isnan(lg).any():
+        raise ValueError("NaN logits are outside the router's domain")
+    T, E = lg.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    l64 = lg.astype(np.float64)
+    expert_ids = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((expert_ids, -l64), axis=-1)          # primary: -logit, then id
+    idx = order[:, :k].astype(np.int32)
+    sel = np.take_along_axis(l64, idx.astype(np.int64), axis=1)
+    if renormalize:
+        ex = np.exp(sel - sel[:, :1])
+        w = ex / ex.sum(axis=1, keepdims=True)
+    else:
+        m = l64.max(axis=1, keepdims=True)
+        w = np.exp(sel - m) / np.exp(l64 - m).sum(axis=1, keepdims=True)
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    return idx, w, counts
+
+
+# ----------------------------------------------------------------------------- dispatch
+
+def permute_maps(idx: np.ndarray, E: int):
+    """The permutation of the T*k (token, slot) pairs into expert-contiguous rows
+    ([1] "Optimisation 2": dispatch rearranges tokens locally by expert).
+
+    Pairs are ordered by (expert, token); a token picks an expert at most once,
+    so the key is unique.  Rows of expert e are [offsets[e], offsets[e+1]),
+    with no padding between groups.
+
+    Returns offsets int64 [E+1] (exclusive scan of the counts), dest_row int64
+    [T,k] (row of pair (t,j)) and src_pair int64 [T*k] (pair t*k+j stored in
+    each row); dest_row and src_pair are inverse permutations.
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    expert = idx.ravel()
+    token = np.arange(T * k) // k
+    src_pair = np.lexsort((token, expert))                     # primary: expert, then token
+    dest_row = np.empty(T * k, dtype=np.int64)
+    dest_row[src_pair] = np.arange(T * k)
+    counts = np.bincount(expert, minlength=E)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return offsets, dest_row.reshape(T, k), src_pair.astype(np.int64)
+
+
+def permute(x: np.ndarray, src_pair: np.ndarray, k: int) -> np.ndarray:
+    """Xp[r] = x[token of the pair stored in row r]."""
+    return np.asarray(x, dtype=np.float64)[np.asarray(src_pair) // k]
+
+
+# ----------------------------------------------------------------------------- compute
+
+def grouped_gemm(A: np.ndarray, B: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+    """Ragged grouped GEMM ([1] "Optimisation 1": one call over all experts, each
+    group computed at its own token count): C[R_e] = A[R_e] @ B[e]^T for the
+    rows R_e = [offsets[e], offsets[e+1]).  A [M,K], B [E,N,K] -> C [M,N].
+    Rows outside every group stay zero (there are none when offsets[E] = M)."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    E, N, K = B.shape
+    C = np.zeros((A.shape[0], N))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            C[lo:hi] = A[lo:hi] @ B[e].T
+    return C
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu(GU: np.ndarray) -> np.ndarray:
+    """H = silu(G) * U with G the first f columns (gate) and U the last f (up)."""
+    f = GU.shape[1] // 2
+    G, U = GU[:, :f], GU[:, f:]
+    return silu(G) * U
+
+
+def expert_ffn(Xp, W1, W2, offsets):
+    """The grouped MLP of [1] Figure 3: GEMM1 (gate+up), SwiGLU, GEMM2 (down)."""
+    GU = grouped_gemm(Xp, W1, offsets)
+    H = swiglu(GU)
+    Yp = grouped_gemm(H, W2, offsets)
+    return GU, H, Yp
+
+
+# ----------------------------------------------------------------------------- combine
+
+def combine(Yp: np.ndarray, dest_row: np.ndarray, w) -> np.ndarray:
+    """y[t] = sum_j w[t,j] * Yp[dest_row[t,j]] ([1] "Optimisation 2": combine routes
+    expert results back to the original token order and accumulates them).
+    ``w=None`` means unit weights (the gradient of dispatch)."""
+    Yp = np.asarray(Yp, dtype=np.float64)
+    T, k = dest_row.shape
+    y = np.zeros((T, Yp.shape[1]))
+    for j in range(k):
+        wj = 1.0 if w is None else np.asarray(w, dtype=np.float64)[:, j:j + 1]
+        y += wj * Yp[dest_row[:, j]]
+    return y
+
+
+# ----------------------------------------------------------------------------- layer
+
+def mx_roundtrip(a: np.ndarray) -> np.ndarray:
+    """Values an MXFP8 operand carries: quantise row-wise along the last axis and
+    dequantise exactly."""
+    shp = a.shape
+    a2 = np.asarray(a, dtype=np.float64).reshape(-1, shp[-1])
+    return mxfp8.dequantize_rowwise(*mxfp8.quantize_rowwise(a2)).reshape(shp)
+
+
+def layer_forward(x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False):
+    """Route -> dispatch -> grouped MLP -> combine ([3] "Method overview").
+
+    With ``mxfp8_operands`` both GEMMs take MXFP8 operands (row-wise scales
+    along the contraction): Xp, W1, H and W2 are each quantised and the GEMMs run
+    on the exactly dequantised values."""
+    E = W1.shape[0]
+    idx, w, counts = route_topk(logits, k, renormalize)
+    offsets, dest_row, src_pair = permute_maps(idx, E)
+    Xp = permute(x, src_pair, k)
+    if mxfp8_operands:
+        Xq, W1q, W2q = mx_roundtrip(Xp), mx_roundtrip(W1), mx_roundtrip(W2)
+        GU = grouped_gemm(Xq, W1q, offsets)
+        H = swiglu(GU)
+        Yp = grouped_gemm(mx_roundtrip(H), W2q, offsets)
+    else:
+        GU, H, Yp = expert_ffn(Xp, W1, W2, offsets)
+    y = combine(Yp, dest_row, w)
+    return dict(idx=idx, w=w, counts=counts, offsets=offsets, dest_row=dest_row,
+                src_pair=src_pair, Xp=Xp, GU=GU, H=H, Yp=Yp, y=y)
+
+
+# ----------------------------------------------------------------------------- backward
+
+def combine_bwd(dy, Yp, dest_row, w):
+    """Gradients of combine: dYp[dest_row[t,j]] = w[t,j] dy[t] and
+    dw[t,j] = <dy[t], Yp[dest_row[t,j]]>."""
+    dy = np.asarray(dy, dtype=np.float64)
+    Yp = np.asarray(Yp, dtype=np.float64)
+    T, k = dest_row.shape
+    dYp = np.zeros_like(Yp)
+    dw = np.zeros((T, k))
+    for j in range(k):
+        dYp[dest_row[:, j]] = np.asarray(w)[:, j:j + 1] * dy
+        dw[:, j] = np.einsum("td,td->t", dy, Yp[dest_row[:, j]])
+    return dYp, dw
+
+
+def grouped_gemm_dgrad(dC, B, offsets):
+    """Gradient of C = A B_e^T with respect to A: dA[R_e] = dC[R_e] @ B[e].
+    dC [M,N], B [E,N,K] -> dA [M,K]."""
+    dC = np.asarray(dC, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    dA = np.zeros((dC.shape[0], B.shape[2]))
+    for e in range(B.shape[0]):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            dA[lo:hi] = dC[lo:hi] @ B[e]
+    return dA
+
+
+def grouped_gemm_wgrad(A, dC, offsets, E):
+    """Gradient with respect to the expert weights: dB[e] = dC[R_e]^T @ A[R_e],
+    a contraction over the ragged rows of each group; an empty group gives an
+    exact zero gradient.  A [M,K], dC [M,N] -> dB [E,N,K]."""
+    A = np.asarray(A, dtype=np.float64)
+    dC = np.asarray(dC, dtype=np.float64)
+    dB = np.zeros((E, dC.shape[1], A.shape[1]))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            dB[e] = dC[lo:hi].T @ A[lo:hi]
+    return dB
+
+
+def dswiglu(dH, GU):
+    """Gradient of H = silu(G) * U:  dU = dH silu(G),
+    dG = dH U sigma(G) (1 + G (1 - sigma(G)))."""
+    f = GU.shape[1] // 2
+    G, U = GU[:, :f], GU[:, f:]
+    s = 1.0 / (1.0 + np.exp(-G))
+    dG = dH * U * s * (1.0 + G * (1.0 - s))
+    dU = dH * G * s
+    return np.concatenate([dG, dU], axis=1)
+
+
+def route_bwd(dw, w, idx, logits, renormalize=True):
+    """Gradient of the routing weights with respect to the logits.
+
+    Renormalised: the weights are a softmax over the selected logits, so
+    dl_i = w_i (dw_i - sum_j w_j dw_j) on the selection and 0 elsewhere.
+    Otherwise the weights are full-softmax probabilities p of the selected
+    experts: dl_e = p_e (g_e - sum_j w_j dw_j) with g_e = dw_j if e = idx_j
+    else 0.  The selection itself is piecewise constant and has no gradient."""
+    dw = np.asarray(dw, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = idx.shape
+    E = logits.shape[1]
+    inner = (w * dw).sum(axis=1, keepdims=True)
+    dl = np.zeros((T, E))
+    rows = np.arange(T)[:, None]
+    if renormalize:
+        dl[rows, idx] = w * (dw - inner)
+    else:
+        l64 = np.asarray(logits, dtype=np.float64)
+        p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        g = np.zeros((T, E))
+        g[rows, idx] = dw
+        dl = p * (g - inner)
+    return dl
+
+
+def layer_backward(fwd, dy, x, logits, W1, W2, k, renormalize=True):
+    """The full backward of ``layer_forward`` (bf16/fp32 operands), returning
+    dx, dlogits, dW1, dW2 and the intermediates dYp, dw, dGU, dXp."""
+    E = W1.shape[0]
+    offsets, dest_row = fwd["offsets"], fwd["dest_row"]
+    dYp, dw = combine_bwd(dy, fwd["Yp"], dest_row, fwd["w"])
+    dH = grouped_gemm_dgrad(dYp, W2, offsets)
+    dGU = dswiglu(dH, fwd["GU"])
+    dW2 = grouped_gemm_wgrad(fwd["H"], dYp, offsets, E)
+    dXp = grouped_gemm_dgrad(dGU, W1, offsets)
+    dW1 = grouped_gemm_wgrad(fwd["Xp"], dGU, offsets, E)
+    dx = combine(dXp, dest_row, None)
+    dlogits = route_bwd(dw, fwd["w"], fwd["idx"], logits, renormalize)
+    return dict(dYp=dYp, dw=dw, dH=dH, dGU=dGU, dW2=dW2, dXp=dXp, dW1=dW1, dx=dx,
+                dlogits=dlogits)
+
+
+# ----------------------------------------------------------------------------- per-token form
+
+def token_forward(x_t, logits_t, W1, W2, k, renormalize=True, mxfp8_operands=False):
+    """Output of one token, y[t] = sum_j w_j FFN_{e_j}(x[t]); used to check
+    large workloads on sampled tokens (a token's output depends only on its own
+    activations, its logits and the weights of the experts it chose).
+    W1/W2 may be callables e -> expert weights, so large weights can be fetched
+    one expert at a time."""
+    idx, w, _ = route_topk(np.asarray(logits_t, dtype=np.float32)[None, :], k, renormalize)
+    get1 = W1 if callable(W1) else (lambda e: W1[e])
+    get2 = W2 if callable(W2) else (lambda e: W2[e])
+    xt = np.asarray(x_t, dtype=np.float64)[None, :]
+    if mxfp8_operands:
+        xt = mx_roundtrip(xt)
+    y = np.zeros(xt.shape[1])
+    for j in range(k):
+        e = int(idx[0, j])
+        w1, w2 = np.asarray(get1(e), np.float64), np.asarray(get2(e), np.float64)
+        if mxfp8_operands:
+            w1, w2 = mx_roundtrip(w1), mx_roundtrip(w2)
+        h = swiglu(xt @ w1.T)
+        if mxfp8_operands:
+            h = mx_roundtrip(h)
+        y += w[0, j] * (h @ w2.T)[0]
+    return y

@@ -1,0 +1,167 @@
+"""Pins for the oracle's grouped MLP, combine and backward (CPU only).
+
+Pinned against: the dense masked-MoE formula (every expert applied to every
+token, masked by the routing weights) written with torch float64 ops; a dense
+SwiGLU FFN (E=1, k=1); torch.bmm when every expert has the same number of rows;
+torch float64 autograd of the dense formula, itself checked by gradcheck
+(finite differences).
+"""
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import moe
+
+
+def _problem(T, d, E, k, f, seed, empty=()):
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    for e in empty:
+        lg[:, e] -= 30.0
+    x = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((E, 2 * f, d)) / np.sqrt(d)
+    W2 = rng.standard_normal((E, d, f)) / np.sqrt(f)
+    return lg, x, W1, W2
+
+
+def _dense_masked_torch(x, logits, W1, W2, idx, renormalize=True):
+    """y[t] = sum_e g[t,e] * FFN_e(x[t]) over ALL experts, with g the routing
+    weights on the selected experts and 0 elsewhere.  Differentiable in torch."""
+    T, E = logits.shape
+    k = idx.shape[1]
+    f = W2.shape[2]
+    if renormalize:
+        g_sel = torch.softmax(torch.gather(logits, 1, idx), dim=1)
+    else:
+        g_sel = torch.gather(torch.softmax(logits, dim=1), 1, idx)
+    g = torch.zeros(T, E, dtype=logits.dtype).scatter(1, idx, g_sel)
+    y = torch.zeros(T, W2.shape[1], dtype=x.dtype)
+    for e in range(E):
+        gu = x @ W1[e].T
+        h = F.silu(gu[:, :f]) * gu[:, f:]
+        y = y + g[:, e:e + 1] * (h @ W2[e].T)
+    return y
+
+
+@pytest.mark.parametrize("T,d,E,k,f,empty", [(40, 16, 6, 2, 12, (3,)), (25, 8, 4, 4, 8, ()),
+                                             (30, 12, 8, 1, 10, (0, 5))])
+def test_layer_equals_dense_masked_moe(T, d, E, k, f, empty):
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=T, empty=empty)
+    fwd = moe.layer_forward(x, lg, W1, W2, k)
+    idx = torch.from_numpy(fwd["idx"].astype(np.int64))
+    want = _dense_masked_torch(torch.from_numpy(x), torch.from_numpy(lg.astype(np.float64)),
+                               torch.from_numpy(W1), torch.from_numpy(W2), idx)
+    np.testing.assert_allclose(fwd["y"], want.numpy(), rtol=1e-11, atol=1e-12)
+    for e in empty:
+        assert fwd["counts"][e] == 0
+
+
+def test_single_expert_is_dense_swiglu_ffn():
+    T, d, f = 33, 16, 20
+    lg, x, W1, W2 = _problem(T, d, 1, 1, f, seed=11)
+    fwd = moe.layer_forward(x, lg, W1, W2, 1)
+    xt, w1, w2 = map(torch.from_numpy, (x, W1[0], W2[0]))
+    want = (F.silu(xt @ w1[:f].T) * (xt @ w1[f:].T)) @ w2.T
+    np.testing.assert_allclose(fwd["y"], want.numpy(), rtol=1e-12, atol=1e-13)
+    assert (fwd["src_pair"] == np.arange(T)).all()
+
+
+def test_equal_counts_is_bmm():
+    E, per, K, N = 5, 7, 12, 9
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((E * per, K))
+    B = rng.standard_normal((E, N, K))
+    offsets = np.arange(E + 1) * per
+    C = moe.grouped_gemm(A, B, offsets)
+    want = torch.bmm(torch.from_numpy(A).view(E, per, K), torch.from_numpy(B).transpose(1, 2))
+    np.testing.assert_allclose(C, want.reshape(E * per, N).numpy(), rtol=1e-13)
+    dC = rng.standard_normal((E * per, N))
+    dA = moe.grouped_gemm_dgrad(dC, B, offsets)
+    np.testing.assert_allclose(dA, torch.bmm(torch.from_numpy(dC).view(E, per, N),
+                                             torch.from_numpy(B)).reshape(E * per, K).numpy(),
+                               rtol=1e-13)
+    dB = moe.grouped_gemm_wgrad(A, dC, offsets, E)
+    np.testing.assert_allclose(dB, torch.bmm(torch.from_numpy(dC).view(E, per, N).transpose(1, 2),
+                                             torch.from_numpy(A).view(E, per, K)).numpy(),
+                               rtol=1e-13)
+
+
+def test_empty_group_zero_wgrad_and_untouched_rows():
+    offsets = np.array([0, 3, 3, 8])
+    rng = np.random.default_rng(6)
+    A, dC = rng.standard_normal((8, 4)), rng.standard_normal((8, 5))
+    dB = moe.grouped_gemm_wgrad(A, dC, offsets, 3)
+    assert (dB[1] == 0).all()
+    np.testing.assert_allclose(dB[0], dC[:3].T @ A[:3])
+
+
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_backward_matches_torch_autograd(renormalize):
+    T, d, E, k, f = 24, 10, 6, 3, 8
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=21, empty=(2,))
+    rng = np.random.default_rng(22)
+    dy = rng.standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k, renormalize)
+    bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k, renormalize)
+
+    tx, tl, t1, t2 = (torch.from_numpy(a).clone().requires_grad_(True)
+                      for a in (x, lg.astype(np.float64), W1, W2))
+    idx = torch.from_numpy(fwd["idx"].astype(np.int64))
+    y = _dense_masked_torch(tx, tl, t1, t2, idx, renormalize)
+    np.testing.assert_allclose(fwd["y"], y.detach().numpy(), rtol=1e-11, atol=1e-12)
+    (y * torch.from_numpy(dy)).sum().backward()
+    for name, t in (("dx", tx), ("dlogits", tl), ("dW1", t1), ("dW2", t2)):
+        np.testing.assert_allclose(bwd[name], t.grad.numpy(), rtol=1e-10, atol=1e-12, err_msg=name)
+    assert (bwd["dW1"][2] == 0).all() and (bwd["dW2"][2] == 0).all()
+    if renormalize:
+        sel = np.zeros((T, E), dtype=bool)
+        np.put_along_axis(sel, fwd["idx"].astype(np.int64), True, axis=1)
+        assert (bwd["dlogits"][~sel] == 0).all()
+        np.testing.assert_allclose(bwd["dlogits"].sum(axis=1), 0.0, atol=1e-12)
+
+
+def test_dense_formula_gradcheck():
+    """Finite differences pin the torch formula used above."""
+    T, d, E, k, f = 5, 4, 3, 2, 3
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=3)
+    idx, _, _ = moe.route_topk(lg, k)
+    idx = torch.from_numpy(idx.astype(np.int64))
+    args = tuple(torch.from_numpy(a).clone().requires_grad_(True)
+                 for a in (x, lg.astype(np.float64), W1, W2))
+    assert torch.autograd.gradcheck(lambda *a: _dense_masked_torch(*a, idx), args)
+
+
+def test_dswiglu_against_autograd():
+    rng = np.random.default_rng(8)
+    GU = rng.standard_normal((7, 10)) * 3
+    dH = rng.standard_normal((7, 5))
+    t = torch.from_numpy(GU).requires_grad_(True)
+    h = F.silu(t[:, :5]) * t[:, 5:]
+    h.backward(torch.from_numpy(dH))
+    np.testing.assert_allclose(moe.dswiglu(dH, GU), t.grad.numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(moe.swiglu(GU), h.detach().numpy(), rtol=1e-13)
+
+
+def test_token_forward_matches_layer():
+    T, d, E, k, f = 20, 8, 5, 2, 6
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=31)
+    fwd = moe.layer_forward(x, lg, W1, W2, k)
+    for t in (0, 7, 19):
+        np.testing.assert_allclose(moe.token_forward(x[t], lg[t], W1, W2, k), fwd["y"][t],
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_mxfp8_layer_close_to_exact_layer():
+    """MXFP8 operands perturb each element by at most 2^-4 relative; the layer
+    output stays within a few percent, and the per-token form agrees exactly."""
+    T, d, E, k, f = 40, 64, 4, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=41)
+    exact = moe.layer_forward(x, lg, W1, W2, k)["y"]
+    fwd = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=True)
+    rel = np.linalg.norm(fwd["y"] - exact) / np.linalg.norm(exact)
+    assert 1e-3 < rel < 0.1
+    for t in (0, 13, 39):
+        np.testing.assert_allclose(moe.token_forward(x[t], lg[t], W1, W2, k, mxfp8_operands=True),
+                                   fwd["y"][t], rtol=1e-12, atol=1e-13)

@@ -1,0 +1,96 @@
+"""The oracle's pins must catch plausible mistakes: plant each one in the
+oracle (on the CPU, via monkeypatch) and check that a pin test fails."""
+
+import numpy as np
+import pytest
+
+from oracle import moe, mxfp8
+import test_oracle_ffn_backward as ffn_pins
+import test_oracle_mxfp8 as mx_pins
+import test_oracle_route_permute as route_pins
+
+
+def _swapped_swiglu(GU):
+    f = GU.shape[1] // 2
+    return moe.silu(GU[:, f:]) * GU[:, :f]
+
+
+def _dswiglu_missing_term(dH, GU):
+    f = GU.shape[1] // 2
+    G, U = GU[:, :f], GU[:, f:]
+    s = 1.0 / (1.0 + np.exp(-G))
+    return np.concatenate([dH * U * s, dH * G * s], axis=1)
+
+
+_real_route = moe.route_topk
+
+
+def _route_ties_to_higher_id(logits, k, renormalize=True):
+    T, E = logits.shape
+    flipped = logits[:, ::-1].copy()
+    idx, w, counts = _real_route(flipped, k, renormalize)
+    return (E - 1 - idx).astype(np.int32), w, counts[::-1].copy()
+
+
+def _permute_unstable(idx, E):
+    offsets, dest, src = moe_permute_real(idx, E)
+    T, k = idx.shape
+    src2 = src.copy()
+    for e in range(E):
+        src2[offsets[e]:offsets[e + 1]] = src[offsets[e]:offsets[e + 1]][::-1]
+    dest2 = np.empty(T * k, dtype=np.int64)
+    dest2[src2] = np.arange(T * k)
+    return offsets, dest2.reshape(T, k), src2
+
+
+moe_permute_real = moe.permute_maps
+
+
+def _encode_ties_away(y):
+    y = np.asarray(y, dtype=np.float64)
+    mag = np.abs(y)
+    hi = np.minimum(np.searchsorted(mxfp8.E4M3_POS, mag, side="left"), 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    pick_hi = (mxfp8.E4M3_POS[hi] - mag) <= (mag - mxfp8.E4M3_POS[lo])
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(mag >= 448, 0x7E, code)
+    return (code | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+
+
+def _wgrad_transposed(A, dC, offsets, E):
+    """dB[e] = A_e^T dC_e instead of dC_e^T A_e (operands swapped)."""
+    out = np.zeros((E, A.shape[1], dC.shape[1]))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        out[e] = A[lo:hi].T @ dC[lo:hi]
+    return out
+
+
+@pytest.mark.parametrize("target,attr,fake,check", [
+    (moe, "swiglu", _swapped_swiglu,
+     lambda: ffn_pins.test_layer_equals_dense_masked_moe(40, 16, 6, 2, 12, (3,))),
+    (moe, "dswiglu", _dswiglu_missing_term,
+     lambda: ffn_pins.test_backward_matches_torch_autograd(True)),
+    (moe, "route_topk", _route_ties_to_higher_id,
+     lambda: route_pins.test_route_bruteforce(64, 8, 2, True)),
+    (moe, "permute_maps", _permute_unstable,
+     lambda: route_pins.test_permutation_against_counting_loop(50, 8, 2)),
+    (mxfp8, "e4m3_encode", _encode_ties_away,
+     lambda: mx_pins.test_e4m3_matches_torch_cast_in_range()),
+    (moe, "grouped_gemm_wgrad", _wgrad_transposed,
+     lambda: ffn_pins.test_equal_counts_is_bmm()),
+], ids=["swiglu-swapped", "dswiglu-term", "tie-break", "unstable-permute", "ties-away",
+        "wgrad-rows"])
+def test_pins_catch_planted_mistake(monkeypatch, target, attr, fake, check):
+    monkeypatch.setattr(target, attr, fake)
+    with pytest.raises(AssertionError):
+        check()
+
+
+def test_pins_catch_scale_exponent_off_by_one(monkeypatch):
+    real = mxfp8.shared_exponent
+    monkeypatch.setattr(mxfp8, "shared_exponent", lambda a: real(a) + 1)
+    with pytest.raises(AssertionError):
+        mx_pins.test_shared_exponent_closed_form(1.0, 119)
+    with pytest.raises(AssertionError):
+        mx_pins.test_quantize_rowwise_properties()
