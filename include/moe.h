@@ -1,0 +1,228 @@
+/*
+ * moe.h -- C ABI of libmoe: the single-GPU hot path of dropless Mixture-of-Experts
+ * training on GB300 (sm_103a).
+ *
+ * The operations follow the dropless-MoE layer described in
+ *   [1] "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer Engine"
+ *       (NVIDIA technical blog; zhiding.cn rewrite), and
+ *   [3] a deep reading of arXiv 2603.07685 (paper-daily.com), "Method overview":
+ *       Route -> Dispatch -> Compute -> Combine.
+ * The pages give no formulas; where they leave a step open the plainest reading
+ * is taken and stated next to the function.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *     The library never allocates device memory; scratch comes from the caller
+ *     (query the size with the matching *_workspace_size function).
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream).  No call
+ *     synchronises the host or copies data back to it; per-expert counts and
+ *     offsets live only on the device, so a whole layer can be captured in a
+ *     CUDA graph ([1] "What dropless MoE needs": the CPU never learns the shapes).
+ *   - Shapes (T tokens, d model dim, E experts, k experts per token, f expert
+ *     hidden dim) are host ints.  Matrices are row-major and densely packed.
+ *   - Host-side argument errors return a status and launch nothing; the message
+ *     is kept in moe_last_error_string() (per thread).
+ *   - `dev_status` (may be NULL) is a device int32 that kernels OR error bits
+ *     into (MOE_DEV_*).  Kernels never trap; the caller reads the word when it
+ *     wants to know.  Zero it once before use.
+ *   - Calls on the same stream may reuse each other's outputs; calls that run
+ *     concurrently must not share output or workspace buffers.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, bad enum */
+  MOE_ERR_UNSUPPORTED = 2, /* device is not sm_103 / dtype combination not built */
+  MOE_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+  MOE_ERR_WORKSPACE = 4    /* caller workspace too small */
+} moe_status_t;
+
+typedef enum {
+  MOE_F32 = 0,  /* float32 storage (GEMMs run on the tensor cores as TF32) */
+  MOE_BF16 = 1, /* bfloat16 */
+  MOE_E4M3 = 2  /* MXFP8: FP8 E4M3 codes plus one E8M0 scale byte per 32 elements */
+} moe_dtype_t;
+
+typedef enum {
+  MOE_EPI_NONE = 0,
+  MOE_EPI_SWIGLU = 1,  /* forward GEMM1: out = silu(gate) * up                */
+  MOE_EPI_DSWIGLU = 2  /* dgrad of GEMM2: out = d(gate, up) from dH and (G, U)  */
+} moe_epilogue_t;
+
+/* Device-side error bits OR-ed into *dev_status. */
+#define MOE_DEV_NAN_LOGIT 1 /* a router logit was NaN (outside the router's domain) */
+#define MOE_DEV_BAD_INDEX 2 /* an expert id / row index outside its range, or counts
+                               inconsistent with topk_idx                        */
+#define MOE_DEV_TIMEOUT 4   /* a bounded pipeline wait gave up; outputs are garbage */
+
+/* One GEMM operand.  For MOE_E4M3, `scales` points at the E8M0 bytes, one per 32
+ * consecutive elements along the contraction dimension ([rows, K/32] row-major);
+ * it is ignored (may be NULL) for the other dtypes. */
+typedef struct {
+  const void* ptr;
+  moe_dtype_t dtype;
+  const uint8_t* scales;
+} moe_operand_t;
+
+int moe_version(void);                    /* (major << 16) | (minor << 8) | patch */
+const char* moe_last_error_string(void);  /* message of this thread's last error */
+
+/* ---------------------------------------------------------------- route ----
+ * Top-k expert selection with softmax routing weights ([1] opening section: a
+ * learnable router activates the top-K experts of each token; [1] "Optimisation
+ * 2": a fused router kernel assigns every token its experts before dispatch).
+ *
+ * logits    [T, E] float32.  -inf is allowed (a masked expert); NaN sets
+ *           MOE_DEV_NAN_LOGIT.
+ * topk_idx  [T, k] int32 out: slot j holds the j-th largest logit's expert;
+ *           equal logits go to the lower expert id.
+ * topk_w    [T, k] float32 out: renormalize != 0 -> softmax over the k selected
+ *           logits (sums to 1); renormalize == 0 -> full-softmax probability of
+ *           each selected expert.
+ * counts    [E] int32 out: tokens routed to each expert (zeroed inside; the sum
+ *           is T*k: dropless, nothing is dropped or padded).
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0.
+ */
+moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                            int32_t* topk_idx, float* topk_w, int32_t* counts,
+                            int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- dispatch --
+ * Local dispatch: reorder the T*k (token, slot) pairs into expert-contiguous
+ * rows ([1] "Optimisation 2": dispatch rearranges tokens locally; Figure 3).
+ * Rows are ordered by (expert, token), unpadded: expert e owns rows
+ * [offsets[e], offsets[e+1]).
+ *
+ * x         [T, d] in x_dtype (MOE_F32 or MOE_BF16).
+ * topk_idx  [T, k] int32 from moe_route_topk; counts [E] int32 likewise.
+ * offsets   [E+1] int32 out: exclusive scan of counts, offsets[E] = T*k.
+ * dest_row  [T, k] int32 out: row that pair (t, j) was written to.
+ * src_pair  [T*k] int32 out: pair t*k+j held by each row (inverse of dest_row).
+ * xp        [T*k, d] out, or NULL for the maps only.  xp_dtype == x_dtype copies
+ *           rows bit-exactly; xp_dtype == MOE_E4M3 (x must be MOE_BF16 or
+ *           MOE_F32, d % 32 == 0) quantises each row to MXFP8 on the way
+ *           ([1] "What dropless MoE needs": group-aware MXFP8 quantisation; a
+ *           row-wise 32-element block never spans two experts), writing codes
+ *           to xp and E8M0 scales to xp_scales [T*k, d/32].
+ * workspace moe_permute_workspace_size(T, k, E) bytes of device scratch.
+ * Limits: E <= 1024, k <= 32, d % 8 == 0 (16-byte rows), 16-byte aligned rows.
+ */
+size_t moe_permute_workspace_size(int T, int k, int E);
+moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, int d,
+                         const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                         int32_t* offsets, int32_t* dest_row, int32_t* src_pair,
+                         void* xp, moe_dtype_t xp_dtype, uint8_t* xp_scales,
+                         void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- quantise --
+ * Group-aware MXFP8 quantisation ([1] "What dropless MoE needs" and
+ * "Optimisation 1": MXFP8 block scaling of the expert matmuls; [3] contribution
+ * 3: grouped quantisation for dynamic shapes).  Encoding per the OCP MX v1.0
+ * definition: per block of 32 elements along a row, X = floor(log2 amax) - 8
+ * clamped to [-127, 127] (an all-zero block gets X = 0), scale byte X + 127,
+ * codes = round-to-nearest-even(v / 2^X) to E4M3, saturated to +-448.
+ *
+ * in     [rows, K] MOE_BF16 or MOE_F32; K % 32 == 0.
+ * codes  [rows, K] uint8 out; scales [rows, K/32] uint8 out.
+ * offsets/E: the expert groups of the rows.  Row-wise blocks lie inside one row
+ *        and so inside one group by construction; offsets may be NULL.
+ * axis   0 = row-wise (the only axis built; others return MOE_ERR_UNSUPPORTED).
+ */
+moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows, int K,
+                                        const int32_t* offsets, int E, int axis,
+                                        uint8_t* codes, uint8_t* scales,
+                                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------- grouped GEMM
+ * Ragged grouped GEMM ([1] "Optimisation 1": one kernel launch covers every
+ * expert and computes only the valid token rows of each; the per-expert sizes
+ * are read on the device, never copied to the host).  Persistent tcgen05/TMEM
+ * kernel fed by TMA.  Rows of expert e are [offsets[e], offsets[e+1]); rows at
+ * or beyond offsets[E] are not written.
+ *
+ * Forward: C[r, :] = A[r, :] . B[e]^T for r in expert e's rows.
+ *   A [M, K] (A->dtype), B [E, N, K] (same dtype), accumulate in fp32.
+ *   epi == MOE_EPI_NONE:   C [M, N] in c_dtype (MOE_BF16 or MOE_F32).
+ *   epi == MOE_EPI_SWIGLU: N = 2f with rows 0..f-1 of B[e] the gate projection
+ *     and f..2f-1 the up projection; C [M, f] = silu(A.Bg^T) * (A.Bu^T).  If
+ *     preact != NULL the pre-activations [M, 2f] (gate | up) are stored too, in
+ *     c_dtype, for the backward.
+ * dtypes: F32 x F32 (TF32 tensor cores), BF16 x BF16, E4M3 x E4M3 (MXFP8 with
+ *   E8M0 scales per 32 along K; both scale pointers required).
+ * Limits: K % 32 == 0, N % 32 == 0 (SWIGLU: f % 32 == 0), E <= 1024,
+ *   16-byte aligned pointers, M < 2^31.
+ */
+moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_operand_t* B,
+                                  const int32_t* offsets, int M, int N, int K, int E,
+                                  moe_epilogue_t epi, void* C, moe_dtype_t c_dtype,
+                                  void* preact, int32_t* dev_status, cudaStream_t stream);
+
+/* Data gradient: dA[r, :] = dC[r, :] . B[e] for r in expert e's rows.
+ *   dC [M, N], B [E, N, K] (both MOE_BF16 or both MOE_F32) -> dA [M, K] in dA_dtype.
+ *   epi == MOE_EPI_DSWIGLU fuses the SwiGLU backward: the product is dH [M, K]
+ *     and `preact` [M, 2K] holds the forward pre-activations (gate | up); the
+ *     output is dA = [dG | dU] of shape [M, 2K] with
+ *     dG = dH * U * s * (1 + G * (1 - s)), s = sigmoid(G), dU = dH * silu(G).
+ * Limits as the forward. */
+moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const moe_operand_t* B,
+                                    const int32_t* offsets, int M, int N, int K, int E,
+                                    moe_epilogue_t epi, const void* preact,
+                                    void* dA, moe_dtype_t dA_dtype,
+                                    int32_t* dev_status, cudaStream_t stream);
+
+/* Weight gradient: dB[e] = dC[R_e]^T . A[R_e], a contraction over the ragged rows
+ * R_e of each expert; an expert with no rows gets an exact zero gradient.
+ *   A [M, K], dC [M, N] (both MOE_BF16 or both MOE_F32) -> dB [E, N, K] in dB_dtype.
+ * Limits as the forward. */
+moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
+                                    const int32_t* offsets, int M, int N, int K, int E,
+                                    void* dB, moe_dtype_t dB_dtype,
+                                    int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- combine ---
+ * Weighted unpermute ([1] "Optimisation 2": combine routes expert outputs back
+ * to the original token order and accumulates them; Figure 3).
+ *   y[t] = sum_{j<k} w[t, j] * yp[dest_row[t, j]], summed in slot order in fp32,
+ *   rounded once to y_dtype.  topk_w == NULL means unit weights (this is also
+ *   the backward of dispatch: dx[t] = sum_j dxp[dest_row[t, j]]).
+ *   yp [T*k, d] in dtype (MOE_BF16 / MOE_F32); y [T, d] in y_dtype.
+ * Limits: d % 8 == 0, k <= 32. */
+moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype, int T, int d, int k,
+                                   const int32_t* dest_row, const float* topk_w,
+                                   void* y, moe_dtype_t y_dtype, int32_t* dev_status,
+                                   cudaStream_t stream);
+
+/* Backward of combine:
+ *   dyp[dest_row[t, j]] = w[t, j] * dy[t]          (dyp [T*k, d] in dtype)
+ *   dw[t, j] = sum_c dy[t, c] * yp[dest_row[t, j], c]   (dw [T, k] float32)
+ *   dy [T, d] and yp [T*k, d] in dtype. */
+moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp, moe_dtype_t dtype,
+                                       int T, int d, int k, const int32_t* dest_row,
+                                       const float* topk_w, void* dyp, float* dw,
+                                       int32_t* dev_status, cudaStream_t stream);
+
+/* Backward of the routing weights with respect to the logits.
+ *   renormalize != 0: dlogits[t, idx_j] = w_j (dw_j - sum_i w_i dw_i), 0 for
+ *   unselected experts.  renormalize == 0: dlogits[t, e] = p_e (g_e - sum_i w_i dw_i)
+ *   with p the full softmax of `logits` and g_e = dw_j where e = idx_j, else 0
+ *   (`logits` is only read in this mode and may be NULL otherwise).
+ *   dw, topk_w [T, k] float32; topk_idx [T, k]; dlogits [T, E] float32 out. */
+moe_status_t moe_route_topk_bwd(const float* dw, const float* topk_w, const int32_t* topk_idx,
+                                const float* logits, int T, int E, int k, int renormalize,
+                                float* dlogits, int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

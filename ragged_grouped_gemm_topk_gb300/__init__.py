@@ -1,0 +1,15 @@
+"""GB300-native (sm_103a) hot path of dropless Mixture-of-Experts training.
+
+Route -> dispatch -> group-aware MXFP8 quantisation -> ragged grouped GEMM with
+fused SwiGLU -> combine, and its backward, as hand-written CUDA kernels behind
+the C ABI of include/moe.h (libmoe.so).  This package is the thin Python side:
+``build`` compiles the library, ``binding`` exposes each C entry point under
+the same name, ``layer`` chains them into a layer, ``workloads`` draws seeded
+synthetic inputs.
+"""
+
+from .binding import (moe_grouped_gemm_dgrad, moe_grouped_gemm_fwd,  # noqa: F401
+                      moe_grouped_gemm_wgrad, moe_permute, moe_permute_workspace_size,
+                      moe_quantize_mxfp8_grouped, moe_route_topk, moe_route_topk_bwd,
+                      moe_unpermute_combine, moe_unpermute_combine_bwd, version)
+from .layer import MoELayer  # noqa: F401

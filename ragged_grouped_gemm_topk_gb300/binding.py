@@ -1,0 +1,189 @@
+"""Python binding of libmoe: one function per C entry point, same names.
+
+Argument marshalling only -- every step runs in the library's CUDA kernels.
+Tensors must be CUDA tensors, contiguous, on the current device; calls are
+enqueued on ``torch.cuda.current_stream()``.  Outputs are allocated with
+torch when not passed in.  MXFP8 operands are uint8 code tensors plus uint8
+E8M0 scale tensors.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+from ._lib import (MOE_BF16, MOE_DEV_BAD_INDEX, MOE_DEV_NAN_LOGIT, MOE_DEV_TIMEOUT,  # noqa: F401
+                   MOE_E4M3, MOE_EPI_DSWIGLU, MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_F32, MoeError)
+
+_DT = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16, torch.uint8: MOE_E4M3}
+_EPI = {"none": MOE_EPI_NONE, "swiglu": MOE_EPI_SWIGLU, "dswiglu": MOE_EPI_DSWIGLU}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmoe takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmoe takes contiguous tensors")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t):
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _operand(t, scales=None):
+    return _lib.Operand(t.data_ptr(), _dt(t), scales.data_ptr() if scales is not None else None)
+
+
+def version() -> int:
+    return _lib.load().moe_version()
+
+
+def moe_route_topk(logits, k, renormalize=True, *, topk_idx=None, topk_w=None, counts=None,
+                   dev_status=None):
+    """logits [T,E] fp32 -> (topk_idx [T,k] int32, topk_w [T,k] fp32, counts [E] int32)."""
+    T, E = logits.shape
+    dev = logits.device
+    topk_idx = topk_idx if topk_idx is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    _lib.call("moe_route_topk", _ptr(logits), T, E, k, int(bool(renormalize)), _ptr(topk_idx),
+              _ptr(topk_w), _ptr(counts), _ptr(dev_status), _stream())
+    return topk_idx, topk_w, counts
+
+
+def moe_permute_workspace_size(T, k, E) -> int:
+    return int(_lib.load().moe_permute_workspace_size(T, k, E))
+
+
+def moe_permute(x, topk_idx, counts, E, *, xp_dtype=None, rows=True, offsets=None, dest_row=None,
+                src_pair=None, xp=None, xp_scales=None, workspace=None, dev_status=None):
+    """Dispatch x [T,d] into expert-contiguous rows.  xp_dtype: None (same as x) or
+    "mxfp8" (fused row-wise MXFP8).  Returns a dict with offsets [E+1], dest_row
+    [T,k], src_pair [T*k] (int32) and, if ``rows``, xp [T*k,d] (+ xp_scales)."""
+    T, k = topk_idx.shape
+    d = x.shape[1] if x is not None else 0
+    dev = topk_idx.device
+    M = T * k
+    offsets = offsets if offsets is not None else torch.empty(E + 1, dtype=torch.int32, device=dev)
+    dest_row = dest_row if dest_row is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    src_pair = src_pair if src_pair is not None else torch.empty(M, dtype=torch.int32, device=dev)
+    quant = xp_dtype == "mxfp8"
+    if rows:
+        if xp is None:
+            xp = torch.empty(M, d, dtype=torch.uint8 if quant else x.dtype, device=dev)
+        if quant and xp_scales is None:
+            xp_scales = torch.empty(M, d // 32, dtype=torch.uint8, device=dev)
+    else:
+        xp = None
+    if workspace is None:
+        workspace = torch.empty(moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    _lib.call("moe_permute", _ptr(x) if rows else None, _dt(x) if x is not None else MOE_BF16, T, d,
+              _ptr(topk_idx), k, E, _ptr(counts), _ptr(offsets), _ptr(dest_row), _ptr(src_pair),
+              _ptr(xp), MOE_E4M3 if quant else (_dt(x) if x is not None else MOE_BF16),
+              _ptr(xp_scales), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream())
+    return dict(offsets=offsets, dest_row=dest_row, src_pair=src_pair, xp=xp, xp_scales=xp_scales)
+
+
+def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=None):
+    """Row-wise MXFP8 of inp [rows,K] (bf16/fp32) -> (codes u8 [rows,K], scales u8 [rows,K/32])."""
+    rows, K = inp.shape
+    codes = codes if codes is not None else torch.empty(rows, K, dtype=torch.uint8, device=inp.device)
+    scales = scales if scales is not None else torch.empty(rows, K // 32, dtype=torch.uint8, device=inp.device)
+    _lib.call("moe_quantize_mxfp8_grouped", _ptr(inp), _dt(inp), rows, K, _ptr(offsets), E, 0,
+              _ptr(codes), _ptr(scales), _stream())
+    return codes, scales
+
+
+def moe_grouped_gemm_fwd(A, B, offsets, *, epi="none", A_scales=None, B_scales=None,
+                         out_dtype=torch.bfloat16, out=None, preact=None, want_preact=False,
+                         dev_status=None):
+    """C = ragged A [M,K] . B[e]^T with B [E,N,K]; epi "swiglu" gives [M, N/2]."""
+    M, K = A.shape
+    E, N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A and B disagree on K")
+    n_out = N // 2 if epi == "swiglu" else N
+    if out is None:
+        out = torch.empty(M, n_out, dtype=out_dtype, device=A.device)
+    if want_preact and preact is None:
+        preact = torch.empty(M, N, dtype=out.dtype, device=A.device)
+    a, b = _operand(A, A_scales), _operand(B, B_scales)
+    _lib.call("moe_grouped_gemm_fwd", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E, _EPI[epi],
+              _ptr(out), _dt(out), _ptr(preact), _ptr(dev_status), _stream())
+    return (out, preact) if want_preact or preact is not None else out
+
+
+def moe_grouped_gemm_dgrad(dC, B, offsets, *, epi="none", preact=None, out_dtype=torch.bfloat16,
+                           out=None, dev_status=None):
+    """dA = ragged dC [M,N] . B[e] with B [E,N,K]; epi "dswiglu" (with preact [M,2K])
+    returns [dG | dU] of shape [M, 2K]."""
+    M, N = dC.shape
+    E, N2, K = B.shape
+    if N2 != N:
+        raise ValueError("dC and B disagree on N")
+    width = 2 * K if epi == "dswiglu" else K
+    if out is None:
+        out = torch.empty(M, width, dtype=out_dtype, device=dC.device)
+    a, b = _operand(dC), _operand(B)
+    _lib.call("moe_grouped_gemm_dgrad", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E, _EPI[epi],
+              _ptr(preact), _ptr(out), _dt(out), _ptr(dev_status), _stream())
+    return out
+
+
+def moe_grouped_gemm_wgrad(A, dC, offsets, E, *, out_dtype=torch.bfloat16, out=None, dev_status=None):
+    """dB[e] = dC[R_e]^T . A[R_e] -> [E, N, K]."""
+    M, K = A.shape
+    M2, N = dC.shape
+    if M2 != M:
+        raise ValueError("A and dC disagree on M")
+    if out is None:
+        out = torch.empty(E, N, K, dtype=out_dtype, device=A.device)
+    a, b = _operand(A), _operand(dC)
+    _lib.call("moe_grouped_gemm_wgrad", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E,
+              _ptr(out), _dt(out), _ptr(dev_status), _stream())
+    return out
+
+
+def moe_unpermute_combine(yp, dest_row, topk_w, *, out_dtype=None, out=None, dev_status=None):
+    """y[t] = sum_j w[t,j] yp[dest_row[t,j]] (topk_w None = unit weights)."""
+    T, k = dest_row.shape
+    d = yp.shape[1]
+    if out is None:
+        out = torch.empty(T, d, dtype=out_dtype or yp.dtype, device=yp.device)
+    _lib.call("moe_unpermute_combine", _ptr(yp), _dt(yp), T, d, k, _ptr(dest_row), _ptr(topk_w),
+              _ptr(out), _dt(out), _ptr(dev_status), _stream())
+    return out
+
+
+def moe_unpermute_combine_bwd(dy, yp, dest_row, topk_w, *, dyp=None, dw=None, dev_status=None):
+    T, k = dest_row.shape
+    d = dy.shape[1]
+    if dyp is None:
+        dyp = torch.empty(T * k, d, dtype=dy.dtype, device=dy.device)
+    if dw is None:
+        dw = torch.empty(T, k, dtype=torch.float32, device=dy.device)
+    _lib.call("moe_unpermute_combine_bwd", _ptr(dy), _ptr(yp), _dt(dy), T, d, k, _ptr(dest_row),
+              _ptr(topk_w), _ptr(dyp), _ptr(dw), _ptr(dev_status), _stream())
+    return dyp, dw
+
+
+def moe_route_topk_bwd(dw, topk_w, topk_idx, E, *, logits=None, renormalize=True, out=None,
+                       dev_status=None):
+    T, k = topk_idx.shape
+    if out is None:
+        out = torch.empty(T, E, dtype=torch.float32, device=dw.device)
+    _lib.call("moe_route_topk_bwd", _ptr(dw), _ptr(topk_w), _ptr(topk_idx), _ptr(logits), T, E, k,
+              int(bool(renormalize)), _ptr(out), _ptr(dev_status), _stream())
+    return out

@@ -1,0 +1,253 @@
+// Weighted unpermute (combine) and its backward.
+//
+// Combine per "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer
+// Engine", "Optimisation 2" (processed tokens are routed back and the expert
+// results accumulated per token) and Figure 3 (back to the original order).
+// One warp owns one token: its k source rows are gathered with 16-byte loads,
+// up to 8 rows in flight per lane, and summed in slot order in fp32.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kThreads = 256;
+
+struct alignas(16) Vec16 {
+  uint32_t w[4];
+};
+
+template <typename T>
+struct Elt;
+template <>
+struct Elt<uint16_t> {
+  static constexpr int kN = 8;
+  __device__ static void unpack(const Vec16& v, float (&f)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16_to_f32(static_cast<uint16_t>(v.w[i] & 0xFFFFu));
+      f[2 * i + 1] = bf16_to_f32(static_cast<uint16_t>(v.w[i] >> 16));
+    }
+  }
+  __device__ static void store(uint8_t* dst, const float (&f)[8]) {
+    Vec16 o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o.w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    *reinterpret_cast<Vec16*>(dst) = o;
+  }
+};
+template <>
+struct Elt<float> {
+  static constexpr int kN = 4;
+  __device__ static void unpack(const Vec16& v, float (&f)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(v.w[i]);
+  }
+  __device__ static void store(uint8_t* dst, const float (&f)[4]) {
+    *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+
+// Store N floats (N = elements of one 16-byte input chunk) in the output dtype.
+template <typename Tout, int N>
+__device__ __forceinline__ void store_out(uint8_t* dst, const float (&f)[N]) {
+  if constexpr (sizeof(Tout) == 2) {
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    if constexpr (N == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; i += 4)
+      *reinterpret_cast<float4*>(dst + 4 * i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
+  }
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kThreads) combine_kernel(
+    const uint8_t* __restrict__ yp, int T, int d, int k, const int32_t* __restrict__ dest_row,
+    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int32_t* status) {
+  constexpr int N = Elt<Tin>::kN;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int M = T * k;
+  const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
+  const size_t out_row = static_cast<size_t>(d) * sizeof(Tout);
+  const int n16 = static_cast<int>(in_row / 16);
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    int src = -1;
+    float w = 0.f;
+    if (lane < k) {
+      const size_t p = static_cast<size_t>(t) * k + lane;
+      src = dest_row[p];
+      w = topk_w ? topk_w[p] : 1.f;
+      if (src < 0 || src >= M) {
+        flag_error(status, MOE_DEV_BAD_INDEX);
+        src = -1;
+      }
+    }
+    for (int base = 0; base < n16; base += 32) {
+      const int c = base + lane;
+      const bool active = c < n16;
+      float acc[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = 0.f;
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        Vec16 v[8];
+        float wj[8];
+        int sj[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sj[u] = __shfl_sync(kFull, src, (j0 + u) & 31);
+          wj[u] = __shfl_sync(kFull, w, (j0 + u) & 31);
+          if (active && j0 + u < k && sj[u] >= 0)
+            v[u] = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj[u]) * in_row)[c];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (active && j0 + u < k && sj[u] >= 0) {
+            float f[N];
+            Elt<Tin>::unpack(v[u], f);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(wj[u], f[i], acc[i]);
+          }
+        }
+      }
+      if (active)
+        store_out<Tout, N>(y + static_cast<size_t>(t) * out_row + static_cast<size_t>(c) * N * sizeof(Tout), acc);
+    }
+  }
+}
+
+// dyp[dest_row[t,j]] = w[t,j] dy[t];  dw[t,j] = <dy[t], yp[dest_row[t,j]]>.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
+    const uint8_t* __restrict__ dy, const uint8_t* __restrict__ yp, int T, int d, int k,
+    const int32_t* __restrict__ dest_row, const float* __restrict__ topk_w,
+    uint8_t* __restrict__ dyp, float* __restrict__ dw, int32_t* status) {
+  constexpr int N = Elt<Tin>::kN;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int M = T * k;
+  const size_t row = static_cast<size_t>(d) * sizeof(Tin);
+  const int n16 = static_cast<int>(row / 16);
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    int src = -1;
+    float w = 0.f;
+    if (lane < k) {
+      const size_t p = static_cast<size_t>(t) * k + lane;
+      src = dest_row[p];
+      w = topk_w[p];
+      if (src < 0 || src >= M) {
+        flag_error(status, MOE_DEV_BAD_INDEX);
+        src = -1;
+      }
+    }
+    const Vec16* dyr = reinterpret_cast<const Vec16*>(dy + static_cast<size_t>(t) * row);
+    for (int j = 0; j < k; ++j) {
+      const int sj = __shfl_sync(kFull, src, j);
+      const float wj = __shfl_sync(kFull, w, j);
+      float part = 0.f;
+      if (sj >= 0) {
+        const Vec16* ypr = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * row);
+        uint8_t* out = dyp + static_cast<size_t>(sj) * row;
+        for (int c = lane; c < n16; c += 32) {
+          float a[N], b[N], o[N];
+          Elt<Tin>::unpack(dyr[c], a);
+          Elt<Tin>::unpack(ypr[c], b);
+#pragma unroll
+          for (int i = 0; i < N; ++i) {
+            part = fmaf(a[i], b[i], part);
+            o[i] = wj * a[i];
+          }
+          Elt<Tin>::store(out + static_cast<size_t>(c) * 16, o);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+      if (lane == 0) dw[static_cast<size_t>(t) * k + j] = part;
+    }
+  }
+}
+
+int grid_for(int T, int sms) {
+  const int wpb = kThreads / 32;
+  int g = (T + wpb - 1) / wpb;
+  const int cap = sms * 8;
+  return g < 1 ? 1 : (g < cap ? g : cap);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype, int T, int d,
+                                              int k, const int32_t* dest_row,
+                                              const float* topk_w, void* y, moe_dtype_t y_dtype,
+                                              int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || d < 0 || k < 1 || k > 32 || d % 8 ||
+      (dtype != MOE_BF16 && dtype != MOE_F32) || (y_dtype != MOE_BF16 && y_dtype != MOE_F32)) {
+    set_error("moe_unpermute_combine: need T, d >= 0, d %% 8 == 0, 1 <= k <= 32, BF16/F32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("moe_unpermute_combine: T*k must fit in int32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (T > 0 && d > 0 && (!yp || !y || !dest_row || !aligned16(yp) || !aligned16(y))) {
+    set_error("moe_unpermute_combine: null or misaligned pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || d == 0) return MOE_OK;
+  const int grid = grid_for(T, sms);
+  const uint8_t* a = static_cast<const uint8_t*>(yp);
+  uint8_t* o = static_cast<uint8_t*>(y);
+  if (dtype == MOE_BF16 && y_dtype == MOE_BF16)
+    combine_kernel<uint16_t, uint16_t><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+  else if (dtype == MOE_BF16)
+    combine_kernel<uint16_t, float><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+  else if (y_dtype == MOE_BF16)
+    combine_kernel<float, uint16_t><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+  else
+    combine_kernel<float, float><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+  return check_launch("moe_unpermute_combine");
+}
+
+extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp,
+                                                  moe_dtype_t dtype, int T, int d, int k,
+                                                  const int32_t* dest_row, const float* topk_w,
+                                                  void* dyp, float* dw, int32_t* dev_status,
+                                                  cudaStream_t stream) {
+  if (T < 0 || d < 0 || k < 1 || k > 32 || d % 8 || (dtype != MOE_BF16 && dtype != MOE_F32)) {
+    set_error("moe_unpermute_combine_bwd: need T, d >= 0, d %% 8 == 0, 1 <= k <= 32, BF16/F32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("moe_unpermute_combine_bwd: T*k must fit in int32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (T > 0 && (!dy || !yp || !dest_row || !topk_w || !dyp || !dw || !aligned16(dy) ||
+                !aligned16(yp) || !aligned16(dyp))) {
+    set_error("moe_unpermute_combine_bwd: null or misaligned pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const int grid = grid_for(T, sms);
+  const uint8_t* a = static_cast<const uint8_t*>(dy);
+  const uint8_t* b = static_cast<const uint8_t*>(yp);
+  uint8_t* o = static_cast<uint8_t*>(dyp);
+  if (dtype == MOE_BF16)
+    combine_bwd_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
+  else
+    combine_bwd_kernel<float><<<grid, kThreads, 0, stream>>>(a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
+  return check_launch("moe_unpermute_combine_bwd");
+}

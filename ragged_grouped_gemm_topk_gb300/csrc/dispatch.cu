@@ -1,0 +1,452 @@
+// Local dispatch (token permutation) and row-wise group-aware MXFP8 quantisation.
+//
+// Dispatch per "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer
+// Engine", "Optimisation 2" (dispatch = local rearrangement of tokens by expert)
+// and Figure 3.  Rows are ordered by (expert, token), so the permutation is
+// unique and the kernels reproduce it exactly without sorting:
+//
+//   rank     one block per 256 tokens; each warp builds, for its 32 tokens, a
+//            32-bit mask per expert (atomicOr in shared memory, order-free), so
+//            a pair's rank among earlier tokens of the same expert is a popcount;
+//            per-warp counts are scanned inside the block and the block's
+//            per-expert totals go to the workspace.
+//   scan     one block: offsets = exclusive scan of counts, then for every expert
+//            an exclusive scan of the block totals down the blocks.
+//   scatter  one warp per token: dest_row / src_pair, then the token's row is
+//            copied with 16-byte loads and stores to its k rows, optionally
+//            quantised to MXFP8 on the way.
+//
+// MXFP8 follows the OCP Microscaling Formats v1.0 conversion (shared exponent
+// floor(log2 amax) - 8, clamped to [-127, 127]; E4M3 round-to-nearest-even with
+// saturation); an all-zero block gets scale byte 127.  Blocks run along a row,
+// and a row belongs to one expert, so no block mixes two experts ("group-aware").
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+constexpr int kRankThreads = 256;                    // 8 warps x 32 tokens per block
+constexpr int kTokensPerRankBlock = kRankThreads;
+constexpr int kScatterThreads = 256;
+
+__global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ local_rank,
+    int32_t* __restrict__ block_hist, int32_t* status) {
+  extern __shared__ uint32_t sm[];
+  uint32_t* mask = sm;                                      // [8][E]
+  int32_t* wbase = reinterpret_cast<int32_t*>(sm + 8 * E);  // [8][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) mask[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kTokensPerRankBlock + warp * 32 + lane;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) {
+        flag_error(status, MOE_DEV_BAD_INDEX);
+        continue;
+      }
+      atomicOr(&mask[warp * E + e], 1u << lane);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      wbase[w * E + e] = run;
+      run += __popc(mask[w * E + e]);
+    }
+    block_hist[static_cast<size_t>(blockIdx.x) * E + e] = run;
+  }
+  __syncthreads();
+  if (t < T) {
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[static_cast<size_t>(t) * k + j];
+      int r = -1;
+      if (e >= 0 && e < E) r = wbase[warp * E + e] + __popc(mask[warp * E + e] & below);
+      local_rank[static_cast<size_t>(t) * k + j] = r;
+    }
+  }
+}
+
+// Single block of 1024 threads; thread e owns expert e.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ counts,
+                                                            int E, int nblk, int total,
+                                                            int32_t* __restrict__ block_hist,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* status) {
+  __shared__ int warp_sum[32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int c = e < E ? counts[e] : 0;
+  int incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(kFull, s, off);
+      if (lane >= off) s += v;
+    }
+    warp_sum[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - c + (warp > 0 ? warp_sum[warp - 1] : 0);
+  if (e < E) {
+    offsets[e] = excl;
+    if (e == E - 1) {
+      offsets[E] = excl + c;
+      if (excl + c != total) flag_error(status, MOE_DEV_BAD_INDEX);
+    }
+    int run = excl;
+    int b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = block_hist[static_cast<size_t>(b + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        block_hist[static_cast<size_t>(b + u) * E + e] = run;
+        run += h[u];
+      }
+    }
+    for (; b < nblk; ++b) {
+      const int h = block_hist[static_cast<size_t>(b) * E + e];
+      block_hist[static_cast<size_t>(b) * E + e] = run;
+      run += h;
+    }
+    if (run != excl + c) flag_error(status, MOE_DEV_BAD_INDEX);
+  }
+  if (E == 0 && e == 0) offsets[0] = 0;
+}
+
+struct alignas(16) Vec16 {
+  uint32_t w[4];
+};
+
+// MXFP8 of one 16-byte chunk held by a lane: returns the E4M3 bytes of its
+// elements; the 32-element block is shared by LPB consecutive lanes.
+template <typename Tin>
+struct Mx;
+
+template <>
+struct Mx<uint16_t> {  // bf16: 8 elements per lane, 4 lanes per block
+  static constexpr int kEpl = 8;
+  static constexpr int kLpb = 4;
+  __device__ static void values(const Vec16& v, float (&f)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = bf16_to_f32(static_cast<uint16_t>(v.w[i] & 0xFFFFu));
+      f[2 * i + 1] = bf16_to_f32(static_cast<uint16_t>(v.w[i] >> 16));
+    }
+  }
+};
+
+template <>
+struct Mx<float> {  // f32: 4 elements per lane, 8 lanes per block
+  static constexpr int kEpl = 4;
+  static constexpr int kLpb = 8;
+  __device__ static void values(const Vec16& v, float (&f)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(v.w[i]);
+  }
+};
+
+// Shared-exponent rule: scale byte and the exact power of two 2^-X to multiply by.
+__device__ __forceinline__ void mx_scale(float amax, uint32_t* sbyte, float* inv) {
+  if (amax == 0.f) {
+    *sbyte = 127u;
+    *inv = 1.f;
+    return;
+  }
+  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent
+  const int s = eb - 8 > 0 ? eb - 8 : 0;                                     // X + 127
+  *sbyte = static_cast<uint32_t>(s);
+  *inv = __uint_as_float(static_cast<uint32_t>(254 - s) << 23);              // 2^(127 - s)
+}
+
+// Quantise one lane's chunk; all 32 lanes must call (inactive lanes pass zeros).
+template <typename Tin>
+__device__ __forceinline__ void mx_chunk(const Vec16& v, uint32_t (&codes)[2], uint32_t* sbyte) {
+  constexpr int EPL = Mx<Tin>::kEpl;
+  float f[EPL];
+  Mx<Tin>::values(v, f);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+  for (int off = 1; off < Mx<Tin>::kLpb; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+  float inv;
+  mx_scale(amax, sbyte, &inv);
+  codes[0] = codes[1] = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; i += 2) {
+    const uint32_t pr = f32x2_to_e4m3x2(f[i] * inv, f[i + 1] * inv);
+    codes[i / 4] |= pr << (16 * ((i / 2) & 1));
+  }
+}
+
+template <typename Tin, bool kQuant>
+__global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
+    const uint8_t* __restrict__ x, int T, int d, const int32_t* __restrict__ idx, int k, int E,
+    const int32_t* local_rank, const int32_t* __restrict__ block_base,
+    int32_t* dest_row, int32_t* __restrict__ src_pair, uint8_t* __restrict__ xp,
+    uint8_t* __restrict__ xp_scales, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
+  const size_t out_row = kQuant ? static_cast<size_t>(d) : in_row;
+  const int n16 = static_cast<int>(in_row / 16);
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    int dest = -1;
+    if (lane < k) {
+      const size_t p = static_cast<size_t>(t) * k + lane;
+      const int e = idx[p];
+      const int r = local_rank[p];
+      if (e >= 0 && e < E && r >= 0)
+        dest = block_base[static_cast<size_t>(t / kTokensPerRankBlock) * E + e] + r;
+      if (dest >= T * k) {
+        flag_error(status, MOE_DEV_BAD_INDEX);
+        dest = -1;
+      }
+      dest_row[p] = dest;
+      if (dest >= 0) src_pair[dest] = static_cast<int32_t>(p);
+    }
+    if (xp == nullptr) continue;
+    const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
+    for (int base = 0; base < n16; base += 32) {
+      const int c = base + lane;
+      const bool active = c < n16;
+      Vec16 v;
+      if (active) {
+        v = src[c];
+      } else {
+        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0;
+      }
+      if constexpr (kQuant) {
+        uint32_t codes[2], sbyte;
+        mx_chunk<Tin>(v, codes, &sbyte);
+        constexpr int EPL = Mx<Tin>::kEpl;
+        for (int j = 0; j < k; ++j) {
+          const int dj = __shfl_sync(kFull, dest, j);
+          if (active && dj >= 0) {
+            uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * EPL;
+            if (EPL == 8)
+              *reinterpret_cast<uint2*>(orow) = make_uint2(codes[0], codes[1]);
+            else
+              *reinterpret_cast<uint32_t*>(orow) = codes[0];
+            if ((lane % Mx<Tin>::kLpb) == 0)
+              xp_scales[static_cast<size_t>(dj) * (d / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+          }
+        }
+      } else {
+        for (int j = 0; j < k; ++j) {
+          const int dj = __shfl_sync(kFull, dest, j);
+          if (active && dj >= 0)
+            reinterpret_cast<Vec16*>(xp + static_cast<size_t>(dj) * out_row)[c] = v;
+        }
+      }
+    }
+  }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
+    const uint8_t* __restrict__ in, int rows, int K, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  constexpr int EPL = Mx<Tin>::kEpl;
+  const size_t in_row = static_cast<size_t>(K) * sizeof(Tin);
+  const int n16 = static_cast<int>(in_row / 16);
+  for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
+    const Vec16* src = reinterpret_cast<const Vec16*>(in + static_cast<size_t>(r) * in_row);
+    for (int base = 0; base < n16; base += 32) {
+      const int c = base + lane;
+      const bool active = c < n16;
+      Vec16 v;
+      if (active) {
+        v = src[c];
+      } else {
+        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0;
+      }
+      uint32_t q[2], sbyte;
+      mx_chunk<Tin>(v, q, &sbyte);
+      if (active) {
+        uint8_t* orow = codes + static_cast<size_t>(r) * K + static_cast<size_t>(c) * EPL;
+        if (EPL == 8)
+          *reinterpret_cast<uint2*>(orow) = make_uint2(q[0], q[1]);
+        else
+          *reinterpret_cast<uint32_t*>(orow) = q[0];
+        if ((lane % Mx<Tin>::kLpb) == 0)
+          scales[static_cast<size_t>(r) * (K / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+      }
+    }
+  }
+}
+
+int scatter_grid(int T, int sms) {
+  const int wpb = kScatterThreads / 32;
+  int g = (T + wpb - 1) / wpb;
+  const int cap = sms * 8;
+  return g < 1 ? 1 : (g < cap ? g : cap);
+}
+
+}  // namespace
+
+// Launches the three permute kernels; shared by the workspace and the
+// fixed-scratch entry points.
+moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
+                            const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                            int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
+                            moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
+                            int32_t* dev_status, cudaStream_t stream, int sms) {
+  const int nblk = (T + kTokensPerRankBlock - 1) / kTokensPerRankBlock;
+  const size_t rank_smem = static_cast<size_t>(2) * 8 * E * sizeof(uint32_t);  // mask + base, [8][E] each
+  if (rank_smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(permute_rank_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(rank_smem));
+    if (e != cudaSuccess) {
+      set_error("moe_permute: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
+  }
+  if (nblk > 0) {
+    permute_rank_kernel<<<nblk, kRankThreads, rank_smem, stream>>>(topk_idx, T, k, E, dest_row,
+                                                                   hist, dev_status);
+  }
+  permute_scan_kernel<<<1, 1024, 0, stream>>>(counts, E, nblk, T * k, hist, offsets, dev_status);
+  if (T == 0) return check_launch("moe_permute");
+  const int grid = scatter_grid(T, sms);
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  uint8_t* xpb = static_cast<uint8_t*>(xp);
+  // dest_row holds each pair's within-block rank until the scatter overwrites that
+  // same element with the pair's final row (read and write by the same thread).
+  if (xp_dtype == MOE_E4M3) {
+    if (x_dtype == MOE_BF16)
+      permute_scatter_kernel<uint16_t, true><<<grid, kScatterThreads, 0, stream>>>(
+          xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
+    else
+      permute_scatter_kernel<float, true><<<grid, kScatterThreads, 0, stream>>>(
+          xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
+  } else if (x_dtype == MOE_BF16) {
+    permute_scatter_kernel<uint16_t, false><<<grid, kScatterThreads, 0, stream>>>(
+        xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
+  } else {
+    permute_scatter_kernel<float, false><<<grid, kScatterThreads, 0, stream>>>(
+        xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
+  }
+  return check_launch("moe_permute");
+}
+
+moe_status_t permute_validate(const void* x, moe_dtype_t x_dtype, int T, int d,
+                              const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                              int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
+                              moe_dtype_t xp_dtype, uint8_t* xp_scales) {
+  if (T < 0 || d < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) {
+    set_error("moe_permute: need T, d >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32)");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("moe_permute: T*k must fit in int32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!counts || !offsets || (T > 0 && (!topk_idx || !dest_row || !src_pair))) {
+    set_error("moe_permute: null pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (xp) {
+    if (!x || (x_dtype != MOE_BF16 && x_dtype != MOE_F32)) {
+      set_error("moe_permute: x must be a BF16 or F32 device buffer");
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (xp_dtype != x_dtype && xp_dtype != MOE_E4M3) {
+      set_error("moe_permute: xp_dtype must equal x_dtype or be MOE_E4M3");
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (d % 8 || !aligned16(x) || !aligned16(xp)) {
+      set_error("moe_permute: d %% 8 == 0 and 16-byte aligned x / xp required");
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (xp_dtype == MOE_E4M3 && (d % 32 || !xp_scales)) {
+      set_error("moe_permute: MXFP8 output needs d %% 32 == 0 and xp_scales");
+      return MOE_ERR_INVALID_ARG;
+    }
+  }
+  return MOE_OK;
+}
+
+size_t permute_hist_bytes(int T, int E) {
+  const size_t nblk = (static_cast<size_t>(T > 0 ? T : 0) + kTokensPerRankBlock - 1) / kTokensPerRankBlock;
+  return nblk * static_cast<size_t>(E > 0 ? E : 0) * sizeof(int32_t);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_permute_workspace_size(int T, int k, int E) {
+  (void)k;
+  const size_t b = permute_hist_bytes(T, E);
+  return b < 256 ? 256 : b;
+}
+
+extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, int d,
+                                    const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                                    int32_t* offsets, int32_t* dest_row, int32_t* src_pair,
+                                    void* xp, moe_dtype_t xp_dtype, uint8_t* xp_scales,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    cudaStream_t stream) {
+  moe_status_t st = permute_validate(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row,
+                                     src_pair, xp, xp_dtype, xp_scales);
+  if (st != MOE_OK) return st;
+  if (!workspace || workspace_bytes < permute_hist_bytes(T, E)) {
+    set_error("moe_permute: workspace of %zu bytes needed", permute_hist_bytes(T, E));
+    return MOE_ERR_WORKSPACE;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp,
+                        xp_dtype, xp_scales, static_cast<int32_t*>(workspace), dev_status, stream,
+                        sms);
+}
+
+extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows,
+                                                   int K, const int32_t* offsets, int E, int axis,
+                                                   uint8_t* codes, uint8_t* scales,
+                                                   cudaStream_t stream) {
+  (void)offsets;
+  (void)E;
+  if (axis != 0) {
+    set_error("moe_quantize_mxfp8_grouped: only axis 0 (row-wise) is built");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (rows < 0 || K < 0 || K % 32 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
+    set_error("moe_quantize_mxfp8_grouped: need rows >= 0, K %% 32 == 0, BF16/F32 input");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (rows > 0 && K > 0 && (!in || !codes || !scales || !aligned16(in) || !aligned16(codes))) {
+    set_error("moe_quantize_mxfp8_grouped: null or misaligned pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0 || K == 0) return MOE_OK;
+  const int grid = scatter_grid(rows, sms);
+  if (in_dtype == MOE_BF16)
+    quantize_rowwise_kernel<uint16_t><<<grid, kScatterThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(in), rows, K, codes, scales);
+  else
+    quantize_rowwise_kernel<float><<<grid, kScatterThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(in), rows, K, codes, scales);
+  return check_launch("moe_quantize_mxfp8_grouped");
+}

@@ -1,0 +1,128 @@
+"""A dropless-MoE layer (route -> dispatch -> grouped MLP -> combine) on libmoe.
+
+Route, dispatch, the two grouped GEMMs of the expert MLP and combine, in the
+order of "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer
+Engine", Figure 3 (and the Route -> Dispatch -> Compute -> Combine stages of
+the arXiv 2603.07685 reading, "Method overview").  All buffers are allocated
+once, at construction, with the static size T*k for the permuted rows (exact
+for dropless routing), so a forward (and backward) pass launches kernels only,
+never reads a count on the host, and can be captured in one CUDA graph.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    """Single-GPU MoE layer with SwiGLU experts.
+
+    W1 [E, 2f, d] (gate rows then up rows) and W2 [E, d, f] in the compute dtype
+    ("f32", "bf16"; "mxfp8" keeps bf16 master weights and quantises them once,
+    at construction, to MXFP8 codes + E8M0 scales along the contraction dim).
+    """
+
+    def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False):
+        self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
+        self.dtype, self.renormalize, self.training = dtype, renormalize, training
+        if training and dtype == "mxfp8":
+            raise NotImplementedError("the MXFP8 backward is not built")
+        dev = W1.device
+        self.device = dev
+        M = T * k
+        self.M = M
+        store = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.store = store
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.W1, self.W2 = W1, W2
+        self.topk_idx = torch.empty(T, k, **i32)
+        self.topk_w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.dest_row = torch.empty(T, k, **i32)
+        self.src_pair = torch.empty(M, **i32)
+        self.workspace = torch.empty(B.moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+        self.dev_status = torch.zeros(1, **i32)
+        self.h = torch.empty(M, f, dtype=store, device=dev)
+        self.yp = torch.empty(M, d, dtype=store, device=dev)
+        self.y = torch.empty(T, d, dtype=store, device=dev)
+        self.gu = torch.empty(M, 2 * f, dtype=store, device=dev) if training else None
+        if dtype == "mxfp8":
+            self.xq = torch.empty(M, d, dtype=torch.uint8, device=dev)
+            self.xs = torch.empty(M, d // 32, dtype=torch.uint8, device=dev)
+            self.hq = torch.empty(M, f, dtype=torch.uint8, device=dev)
+            self.hs = torch.empty(M, f // 32, dtype=torch.uint8, device=dev)
+            self.W1q, self.W1s = B.moe_quantize_mxfp8_grouped(W1.reshape(E * 2 * f, d))
+            self.W2q, self.W2s = B.moe_quantize_mxfp8_grouped(W2.reshape(E * d, f))
+            self.W1q, self.W1s = self.W1q.view(E, 2 * f, d), self.W1s.view(E, 2 * f, d // 32)
+            self.W2q, self.W2s = self.W2q.view(E, d, f), self.W2s.view(E, d, f // 32)
+            self.xp = None
+        else:
+            self.xp = torch.empty(M, d, dtype=store, device=dev)
+        if training:
+            self.dyp = torch.empty(M, d, dtype=store, device=dev)
+            self.dw = torch.empty(T, k, dtype=torch.float32, device=dev)
+            self.dgu = torch.empty(M, 2 * f, dtype=store, device=dev)
+            self.dxp = torch.empty(M, d, dtype=store, device=dev)
+            self.dx = torch.empty(T, d, dtype=store, device=dev)
+            self.dlogits = torch.empty(T, E, dtype=torch.float32, device=dev)
+            self.dW1 = torch.empty_like(W1)
+            self.dW2 = torch.empty_like(W2)
+
+    # ------------------------------------------------------------------ forward
+    def route(self, logits):
+        B.moe_route_topk(logits, self.k, self.renormalize, topk_idx=self.topk_idx,
+                         topk_w=self.topk_w, counts=self.counts, dev_status=self.dev_status)
+
+    def dispatch(self, x):
+        if self.dtype == "mxfp8":
+            B.moe_permute(x, self.topk_idx, self.counts, self.E, xp_dtype="mxfp8", offsets=self.offsets,
+                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xq,
+                          xp_scales=self.xs, workspace=self.workspace, dev_status=self.dev_status)
+        else:
+            B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
+                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
+                          workspace=self.workspace, dev_status=self.dev_status)
+
+    def expert_mlp(self):
+        if self.dtype == "mxfp8":
+            B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
+                                   B_scales=self.W1s, out=self.h, dev_status=self.dev_status)
+            B.moe_quantize_mxfp8_grouped(self.h, self.offsets, self.E, codes=self.hq, scales=self.hs)
+            B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
+                                   out=self.yp, dev_status=self.dev_status)
+        else:
+            B.moe_grouped_gemm_fwd(self.xp, self.W1, self.offsets, epi="swiglu", out=self.h,
+                                   preact=self.gu, dev_status=self.dev_status)
+            B.moe_grouped_gemm_fwd(self.h, self.W2, self.offsets, out=self.yp, dev_status=self.dev_status)
+
+    def combine(self):
+        B.moe_unpermute_combine(self.yp, self.dest_row, self.topk_w, out=self.y,
+                                dev_status=self.dev_status)
+
+    def forward(self, x, logits):
+        self.route(logits)
+        self.dispatch(x)
+        self.expert_mlp()
+        self.combine()
+        return self.y
+
+    # ------------------------------------------------------------------ backward
+    def backward(self, dy, logits=None):
+        """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward)."""
+        if not self.training:
+            raise RuntimeError("construct the layer with training=True")
+        st = self.dev_status
+        B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
+                                    dev_status=st)
+        B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
+                                 out=self.dgu, dev_status=st)
+        B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
+        B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
+        B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
+        B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=self.dx, dev_status=st)
+        B.moe_route_topk_bwd(self.dw, self.topk_w, self.topk_idx, self.E, logits=logits,
+                             renormalize=self.renormalize, out=self.dlogits, dev_status=st)
+        return self.dx, self.dlogits, self.dW1, self.dW2

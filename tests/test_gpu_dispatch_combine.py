@@ -1,0 +1,226 @@
+"""GPU parity: routing, dispatch (plain and fused MXFP8), quantisation, combine,
+combine backward and router backward against the float64 oracle.
+
+Integers (expert ids, counts, offsets, both permutation maps) and MXFP8
+bytes must match bit-exactly; routing weights within 1e-6; floating outputs
+within the bound their arithmetic allows.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import ragged_grouped_gemm_topk_gb300 as moe_gpu
+from ragged_grouped_gemm_topk_gb300 import workloads as W
+from oracle import moe as om
+from oracle import mxfp8 as omx
+from _parity import TOL_W, f64, i64, logits_dev, need_gpu, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+# Full-size routing/dispatch for every workload (integer work is cheap to check
+# in full), plus reduced shapes with awkward sizes.
+ROUTE_CASES = [w.name for w in W.WORKLOADS]
+SMALL = [
+    W.WORKLOADS[0].scaled(T=1, name="T1"),
+    W.WORKLOADS[0].scaled(T=257, E=5, k=3, d=40, name="ragged-T257"),
+    W.WORKLOADS[2].scaled(T=1000, E=128, k=8, d=64, name="zipf-E128"),
+    W.WORKLOADS[3].scaled(T=300, E=256, k=8, d=96, name="zipf-E256-empty"),
+    W.WORKLOADS[0].scaled(T=64, E=1, k=1, d=32, name="E1"),
+    W.WORKLOADS[0].scaled(T=50, E=6, k=6, d=32, name="k=E"),
+    W.WORKLOADS[0].scaled(T=77, E=1000, k=32, d=32, name="E1000-k32"),
+]
+
+
+def _route_check(w, renormalize=True):
+    lg = logits_dev(w)
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, w.k, renormalize)
+    o_idx, o_w, o_counts = om.route_topk(lg.cpu().numpy(), w.k, renormalize)
+    assert (i64(idx) == o_idx).all()
+    assert np.abs(f64(wt) - o_w).max() <= TOL_W
+    assert (i64(counts) == o_counts).all()
+    return lg, idx, wt, counts, o_idx
+
+
+@pytest.mark.parametrize("name", ROUTE_CASES)
+def test_route_full_size(name):
+    need_gpu()
+    _route_check(W.BY_NAME[name])
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_route_small(w, renormalize):
+    need_gpu()
+    _route_check(w, renormalize)
+
+
+def test_route_ties_and_masked():
+    need_gpu()
+    lg = torch.tensor([[1, 3, 2, 3], [0, 0, 0, 0], [-np.inf, 5, -np.inf, -np.inf]],
+                      dtype=torch.float32).cuda()
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, 2)
+    assert idx.cpu().tolist() == [[1, 3], [0, 1], [1, 0]]
+    got = wt.cpu().numpy()
+    np.testing.assert_allclose(got[:2], 0.5, atol=TOL_W)
+    assert got[2, 0] == 1.0 and got[2, 1] == 0.0
+    assert counts.cpu().tolist() == [2, 3, 0, 1]
+
+
+def test_route_nan_flags_status():
+    need_gpu()
+    lg = torch.zeros(4, 8, device="cuda")
+    lg[2, 3] = float("nan")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe_gpu.moe_route_topk(lg, 2, dev_status=st)
+    assert int(st.item()) & moe_gpu.binding.MOE_DEV_NAN_LOGIT
+
+
+def _dispatch_check(w, x, quant=False):
+    lg, idx, wt, counts, o_idx = _route_check(w)
+    out = moe_gpu.moe_permute(x, idx, counts, w.E, xp_dtype="mxfp8" if quant else None)
+    o_off, o_dest, o_src = om.permute_maps(o_idx, w.E)
+    assert (i64(out["offsets"]) == o_off).all()
+    assert (i64(out["dest_row"]) == o_dest).all()
+    assert (i64(out["src_pair"]) == o_src).all()
+    return out, (o_off, o_dest, o_src), idx, wt
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_permute_rows_bit_exact(w):
+    need_gpu()
+    x = W.make_x(w, "cuda")
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x)
+    want = x.cpu()[torch.from_numpy(o_src // w.k)]
+    assert torch.equal(out["xp"].cpu().view(torch.int16) if x.dtype == torch.bfloat16 else out["xp"].cpu(),
+                       want.view(torch.int16) if x.dtype == torch.bfloat16 else want)
+
+
+@pytest.mark.parametrize("name", ["mixtral-bf16", "qwen3-235b-bf16", "dsv3-bf16-train"])
+def test_permute_full_size(name):
+    need_gpu()
+    w = W.BY_NAME[name]
+    x = W.make_x(w, "cuda")
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x)
+    # the copied rows: every row equals its source token's row, bit for bit
+    src_tok = torch.from_numpy(o_src // w.k).cuda()
+    assert torch.equal(out["xp"].view(torch.int16), x.view(torch.int16)[src_tok])
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[3], W.WORKLOADS[3].scaled(T=512, name="dsv3-T512")],
+                         ids=lambda w: w.name)
+def test_permute_fused_mxfp8_bit_exact(w):
+    need_gpu()
+    x = W.make_x(w, "cuda").to(torch.bfloat16)
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x, quant=True)
+    xo = f64(x)[o_src // w.k]
+    codes, scales = omx.quantize_rowwise(xo)
+    assert (out["xp"].cpu().numpy() == codes).all()
+    assert (out["xp_scales"].cpu().numpy() == scales).all()
+
+
+def test_permute_fused_mxfp8_full_dsv3():
+    need_gpu()
+    w = W.BY_NAME["dsv3-mxfp8"]
+    x = W.make_x(w, "cuda")
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x, quant=True)
+    # quantisation is row-wise: check a seeded sample of 2048 rows in full
+    rows = np.random.default_rng(0).choice(w.M, 2048, replace=False)
+    xo = f64(x[torch.from_numpy(o_src[rows] // w.k).cuda()])
+    codes, scales = omx.quantize_rowwise(xo)
+    r = torch.from_numpy(rows).cuda()
+    assert (out["xp"][r].cpu().numpy() == codes).all()
+    assert (out["xp_scales"][r].cpu().numpy() == scales).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_rowwise_bit_exact(dtype):
+    need_gpu()
+    a = W.make_matrix(333, 2048, seed=5, dtype=dtype, device="cuda")
+    a[7, 64:96] = 0                                     # an all-zero block
+    a[8] *= 1e-30 if dtype == torch.float32 else 1.0   # tiny magnitudes
+    a[9, :32] = 448.0 * 2.0 ** 20                       # saturation boundary
+    a[10, 0] = -0.0
+    if dtype == torch.float32:
+        a[11, :32] = 1e-40                              # subnormal block maximum
+    codes, scales = moe_gpu.moe_quantize_mxfp8_grouped(a)
+    c, s = omx.quantize_rowwise(f64(a))
+    assert (codes.cpu().numpy() == c).all()
+    assert (scales.cpu().numpy() == s).all()
+
+
+def _combine_bound(yp64, dest, w):
+    """|fp32 sum of k products rounded once to bf16 - exact| <= 2^-8 * sum_j |w_j yp_j|."""
+    T, k = dest.shape
+    mag = np.zeros((T, yp64.shape[1]))
+    for j in range(k):
+        mag += np.abs(w[:, j:j + 1] * yp64[dest[:, j]])
+    return 2.0 ** -8 * mag + 1e-30
+
+
+@pytest.mark.parametrize("w", SMALL + [W.BY_NAME["qwen3-235b-bf16"], W.BY_NAME["dsv3-bf16-train"]],
+                         ids=lambda w: w.name)
+def test_combine(w):
+    need_gpu()
+    lg, idx, wt, counts, o_idx = _route_check(w)
+    out = moe_gpu.moe_permute(None, idx, counts, w.E, rows=False)
+    yp = W.make_matrix(w.M, w.d, seed=77, dtype=w.torch_dtype, device="cuda")
+    y = moe_gpu.moe_unpermute_combine(yp, out["dest_row"], wt)
+    o_w = om.route_topk(lg.cpu().numpy(), w.k)[1]
+    o_dest = om.permute_maps(o_idx, w.E)[1]
+    yp64 = f64(yp)
+    want = om.combine(yp64, o_dest, o_w)
+    got = f64(y)
+    assert (np.abs(got - want) <= _combine_bound(yp64, o_dest, o_w) + 1e-6 * np.abs(want)).all()
+    assert rel_l2(got, want) < 4e-3
+
+
+@pytest.mark.parametrize("k", [1, 2, 8])
+def test_combine_of_permute_identity_bit_exact(k):
+    """k=1 with unit weights, or w = 1/k: combine(permute(x)) == x exactly."""
+    need_gpu()
+    w = W.WORKLOADS[2].scaled(T=999, E=16, k=k, d=256, name=f"id-k{k}")
+    x = W.make_x(w, "cuda")
+    lg = logits_dev(w)
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, k)
+    out = moe_gpu.moe_permute(x, idx, counts, w.E)
+    ones = torch.full_like(wt, 1.0 / k)
+    y = moe_gpu.moe_unpermute_combine(out["xp"], out["dest_row"], ones)
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16))
+    if k == 1:
+        y1 = moe_gpu.moe_unpermute_combine(out["xp"], out["dest_row"], None)
+        assert torch.equal(y1.view(torch.int16), x.view(torch.int16))
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], W.BY_NAME["dsv3-bf16-train"].scaled(T=2048, name="dsv3-T2048")],
+                         ids=lambda w: w.name)
+def test_combine_bwd(w):
+    need_gpu()
+    lg, idx, wt, counts, o_idx = _route_check(w)
+    out = moe_gpu.moe_permute(None, idx, counts, w.E, rows=False)
+    yp = W.make_matrix(w.M, w.d, seed=78, dtype=w.torch_dtype, device="cuda")
+    dy = W.make_dy(w, "cuda")
+    dyp, dw = moe_gpu.moe_unpermute_combine_bwd(dy, yp, out["dest_row"], wt)
+    o_w = om.route_topk(lg.cpu().numpy(), w.k)[1]
+    o_dest = om.permute_maps(o_idx, w.E)[1]
+    want_dyp, want_dw = om.combine_bwd(f64(dy), f64(yp), o_dest, o_w)
+    assert rel_l2(f64(dyp), want_dyp) < 4e-3
+    assert rel_l2(f64(dw), want_dw) < 1e-5
+
+
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_route_bwd(renormalize):
+    need_gpu()
+    w = W.WORKLOADS[3].scaled(T=700, name="rb")
+    lg = logits_dev(w)
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, w.k, renormalize)
+    dw = W.make_matrix(w.T, w.k, seed=3, dtype=torch.float32, device="cuda")
+    dl = moe_gpu.moe_route_topk_bwd(dw, wt, idx, w.E, logits=lg, renormalize=renormalize)
+    o_idx, o_w, _ = om.route_topk(lg.cpu().numpy(), w.k, renormalize)
+    want = om.route_bwd(f64(dw), o_w, o_idx, lg.cpu().numpy(), renormalize)
+    got = f64(dl)
+    assert np.abs(got - want).max() < 1e-5
+    if renormalize:
+        sel = np.zeros_like(want, dtype=bool)
+        np.put_along_axis(sel, o_idx.astype(np.int64), True, axis=1)
+        assert (got[~sel] == 0).all()

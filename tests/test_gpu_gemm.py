@@ -1,0 +1,104 @@
+"""GPU parity of the ragged grouped GEMM (tcgen05) against the float64 oracle.
+
+Ragged groups with empty experts, single rows, exact tile multiples and tails,
+several K blocks and column tiles, partial last column tiles, TF32 and BF16,
+with and without the fused SwiGLU epilogue.  Rows beyond offsets[E] must stay
+untouched.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import ragged_grouped_gemm_topk_gb300 as moe_gpu
+from ragged_grouped_gemm_topk_gb300 import workloads as W
+from oracle import moe as om
+from _parity import TOL_BF16, f64, need_gpu, ragged_offsets, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+COUNTS = {
+    "mixed": [0, 1, 130, 257, 3, 128, 0, 64],
+    "one-expert": [700],
+    "all-in-last": [0, 0, 0, 385],
+    "singles": [1] * 37,
+}
+
+
+def _mats(M, K, N, E, dtype, seed):
+    A = W.make_matrix(M, K, seed=seed, dtype=dtype, device="cuda")
+    B = W.make_matrix(E * N, K, seed=seed + 1, dtype=dtype, device="cuda", scale=K ** -0.5).view(E, N, K)
+    return A, B
+
+
+@pytest.mark.parametrize("counts", list(COUNTS), ids=str)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "tf32"])
+@pytest.mark.parametrize("K,N", [(256, 512), (1024, 320), (96, 64)])
+def test_fwd_plain(counts, dtype, K, N):
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 5                      # 5 trailing rows outside every group
+    A, B = _mats(M, K, N, E, dtype, seed=K + N)
+    off = ragged_offsets(cnt)
+    C = torch.full((M, N), float("nan"), dtype=dtype, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(A, B, off, out=C)
+    want = om.grouped_gemm(f64(A), f64(B), off.cpu().numpy())
+    got = f64(C)
+    rows = int(sum(cnt))
+    assert np.isnan(got[rows:]).all(), "rows past offsets[E] were written"
+    err = rel_l2(got[:rows], want[:rows])
+    assert err < TOL_BF16, err
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "tf32"])
+@pytest.mark.parametrize("K,f", [(256, 256), (512, 160), (64, 32)])
+def test_fwd_swiglu(counts, dtype, K, f):
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt))
+    A, B = _mats(M, K, 2 * f, E, dtype, seed=K + f)
+    off = ragged_offsets(cnt)
+    H, GU = moe_gpu.moe_grouped_gemm_fwd(A, B, off, epi="swiglu", out_dtype=dtype, want_preact=True)
+    GU_want = om.grouped_gemm(f64(A), f64(B), off.cpu().numpy())
+    H_want = om.swiglu(GU_want)
+    assert rel_l2(f64(GU), GU_want) < TOL_BF16
+    assert rel_l2(f64(H), H_want) < TOL_BF16
+    H2 = moe_gpu.moe_grouped_gemm_fwd(A, B, off, epi="swiglu", out_dtype=dtype)
+    assert torch.equal(H2, H)
+
+
+def test_fwd_empty_rows_and_zero_M():
+    need_gpu()
+    A, B = _mats(0, 64, 64, 3, torch.bfloat16, seed=1)
+    off = ragged_offsets([0, 0, 0])
+    C = moe_gpu.moe_grouped_gemm_fwd(A, B, off)
+    assert C.shape == (0, 64)
+    # all experts empty but rows allocated: nothing is written
+    A, B = _mats(40, 64, 64, 3, torch.bfloat16, seed=2)
+    C = torch.full((40, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(A, B, off, out=C)
+    assert (C == 7.0).all()
+
+
+def test_fwd_rejects_bad_shapes():
+    need_gpu()
+    A, B = _mats(16, 48, 64, 2, torch.bfloat16, seed=3)
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_grouped_gemm_fwd(A, B, ragged_offsets([8, 8]))          # K % 32 != 0
+    A, B = _mats(16, 64, 64, 2, torch.bfloat16, seed=3)
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_grouped_gemm_fwd(A, B.float(), ragged_offsets([8, 8]))  # mixed dtypes
+
+
+def test_fwd_bad_offsets_flag_status():
+    need_gpu()
+    A, B = _mats(64, 64, 64, 2, torch.bfloat16, seed=4)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    off = torch.tensor([0, 40, 100], dtype=torch.int32, device="cuda")     # past M
+    C = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(A, B, off, out=C, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & moe_gpu.binding.MOE_DEV_BAD_INDEX

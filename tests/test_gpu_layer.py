@@ -1,0 +1,156 @@
+"""End-to-end parity of the whole layer (route -> dispatch -> grouped MLP ->
+combine) on the seeded workloads, through MoELayer (the launch sequence the
+benchmark times).
+
+The tiny workload is checked in full against the float64 oracle.  The large
+ones are checked in full for every integer output and on samples for the
+floating ones: a token's output depends only on its own row, its logits and
+its experts' weights, so the oracle evaluates sampled tokens one by one, and
+sampled rows of each grouped GEMM stage for a set of experts (hottest, median,
+smallest non-empty, and random ones).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import ragged_grouped_gemm_topk_gb300 as moe_gpu
+from ragged_grouped_gemm_topk_gb300 import workloads as W
+from oracle import moe as om
+from _parity import TOL_BF16, TOL_MXFP8, f64, i64, logits_dev, need_gpu, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def _build(w, training=False):
+    x = W.make_x(w, "cuda")
+    W1 = W.make_w1(w, "cuda")
+    W2 = W.make_w2(w, "cuda")
+    lg = logits_dev(w)
+    layer = moe_gpu.MoELayer(w.T, w.d, w.E, w.k, w.f, W1, W2, dtype=w.dtype,
+                             renormalize=w.renormalize, training=training)
+    return layer, x, W1, W2, lg
+
+
+def test_tiny_fp32_full():
+    need_gpu()
+    w = W.BY_NAME["tiny-fp32"]
+    layer, x, W1, W2, lg = _build(w)
+    y = layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    ref = om.layer_forward(f64(x), lg.cpu().numpy(), f64(W1), f64(W2), w.k)
+    assert (i64(layer.topk_idx) == ref["idx"]).all()
+    assert (i64(layer.offsets) == ref["offsets"]).all()
+    assert (i64(layer.dest_row) == ref["dest_row"]).all()
+    assert (i64(layer.src_pair) == ref["src_pair"]).all()
+    assert rel_l2(f64(layer.h), ref["H"]) < TOL_BF16
+    assert rel_l2(f64(layer.yp), ref["Yp"]) < TOL_BF16
+    assert rel_l2(f64(y), ref["y"]) < TOL_BF16
+
+
+def _sample_experts(counts, rng, n_random=2):
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    picks = {int(order[-1]), int(order[len(order) // 2]), int(order[0])}
+    picks |= {int(e) for e in rng.choice(nz, size=min(n_random, len(nz)), replace=False)}
+    return sorted(picks)
+
+
+def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=6, rows_per_expert=12, seed=0):
+    """Full integer parity + sampled float parity for a large workload."""
+    rng = np.random.default_rng(seed)
+    lg_h = lg.cpu().numpy()
+    idx, wt, counts = om.route_topk(lg_h, w.k, w.renormalize)
+    offsets, dest, src = om.permute_maps(idx, w.E)
+    assert (i64(layer.topk_idx) == idx).all()
+    assert np.abs(f64(layer.topk_w) - wt).max() <= 1e-6
+    assert (i64(layer.counts) == counts).all()
+    assert (i64(layer.offsets) == offsets).all()
+    assert (i64(layer.dest_row) == dest).all()
+    assert (i64(layer.src_pair) == src).all()
+    mx = w.dtype == "mxfp8"
+    tol = TOL_MXFP8 if mx else TOL_BF16
+    cache = {}
+
+    def get(e, which):
+        if (e, which) not in cache:
+            cache[(e, which)] = f64((W1 if which == 1 else W2)[e])
+        return cache[(e, which)]
+
+    # per-stage: sampled rows of GEMM1 (+SwiGLU) and GEMM2 for chosen experts
+    h_got, h_want, y_got, y_want = [], [], [], []
+    for e in _sample_experts(counts, rng):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        rows = np.sort(rng.choice(np.arange(lo, hi), size=min(rows_per_expert, hi - lo), replace=False))
+        xr = f64(x[torch.from_numpy(src[rows] // w.k).cuda()])
+        w1, w2 = get(e, 1), get(e, 2)
+        if mx:
+            xr, w1, w2 = om.mx_roundtrip(xr), om.mx_roundtrip(w1), om.mx_roundtrip(w2)
+        h = om.swiglu(xr @ w1.T)
+        yp = (om.mx_roundtrip(h) if mx else h) @ w2.T
+        r = torch.from_numpy(rows).cuda()
+        h_got.append(f64(layer.h[r]))
+        h_want.append(h)
+        y_got.append(f64(layer.yp[r]))
+        y_want.append(yp)
+    assert rel_l2(np.concatenate(h_got), np.concatenate(h_want)) < tol
+    assert rel_l2(np.concatenate(y_got), np.concatenate(y_want)) < tol
+
+    # sampled tokens end to end
+    toks = np.sort(rng.choice(w.T, size=n_tokens, replace=False))
+    got = f64(layer.y[torch.from_numpy(toks).cuda()])
+    want = np.stack([om.token_forward(f64(x[t]), lg_h[t], lambda e: get(e, 1), lambda e: get(e, 2),
+                                      w.k, w.renormalize, mxfp8_operands=mx) for t in toks])
+    assert rel_l2(got, want) < tol
+
+
+@pytest.mark.parametrize("name", ["mixtral-bf16", "qwen3-235b-bf16"])
+def test_large_forward(name):
+    need_gpu()
+    w = W.BY_NAME[name]
+    layer, x, W1, W2, lg = _build(w)
+    layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    check_large_forward(w, layer, x, W1, W2, lg)
+
+
+@pytest.mark.parametrize("w", [W.BY_NAME["qwen3-235b-bf16"].scaled(T=640, d=512, f=384, name="qwen-small"),
+                               W.BY_NAME["dsv3-bf16-train"].scaled(T=256, d=256, f=128, name="dsv3-small"),
+                               W.BY_NAME["mixtral-bf16"].scaled(T=300, d=128, f=448, name="mixtral-small")],
+                         ids=lambda w: w.name)
+def test_scaled_forward_full(w):
+    """Reduced shapes checked in full (every output element)."""
+    need_gpu()
+    layer, x, W1, W2, lg = _build(w)
+    y = layer.forward(x, lg)
+    torch.cuda.synchronize()
+    ref = om.layer_forward(f64(x), lg.cpu().numpy(), f64(W1), f64(W2), w.k)
+    assert (i64(layer.src_pair) == ref["src_pair"]).all()
+    assert rel_l2(f64(layer.h), ref["H"]) < TOL_BF16
+    assert rel_l2(f64(layer.yp), ref["Yp"]) < TOL_BF16
+    assert rel_l2(f64(y), ref["y"]) < TOL_BF16
+
+
+def test_graph_replay_with_new_logits():
+    """Capture the forward once; replaying with new logits changes the counts on
+    the device only, and every replay still matches the oracle."""
+    need_gpu()
+    w = W.BY_NAME["qwen3-235b-bf16"].scaled(T=512, d=256, f=256, name="graph")
+    layer, x, W1, W2, lg = _build(w)
+    lg_buf = lg.clone()
+    layer.forward(x, lg_buf)                 # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, lg_buf)
+    for s in range(3):
+        new = torch.from_numpy(np.random.default_rng(100 + s).standard_normal((w.T, w.E)).astype(np.float32) * (1 + s))
+        lg_buf.copy_(new)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = om.layer_forward(f64(x), new.numpy(), f64(W1), f64(W2), w.k)
+        assert (i64(layer.counts) == ref["counts"]).all()
+        assert (i64(layer.src_pair) == ref["src_pair"]).all()
+        assert rel_l2(f64(layer.y), ref["y"]) < TOL_BF16
