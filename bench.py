@@ -1,0 +1,411 @@
+"""Benchmark of the dropless-MoE layer hot path on GB300.
+
+One step = one pass of the whole layer (route -> dispatch -> grouped GEMM1 +
+SwiGLU -> [MXFP8 quantise] -> grouped GEMM2 -> combine, plus the backward for
+training workloads) over one batch of seeded synthetic input already resident
+in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs one independent replica per GPU (torchrun, one rank per GPU): the
+layer has no exchange step on one GPU, so ranks share nothing but a barrier and
+the max-over-ranks time; ``value`` is the units all ranks processed / that time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer grouped-GEMM TFLOPS & permute/combine GB/s on 1 GB300 vs roofline"
+DEFAULT_WORKLOAD = "mixtral-bf16"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--T", type=int, default=None, help="override tokens (small profiling cases)")
+    ap.add_argument("--f", type=int, default=None, help="override expert hidden dim (profiling)")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.p = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.close()
+        rows = [r.split(", ") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip() == "Active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def stage_bytes(w):
+    """Algorithmic bytes of the bandwidth stages (each moved once)."""
+    s = 4 if w.dtype == "f32" else 2
+    xp_s = 1 if w.dtype == "mxfp8" else s
+    permute = w.T * w.d * s + w.M * w.d * xp_s + (w.M * w.d // 32 if w.dtype == "mxfp8" else 0) \
+        + w.T * w.k * 4 * 3 + w.M * 4
+    combine = w.M * w.d * s + w.T * w.d * s + w.T * w.k * 8
+    return permute, combine
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import ragged_grouped_gemm_topk_gb300 as pkg
+    from ragged_grouped_gemm_topk_gb300 import build as pbuild
+    from ragged_grouped_gemm_topk_gb300 import workloads as W
+
+    pbuild.build()
+    w = W.BY_NAME[args.workload]
+    if args.T or args.f:
+        w = w.scaled(T=args.T, f=args.f, name=f"{w.name}-T{args.T or w.T}-f{args.f or w.f}")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = W.make_x(w, dev)
+    W1, W2 = W.make_w1(w, dev), W.make_w2(w, dev)
+    lg_h = W.make_logits(w)
+    lg = torch.from_numpy(lg_h).to(dev)
+    dy = W.make_dy(w, dev) if w.backward else None
+    layer = pkg.MoELayer(w.T, w.d, w.E, w.k, w.f, W1, W2, dtype=w.dtype, renormalize=w.renormalize,
+                         training=w.backward)
+    stream = torch.cuda.current_stream()
+
+    stages = ["route", "dispatch", "mlp", "combine"] + (["backward"] if w.backward else [])
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        layer.route(lg)
+        mark(1)
+        layer.dispatch(x)
+        mark(2)
+        if ev is not None and w.dtype != "mxfp8":
+            # time GEMM1 alone inside the MLP stage (the dominant kernel)
+            pkg.moe_grouped_gemm_fwd(layer.xp, layer.W1, layer.offsets, epi="swiglu", out=layer.h,
+                                     preact=layer.gu, dev_status=layer.dev_status)
+            mark(3)
+            pkg.moe_grouped_gemm_fwd(layer.h, layer.W2, layer.offsets, out=layer.yp,
+                                     dev_status=layer.dev_status)
+        elif ev is not None:
+            pkg.moe_grouped_gemm_fwd(layer.xq, layer.W1q, layer.offsets, epi="swiglu", A_scales=layer.xs,
+                                     B_scales=layer.W1s, out=layer.h, dev_status=layer.dev_status)
+            mark(3)
+            pkg.moe_quantize_mxfp8_grouped(layer.h, codes=layer.hq, scales=layer.hs)
+            pkg.moe_grouped_gemm_fwd(layer.hq, layer.W2q, layer.offsets, A_scales=layer.hs,
+                                     B_scales=layer.W2s, out=layer.yp, dev_status=layer.dev_status)
+        else:
+            layer.expert_mlp()
+        mark(4)
+        layer.combine()
+        mark(5)
+        if w.backward:
+            layer.backward(dy, lg)
+            mark(6)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n_ev = 7 if w.backward else 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    clk = clocks.stop()
+    if int(layer.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.dev_status.item())}")
+    per = {k: 0.0 for k in ("route", "dispatch", "gemm1", "gemm2", "combine", "backward", "step")}
+    for e in evs:
+        per["route"] += e[0].elapsed_time(e[1])
+        per["dispatch"] += e[1].elapsed_time(e[2])
+        per["gemm1"] += e[2].elapsed_time(e[3])
+        per["gemm2"] += e[3].elapsed_time(e[4])
+        per["combine"] += e[4].elapsed_time(e[5])
+        if w.backward:
+            per["backward"] += e[5].elapsed_time(e[6])
+        per["step"] += e[0].elapsed_time(e[-1])
+    per = {k: v / args.steps for k, v in per.items()}           # ms per step
+    ms = max_over_ranks(per["step"], world)
+    flops = w.fwd_flops * (3 if w.backward else 1)
+    value = world * flops / (ms * 1e-3) / 1e12
+    pk = peaks()
+    g1_flops = 4.0 * w.M * w.d * w.f
+    g1_tflops = g1_flops / (per["gemm1"] * 1e-3) / 1e12
+    dtype_peak = pk["bf16_sus"] * (2.0 if w.dtype == "mxfp8" else (0.5 if w.dtype == "f32" else 1.0))
+    perm_b, comb_b = stage_bytes(w)
+    launches = layer.launches_per_forward() + (layer.launches_per_backward() if w.backward else 0)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"gemm1_traffic_{w.name}.json")
+    if os.path.exists(prof):
+        traffic = json.load(open(prof)).get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"f32": "tf32", "bf16": "bf16", "mxfp8": "mxfp8-e4m3"}[w.dtype],
+        "data": "synthetic (seeded; no dataset or trained weights)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f,
+                   "M_rows": w.M, "backward": w.backward,
+                   "l2": f"inputs larger than L2: {(W1.numel() + W2.numel()) * W1.element_size() / 1e9:.2f} GB of expert weights streamed per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "stages_ms": {k: round(v, 4) for k, v in per.items()},
+        "permute_gbs": round(perm_b / (per["dispatch"] * 1e-3) / 1e9, 1),
+        "combine_gbs": round(comb_b / (per["combine"] * 1e-3) / 1e9, 1),
+        "roofline": {"kernel": "grouped GEMM1 (gate+up, fused SwiGLU)", "bound": "tensor",
+                     "achieved": round(g1_tflops, 1), "peak": round(dtype_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(g1_tflops / dtype_peak, 4),
+                     "peak_source": f"{pk['source']} bf16 sustained" + (" x2 (fp8 nominal ratio)" if w.dtype == "mxfp8" else "")
+                     + (" x0.5 (tf32 nominal ratio)" if w.dtype == "f32" else ""),
+                     "traffic": traffic,
+                     "hbm_frac_permute": round(perm_b / (per["dispatch"] * 1e-3) / 1e9 / pk["hbm"], 4),
+                     "hbm_frac_combine": round(comb_b / (per["combine"] * 1e-3) / 1e9 / pk["hbm"], 4)},
+        "clocks": clk,
+        "gpu_launches": launches * args.steps,
+        "wall_s_timed": round(wall, 3),
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, w, layer, x, lg_h, dy, world, flops)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
+    return line
+
+
+def e2e(args, w, layer, x, lg_h, dy, world, flops):
+    """Same metric through the public API with host buffers: every step copies
+    that step's inputs from pinned host memory and reads the result back."""
+    import torch
+    xh = x.cpu().pin_memory()
+    lgh = torch.from_numpy(lg_h).pin_memory()
+    yh = torch.empty(w.T, w.d, dtype=x.dtype).pin_memory()
+    dyh = dy.cpu().pin_memory() if dy is not None else None
+    xd, lgd = torch.empty_like(x), torch.empty(lgh.shape, dtype=torch.float32, device=x.device)
+    dyd = torch.empty_like(dy) if dy is not None else None
+    dxh = torch.empty(w.T, w.d, dtype=x.dtype).pin_memory() if dy is not None else None
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        lgd.copy_(lgh, non_blocking=True)
+        y = layer.forward(xd, lgd)
+        yh.copy_(y, non_blocking=True)
+        if dy is not None:
+            dyd.copy_(dyh, non_blocking=True)
+            dx, _, _, _ = layer.backward(dyd, lgd)
+            dxh.copy_(dx, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
+    h2d = xh.numel() * xh.element_size() + lgh.numel() * 4 + (dyh.numel() * dyh.element_size() if dyh is not None else 0)
+    d2h = yh.numel() * yh.element_size() + (dxh.numel() * dxh.element_size() if dxh is not None else 0)
+    return {"value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_sample(w, n_tokens):
+    """Inputs for the oracle on a bounded sample: the first n_tokens tokens of the
+    workload (their activations and logits).  Only the experts those tokens route
+    to are kept (their logit columns and weights): the top-k of every sampled
+    token lies inside that set, so routing, weights and outputs are those of the
+    full layer.  For timing, every kept expert carries the same seeded weight
+    values (a broadcast view, so the host holds one expert's weights)."""
+    import numpy as np
+    import torch
+    from ragged_grouped_gemm_topk_gb300 import workloads as W
+    from oracle import moe as om
+    lg = W.make_logits(w)[:n_tokens]
+    g = torch.Generator().manual_seed(1000 * w.seed + 1)
+    x = torch.randn(n_tokens, w.d, generator=g).to(w.torch_dtype).double().numpy()
+    idx, _, _ = om.route_topk(lg, w.k, w.renormalize)
+    used = np.unique(idx)
+    gw = torch.Generator().manual_seed(1000 * w.seed + 2)
+    w1 = (torch.randn(2 * w.f, w.d, generator=gw) / w.d ** 0.5).to(w.torch_dtype).double().numpy()
+    w2 = (torch.randn(w.d, w.f, generator=gw) / w.f ** 0.5).to(w.torch_dtype).double().numpy()
+    W1 = np.broadcast_to(w1, (len(used),) + w1.shape)
+    W2 = np.broadcast_to(w2, (len(used),) + w2.shape)
+    return x, np.ascontiguousarray(lg[:, used]), W1, W2
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """Time the float64 oracle, as it stands, on a bounded token sample on the
+    host cores; report TFLOPS of the algorithmic layer FLOPs it covered."""
+    from oracle import moe as om
+    cores = len(os.sched_getaffinity(0))
+    n = 2
+    per_tok = None
+    while True:
+        x, lg, W1, W2 = oracle_sample(w, n)
+        t0 = time.perf_counter()
+        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8")
+        if w.backward:
+            dy = x * 0 + 1.0
+            om.layer_backward(fwd, dy, x, lg, W1, W2, w.k, w.renormalize)
+        dt = time.perf_counter() - t0
+        per_tok = dt / n
+        if dt > budget_s / 3 or n >= w.T:
+            break
+        n = min(w.T, max(n * 2, int(n * budget_s / 2 / max(dt, 1e-3))))
+    flops = w.fwd_flops * (3 if w.backward else 1) * n / w.T
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} with the experts they route to "
+                      f"(float64 numpy oracle), {dt:.1f} s",
+            "s_per_token": per_tok}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the float64 CPU oracle on the same workload, each step a
+    bounded token sample, timed on the host cores (rank 0 only)."""
+    from ragged_grouped_gemm_topk_gb300 import workloads as W
+    from oracle import moe as om
+    w = W.BY_NAME[args.workload]
+    if rank != 0:
+        return None
+    n = 16 if w.dtype != "mxfp8" else 4
+    x, lg, W1, W2 = oracle_sample(w, n)
+    mx = w.dtype == "mxfp8"
+    for _ in range(args.warmup):
+        om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
+        if w.backward:
+            om.layer_backward(fwd, x * 0 + 1.0, x, lg, W1, W2, w.k, w.renormalize)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = w.fwd_flops * (3 if w.backward else 1) * n / w.T
+    value = flops / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} of {w.T} tokens per step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

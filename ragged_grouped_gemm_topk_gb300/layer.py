@@ -109,6 +109,15 @@ class MoELayer:
         self.combine()
         return self.y
 
+    def launches_per_forward(self) -> int:
+        """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
+        scan, scatter), GEMM1, [MXFP8 quantise of H], GEMM2, combine."""
+        return 2 + 3 + 2 + (1 if self.dtype == "mxfp8" else 0) + 1
+
+    def launches_per_backward(self) -> int:
+        """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd."""
+        return 7
+
     # ------------------------------------------------------------------ backward
     def backward(self, dy, logits=None):
         """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward)."""

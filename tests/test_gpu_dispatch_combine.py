@@ -107,7 +107,8 @@ def test_permute_full_size(name):
     assert torch.equal(out["xp"].view(torch.int16), x.view(torch.int16)[src_tok])
 
 
-@pytest.mark.parametrize("w", [SMALL[1], SMALL[3], W.WORKLOADS[3].scaled(T=512, name="dsv3-T512")],
+@pytest.mark.parametrize("w", [SMALL[1].scaled(d=64, name="ragged-T257-d64"), SMALL[3],
+                               W.WORKLOADS[3].scaled(T=512, name="dsv3-T512")],
                          ids=lambda w: w.name)
 def test_permute_fused_mxfp8_bit_exact(w):
     need_gpu()
@@ -117,6 +118,16 @@ def test_permute_fused_mxfp8_bit_exact(w):
     codes, scales = omx.quantize_rowwise(xo)
     assert (out["xp"].cpu().numpy() == codes).all()
     assert (out["xp_scales"].cpu().numpy() == scales).all()
+
+
+def test_permute_mxfp8_rejects_width_not_multiple_of_32():
+    need_gpu()
+    w = SMALL[1]                                     # d = 40
+    x = W.make_x(w, "cuda").to(torch.bfloat16)
+    lg = logits_dev(w)
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, w.k)
+    with pytest.raises(moe_gpu.binding.MoeError, match="d % 32"):
+        moe_gpu.moe_permute(x, idx, counts, w.E, xp_dtype="mxfp8")
 
 
 def test_permute_fused_mxfp8_full_dsv3():
