@@ -1,24 +1,36 @@
-// Ragged grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// Ragged grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA):
+// forward, data gradient and weight gradient.
 //
 // "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer Engine",
 // "Optimisation 1: grouped GEMM": one launch covers every expert's matmul, each
 // computed at its own (data-dependent) token count, with no device-to-host copy
 // of the counts and no padding to a worst-case capacity.
 //
-// Design (one persistent CTA per SM, 6 warps):
-//   warp 0     TMA producer: streams K-blocks of the A rows and B rows of the
-//              current tile into a 4-stage shared-memory ring (128-byte swizzle).
-//   warp 1     allocates TMEM; one lane issues tcgen05.mma (M=128, N=256) into a
-//              double-buffered fp32 accumulator in TMEM and commits each stage
-//              back to the producer and each finished tile to the epilogue.
-//   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one row per
-//              thread), apply the fused epilogue and store rows with 16-byte
-//              stores, masked at the expert's last row.
-// Tiles are enumerated on the device from `offsets`: expert e has
-// ceil(count_e / 128) row tiles times the column tiles; row tiles vary fastest
-// so neighbouring CTAs share the same weight slice in L2.  Rows past an expert's
-// end inside its last tile belong to the next expert (or lie past M and are
-// zero-filled by TMA): they are computed but never stored.
+// One persistent CTA per SM, 6 warps:
+//   warp 0     TMA producer: streams the A and B slices of the current tile into a
+//              4-stage shared-memory ring (48 KB per stage, 128-byte swizzle).
+//   warp 1     allocates TMEM; one lane issues tcgen05.mma (M=128, N=256, K=16 per
+//              instruction) into a double-buffered fp32 accumulator in TMEM and
+//              commits each stage back to the producer and each tile to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (TMEM lane = tile row, one
+//              row per thread), the fused epilogue, 16-byte stores masked at the
+//              group's last row and the matrix edge.
+// Tiles are enumerated on the device from `offsets`, so the host never learns the
+// per-expert sizes:
+//   forward / dgrad  expert e owns ceil(count_e / 128) row tiles x the column
+//                    tiles; row tiles vary fastest so neighbouring CTAs share a
+//                    weight slice in L2.  Rows of the last row tile past the
+//                    group's end are computed but never stored.
+//   wgrad            every expert owns ceil(N/128) x ceil(K/256) tiles of dB[e];
+//                    the contraction runs over the group's own rows in 64-row
+//                    blocks; rows of the last block past the group's end are
+//                    zeroed in shared memory (and whole 16-row MMA steps beyond it
+//                    skipped), and an empty group writes exact zeros.
+// Operand majors: forward A and B, and dgrad A, are K-major; dgrad B (the weight
+// read along its output dim) and both wgrad operands are MN-major.  MN-major
+// tiles arrive as 64-column x 64-row TMA boxes (128 B rows, 128-byte swizzle);
+// their descriptors step 8 KB between 64-column chunks (leading byte offset) and
+// 1 KB between 8-row groups (stride byte offset).
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -28,23 +40,30 @@ namespace moe {
 namespace gemm {
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;              // MMA N (SwiGLU: 128 gate + 128 up rows)
-constexpr int kBKBytes = 128;         // one 128-byte swizzle atom of K per stage
+constexpr int kBN = 256;                          // MMA N
+constexpr int kBKBytes = 128;                     // K-major: one swizzle atom of K per stage
+constexpr int kMnRows = 64;                       // MN-major: contraction rows per stage
 constexpr int kStages = 4;
 constexpr int kAStage = kBM * kBKBytes;           // 16 KB
 constexpr int kBStage = kBN * kBKBytes;           // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;    // 48 KB
+constexpr int kBox = 8192;                        // one 64 x 64 bf16 MN-major box
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * kBN;                // double-buffered accumulator
 constexpr int kMaxE = 1024;
 
-// Instruction descriptor (kind::f16 / kind::tf32): D=f32, A/B format, K-major
-// operands, N >> 3 at bit 17, M >> 4 at bit 24.
+enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
+enum { kEpiNone = 0, kEpiSwiglu = 1, kEpiDswiglu = 2 };
+
+// Instruction descriptor (kind::f16 / kind::tf32): D = f32 (bit 4), A/B format
+// (bits 7-9 / 10-12: 1 = bf16, 2 = tf32), A/B major (bits 15 / 16: 1 = MN-major),
+// N >> 3 at bit 17, M >> 4 at bit 24.
 template <int kKind>
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn, int b_mn) {
   return (1u << 4) | (static_cast<uint32_t>(kKind == 0 ? 2 : 1) << 7) |
-         (static_cast<uint32_t>(kKind == 0 ? 2 : 1) << 10) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+         (static_cast<uint32_t>(kKind == 0 ? 2 : 1) << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 struct Smem {
@@ -62,60 +81,113 @@ struct Smem {
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Smem);
 
-struct TileInfo {
-  int e;      // expert
-  int row0;   // first row of the tile (global row index)
-  int rows;   // valid rows in the tile (<= 128)
-  int n0;     // first output column (or first B row)
+struct Params {
+  const int32_t* offsets;
+  int M, N, K, E;
+  void* out;               // C / dA / dB
+  void* preact_out;        // forward SwiGLU: G|U store (may be null)
+  const void* preact_in;   // dgrad dSwiGLU: G|U input
+  int32_t* status;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const Smem& s, int tile, int E, int nt) {
+struct Tile {
+  int e;
+  int row0;    // fwd/dgrad: first row; wgrad: first row of the group
+  int rows;    // fwd/dgrad: valid rows (<= 128); wgrad: rows of the group
+  int col0;    // first output column (fwd/dgrad) / first dB column (wgrad)
+  int n0;      // wgrad: first dB row
+  int kblocks; // contraction blocks
+};
+
+__device__ __forceinline__ bool group_ok(int beg, int end, int M) { return beg >= 0 && end >= beg && end <= M; }
+
+template <int kMode, int kEpi>
+struct Geo {
+  int nt;       // column tiles per row tile (fwd/dgrad); dB row tiles (wgrad)
+  int nt2;      // wgrad: dB column tiles
+  int n_out;    // output columns (fwd/dgrad)
+  int bn_out;   // output columns per tile
+  int kb_fixed; // contraction blocks (fwd/dgrad)
+  __device__ Geo(const Params& p, int elem_bytes) {
+    if (kMode == kWgrad) {
+      nt = (p.N + kBM - 1) / kBM;
+      nt2 = (p.K + kBN - 1) / kBN;
+      n_out = p.K;
+      bn_out = kBN;
+      kb_fixed = 0;
+    } else {
+      n_out = kMode == kFwd ? (kEpi == kEpiSwiglu ? p.N / 2 : p.N) : p.K;
+      bn_out = kEpi == kEpiSwiglu ? kBN / 2 : kBN;
+      nt = (n_out + bn_out - 1) / bn_out;
+      nt2 = 1;
+      kb_fixed = kMode == kFwd ? (p.K * elem_bytes + kBKBytes - 1) / kBKBytes
+                               : (p.N + kMnRows - 1) / kMnRows;
+    }
+  }
+  __device__ int tiles_of(int cnt) const {
+    if (kMode == kWgrad) return nt * nt2;
+    return ((cnt + kBM - 1) / kBM) * nt;
+  }
+};
+
+template <int kMode, int kEpi>
+__device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>& g, int tile, int E, int M) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (s.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
   }
-  const int e = lo;
-  const int local = tile - s.prefix[e];
-  const int cnt = s.offs[e + 1] - s.offs[e];
-  const int mt = (cnt + kBM - 1) / kBM;
-  const int m_tile = local % mt;
-  const int n_tile = local / mt;
-  TileInfo t;
-  t.e = e;
-  t.row0 = s.offs[e] + m_tile * kBM;
-  const int left = s.offs[e + 1] - t.row0;
-  t.rows = left < kBM ? left : kBM;
-  t.n0 = n_tile;  // scaled by the caller
+  Tile t;
+  t.e = lo;
+  const int local = tile - s.prefix[lo];
+  const int beg = s.offs[lo];
+  const int cnt = group_ok(beg, s.offs[lo + 1], M) ? s.offs[lo + 1] - beg : 0;
+  if (kMode == kWgrad) {
+    t.n0 = (local % g.nt) * kBM;
+    t.col0 = (local / g.nt) * kBN;
+    t.row0 = cnt > 0 ? beg : 0;
+    t.rows = cnt;
+    t.kblocks = (cnt + kMnRows - 1) / kMnRows;
+  } else {
+    const int mt = (cnt + kBM - 1) / kBM;   // >= 1: only non-empty groups own tiles
+    t.row0 = beg + (local % mt) * kBM;
+    const int left = beg + cnt - t.row0;
+    t.rows = left < kBM ? left : kBM;
+    t.col0 = (local / mt) * g.bn_out;
+    t.n0 = 0;
+    t.kblocks = g.kb_fixed;
+  }
   return t;
 }
 
-// Build the per-expert tile prefix in shared memory (all threads participate).
-__device__ void build_tiles(Smem& s, const int32_t* offsets, int E, int M, int nt, int32_t* status) {
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) s.offs[e] = offsets[e];
+// Per-expert tile prefix in shared memory (all threads participate).  A group
+// whose offsets are out of range is flagged and treated as empty.
+template <int kMode, int kEpi>
+__device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p) {
+  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s.offs[e] = p.offsets[e];
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     int cnt = s.offs[e + 1] - s.offs[e];
-    if (cnt < 0 || s.offs[e + 1] > M || s.offs[e] < 0) {
-      flag_error(status, MOE_DEV_BAD_INDEX);
+    if (!group_ok(s.offs[e], s.offs[e + 1], p.M)) {
+      if (blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
       cnt = 0;
     }
-    s.prefix[e + 1] = ((cnt + kBM - 1) / kBM) * nt;
+    s.prefix[e + 1] = g.tiles_of(cnt);
   }
   if (threadIdx.x == 0) s.prefix[0] = 0;
   __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int carry = 0;
-    for (int base = 1; base <= E; base += 32) {
+    for (int base = 1; base <= p.E; base += 32) {
       const int i = base + lane;
-      int v = i <= E ? s.prefix[i] : 0;
+      int v = i <= p.E ? s.prefix[i] : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int u = __shfl_up_sync(0xFFFFFFFFu, v, off);
         if (lane >= off) v += u;
       }
-      if (i <= E) s.prefix[i] = v + carry;
+      if (i <= p.E) s.prefix[i] = v + carry;
       carry += __shfl_sync(0xFFFFFFFFu, v, 31);
     }
     if (lane == 0) s.total_tiles = carry;
@@ -124,6 +196,7 @@ __device__ void build_tiles(Smem& s, const int32_t* offsets, int E, int M, int n
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g * __frcp_rn(1.f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return __frcp_rn(1.f + __expf(-g)); }
 
 // Store 32 consecutive fp32 values as OutT (16-byte stores).
 template <typename OutT>
@@ -141,22 +214,40 @@ __device__ __forceinline__ void store32(OutT* dst, const float (&v)[32]) {
   }
 }
 
-// kKind: 0 = tf32 (fp32 storage), 1 = bf16.  kSwiglu: fused SwiGLU epilogue.
-template <int kKind, bool kSwiglu, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fwd_kernel(
-    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-    const int32_t* __restrict__ offsets, int M, int N, int K, int E, OutT* __restrict__ C,
-    OutT* __restrict__ preact, int32_t* status) {
+// Load 32 consecutive values (bf16 or fp32) as fp32.
+template <typename T>
+__device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 u = s4[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = bf16_to_f32(static_cast<uint16_t>(w[i] & 0xFFFFu));
+        v[8 * q + 2 * i + 1] = bf16_to_f32(static_cast<uint16_t>(w[i] >> 16));
+      }
+    }
+  } else {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 u = s4[q];
+      v[4 * q] = u.x; v[4 * q + 1] = u.y; v[4 * q + 2] = u.z; v[4 * q + 3] = u.w;
+    }
+  }
+}
+
+template <int kKind, int kMode, int kEpi, typename OutT>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Smem& s = *reinterpret_cast<Smem*>(tiles + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const int n_out = kSwiglu ? N / 2 : N;                 // output columns
-  const int bn_out = kSwiglu ? kBN / 2 : kBN;            // output columns per tile
-  const int nt = (n_out + bn_out - 1) / bn_out;
-  const int kb_count = (K * (kKind == 0 ? 4 : 2) + kBKBytes - 1) / kBKBytes;
-  const int bk_elems = kBKBytes / (kKind == 0 ? 4 : 2);
+  constexpr int eb = kKind == 0 ? 4 : 2;
+  const Geo<kMode, kEpi> g(p, eb);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -179,116 +270,201 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fwd_kernel(
     tmem_relinquish();
     tc_fence_before();
   }
-  build_tiles(s, offsets, E, M, nt, status);   // contains __syncthreads
+  build_tiles(s, g, p);   // contains __syncthreads
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int total = s.total_tiles;
 
   if (warp == 0) {
+    // ------------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-        const TileInfo ti = tile_info(s, tile, E, nt);
-        const int n0 = ti.n0 * bn_out;
-        for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait(&s.empty[stage], phase ^ 1u, status, &s.abort)) break;
+        const Tile t = tile_info(s, g, tile, p.E, p.M);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.status, &s.abort)) break;
           uint8_t* sa = tiles + stage * kStageBytes;
           uint8_t* sb = sa + kAStage;
-          mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-          const int kx = kb * bk_elems;
-          tma_load_2d(sa, &tmA, &s.full[stage], kx, ti.row0);
-          if (kSwiglu) {
-            tma_load_3d(sb, &tmB, &s.full[stage], kx, n0, ti.e);
-            tma_load_3d(sb + kBStage / 2, &tmB, &s.full[stage], kx, n_out + n0, ti.e);
+          uint64_t* bar = &s.full[stage];
+          mbar_arrive_expect_tx(bar, kStageBytes);
+          if (kMode == kFwd) {
+            const int kx = kb * (kBKBytes / eb);
+            tma_load_2d(sa, &tmA, bar, kx, t.row0);
+            if (kEpi == kEpiSwiglu) {
+              tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
+              tma_load_3d(sb + kBStage / 2, &tmB, bar, kx, g.n_out + t.col0, t.e);
+            } else {
+              tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
+            }
+          } else if (kMode == kDgrad) {
+            const int nx = kb * kMnRows;                  // contraction index (N of B)
+            tma_load_2d(sa, &tmA, bar, nx, t.row0);
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j) tma_load_3d(sb + j * kBox, &tmB, bar, t.col0 + 64 * j, nx, t.e);
           } else {
-            tma_load_3d(sb, &tmB, &s.full[stage], kx, n0, ti.e);
+            const int r = t.row0 + kb * kMnRows;          // contraction index (rows of the group)
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBox, &tmA, bar, t.n0 + 64 * j, r);
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kBox, &tmB, bar, t.col0 + 64 * j, r);
           }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc<kKind>(kBM, kBN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-        if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, status, &s.abort)) break;
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.status, &s.abort)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < kb_count; ++kb) {
-          if (!mbar_wait(&s.full[stage], phase, status, &s.abort)) break;
-          tc_fence_after();
-          const uint32_t sa = smem_u32(tiles + stage * kStageBytes);
-          const uint32_t sb = sa + kAStage;
-#pragma unroll
-          for (int kk = 0; kk < kBKBytes / 32; ++kk) {
-            const uint64_t ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
-            const uint64_t bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
+        uint8_t* sa_ptr = tiles + stage * kStageBytes;
+        const uint32_t sa = smem_u32(sa_ptr);
+        const uint32_t sb = sa + kAStage;
+        int steps = 4;
+        if (kMode == kWgrad) {
+          // Last block of the group: zero rows [valid, 16*steps) of the A operand
+          // (dC^T) so the next group's rows contribute nothing, and skip 16-row
+          // MMA steps that lie wholly past the group.
+          const int valid = t.rows - kb * kMnRows;
+          if (valid < kMnRows) {
+            steps = (valid + 15) / 16;
+            const int zrows = steps * 16 - valid;
+            for (int i = lane; i < zrows * 8 * (kBM / 64); i += 32) {
+              const int box = i / (zrows * 8), rem = i % (zrows * 8);
+              const int row = valid + rem / 8, chunk = rem % 8;
+              *reinterpret_cast<uint4*>(sa_ptr + box * kBox + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          for (int kk = 0; kk < steps; ++kk) {
+            uint64_t ad, bd;
+            if (kMode == kWgrad) ad = make_sdesc(sa + kk * 2048, kBox, 1024, 2);
+            else ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
+            if (kMode == kFwd) bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
+            else bd = make_sdesc(sb + kk * 2048, kBox, 1024, 2);
             tc_mma<kKind>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&s.empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        tc_commit(&s.tfull[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
+      if (lane == 0) tc_commit(&s.tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   } else {
-    // Epilogue warps 2..5 -> TMEM lane quarter (warp % 4).
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;            // tile row owned by this thread
+    OutT* out = static_cast<OutT*>(p.out);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-      const TileInfo ti = tile_info(s, tile, E, nt);
-      const int n0 = ti.n0 * bn_out;
-      if (!mbar_wait(&s.tfull[acc], acc_phase, status, &s.abort)) break;
+      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      const bool valid = r < ti.rows;
-      const size_t grow = static_cast<size_t>(ti.row0 + r);
-      if constexpr (kSwiglu) {
+      if (kMode == kWgrad) {
+        const bool valid = t.n0 + r < p.N;
+        OutT* dst = out + (static_cast<size_t>(t.e) * p.N + t.n0 + r) * p.K;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          float f[32];
+          if (t.rows > 0) {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = 0.f;
+          }
+          const int col = t.col0 + c * 32;
+          if (valid && col < p.K) store32<OutT>(dst + col, f);
+        }
+      } else if (kEpi == kEpiSwiglu) {
+        const bool valid = r < t.rows;
+        const size_t grow = static_cast<size_t>(t.row0 + r);
+        OutT* pre = static_cast<OutT*>(p.preact_out);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld32(tb + c * 32, g);
-          tmem_ld32(tb + 128 + c * 32, u);
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tb + c * 32, gv);
+          tmem_ld32(tb + 128 + c * 32, uv);
           tmem_ld_wait();
-          const int col = n0 + c * 32;
-          if (valid && col < n_out) {
+          const int col = t.col0 + c * 32;
+          if (valid && col < g.n_out) {
             float h[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gv = __uint_as_float(g[i]);
-              h[i] = silu_f(gv) * __uint_as_float(u[i]);
-            }
-            store32<OutT>(C + grow * n_out + col, h);
-            if (preact != nullptr) {
+            for (int i = 0; i < 32; ++i) h[i] = silu_f(__uint_as_float(gv[i])) * __uint_as_float(uv[i]);
+            store32<OutT>(out + grow * g.n_out + col, h);
+            if (pre != nullptr) {
               float gf[32], uf[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                gf[i] = __uint_as_float(g[i]);
-                uf[i] = __uint_as_float(u[i]);
+                gf[i] = __uint_as_float(gv[i]);
+                uf[i] = __uint_as_float(uv[i]);
               }
-              store32<OutT>(preact + grow * N + col, gf);
-              store32<OutT>(preact + grow * N + n_out + col, uf);
+              store32<OutT>(pre + grow * p.N + col, gf);
+              store32<OutT>(pre + grow * p.N + g.n_out + col, uf);
             }
           }
         }
-      } else {
+      } else if (kEpi == kEpiDswiglu) {
+        // the product is dH [M, K]; preact (G | U) is [M, 2K]; output [dG | dU]
+        const bool valid = r < t.rows;
+        const size_t grow = static_cast<size_t>(t.row0 + r);
+        const OutT* pre = static_cast<const OutT*>(p.preact_in);
+        const int f = p.K;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tb + c * 32, v);
           tmem_ld_wait();
-          const int col = n0 + c * 32;
-          if (valid && col < n_out) {
+          const int col = t.col0 + c * 32;
+          if (valid && col < f) {
+            float gf[32], uf[32], dg[32], du[32];
+            load32<OutT>(pre + grow * 2 * f + col, gf);
+            load32<OutT>(pre + grow * 2 * f + f + col, uf);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float dh = __uint_as_float(v[i]);
+              const float sg = sigmoid_f(gf[i]);
+              du[i] = dh * gf[i] * sg;
+              dg[i] = dh * uf[i] * sg * (1.f + gf[i] * (1.f - sg));
+            }
+            store32<OutT>(out + grow * 2 * f + col, dg);
+            store32<OutT>(out + grow * 2 * f + f + col, du);
+          }
+        }
+      } else {
+        const bool valid = r < t.rows;
+        const size_t grow = static_cast<size_t>(t.row0 + r);
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_ld_wait();
+          const int col = t.col0 + c * 32;
+          if (valid && col < g.n_out) {
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            store32<OutT>(C + grow * n_out + col, f);
+            store32<OutT>(out + grow * g.n_out + col, f);
           }
         }
       }
@@ -310,20 +486,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fwd_kernel(
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   }
   return fn;
 }
 
-// Tiled tensor map over a row-major tensor with dims (innermost first) and the
-// given box; 128-byte swizzle, zero fill out of bounds.
+// Tiled tensor map over a dense row-major tensor: dims innermost first, box
+// sizes, 128-byte swizzle, zero fill out of bounds.
 bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* ptr, int rank,
-              const uint64_t* dims, const uint32_t* box, CUtensorMapSwizzle swz) {
+              const uint64_t* dims, const uint32_t* box) {
   auto fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -340,8 +516,8 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const vo
     stride *= dims[i];
   }
   CUresult r = fn(map, dt, rank, const_cast<void*>(ptr), gdim, gstride, bdim, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return false;
@@ -359,15 +535,44 @@ bool ensure_smem(Kern k, size_t bytes) {
   return true;
 }
 
-template <int kKind, bool kSwiglu, typename OutT>
-moe_status_t launch_fwd(const CUtensorMap& ta, const CUtensorMap& tb, const int32_t* offsets, int M,
-                        int N, int K, int E, void* C, void* preact, int32_t* status,
-                        cudaStream_t stream, int sms) {
-  auto kern = grouped_gemm_fwd_kernel<kKind, kSwiglu, OutT>;
+template <int kKind, int kMode, int kEpi, typename OutT>
+moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t stream,
+                    int sms, const char* what) {
+  auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, kSmemBytes)) return MOE_ERR_CUDA;
-  kern<<<sms, kThreads, kSmemBytes, stream>>>(ta, tb, offsets, M, N, K, E, static_cast<OutT*>(C),
-                                              static_cast<OutT*>(preact), status);
-  return check_launch("moe_grouped_gemm_fwd");
+  kern<<<sms, kThreads, kSmemBytes, stream>>>(ta, tb, p);
+  return check_launch(what);
+}
+
+int elem_bytes(moe_dtype_t t) { return t == MOE_F32 ? 4 : (t == MOE_BF16 ? 2 : 1); }
+
+CUtensorMapDataType map_type(moe_dtype_t t) {
+  return t == MOE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                      : (t == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+moe_status_t common_checks(const char* fn, const moe_operand_t* A, const moe_operand_t* B,
+                           const int32_t* offsets, int M, int N, int K, int E, const void* out, int* sms) {
+  if (!A || !B) {
+    set_error("%s: null operand", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > kMaxE || K % 32 || N % 32) {
+    set_error("%s: need M >= 0, N %% 32 == 0, K %% 32 == 0, 1 <= E <= %d (M=%d N=%d K=%d E=%d)", fn,
+              kMaxE, M, N, K, E);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (A->dtype != B->dtype) {
+    set_error("%s: both operands must have the same dtype", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!offsets || (M > 0 && (!A->ptr || !B->ptr || !out)) || !aligned16(A->ptr) || !aligned16(B->ptr) ||
+      !aligned16(out)) {
+    set_error("%s: null or misaligned pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!device_is_sm103(sms)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
 }
 
 }  // namespace gemm
@@ -376,64 +581,48 @@ moe_status_t launch_fwd(const CUtensorMap& ta, const CUtensorMap& tb, const int3
 using namespace moe;
 using namespace moe::gemm;
 
-static int elem_bytes(moe_dtype_t t) { return t == MOE_F32 ? 4 : (t == MOE_BF16 ? 2 : 1); }
-
 extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_operand_t* B,
                                              const int32_t* offsets, int M, int N, int K, int E,
                                              moe_epilogue_t epi, void* C, moe_dtype_t c_dtype,
                                              void* preact, int32_t* dev_status,
                                              cudaStream_t stream) {
-  if (!A || !B) {
-    set_error("moe_grouped_gemm_fwd: null operand");
-    return MOE_ERR_INVALID_ARG;
-  }
-  if (M < 0 || N <= 0 || K <= 0 || E < 1 || E > kMaxE || K % 32 || N % 32 ||
-      (epi == MOE_EPI_SWIGLU && N % 64) || (epi != MOE_EPI_NONE && epi != MOE_EPI_SWIGLU)) {
-    set_error("moe_grouped_gemm_fwd: need M >= 0, K %% 32 == 0, N %% 32 == 0 (SwiGLU: N %% 64), 1 <= E <= %d, epi NONE|SWIGLU (M=%d N=%d K=%d E=%d)",
-              kMaxE, M, N, K, E);
-    return MOE_ERR_INVALID_ARG;
-  }
-  if (A->dtype != B->dtype || (c_dtype != MOE_BF16 && c_dtype != MOE_F32)) {
-    set_error("moe_grouped_gemm_fwd: A and B must share a dtype; C must be BF16 or F32");
-    return MOE_ERR_INVALID_ARG;
-  }
-  if (!offsets || (M > 0 && (!A->ptr || !B->ptr || !C)) || !aligned16(A->ptr) || !aligned16(B->ptr) ||
-      !aligned16(C) || !aligned16(preact)) {
-    set_error("moe_grouped_gemm_fwd: null or misaligned pointer");
-    return MOE_ERR_INVALID_ARG;
-  }
+  const char* fn = "moe_grouped_gemm_fwd";
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = common_checks(fn, A, B, offsets, M, N, K, E, C, &sms);
+  if (st != MOE_OK) return st;
+  if ((epi != MOE_EPI_NONE && epi != MOE_EPI_SWIGLU) || (epi == MOE_EPI_SWIGLU && N % 64) ||
+      (c_dtype != MOE_BF16 && c_dtype != MOE_F32) || !aligned16(preact)) {
+    set_error("%s: epi NONE|SWIGLU (SWIGLU: N %% 64 == 0), C BF16|F32, aligned preact", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (M == 0) return MOE_OK;
   if (A->dtype == MOE_E4M3) {
-    set_error("moe_grouped_gemm_fwd: MXFP8 operands are not built in this library");
+    set_error("%s: MXFP8 operands are not built in this library", fn);
     return MOE_ERR_UNSUPPORTED;
   }
   const int eb = elem_bytes(A->dtype);
-  const CUtensorMapDataType dt =
-      A->dtype == MOE_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t bk = kBKBytes / eb;
   CUtensorMap ta, tb;
   const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
   const uint32_t abox[2] = {bk, kBM};
   const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint32_t bbox[3] = {bk, static_cast<uint32_t>(epi == MOE_EPI_SWIGLU ? kBN / 2 : kBN), 1};
-  if (!make_map(&ta, dt, eb, A->ptr, 2, adims, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&tb, dt, eb, B->ptr, 3, bdims, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_map(&ta, map_type(A->dtype), eb, A->ptr, 2, adims, abox) ||
+      !make_map(&tb, map_type(A->dtype), eb, B->ptr, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
+  Params p{offsets, M, N, K, E, C, preact, nullptr, dev_status};
   const bool sw = epi == MOE_EPI_SWIGLU;
+  const bool f32 = c_dtype == MOE_F32;
   if (A->dtype == MOE_F32) {
-    if (c_dtype == MOE_F32)
-      return sw ? launch_fwd<0, true, float>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms)
-                : launch_fwd<0, false, float>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms);
-    return sw ? launch_fwd<0, true, uint16_t>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms)
-              : launch_fwd<0, false, uint16_t>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms);
+    if (sw) return f32 ? launch<0, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn)
+                       : launch<0, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn);
+    return f32 ? launch<0, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn)
+               : launch<0, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
   }
-  if (c_dtype == MOE_F32)
-    return sw ? launch_fwd<1, true, float>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms)
-              : launch_fwd<1, false, float>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms);
-  return sw ? launch_fwd<1, true, uint16_t>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms)
-            : launch_fwd<1, false, uint16_t>(ta, tb, offsets, M, N, K, E, C, preact, dev_status, stream, sms);
+  if (sw) return f32 ? launch<1, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn)
+                     : launch<1, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn);
+  return f32 ? launch<1, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn)
+             : launch<1, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const moe_operand_t* B,
@@ -441,18 +630,56 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
                                                moe_epilogue_t epi, const void* preact, void* dA,
                                                moe_dtype_t dA_dtype, int32_t* dev_status,
                                                cudaStream_t stream) {
-  (void)dC; (void)B; (void)offsets; (void)M; (void)N; (void)K; (void)E; (void)epi; (void)preact;
-  (void)dA; (void)dA_dtype; (void)dev_status; (void)stream;
-  set_error("moe_grouped_gemm_dgrad: not built yet");
-  return MOE_ERR_UNSUPPORTED;
+  const char* fn = "moe_grouped_gemm_dgrad";
+  int sms = 0;
+  moe_status_t st = common_checks(fn, dC, B, offsets, M, N, K, E, dA, &sms);
+  if (st != MOE_OK) return st;
+  if (dC->dtype != MOE_BF16 || dA_dtype != MOE_BF16) {
+    set_error("%s: BF16 operands and output only", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if ((epi != MOE_EPI_NONE && epi != MOE_EPI_DSWIGLU) ||
+      (epi == MOE_EPI_DSWIGLU && (!preact || !aligned16(preact)))) {
+    set_error("%s: epi NONE|DSWIGLU (DSWIGLU needs an aligned preact [M, 2K])", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M == 0) return MOE_OK;
+  CUtensorMap ta, tb;
+  const uint64_t adims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const uint32_t abox[2] = {64, kBM};
+  const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+  const uint32_t bbox[3] = {64, kMnRows, 1};
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC->ptr, 2, adims, abox) ||
+      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B->ptr, 3, bdims, bbox))
+    return MOE_ERR_INVALID_ARG;
+  Params p{offsets, M, N, K, E, dA, nullptr, preact, dev_status};
+  if (epi == MOE_EPI_DSWIGLU) return launch<1, kDgrad, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn);
+  return launch<1, kDgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
                                                const int32_t* offsets, int M, int N, int K, int E,
                                                void* dB, moe_dtype_t dB_dtype, int32_t* dev_status,
                                                cudaStream_t stream) {
-  (void)A; (void)dC; (void)offsets; (void)M; (void)N; (void)K; (void)E; (void)dB; (void)dB_dtype;
-  (void)dev_status; (void)stream;
-  set_error("moe_grouped_gemm_wgrad: not built yet");
-  return MOE_ERR_UNSUPPORTED;
+  const char* fn = "moe_grouped_gemm_wgrad";
+  int sms = 0;
+  moe_status_t st = common_checks(fn, A, dC, offsets, M, N, K, E, dB, &sms);
+  if (st != MOE_OK) return st;
+  if (A->dtype != MOE_BF16 || dB_dtype != MOE_BF16) {
+    set_error("%s: BF16 operands and output only", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  CUtensorMap ta, tb;
+  // The MMA's A operand is dC^T (rows n, contraction over the group's rows); its
+  // B operand is A.  Both are read as 64 x 64 MN-major boxes.
+  const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M > 0 ? M : 1)};
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M > 0 ? M : 1)};
+  const uint32_t box[2] = {64, kMnRows};
+  const void* cptr = dC->ptr ? dC->ptr : dB;   // M == 0: never read, only a valid address
+  const void* aptr = A->ptr ? A->ptr : dB;
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cptr, 2, cdims, box) ||
+      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aptr, 2, adims, box))
+    return MOE_ERR_INVALID_ARG;
+  Params p{offsets, M, N, K, E, dB, nullptr, nullptr, dev_status};
+  return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
 }

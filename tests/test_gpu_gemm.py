@@ -102,3 +102,70 @@ def test_fwd_bad_offsets_flag_status():
     moe_gpu.moe_grouped_gemm_fwd(A, B, off, out=C, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & moe_gpu.binding.MOE_DEV_BAD_INDEX
+
+
+# ----------------------------------------------------------------------------- backward GEMMs
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "all-in-last"], ids=str)
+@pytest.mark.parametrize("N,K", [(256, 512), (96, 320), (1024, 64)])
+def test_dgrad_plain(counts, N, K):
+    """dA = dC . B[e]: contraction over N (B read MN-major), output width K."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 3
+    dC = W.make_matrix(M, N, seed=N + K, dtype=torch.bfloat16, device="cuda")
+    B = W.make_matrix(E * N, K, seed=N + K + 1, dtype=torch.bfloat16, device="cuda",
+                      scale=N ** -0.5).view(E, N, K)
+    off = ragged_offsets(cnt)
+    dA = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_dgrad(dC, B, off, out=dA)
+    want = om.grouped_gemm_dgrad(f64(dC), f64(B), off.cpu().numpy())
+    got = f64(dA)
+    rows = int(sum(cnt))
+    assert np.isnan(got[rows:]).all()
+    assert rel_l2(got[:rows], want[:rows]) < TOL_BF16
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+@pytest.mark.parametrize("d,f", [(256, 256), (512, 96), (128, 1024)])
+def test_dgrad_dswiglu(counts, d, f):
+    """GEMM2 data gradient with the SwiGLU backward fused: [dG | dU] from dYp, W2 and G|U."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt))
+    dyp = W.make_matrix(M, d, seed=d + f, dtype=torch.bfloat16, device="cuda")
+    W2 = W.make_matrix(E * d, f, seed=d + f + 1, dtype=torch.bfloat16, device="cuda",
+                       scale=f ** -0.5).view(E, d, f)
+    GU = W.make_matrix(M, 2 * f, seed=d + f + 2, dtype=torch.bfloat16, device="cuda", scale=2.0)
+    off = ragged_offsets(cnt)
+    dGU = moe_gpu.moe_grouped_gemm_dgrad(dyp, W2, off, epi="dswiglu", preact=GU)
+    dH = om.grouped_gemm_dgrad(f64(dyp), f64(W2), off.cpu().numpy())
+    want = om.dswiglu(dH, f64(GU))
+    assert dGU.shape == (M, 2 * f)
+    assert rel_l2(f64(dGU), want) < TOL_BF16
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "all-in-last", "one-expert"], ids=str)
+@pytest.mark.parametrize("N,K", [(256, 512), (160, 96), (64, 1024)])
+def test_wgrad(counts, N, K):
+    """dB[e] = dC[R_e]^T A[R_e]: a contraction over each group's ragged rows; empty
+    groups give exact zeros; rows of neighbouring groups never leak in."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 7                     # trailing rows outside every group
+    A = W.make_matrix(M, K, seed=N + K, dtype=torch.bfloat16, device="cuda")
+    dC = W.make_matrix(M, N, seed=N + K + 3, dtype=torch.bfloat16, device="cuda")
+    A[int(sum(cnt)):] = 1e4                   # poison the rows no group owns
+    off = ragged_offsets(cnt)
+    dB = torch.full((E, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_wgrad(A, dC, off, E, out=dB)
+    want = om.grouped_gemm_wgrad(f64(A), f64(dC), off.cpu().numpy(), E)
+    got = f64(dB)
+    for e in range(E):
+        if cnt[e] == 0:
+            assert (got[e] == 0).all() and not np.signbit(got[e]).any(), f"expert {e} not exactly zero"
+    assert not np.isnan(got).any()
+    assert rel_l2(got, want) < TOL_BF16

@@ -154,3 +154,33 @@ def test_graph_replay_with_new_logits():
         assert (i64(layer.counts) == ref["counts"]).all()
         assert (i64(layer.src_pair) == ref["src_pair"]).all()
         assert rel_l2(f64(layer.y), ref["y"]) < TOL_BF16
+
+
+@pytest.mark.parametrize("w", [W.BY_NAME["dsv3-bf16-train"].scaled(T=256, d=256, f=128, name="dsv3-train-small"),
+                               W.BY_NAME["dsv3-bf16-train"].scaled(T=700, E=16, d=192, f=320, name="train-E16"),
+                               W.BY_NAME["mixtral-bf16"].scaled(T=300, d=128, f=448, name="mixtral-train-small")],
+                         ids=lambda w: w.name)
+def test_scaled_backward_full(w):
+    """Forward + backward of the layer against the float64 oracle, every element."""
+    need_gpu()
+    layer, x, W1, W2, lg = _build(w, training=True)
+    dy = W.make_dy(w, "cuda")
+    layer.forward(x, lg)
+    dx, dlogits, dW1, dW2 = layer.backward(dy, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    lg_h = lg.cpu().numpy()
+    ref = om.layer_forward(f64(x), lg_h, f64(W1), f64(W2), w.k)
+    bwd = om.layer_backward(ref, f64(dy), f64(x), lg_h, f64(W1), f64(W2), w.k)
+    assert rel_l2(f64(layer.gu), ref["GU"]) < TOL_BF16
+    assert rel_l2(f64(layer.dyp), bwd["dYp"]) < TOL_BF16
+    assert rel_l2(f64(layer.dw), bwd["dw"]) < TOL_BF16
+    assert rel_l2(f64(layer.dgu), bwd["dGU"]) < TOL_BF16
+    assert rel_l2(f64(layer.dxp), bwd["dXp"]) < TOL_BF16
+    assert rel_l2(f64(dW2), bwd["dW2"]) < TOL_BF16
+    assert rel_l2(f64(dW1), bwd["dW1"]) < TOL_BF16
+    assert rel_l2(f64(dx), bwd["dx"]) < TOL_BF16
+    assert rel_l2(f64(dlogits), bwd["dlogits"]) < TOL_BF16
+    empty = np.nonzero(ref["counts"] == 0)[0]
+    for e in empty:
+        assert (f64(dW1[e]) == 0).all() and (f64(dW2[e]) == 0).all()
