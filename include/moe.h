@@ -125,6 +125,28 @@ moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, int d,
                          void* workspace, size_t workspace_bytes,
                          int32_t* dev_status, cudaStream_t stream);
 
+/* Allocation-free variant of moe_permute.  The pages have no counterpart: it
+ * exists for callers that cannot allocate device memory -- a plugin that is only
+ * handed input and output pointers by the runtime that owns the allocator, a
+ * serving process whose device memory is all reserved up front by its own pool,
+ * or code that must not allocate while a stream is being captured.  Arguments,
+ * layouts, outputs and errors are those of moe_permute, without the workspace.
+ *
+ * Scratch: a fixed 1 MiB array inside the library's own device memory (held on
+ * every GPU that loads the library until the process exits).  The call needs
+ * ceil(T / 256) * E int32 of it and returns MOE_ERR_WORKSPACE beyond 262144
+ * (T = 65536 tokens with E = 1024 experts fits exactly).  It allocates nothing
+ * and frees nothing.
+ * All calls share the one array: calls whose kernels can overlap on the GPU
+ * (other streams, other host threads) race and give wrong results -- serialise
+ * them.  The first call on a device looks up the array's device address; make
+ * that first call before any stream capture. */
+moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, int T, int d,
+                                 const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                                 int32_t* offsets, int32_t* dest_row, int32_t* src_pair,
+                                 void* xp, moe_dtype_t xp_dtype, uint8_t* xp_scales,
+                                 int32_t* dev_status, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- quantise --
  * Group-aware MXFP8 quantisation ([1] "What dropless MoE needs" and
  * "Optimisation 1": MXFP8 block scaling of the expert matmuls; [3] contribution

@@ -35,6 +35,7 @@ SIGNATURES = {
     "moe_permute_workspace_size": (sz, [i32, i32, i32]),
     "moe_permute": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz,
                          vp, vp]),
+    "moe_permute_noalloc": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp]),
     "moe_quantize_mxfp8_grouped": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp]),
     "moe_grouped_gemm_fwd": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]),
     "moe_grouped_gemm_dgrad": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
