@@ -317,3 +317,64 @@ def token_forward(x_t, logits_t, W1, W2, k, renormalize=True, mxfp8_operands=Fal
             h = mx_roundtrip(h)
         y += w[0, j] * (h @ w2.T)[0]
     return y
+
+
+def token_backward(x_t, logits_t, dy_t, W1, W2, k, renormalize=True):
+    """Backward of one token's output y[t] = sum_j w_j FFN_{e_j}(x[t]) with upstream
+    gradient dy[t]: returns (dx[t], dlogits[t]).  The same steps as
+    ``layer_backward`` restricted to one token (a token's gradients depend only on
+    its own row, logits, upstream gradient and its experts' weights).  W1/W2 may be
+    callables e -> expert weights."""
+    lg = np.asarray(logits_t, dtype=np.float32)[None, :]
+    idx, w, _ = route_topk(lg, k, renormalize)
+    get1 = W1 if callable(W1) else (lambda e: W1[e])
+    get2 = W2 if callable(W2) else (lambda e: W2[e])
+    xt = np.asarray(x_t, dtype=np.float64)[None, :]
+    dyt = np.asarray(dy_t, dtype=np.float64)[None, :]
+    dx = np.zeros(xt.shape[1])
+    dw = np.zeros((1, k))
+    for j in range(k):
+        e = int(idx[0, j])
+        w1, w2 = np.asarray(get1(e), np.float64), np.asarray(get2(e), np.float64)
+        GU = xt @ w1.T
+        yp = swiglu(GU) @ w2.T
+        dw[0, j] = float((dyt * yp).sum())
+        dH = (w[0, j] * dyt) @ w2
+        dx += (dswiglu(dH, GU) @ w1)[0]
+    dl = route_bwd(dw, w, idx, lg, renormalize)[0]
+    return dx, dl
+
+
+def expert_wgrad_sampled(X_e, dYp_e, w1, w2, w1_rows, w2_cols):
+    """Selected rows of dW1[e] and columns of dW2[e] for one expert, from its own
+    rows X_e [c, d] and upstream dYp_e [c, d]; w1 [2f, d], w2 [d, f].
+
+    Row n of dW1 = sum_r dGU[r, n] X_e[r]; dGU[:, n] needs only the gate/up
+    columns n mod f of GU and column n mod f of dH = dYp_e w2.  Column c of dW2 =
+    sum_r dYp_e[r] H[r, c]; H[:, c] needs gate/up columns c.  So each sampled row or
+    column costs O(rows * d) and the full [c, 2f] intermediates are never formed."""
+    X = np.asarray(X_e, dtype=np.float64)
+    dY = np.asarray(dYp_e, dtype=np.float64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    f = w2.shape[1]
+
+    def cols(c):
+        g = X @ w1[c]
+        u = X @ w1[f + c]
+        return g, u
+
+    dw1 = np.zeros((len(w1_rows), X.shape[1]))
+    for i, n in enumerate(w1_rows):
+        c = int(n) % f
+        g, u = cols(c)
+        dh = dY @ w2[:, c]
+        s = 1.0 / (1.0 + np.exp(-g))
+        dgu = dh * u * s * (1.0 + g * (1.0 - s)) if n < f else dh * g * s
+        dw1[i] = dgu @ X
+    dw2 = np.zeros((w2.shape[0], len(w2_cols)))
+    for i, c in enumerate(w2_cols):
+        g, u = cols(int(c))
+        h = silu(g) * u
+        dw2[:, i] = dY.T @ h
+    return dw1, dw2

@@ -165,3 +165,31 @@ def test_mxfp8_layer_close_to_exact_layer():
     for t in (0, 13, 39):
         np.testing.assert_allclose(moe.token_forward(x[t], lg[t], W1, W2, k, mxfp8_operands=True),
                                    fwd["y"][t], rtol=1e-12, atol=1e-13)
+
+
+def test_token_backward_matches_layer_backward():
+    T, d, E, k, f = 20, 8, 5, 2, 6
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=51)
+    dy = np.random.default_rng(52).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k)
+    bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k)
+    for t in (0, 11, 19):
+        dx, dl = moe.token_backward(x[t], lg[t], dy[t], W1, W2, k)
+        np.testing.assert_allclose(dx, bwd["dx"][t], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dl, bwd["dlogits"][t], rtol=1e-11, atol=1e-13)
+
+
+def test_expert_wgrad_sampled_matches_full_wgrad():
+    T, d, E, k, f = 30, 8, 4, 2, 6
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=61)
+    dy = np.random.default_rng(62).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k)
+    bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k)
+    off = fwd["offsets"]
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        rows = [0, f - 1, f, 2 * f - 1]
+        cols = [0, 3, f - 1]
+        dw1, dw2 = moe.expert_wgrad_sampled(fwd["Xp"][lo:hi], bwd["dYp"][lo:hi], W1[e], W2[e], rows, cols)
+        np.testing.assert_allclose(dw1, bwd["dW1"][e][rows], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dw2, bwd["dW2"][e][:, cols], rtol=1e-11, atol=1e-13)
