@@ -229,6 +229,14 @@ __device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// Copy 32 rows x 16 bytes from shared memory (no-swizzle descriptor) into TMEM
+// lanes 0-31 x 4 columns, replicated into all four 32-lane quarters.  With the
+// 512-byte scale-factor atom (byte (m % 32) * 16 + (m / 32) * 4 + kb for row m of
+// 128 and scale block kb of 4) this is the layout block-scaled MMAs read.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

@@ -48,8 +48,9 @@ constexpr int kAStage = kBM * kBKBytes;           // 16 KB
 constexpr int kBStage = kBN * kBKBytes;           // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;    // 48 KB
 constexpr int kBox = 8192;                        // one 64 x 64 bf16 MN-major box
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 2 * kBN;                // double-buffered accumulator
+constexpr int kSfAStage = 2048;                   // MXFP8: raw A scales, 128 rows x 16 bytes
+constexpr int kSfBStage = 4096;                   // MXFP8: raw B scales, 256 rows x 16 bytes
+constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
 enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
@@ -69,6 +70,7 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn, int b_
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t sfready[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -79,7 +81,27 @@ struct Smem {
   int offs[kMaxE + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Smem);
+// Per-kind configuration.  kind 0 = tf32, 1 = bf16: 6 warps, double-buffered
+// accumulator (2 x 256 TMEM columns).  kind 2 = MXFP8: a 7th warp lays the E8M0
+// scales of each stage out as 512-byte scale atoms; the accumulator is single
+// (TMEM columns 0-255) because columns 256-383 hold one 32-column scale slot per
+// stage (A scales at +0, B scales at +16), every slot 32-column aligned.
+template <int kKind>
+struct Cfg {
+  static constexpr bool kMx = kKind == 2;
+  static constexpr int kStage = kStageBytes + (kMx ? kSfAStage + kSfBStage : 0);
+  static constexpr int kThreads = kMx ? 224 : 192;
+  static constexpr int kAcc = kMx ? 1 : 2;
+  static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStage + sizeof(Smem);
+};
+
+// Block-scaled instruction descriptor (kind::mxf8f6f4): E4M3 A and B (format 0),
+// K-major, N >> 3 at bit 17, E8M0 scales (bit 23), M >> 4 at bit 24; the scale
+// byte of each k-step is selected by the A / B scale ids (bits 29-30 / 4-5).
+__host__ __device__ constexpr uint32_t make_idesc_mx(int m, int n) {
+  return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
+}
 
 struct Params {
   const int32_t* offsets;
@@ -240,19 +262,22 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 }
 
 template <int kKind, int kMode, int kEpi, typename OutT>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+__global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
+  using C = Cfg<kKind>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& s = *reinterpret_cast<Smem*>(tiles + kStages * kStageBytes);
+  Smem& s = *reinterpret_cast<Smem*>(tiles + kStages * C::kStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int eb = kKind == 0 ? 4 : 2;
+  constexpr int eb = C::kEb;
   const Geo<kMode, kEpi> g(p, eb);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
+      mbar_init(&s.sfready[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -264,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (C::kMx) {
+      tma_prefetch_desc(&tmSA);
+      tma_prefetch_desc(&tmSB);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -284,10 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         const Tile t = tile_info(s, g, tile, p.E, p.M);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.status, &s.abort)) break;
-          uint8_t* sa = tiles + stage * kStageBytes;
+          uint8_t* sa = tiles + stage * C::kStage;
           uint8_t* sb = sa + kAStage;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, kStageBytes);
+          mbar_arrive_expect_tx(bar, C::kStage);
           if (kMode == kFwd) {
             const int kx = kb * (kBKBytes / eb);
             tma_load_2d(sa, &tmA, bar, kx, t.row0);
@@ -296,6 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
               tma_load_3d(sb + kBStage / 2, &tmB, bar, kx, g.n_out + t.col0, t.e);
             } else {
               tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
+            }
+            if (C::kMx) {
+              // raw E8M0 rows: 16 scale bytes (4 stages' worth) per row; the
+              // stage's 4 bytes sit at 4 * (kb % 4) inside each row
+              uint8_t* ssa = sa + kStageBytes;
+              uint8_t* ssb = ssa + kSfAStage;
+              const int sx = 16 * (kb / 4);
+              const int brow = t.e * p.N;
+              tma_load_2d(ssa, &tmSA, bar, sx, t.row0);
+              if (kEpi == kEpiSwiglu) {
+                tma_load_2d(ssb, &tmSB, bar, sx, brow + t.col0);
+                tma_load_2d(ssb + kSfBStage / 2, &tmSB, bar, sx, brow + g.n_out + t.col0);
+              } else {
+                tma_load_2d(ssb, &tmSB, bar, sx, brow + t.col0);
+                tma_load_2d(ssb + kSfBStage / 2, &tmSB, bar, sx, brow + t.col0 + kBM);
+              }
             }
           } else if (kMode == kDgrad) {
             const int nx = kb * kMnRows;                  // contraction index (N of B)
@@ -315,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
+    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, kBN)
+                                      : make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
@@ -324,9 +370,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       tc_fence_after();
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
       for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (C::kMx) {
+          if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(tiles + stage * C::kStage);
+            const uint32_t sb = sa + kAStage;
+            const uint32_t ssa = sa + kStageBytes;
+            const uint32_t ssb = ssa + kSfAStage;
+            // scale slot of this stage: A atom at +0 (4 columns), B atoms at +16, +20
+            const uint32_t slot = tmem + 256u + 32u * static_cast<uint32_t>(stage);
+            tc_cp_32x128b_warpx4(slot, make_sdesc(ssa, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + 16, make_sdesc(ssb, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + 20, make_sdesc(ssb + 512, 0, 128, 0));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
+              const uint64_t bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
+              const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
+              tc_mma_mxf8(d_tmem, ad, bd, id, slot, slot + 16, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(&s.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          continue;
+        }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
         tc_fence_after();
-        uint8_t* sa_ptr = tiles + stage * kStageBytes;
+        uint8_t* sa_ptr = tiles + stage * C::kStage;
         const uint32_t sa = smem_u32(sa_ptr);
         const uint32_t sb = sa + kAStage;
         int steps = 4;
@@ -363,9 +435,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       if (lane == 0) tc_commit(&s.tfull[acc]);
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
-  } else {
+  } else if (C::kMx && warp == 6) {
+    // ------------------------------------------------------------------ MXFP8 scale layout
+    // Re-lay each stage's raw scale rows (row r: 16 bytes, the stage's 4 at byte
+    // `off`) as 512-byte atoms in place: atom byte (m % 32) * 16 + (m / 32) * 4 + kb.
+    // Lane L writes bytes [16L, 16L + 16) of each atom, which only lane L reads
+    // (raw row L, and raw row 32 + L for the second B atom), after its reads.
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
+        uint8_t* ssa = tiles + stage * C::kStage + kStageBytes;
+        uint8_t* ssb = ssa + kSfAStage;
+        const int off = 4 * (kb % 4);
+        uint32_t va[4], vb[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) va[j] = *reinterpret_cast<const uint32_t*>(ssa + (lane + 32 * j) * 16 + off);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) vb[j] = *reinterpret_cast<const uint32_t*>(ssb + (lane + 32 * j) * 16 + off);
+        __syncwarp();
+        *reinterpret_cast<uint4*>(ssa + lane * 16) = make_uint4(va[0], va[1], va[2], va[3]);
+        *reinterpret_cast<uint4*>(ssb + lane * 16) = make_uint4(vb[0], vb[1], vb[2], vb[3]);
+        *reinterpret_cast<uint4*>(ssb + 512 + lane * 16) = make_uint4(vb[4], vb[5], vb[6], vb[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sfready[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int r = q * 32 + lane;            // tile row owned by this thread
@@ -470,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       tc_fence_before();
       mbar_arrive(&s.tempty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
   }
   tc_fence_before();
@@ -497,9 +599,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tiled tensor map over a dense row-major tensor: dims innermost first, box
-// sizes, 128-byte swizzle, zero fill out of bounds.
+// sizes, 128-byte swizzle (or none), zero fill out of bounds.
 bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* ptr, int rank,
-              const uint64_t* dims, const uint32_t* box) {
+              const uint64_t* dims, const uint32_t* box,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -516,7 +619,7 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const vo
     stride *= dims[i];
   }
   CUresult r = fn(map, dt, rank, const_cast<void*>(ptr), gdim, gstride, bdim, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -537,10 +640,13 @@ bool ensure_smem(Kern k, size_t bytes) {
 
 template <int kKind, int kMode, int kEpi, typename OutT>
 moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t stream,
-                    int sms, const char* what) {
+                    int sms, const char* what, const CUtensorMap* tsa = nullptr,
+                    const CUtensorMap* tsb = nullptr) {
+  using C = Cfg<kKind>;
+  static_assert(C::kSmem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
-  if (!ensure_smem(kern, kSmemBytes)) return MOE_ERR_CUDA;
-  kern<<<sms, kThreads, kSmemBytes, stream>>>(ta, tb, p);
+  if (!ensure_smem(kern, C::kSmem)) return MOE_ERR_CUDA;
+  kern<<<sms, C::kThreads, C::kSmem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
   return check_launch(what);
 }
 
@@ -595,11 +701,12 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
     set_error("%s: epi NONE|SWIGLU (SWIGLU: N %% 64 == 0), C BF16|F32, aligned preact", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (M == 0) return MOE_OK;
-  if (A->dtype == MOE_E4M3) {
-    set_error("%s: MXFP8 operands are not built in this library", fn);
-    return MOE_ERR_UNSUPPORTED;
+  if (A->dtype == MOE_E4M3 && (!A->scales || !B->scales || K % 512 || !aligned16(A->scales) ||
+                               !aligned16(B->scales))) {
+    set_error("%s: MXFP8 needs 16-byte aligned A and B scales and K %% 512 == 0", fn);
+    return MOE_ERR_INVALID_ARG;
   }
+  if (M == 0) return MOE_OK;
   const int eb = elem_bytes(A->dtype);
   const uint32_t bk = kBKBytes / eb;
   CUtensorMap ta, tb;
@@ -613,6 +720,20 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   Params p{offsets, M, N, K, E, C, preact, nullptr, dev_status};
   const bool sw = epi == MOE_EPI_SWIGLU;
   const bool f32 = c_dtype == MOE_F32;
+  if (A->dtype == MOE_E4M3) {
+    // E8M0 scales, [rows, K/32] bytes, read 16 bytes (4 stages' worth) per row
+    CUtensorMap tsa, tsb;
+    const uint64_t sadims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M)};
+    const uint64_t sbdims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(N) * static_cast<uint64_t>(E)};
+    const uint32_t sbox[2] = {16, kBM};
+    if (!make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_INVALID_ARG;
+    if (sw) return f32 ? launch<2, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
+                       : launch<2, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+    return f32 ? launch<2, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
+               : launch<2, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+  }
   if (A->dtype == MOE_F32) {
     if (sw) return f32 ? launch<0, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn)
                        : launch<0, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn);

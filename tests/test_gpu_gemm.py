@@ -169,3 +169,65 @@ def test_wgrad(counts, N, K):
             assert (got[e] == 0).all() and not np.signbit(got[e]).any(), f"expert {e} not exactly zero"
     assert not np.isnan(got).any()
     assert rel_l2(got, want) < TOL_BF16
+
+
+# ----------------------------------------------------------------------------- MXFP8 forward
+
+from oracle import mxfp8 as omx  # noqa: E402
+from _parity import TOL_MXFP8  # noqa: E402
+
+
+def _quantize(t):
+    """Row-wise MXFP8 on the GPU; the oracle quantises the same values itself and
+    the codes must agree bit for bit."""
+    rows = t.reshape(-1, t.shape[-1])
+    codes, scales = moe_gpu.moe_quantize_mxfp8_grouped(rows)
+    c, s = omx.quantize_rowwise(f64(rows))
+    assert (codes.cpu().numpy() == c).all() and (scales.cpu().numpy() == s).all()
+    return codes.view(t.shape), scales.view(*t.shape[:-1], t.shape[-1] // 32), omx.dequantize_rowwise(c, s)
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
+@pytest.mark.parametrize("K,N", [(512, 256), (1024, 320), (2048, 64)])
+def test_fwd_mxfp8_plain(counts, K, N):
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 2
+    A, B = _mats(M, K, N, E, torch.bfloat16, seed=K + N + 7)
+    Aq, As, A_deq = _quantize(A)
+    Bq, Bs, B_deq = _quantize(B)
+    off = ragged_offsets(cnt)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, A_scales=As, B_scales=Bs, out=C)
+    want = om.grouped_gemm(A_deq, B_deq.reshape(E, N, K), off.cpu().numpy())
+    got = f64(C)
+    rows = int(sum(cnt))
+    assert np.isnan(got[rows:]).all()
+    err = rel_l2(got[:rows], want[:rows])
+    assert err < TOL_MXFP8 and err < 1e-2, err       # same quantised inputs: only fp32/bf16 rounding
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+@pytest.mark.parametrize("K,f", [(512, 128), (1024, 256), (512, 96)])
+def test_fwd_mxfp8_swiglu(counts, K, f):
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt))
+    A, B = _mats(M, K, 2 * f, E, torch.bfloat16, seed=K + f + 9)
+    Aq, As, A_deq = _quantize(A)
+    Bq, Bs, B_deq = _quantize(B)
+    off = ragged_offsets(cnt)
+    H = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi="swiglu", A_scales=As, B_scales=Bs)
+    want = om.swiglu(om.grouped_gemm(A_deq, B_deq.reshape(E, 2 * f, K), off.cpu().numpy()))
+    assert rel_l2(f64(H), want) < 1e-2
+
+
+def test_fwd_mxfp8_requires_scales_and_k_multiple_of_512():
+    need_gpu()
+    A, B = _mats(64, 256, 64, 2, torch.bfloat16, seed=1)
+    Aq, As, _ = _quantize(A)
+    Bq, Bs, _ = _quantize(B)
+    with pytest.raises(moe_gpu.binding.MoeError, match="512"):
+        moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, ragged_offsets([32, 32]), A_scales=As, B_scales=Bs)

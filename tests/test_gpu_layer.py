@@ -184,3 +184,91 @@ def test_scaled_backward_full(w):
     empty = np.nonzero(ref["counts"] == 0)[0]
     for e in empty:
         assert (f64(dW1[e]) == 0).all() and (f64(dW2[e]) == 0).all()
+
+
+def test_mxfp8_layer_scaled_full():
+    """DeepSeek-V3-shaped MXFP8 layer at reduced size, every output element,
+    against the oracle's own MXFP8 chain (it quantises X, W1, H and W2 itself)."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-mxfp8"].scaled(T=400, d=512, f=512, name="dsv3-mx-small")
+    layer, x, W1, W2, lg = _build(w)
+    y = layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    ref = om.layer_forward(f64(x), lg.cpu().numpy(), f64(W1), f64(W2), w.k, mxfp8_operands=True)
+    assert (i64(layer.src_pair) == ref["src_pair"]).all()
+    assert rel_l2(f64(layer.h), ref["H"]) < TOL_MXFP8
+    assert rel_l2(f64(y), ref["y"]) < TOL_MXFP8
+
+
+def test_mxfp8_layer_full_size_sampled():
+    need_gpu()
+    w = W.BY_NAME["dsv3-mxfp8"]
+    layer, x, W1, W2, lg = _build(w)
+    layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=4, rows_per_expert=8)
+
+
+def test_train_full_size_sampled():
+    """The DeepSeek-V3-shaped training step at full size: integer outputs in full,
+    forward on samples, dx / dlogits of sampled tokens, and sampled rows of dW1 /
+    columns of dW2 for the hottest, median and smallest non-empty experts (the
+    contraction over all of each expert's rows); empty experts exactly zero."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-bf16-train"]
+    layer, x, W1, W2, lg = _build(w, training=True)
+    dy = W.make_dy(w, "cuda")
+    layer.forward(x, lg)
+    layer.backward(dy, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=2, rows_per_expert=8)
+
+    rng = np.random.default_rng(5)
+    lg_h = lg.cpu().numpy()
+    idx, wt, counts = om.route_topk(lg_h, w.k)
+    offsets, dest, src = om.permute_maps(idx, w.E)
+    cache = {}
+
+    def get(e, which):
+        if (e, which) not in cache:
+            cache[(e, which)] = f64((W1 if which == 1 else W2)[e])
+        return cache[(e, which)]
+
+    toks = np.sort(rng.choice(w.T, size=2, replace=False))
+    got_dx, want_dx, got_dl, want_dl = [], [], [], []
+    for t in toks:
+        dx_t, dl_t = om.token_backward(f64(x[t]), lg_h[t], f64(dy[t]), lambda e: get(e, 1),
+                                       lambda e: get(e, 2), w.k)
+        got_dx.append(f64(layer.dx[t]))
+        want_dx.append(dx_t)
+        got_dl.append(f64(layer.dlogits[t]))
+        want_dl.append(dl_t)
+    assert rel_l2(np.stack(got_dx), np.stack(want_dx)) < TOL_BF16
+    assert rel_l2(np.stack(got_dl), np.stack(want_dl)) < TOL_BF16
+
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    got1, want1, got2, want2 = [], [], [], []
+    for e in (int(order[-1]), int(order[len(order) // 2]), int(order[0])):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        pairs = src[lo:hi]
+        tok = torch.from_numpy(pairs // w.k).cuda()
+        X_e = f64(x[tok])
+        dYp_e = wt[pairs // w.k, pairs % w.k][:, None] * f64(dy[tok])
+        rows = np.sort(rng.choice(2 * w.f, size=6, replace=False))
+        cols = np.sort(rng.choice(w.f, size=6, replace=False))
+        dw1, dw2 = om.expert_wgrad_sampled(X_e, dYp_e, get(e, 1), get(e, 2), rows, cols)
+        got1.append(f64(layer.dW1[e][torch.from_numpy(rows).cuda()]))
+        want1.append(dw1)
+        got2.append(f64(layer.dW2[e][:, torch.from_numpy(cols).cuda()]))
+        want2.append(dw2)
+    assert rel_l2(np.concatenate(got1), np.concatenate(want1)) < TOL_BF16
+    assert rel_l2(np.concatenate(got2, axis=1), np.concatenate(want2, axis=1)) < TOL_BF16
+    empty = np.nonzero(counts == 0)[0]
+    assert len(empty) > 0
+    e_t = torch.from_numpy(empty).cuda()
+    assert int(torch.count_nonzero(layer.dW1[e_t]).item()) == 0
+    assert int(torch.count_nonzero(layer.dW2[e_t]).item()) == 0
