@@ -3,8 +3,9 @@
 // Combine per "Accelerating Dropless MoE Training in JAX with NVIDIA Transformer
 // Engine", "Optimisation 2" (processed tokens are routed back and the expert
 // results accumulated per token) and Figure 3 (back to the original order).
-// One warp owns one token: its k source rows are gathered with 16-byte loads,
-// up to 8 rows in flight per lane, and summed in slot order in fp32.
+// A warp owns one column slice of one token: the token's k source rows are
+// gathered with 16-byte loads, up to 8 rows in flight per lane, and summed in slot
+// order in fp32.
 #include "common.cuh"
 
 namespace moe {
@@ -67,6 +68,11 @@ __device__ __forceinline__ void store_out(uint8_t* dst, const float (&f)[N]) {
   }
 }
 
+// Work item = (token, column slice of kSliceChunks 16-byte chunks), so that a
+// few thousand tokens still spread over every SM; each lane keeps up to 8 source
+// rows' loads in flight per chunk.
+constexpr int kSliceChunks = 128;
+
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint8_t* __restrict__ yp, int T, int d, int k, const int32_t* __restrict__ dest_row,
@@ -78,7 +84,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
   const size_t out_row = static_cast<size_t>(d) * sizeof(Tout);
   const int n16 = static_cast<int>(in_row / 16);
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+  const int nslice = (n16 + kSliceChunks - 1) / kSliceChunks;
+  const long long tasks = static_cast<long long>(T) * nslice;
+  for (long long task = static_cast<long long>(blockIdx.x) * wpb + (threadIdx.x >> 5); task < tasks;
+       task += static_cast<long long>(gridDim.x) * wpb) {
+    const int t = static_cast<int>(task / nslice);
+    const int slice = static_cast<int>(task % nslice);
     int src = -1;
     float w = 0.f;
     if (lane < k) {
@@ -86,13 +97,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
       src = dest_row[p];
       w = topk_w ? topk_w[p] : 1.f;
       if (src < 0 || src >= M) {
-        flag_error(status, MOE_DEV_BAD_INDEX);
+        if (slice == 0) flag_error(status, MOE_DEV_BAD_INDEX);
         src = -1;
       }
     }
-    for (int base = 0; base < n16; base += 32) {
+    const int c_end = min(n16, (slice + 1) * kSliceChunks);
+    for (int base = slice * kSliceChunks; base < c_end; base += 32) {
       const int c = base + lane;
-      const bool active = c < n16;
+      const bool active = c < c_end;
       float acc[N];
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = 0.f;
@@ -123,7 +135,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   }
 }
 
-// dyp[dest_row[t,j]] = w[t,j] dy[t];  dw[t,j] = <dy[t], yp[dest_row[t,j]]>.
+// One warp per (token, slot): dyp[dest_row[t,j]] = w[t,j] dy[t] and
+// dw[t,j] = <dy[t], yp[dest_row[t,j]]> (warp reduction).  dy[t] is re-read by the
+// token's k warps, from L2.
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const uint8_t* __restrict__ dy, const uint8_t* __restrict__ yp, int T, int d, int k,
@@ -135,50 +149,42 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   const int M = T * k;
   const size_t row = static_cast<size_t>(d) * sizeof(Tin);
   const int n16 = static_cast<int>(row / 16);
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
-    int src = -1;
-    float w = 0.f;
-    if (lane < k) {
-      const size_t p = static_cast<size_t>(t) * k + lane;
-      src = dest_row[p];
-      w = topk_w[p];
-      if (src < 0 || src >= M) {
-        flag_error(status, MOE_DEV_BAD_INDEX);
-        src = -1;
-      }
-    }
-    const Vec16* dyr = reinterpret_cast<const Vec16*>(dy + static_cast<size_t>(t) * row);
-    for (int j = 0; j < k; ++j) {
-      const int sj = __shfl_sync(kFull, src, j);
-      const float wj = __shfl_sync(kFull, w, j);
-      float part = 0.f;
-      if (sj >= 0) {
-        const Vec16* ypr = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * row);
-        uint8_t* out = dyp + static_cast<size_t>(sj) * row;
-        for (int c = lane; c < n16; c += 32) {
-          float a[N], b[N], o[N];
-          Elt<Tin>::unpack(dyr[c], a);
-          Elt<Tin>::unpack(ypr[c], b);
+  const long long pairs = static_cast<long long>(T) * k;
+  for (long long p = static_cast<long long>(blockIdx.x) * wpb + (threadIdx.x >> 5); p < pairs;
+       p += static_cast<long long>(gridDim.x) * wpb) {
+    const int t = static_cast<int>(p / k);
+    const int sj = dest_row[p];
+    const float wj = topk_w[p];
+    float part = 0.f;
+    if (sj >= 0 && sj < M) {
+      const Vec16* dyr = reinterpret_cast<const Vec16*>(dy + static_cast<size_t>(t) * row);
+      const Vec16* ypr = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * row);
+      uint8_t* out = dyp + static_cast<size_t>(sj) * row;
+      for (int c = lane; c < n16; c += 32) {
+        float a[N], b[N], o[N];
+        Elt<Tin>::unpack(dyr[c], a);
+        Elt<Tin>::unpack(ypr[c], b);
 #pragma unroll
-          for (int i = 0; i < N; ++i) {
-            part = fmaf(a[i], b[i], part);
-            o[i] = wj * a[i];
-          }
-          Elt<Tin>::store(out + static_cast<size_t>(c) * 16, o);
+        for (int i = 0; i < N; ++i) {
+          part = fmaf(a[i], b[i], part);
+          o[i] = wj * a[i];
         }
+        Elt<Tin>::store(out + static_cast<size_t>(c) * 16, o);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
-      if (lane == 0) dw[static_cast<size_t>(t) * k + j] = part;
+    } else if (lane == 0) {
+      flag_error(status, MOE_DEV_BAD_INDEX);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    if (lane == 0) dw[p] = part;
   }
 }
 
-int grid_for(int T, int sms) {
+int grid_for(long long tasks, int sms) {
   const int wpb = kThreads / 32;
-  int g = (T + wpb - 1) / wpb;
-  const int cap = sms * 8;
-  return g < 1 ? 1 : (g < cap ? g : cap);
+  const long long g = (tasks + wpb - 1) / wpb;
+  const long long cap = static_cast<long long>(sms) * 8;
+  return static_cast<int>(g < 1 ? 1 : (g < cap ? g : cap));
 }
 
 }  // namespace
@@ -206,7 +212,8 @@ extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype,
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (T == 0 || d == 0) return MOE_OK;
-  const int grid = grid_for(T, sms);
+  const long long n16 = static_cast<long long>(d) * (dtype == MOE_BF16 ? 2 : 4) / 16;
+  const int grid = grid_for(static_cast<long long>(T) * ((n16 + kSliceChunks - 1) / kSliceChunks), sms);
   const uint8_t* a = static_cast<const uint8_t*>(yp);
   uint8_t* o = static_cast<uint8_t*>(y);
   if (dtype == MOE_BF16 && y_dtype == MOE_BF16)
@@ -241,7 +248,7 @@ extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  const int grid = grid_for(T, sms);
+  const int grid = grid_for(static_cast<long long>(T) * k, sms);
   const uint8_t* a = static_cast<const uint8_t*>(dy);
   const uint8_t* b = static_cast<const uint8_t*>(yp);
   uint8_t* o = static_cast<uint8_t*>(dyp);

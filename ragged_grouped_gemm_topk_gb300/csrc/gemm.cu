@@ -13,8 +13,9 @@
 //              instruction) into a double-buffered fp32 accumulator in TMEM and
 //              commits each stage back to the producer and each tile to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (TMEM lane = tile row, one
-//              row per thread), the fused epilogue, 16-byte stores masked at the
-//              group's last row and the matrix edge.
+//              row per thread), the fused epilogue, release of the accumulator,
+//              then 16-byte stores masked at the group's last row and the matrix
+//              edge (wgrad: a shared-memory staging tile written by TMA store).
 // Tiles are enumerated on the device from `offsets`, so the host never learns the
 // per-expert sizes:
 //   forward / dgrad  expert e owns ceil(count_e / 128) row tiles x the column
@@ -93,8 +94,18 @@ struct Cfg {
   static constexpr int kThreads = kMx ? 224 : 192;
   static constexpr int kAcc = kMx ? 1 : 2;
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
-  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStage + sizeof(Smem);
 };
+
+// wgrad keeps 3 pipeline stages and stages each epilogue warp's 32 x 256 bf16 dW
+// rows (16 KB) in shared memory for the TMA store.
+constexpr int kWgStage = 16384;
+template <int kKind, int kMode>
+constexpr int stages_for() { return kMode == kWgrad ? 3 : kStages; }
+template <int kKind, int kMode>
+constexpr size_t smem_for() {
+  return 1024 + static_cast<size_t>(stages_for<kKind, kMode>()) * Cfg<kKind>::kStage +
+         (kMode == kWgrad ? 4 * kWgStage : 0) + sizeof(Smem);
+}
 
 // Block-scaled instruction descriptor (kind::mxf8f6f4): E4M3 A and B (format 0),
 // K-major, N >> 3 at bit 17, E8M0 scales (bit 23), M >> 4 at bit 24; the scale
@@ -266,9 +277,10 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
   using C = Cfg<kKind>;
+  constexpr int NS = stages_for<kKind, kMode>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& s = *reinterpret_cast<Smem*>(tiles + kStages * C::kStage);
+  Smem& s = *reinterpret_cast<Smem*>(tiles + NS * C::kStage + (kMode == kWgrad ? 4 * kWgStage : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int eb = C::kEb;
   const Geo<kMode, kEpi> g(p, eb);
@@ -354,7 +366,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kBox, &tmB, bar, t.col0 + 64 * j, r);
           }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
         }
       }
     }
@@ -393,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
             tc_commit(&s.empty[stage]);
           }
           __syncwarp();
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
           continue;
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
           tc_commit(&s.empty[stage]);
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == NS) { stage = 0; phase ^= 1u; }
       }
       if (lane == 0) tc_commit(&s.tfull[acc]);
       __syncwarp();
@@ -464,11 +476,14 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.sfready[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == NS) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue
+    // The accumulator is released (tempty) as soon as its last TMEM read is done;
+    // the global stores of the tile follow from registers (or, for wgrad, from a
+    // shared-memory staging buffer by TMA), overlapping the next tile's MMAs.
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int r = q * 32 + lane;            // tile row owned by this thread
     OutT* out = static_cast<OutT*>(p.out);
@@ -479,54 +494,105 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
       if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      if (kMode == kWgrad) {
-        const bool valid = t.n0 + r < p.N;
-        OutT* dst = out + (static_cast<size_t>(t.e) * p.N + t.n0 + r) * p.K;
+      bool released = false;
+      if constexpr (kMode == kWgrad) {
+        // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns, staged as four
+        // 64-column, 128-byte-swizzled boxes and written by TMA (clipped at N and K).
+        uint8_t* stg = tiles + NS * C::kStage + q * kWgStage;
+        if (lane == 0) bulk_wait_read0();   // the previous tile's stores have read stg
+        __syncwarp();
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
-          float f[32];
+          uint32_t pk[16];
           if (t.rows > 0) {
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = 0.f;
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;
           }
-          const int col = t.col0 + c * 32;
-          if (valid && col < p.K) store32<OutT>(dst + col, f);
+          uint8_t* box = stg + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int chunk = (c & 1) * 4 + h;
+            *reinterpret_cast<uint4*>(box + ((chunk ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+          }
         }
-      } else if (kEpi == kEpiSwiglu) {
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+        released = true;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_store_3d(&tmSA, stg + j * 4096, t.col0 + 64 * j, t.n0 + 32 * q, t.e);
+          bulk_commit();
+        }
+      } else if constexpr (kEpi == kEpiSwiglu) {
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
         OutT* pre = static_cast<OutT*>(p.preact_out);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(tb + c * 32, gv);
-          tmem_ld32(tb + 128 + c * 32, uv);
-          tmem_ld_wait();
-          const int col = t.col0 + c * 32;
-          if (valid && col < g.n_out) {
-            float h[32];
+        if (sizeof(OutT) == 2 && pre == nullptr) {
+          uint32_t pk[64];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = silu_f(__uint_as_float(gv[i])) * __uint_as_float(uv[i]);
-            store32<OutT>(out + grow * g.n_out + col, h);
-            if (pre != nullptr) {
-              float gf[32], uf[32];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tb + c * 32, gv);
+            tmem_ld32(tb + 128 + c * 32, uv);
+            tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                gf[i] = __uint_as_float(gv[i]);
-                uf[i] = __uint_as_float(uv[i]);
+            for (int i = 0; i < 16; ++i)
+              pk[c * 16 + i] = pack_bf16x2(silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]),
+                                           silu_f(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]));
+          }
+          tc_fence_before();
+          mbar_arrive(&s.tempty[acc]);
+          released = true;
+          if (valid) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int col = t.col0 + c * 32;
+              if (col < g.n_out) {
+                uint4* d4 = reinterpret_cast<uint4*>(out + grow * g.n_out + col);
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                  d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
+                                     pk[c * 16 + 4 * h + 3]);
               }
-              store32<OutT>(pre + grow * p.N + col, gf);
-              store32<OutT>(pre + grow * p.N + g.n_out + col, uf);
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tb + c * 32, gv);
+            tmem_ld32(tb + 128 + c * 32, uv);
+            tmem_ld_wait();
+            const int col = t.col0 + c * 32;
+            if (valid && col < g.n_out) {
+              float h[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] = silu_f(__uint_as_float(gv[i])) * __uint_as_float(uv[i]);
+              store32<OutT>(out + grow * g.n_out + col, h);
+              if (pre != nullptr) {
+                float gf[32], uf[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  gf[i] = __uint_as_float(gv[i]);
+                  uf[i] = __uint_as_float(uv[i]);
+                }
+                store32<OutT>(pre + grow * p.N + col, gf);
+                store32<OutT>(pre + grow * p.N + g.n_out + col, uf);
+              }
             }
           }
         }
-      } else if (kEpi == kEpiDswiglu) {
+      } else if constexpr (kEpi == kEpiDswiglu) {
         // the product is dH [M, K]; preact (G | U) is [M, 2K]; output [dG | dU]
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
@@ -556,23 +622,57 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
       } else {
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_ld_wait();
-          const int col = t.col0 + c * 32;
-          if (valid && col < g.n_out) {
-            float f[32];
+        if constexpr (sizeof(OutT) == 2) {
+          uint32_t pk[128];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            store32<OutT>(out + grow * g.n_out + col, f);
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
+          tc_fence_before();
+          mbar_arrive(&s.tempty[acc]);
+          released = true;
+          if (valid) {
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+              const int col = t.col0 + c * 32;
+              if (col < g.n_out) {
+                uint4* d4 = reinterpret_cast<uint4*>(out + grow * g.n_out + col);
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                  d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
+                                     pk[c * 16 + 4 * h + 3]);
+              }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
+            const int col = t.col0 + c * 32;
+            if (valid && col < g.n_out) {
+              float f[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+              store32<OutT>(out + grow * g.n_out + col, f);
+            }
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&s.tempty[acc]);
+      if (!released) {
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+      }
       if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
+    }
+    if constexpr (kMode == kWgrad) {
+      if (lane == 0) bulk_wait_all0();      // every dW store has landed
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -643,10 +743,11 @@ moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& 
                     int sms, const char* what, const CUtensorMap* tsa = nullptr,
                     const CUtensorMap* tsb = nullptr) {
   using C = Cfg<kKind>;
-  static_assert(C::kSmem <= 232448, "shared memory budget");
+  constexpr size_t smem = smem_for<kKind, kMode>();
+  static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
-  if (!ensure_smem(kern, C::kSmem)) return MOE_ERR_CUDA;
-  kern<<<sms, C::kThreads, C::kSmem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
+  if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
+  kern<<<sms, C::kThreads, smem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
   return check_launch(what);
 }
 
@@ -801,6 +902,11 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cptr, 2, cdims, box) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aptr, 2, adims, box))
     return MOE_ERR_INVALID_ARG;
+  // dB [E, N, K] is written by TMA from 64-column x 32-row staging boxes
+  CUtensorMap td;
+  const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+  const uint32_t dbox[3] = {64, 32, 1};
+  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox)) return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dB, nullptr, nullptr, dev_status};
-  return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
+  return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &td, nullptr);
 }

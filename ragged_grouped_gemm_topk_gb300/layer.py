@@ -98,16 +98,18 @@ class MoELayer:
                                    preact=self.gu, dev_status=self.dev_status)
             B.moe_grouped_gemm_fwd(self.h, self.W2, self.offsets, out=self.yp, dev_status=self.dev_status)
 
-    def combine(self):
-        B.moe_unpermute_combine(self.yp, self.dest_row, self.topk_w, out=self.y,
+    def combine(self, out=None):
+        y = self.y if out is None else out
+        B.moe_unpermute_combine(self.yp, self.dest_row, self.topk_w, out=y,
                                 dev_status=self.dev_status)
+        return y
 
-    def forward(self, x, logits):
+    def forward(self, x, logits, out=None):
+        """y [T, d] (written to ``out`` when given, else to the layer's own buffer)."""
         self.route(logits)
         self.dispatch(x)
         self.expert_mlp()
-        self.combine()
-        return self.y
+        return self.combine(out)
 
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
@@ -119,8 +121,9 @@ class MoELayer:
         return 7
 
     # ------------------------------------------------------------------ backward
-    def backward(self, dy, logits=None):
-        """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward)."""
+    def backward(self, dy, logits=None, dx_out=None):
+        """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward);
+        dx goes to ``dx_out`` when given."""
         if not self.training:
             raise RuntimeError("construct the layer with training=True")
         st = self.dev_status
@@ -131,7 +134,8 @@ class MoELayer:
         B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
         B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
         B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
-        B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=self.dx, dev_status=st)
+        dx = self.dx if dx_out is None else dx_out
+        B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=dx, dev_status=st)
         B.moe_route_topk_bwd(self.dw, self.topk_w, self.topk_idx, self.E, logits=logits,
                              renormalize=self.renormalize, out=self.dlogits, dev_status=st)
-        return self.dx, self.dlogits, self.dW1, self.dW2
+        return dx, self.dlogits, self.dW1, self.dW2
