@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--T", type=int, default=None, help="override tokens (small profiling cases)")
     ap.add_argument("--f", type=int, default=None, help="override expert hidden dim (profiling)")
+    ap.add_argument("--E", type=int, default=None, help="override expert count (profiling)")
     return ap.parse_args()
 
 
@@ -149,8 +150,9 @@ def run_ours(args, world, rank, local):
 
     pbuild.build()
     w = W.BY_NAME[args.workload]
-    if args.T or args.f:
-        w = w.scaled(T=args.T, f=args.f, name=f"{w.name}-T{args.T or w.T}-f{args.f or w.f}")
+    if args.T or args.f or args.E:
+        w = w.scaled(T=args.T, f=args.f, E=args.E,
+                     name=f"{w.name}-T{args.T or w.T}-f{args.f or w.f}-E{args.E or w.E}")
     dev = torch.device("cuda", torch.cuda.current_device())
     x = W.make_x(w, dev)
     W1, W2 = W.make_w1(w, dev), W.make_w2(w, dev)

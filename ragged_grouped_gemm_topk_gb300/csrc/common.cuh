@@ -148,6 +148,19 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+// Shared -> global contiguous copy of `bytes` (multiple of 16, both 16-byte aligned).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+// Allow at most 8 of this thread's bulk groups to be still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read8() {
+  asm volatile("cp.async.bulk.wait_group.read 8;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until this thread's committed bulk stores have finished reading shared memory.

@@ -49,8 +49,10 @@ constexpr int kAStage = kBM * kBKBytes;           // 16 KB
 constexpr int kBStage = kBN * kBKBytes;           // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;    // 48 KB
 constexpr int kBox = 8192;                        // one 64 x 64 bf16 MN-major box
-constexpr int kSfAStage = 2048;                   // MXFP8: raw A scales, 128 rows x 16 bytes
-constexpr int kSfBStage = 4096;                   // MXFP8: raw B scales, 256 rows x 16 bytes
+constexpr int kSfAStage = 2048;                   // MXFP8: raw A scale rows, 128 x 16 bytes
+constexpr int kSfBStage = 4096;                   // MXFP8: raw B scale rows, 256 x 16 bytes
+constexpr int kSfSlot = kSfAStage + kSfBStage;    // one raw scale slot (4 K-blocks' worth)
+constexpr int kAtoms = 2048;                      // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
@@ -72,40 +74,57 @@ struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t sfready[kStages];
+  uint64_t sfull[2];       // MXFP8 raw scale slots loaded
+  uint64_t sempty[2];      // MXFP8 raw scale slots read into registers
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
   int abort;
   int total_tiles;
-  int pad;
-  int prefix[kMaxE + 1];
+  int nnz;                 // wgrad: experts with rows
+  int prefix[kMaxE + 1];   // fwd/dgrad: tile prefix; wgrad: expert ids, non-empty then empty
   int offs[kMaxE + 1];
 };
 
-// Per-kind configuration.  kind 0 = tf32, 1 = bf16: 6 warps, double-buffered
-// accumulator (2 x 256 TMEM columns).  kind 2 = MXFP8: a 7th warp lays the E8M0
-// scales of each stage out as 512-byte scale atoms; the accumulator is single
-// (TMEM columns 0-255) because columns 256-383 hold one 32-column scale slot per
-// stage (A scales at +0, B scales at +16), every slot 32-column aligned.
+// Per-kind configuration.  kind 0 = tf32, 1 = bf16: 6 warps.  kind 2 = MXFP8: a
+// 7th warp lays the E8M0 scales of each stage out as 512-byte scale atoms, which
+// are copied to TMEM scale slots (see Tl for the TMEM layout).
 template <int kKind>
 struct Cfg {
   static constexpr bool kMx = kKind == 2;
-  static constexpr int kStage = kStageBytes + (kMx ? kSfAStage + kSfBStage : 0);
-  static constexpr int kThreads = kMx ? 224 : 192;
-  static constexpr int kAcc = kMx ? 1 : 2;
+  static constexpr int kStage = kStageBytes + (kMx ? kAtoms : 0);
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
-// wgrad keeps 3 pipeline stages and stages each epilogue warp's 32 x 256 bf16 dW
-// rows (16 KB) in shared memory for the TMA store.
+// wgrad keeps 3 pipeline stages, stages each epilogue warp's 32 x 256 bf16 dW rows
+// (16 KB) in shared memory for the TMA store, and holds an 8 KB zero buffer from
+// which a 7th warp bulk-stores the dW of experts without rows.
 constexpr int kWgStage = 16384;
+constexpr int kZeroBuf = 8192;
 template <int kKind, int kMode>
 constexpr int stages_for() { return kMode == kWgrad ? 3 : kStages; }
 template <int kKind, int kMode>
+constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
+template <int kKind, int kMode>
+constexpr size_t extra_smem() { return kMode == kWgrad ? 4 * kWgStage + kZeroBuf : (kKind == 2 ? 2 * kSfSlot : 0); }
+template <int kKind, int kMode>
 constexpr size_t smem_for() {
   return 1024 + static_cast<size_t>(stages_for<kKind, kMode>()) * Cfg<kKind>::kStage +
-         (kMode == kWgrad ? 4 * kWgStage : 0) + sizeof(Smem);
+         extra_smem<kKind, kMode>() + sizeof(Smem);
 }
+
+// Tile shape and TMEM layout per instantiation: 128 x 256 tiles everywhere.
+// tf32 / bf16 double-buffer the accumulator (2 x 256 TMEM columns).  MXFP8 keeps
+// one accumulator (columns 0-255) so that columns 256-383 can hold one 32-column
+// scale slot per pipeline stage (A scales at +0, B scales at +16).
+template <int kKind, int kMode, int kEpi>
+struct Tl {
+  static constexpr int BN = kBN;
+  static constexpr int kAcc = kKind == 2 ? 1 : 2;
+  static constexpr uint32_t kSfBase = 256u;
+  static constexpr uint32_t kSfStride = 32u;
+  static constexpr uint32_t kSfB = 16u;
+};
 
 // Block-scaled instruction descriptor (kind::mxf8f6f4): E4M3 A and B (format 0),
 // K-major, N >> 3 at bit 17, E8M0 scales (bit 23), M >> 4 at bit 24; the scale
@@ -141,7 +160,7 @@ struct Geo {
   int n_out;    // output columns (fwd/dgrad)
   int bn_out;   // output columns per tile
   int kb_fixed; // contraction blocks (fwd/dgrad)
-  __device__ Geo(const Params& p, int elem_bytes) {
+  __device__ Geo(const Params& p, int elem_bytes, int bn) {
     if (kMode == kWgrad) {
       nt = (p.N + kBM - 1) / kBM;
       nt2 = (p.K + kBN - 1) / kBN;
@@ -150,7 +169,7 @@ struct Geo {
       kb_fixed = 0;
     } else {
       n_out = kMode == kFwd ? (kEpi == kEpiSwiglu ? p.N / 2 : p.N) : p.K;
-      bn_out = kEpi == kEpiSwiglu ? kBN / 2 : kBN;
+      bn_out = kEpi == kEpiSwiglu ? bn / 2 : bn;
       nt = (n_out + bn_out - 1) / bn_out;
       nt2 = 1;
       kb_fixed = kMode == kFwd ? (p.K * elem_bytes + kBKBytes - 1) / kBKBytes
@@ -165,14 +184,22 @@ struct Geo {
 
 template <int kMode, int kEpi>
 __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>& g, int tile, int E, int M) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+  int lo = 0, local = 0;
+  if (kMode == kWgrad) {
+    // only experts with rows own tiles (in id order); empty ones are zero-filled
+    const int tpe = g.nt * g.nt2;
+    lo = s.prefix[tile / tpe];
+    local = tile % tpe;
+  } else {
+    int hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s.prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    local = tile - s.prefix[lo];
   }
   Tile t;
   t.e = lo;
-  const int local = tile - s.prefix[lo];
   const int beg = s.offs[lo];
   const int cnt = group_ok(beg, s.offs[lo + 1], M) ? s.offs[lo + 1] - beg : 0;
   if (kMode == kWgrad) {
@@ -199,6 +226,39 @@ template <int kMode, int kEpi>
 __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p) {
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s.offs[e] = p.offsets[e];
   __syncthreads();
+  if (kMode == kWgrad) {
+    // expert list: groups with rows in id order, then empty (or invalid) ones
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      int nh = 0;
+      for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        bool rows = false;
+        if (e < p.E) {
+          const bool ok = group_ok(s.offs[e], s.offs[e + 1], p.M);
+          if (!ok && blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
+          rows = ok && s.offs[e + 1] > s.offs[e];
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, rows);
+        if (rows) s.prefix[nh + __popc(m & ((1u << lane) - 1u))] = e;
+        nh += __popc(m);
+      }
+      int nl = 0;
+      for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        const bool none = e < p.E && !(group_ok(s.offs[e], s.offs[e + 1], p.M) && s.offs[e + 1] > s.offs[e]);
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, none);
+        if (none) s.prefix[nh + nl + __popc(m & ((1u << lane) - 1u))] = e;
+        nl += __popc(m);
+      }
+      if (lane == 0) {
+        s.nnz = nh;
+        s.total_tiles = nh * g.nt * g.nt2;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     int cnt = s.offs[e + 1] - s.offs[e];
     if (!group_ok(s.offs[e], s.offs[e + 1], p.M)) {
@@ -273,23 +333,29 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 }
 
 template <int kKind, int kMode, int kEpi, typename OutT>
-__global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
+__global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
   using C = Cfg<kKind>;
   constexpr int NS = stages_for<kKind, kMode>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& s = *reinterpret_cast<Smem*>(tiles + NS * C::kStage + (kMode == kWgrad ? 4 * kWgStage : 0));
+  Smem& s = *reinterpret_cast<Smem*>(tiles + NS * C::kStage + extra_smem<kKind, kMode>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int eb = C::kEb;
-  const Geo<kMode, kEpi> g(p, eb);
+  using TL = Tl<kKind, kMode, kEpi>;
+  constexpr int BN = TL::BN;
+  const Geo<kMode, kEpi> g(p, eb, BN);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.empty[i], 1);
       mbar_init(&s.sfready[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.sfull[i], 1);
+      mbar_init(&s.sempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
@@ -319,16 +385,34 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, ss = 0;
+      uint32_t phase = 0, ss_phase = 0;
       for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
         const Tile t = tile_info(s, g, tile, p.E, p.M);
         for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (C::kMx && kMode == kFwd && kb % 4 == 0) {
+            // raw E8M0 rows, 16 bytes per row = the scales of 4 K-blocks, into slot ss
+            if (!mbar_wait(&s.sempty[ss], ss_phase ^ 1u, p.status, &s.abort)) break;
+            uint8_t* rsa = tiles + kStages * C::kStage + ss * kSfSlot;
+            uint8_t* rsb = rsa + kSfAStage;
+            const int sx = 16 * (kb / 4);
+            const int brow = t.e * p.N;
+            mbar_arrive_expect_tx(&s.sfull[ss], kSfSlot);
+            tma_load_2d(rsa, &tmSA, &s.sfull[ss], sx, t.row0);
+            if (kEpi == kEpiSwiglu) {
+              tma_load_2d(rsb, &tmSB, &s.sfull[ss], sx, brow + t.col0);
+              tma_load_2d(rsb + kSfBStage / 2, &tmSB, &s.sfull[ss], sx, brow + g.n_out + t.col0);
+            } else {
+              tma_load_2d(rsb, &tmSB, &s.sfull[ss], sx, brow + t.col0);
+              tma_load_2d(rsb + kSfBStage / 2, &tmSB, &s.sfull[ss], sx, brow + t.col0 + kBM);
+            }
+            if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
+          }
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.status, &s.abort)) break;
           uint8_t* sa = tiles + stage * C::kStage;
           uint8_t* sb = sa + kAStage;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, C::kStage);
+          mbar_arrive_expect_tx(bar, kStageBytes);
           if (kMode == kFwd) {
             const int kx = kb * (kBKBytes / eb);
             tma_load_2d(sa, &tmA, bar, kx, t.row0);
@@ -337,22 +421,6 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
               tma_load_3d(sb + kBStage / 2, &tmB, bar, kx, g.n_out + t.col0, t.e);
             } else {
               tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
-            }
-            if (C::kMx) {
-              // raw E8M0 rows: 16 scale bytes (4 stages' worth) per row; the
-              // stage's 4 bytes sit at 4 * (kb % 4) inside each row
-              uint8_t* ssa = sa + kStageBytes;
-              uint8_t* ssb = ssa + kSfAStage;
-              const int sx = 16 * (kb / 4);
-              const int brow = t.e * p.N;
-              tma_load_2d(ssa, &tmSA, bar, sx, t.row0);
-              if (kEpi == kEpiSwiglu) {
-                tma_load_2d(ssb, &tmSB, bar, sx, brow + t.col0);
-                tma_load_2d(ssb + kSfBStage / 2, &tmSB, bar, sx, brow + g.n_out + t.col0);
-              } else {
-                tma_load_2d(ssb, &tmSB, bar, sx, brow + t.col0);
-                tma_load_2d(ssb + kSfBStage / 2, &tmSB, bar, sx, brow + t.col0 + kBM);
-              }
             }
           } else if (kMode == kDgrad) {
             const int nx = kb * kMnRows;                  // contraction index (N of B)
@@ -372,7 +440,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, kBN)
+    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, BN)
                                       : make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -380,7 +448,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
       const Tile t = tile_info(s, g, tile, p.E, p.M);
       if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.status, &s.abort)) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kBN);
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (C::kMx) {
           if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
@@ -388,19 +456,19 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
           if (lane == 0) {
             const uint32_t sa = smem_u32(tiles + stage * C::kStage);
             const uint32_t sb = sa + kAStage;
-            const uint32_t ssa = sa + kStageBytes;
-            const uint32_t ssb = ssa + kSfAStage;
-            // scale slot of this stage: A atom at +0 (4 columns), B atoms at +16, +20
-            const uint32_t slot = tmem + 256u + 32u * static_cast<uint32_t>(stage);
+            const uint32_t ssa = sa + kStageBytes;       // this stage's scale atoms
+            const uint32_t ssb = ssa + 512;
+            // scale slot of this stage: A atom at +0 (4 columns), B atoms at +kSfB, +kSfB+4
+            const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
             tc_cp_32x128b_warpx4(slot, make_sdesc(ssa, 0, 128, 0));
-            tc_cp_32x128b_warpx4(slot + 16, make_sdesc(ssb, 0, 128, 0));
-            tc_cp_32x128b_warpx4(slot + 20, make_sdesc(ssb + 512, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + TL::kSfB, make_sdesc(ssb, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + TL::kSfB + 4, make_sdesc(ssb + 512, 0, 128, 0));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
               const uint64_t bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
               const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
-              tc_mma_mxf8(d_tmem, ad, bd, id, slot, slot + 16, (kb | kk) != 0 ? 1u : 0u);
+              tc_mma_mxf8(d_tmem, ad, bd, id, slot, slot + TL::kSfB, (kb | kk) != 0 ? 1u : 0u);
             }
             tc_commit(&s.empty[stage]);
           }
@@ -447,38 +515,70 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
       }
       if (lane == 0) tc_commit(&s.tfull[acc]);
       __syncwarp();
-      if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
   } else if (C::kMx && warp == 6) {
     // ------------------------------------------------------------------ MXFP8 scale layout
-    // Re-lay each stage's raw scale rows (row r: 16 bytes, the stage's 4 at byte
-    // `off`) as 512-byte atoms in place: atom byte (m % 32) * 16 + (m / 32) * 4 + kb.
-    // Lane L writes bytes [16L, 16L + 16) of each atom, which only lane L reads
-    // (raw row L, and raw row 32 + L for the second B atom), after its reads.
-    int stage = 0;
-    uint32_t phase = 0;
+    // Every 4 K-blocks: take the raw scale rows of the slot (row r: 16 bytes, the
+    // scales of 4 K-blocks) into registers and free the slot.  Every K-block: write
+    // its 512-byte atoms (byte (m % 32) * 16 + (m / 32) * 4 + j for row m of 128 and
+    // 32-element block j of the K-block) into the stage's atom area, once the stage's
+    // previous atoms have been consumed (the stage is full again).
+    int stage = 0, ss = 0;
+    uint32_t phase = 0, ss_phase = 0;
+    uint4 ra[4], rb[8];
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
       const Tile t = tile_info(s, g, tile, p.E, p.M);
       for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (kb % 4 == 0) {
+          if (!mbar_wait(&s.sfull[ss], ss_phase, p.status, &s.abort)) break;
+          const uint8_t* rsa = tiles + kStages * C::kStage + ss * kSfSlot;
+          const uint8_t* rsb = rsa + kSfAStage;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ra[j] = *reinterpret_cast<const uint4*>(rsa + (lane + 32 * j) * 16);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) rb[j] = *reinterpret_cast<const uint4*>(rsb + (lane + 32 * j) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.sempty[ss]);
+          if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
+        }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
-        uint8_t* ssa = tiles + stage * C::kStage + kStageBytes;
-        uint8_t* ssb = ssa + kSfAStage;
-        const int off = 4 * (kb % 4);
-        uint32_t va[4], vb[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) va[j] = *reinterpret_cast<const uint32_t*>(ssa + (lane + 32 * j) * 16 + off);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) vb[j] = *reinterpret_cast<const uint32_t*>(ssb + (lane + 32 * j) * 16 + off);
-        __syncwarp();
-        *reinterpret_cast<uint4*>(ssa + lane * 16) = make_uint4(va[0], va[1], va[2], va[3]);
-        *reinterpret_cast<uint4*>(ssb + lane * 16) = make_uint4(vb[0], vb[1], vb[2], vb[3]);
-        *reinterpret_cast<uint4*>(ssb + 512 + lane * 16) = make_uint4(vb[4], vb[5], vb[6], vb[7]);
+        uint8_t* at = tiles + stage * C::kStage + kStageBytes;
+        const int w = kb % 4;
+        auto word = [w](const uint4& v) { return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w)); };
+        *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(word(ra[0]), word(ra[1]), word(ra[2]), word(ra[3]));
+        *reinterpret_cast<uint4*>(at + 512 + lane * 16) = make_uint4(word(rb[0]), word(rb[1]), word(rb[2]), word(rb[3]));
+        *reinterpret_cast<uint4*>(at + 1024 + lane * 16) = make_uint4(word(rb[4]), word(rb[5]), word(rb[6]), word(rb[7]));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s.sfready[stage]);
         if (++stage == NS) { stage = 0; phase ^= 1u; }
       }
     }
+  } else if (kMode == kWgrad && warp == 6) {
+    // ------------------------------------------------------------------ wgrad zero fill
+    // Experts without rows own no tiles; their dW (exact zeros) is written here with
+    // bulk stores from a zeroed shared buffer, alongside the MMA work.  An expert's
+    // dW is N*K*2 bytes, a multiple of 2048 since N and K are multiples of 32.
+    uint8_t* zb = tiles + NS * C::kStage + 4 * kWgStage;
+    for (int i = lane; i < kZeroBuf / 16; i += 32) reinterpret_cast<uint4*>(zb)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const size_t per = static_cast<size_t>(p.N) * p.K * 2;
+      const uint32_t chunk = per % kZeroBuf == 0 ? kZeroBuf : 2048u;
+      const size_t cpe = per / chunk;
+      const size_t chunks = static_cast<size_t>(p.E - s.nnz) * cpe;
+      uint8_t* outb = static_cast<uint8_t*>(p.out);
+      for (size_t c = blockIdx.x; c < chunks && !s.abort; c += gridDim.x) {
+        const int e = s.prefix[s.nnz + static_cast<int>(c / cpe)];
+        bulk_store(outb + static_cast<size_t>(e) * per + (c % cpe) * chunk, zb, chunk);
+        bulk_commit();
+        bulk_wait_read8();
+      }
+      bulk_wait_all0();
+    }
+    __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue
     // The accumulator is released (tempty) as soon as its last TMEM read is done;
@@ -493,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
       const Tile t = tile_info(s, g, tile, p.E, p.M);
       if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       bool released = false;
       if constexpr (kMode == kWgrad) {
         // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns, staged as four
@@ -623,9 +723,9 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
         if constexpr (sizeof(OutT) == 2) {
-          uint32_t pk[128];
+          uint32_t pk[BN / 2];
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
+          for (int c = 0; c < BN / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
@@ -637,7 +737,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
           released = true;
           if (valid) {
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
               const int col = t.col0 + c * 32;
               if (col < g.n_out) {
                 uint4* d4 = reinterpret_cast<uint4*>(out + grow * g.n_out + col);
@@ -650,7 +750,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
           }
         } else {
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
+          for (int c = 0; c < BN / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
@@ -668,7 +768,7 @@ __global__ void __launch_bounds__(Cfg<kKind>::kThreads, 1) grouped_gemm_kernel(
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
       }
-      if (++acc == C::kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
     if constexpr (kMode == kWgrad) {
       if (lane == 0) bulk_wait_all0();      // every dW store has landed
@@ -747,7 +847,7 @@ moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& 
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  kern<<<sms, C::kThreads, smem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
+  kern<<<sms, threads_for<kKind, kMode>(), smem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
   return check_launch(what);
 }
 
