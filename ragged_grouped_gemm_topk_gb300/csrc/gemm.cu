@@ -96,13 +96,15 @@ struct Cfg {
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
-// wgrad keeps 3 pipeline stages, stages each epilogue warp's 32 x 256 bf16 dW rows
-// (16 KB) in shared memory for the TMA store, and holds an 8 KB zero buffer from
-// which a 7th warp bulk-stores the dW of experts without rows.
-constexpr int kWgStage = 16384;
+// wgrad: each epilogue warp stages kWgBoxes 64-column boxes of its 32 dW rows
+// (4 KB each) for the TMA store, and an 8 KB zero buffer feeds a 7th warp that
+// bulk-stores the dW of experts without rows; with one box per warp the 4-stage
+// operand ring still fits.
+constexpr int kWgBoxes = 1;
+constexpr int kWgStage = 4096 * kWgBoxes;
 constexpr int kZeroBuf = 8192;
 template <int kKind, int kMode>
-constexpr int stages_for() { return kMode == kWgrad ? 3 : kStages; }
+constexpr int stages_for() { return (kMode == kWgrad && kWgBoxes > 1) ? 3 : kStages; }
 template <int kKind, int kMode>
 constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
@@ -596,42 +598,42 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       bool released = false;
       if constexpr (kMode == kWgrad) {
-        // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns, staged as four
-        // 64-column, 128-byte-swizzled boxes and written by TMA (clipped at N and K).
+        // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns, written by TMA (clipped
+        // at N and K) in rounds of kWgBoxes 64-column, 128-byte-swizzled boxes staged
+        // in this warp's shared buffer.
         uint8_t* stg = tiles + NS * C::kStage + q * kWgStage;
-        if (lane == 0) bulk_wait_read0();   // the previous tile's stores have read stg
-        __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t pk[16];
-          if (t.rows > 0) {
-            uint32_t v[32];
-            tmem_ld32(tb + c * 32, v);
+        for (int round = 0; round < 4 / kWgBoxes; ++round) {
+          if (lane == 0) bulk_wait_read0();   // the previous round's stores have read stg
+          __syncwarp();
+#pragma unroll 1
+          for (int cc = 0; cc < 2 * kWgBoxes; ++cc) {
+            uint32_t v[32], pk[16];
+            tmem_ld32(tb + (round * 2 * kWgBoxes + cc) * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          } else {
+            uint8_t* box = stg + (cc >> 1) * 4096 + lane * 128;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+            for (int h = 0; h < 4; ++h) {
+              const int chunk = (cc & 1) * 4 + h;
+              *reinterpret_cast<uint4*>(box + ((chunk ^ (lane & 7)) * 16)) =
+                  make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+            }
           }
-          uint8_t* box = stg + (c >> 1) * 4096 + lane * 128;
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int chunk = (c & 1) * 4 + h;
-            *reinterpret_cast<uint4*>(box + ((chunk ^ (lane & 7)) * 16)) =
-                make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+          if (round == 4 / kWgBoxes - 1) {
+            tc_fence_before();
+            mbar_arrive(&s.tempty[acc]);
+            released = true;
           }
-        }
-        tc_fence_before();
-        mbar_arrive(&s.tempty[acc]);
-        released = true;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_store_3d(&tmSA, stg + j * 4096, t.col0 + 64 * j, t.n0 + 32 * q, t.e);
-          bulk_commit();
+            for (int j = 0; j < kWgBoxes; ++j)
+              tma_store_3d(&tmSA, stg + j * 4096, t.col0 + 64 * (round * kWgBoxes + j), t.n0 + 32 * q, t.e);
+            bulk_commit();
+          }
         }
       } else if constexpr (kEpi == kEpiSwiglu) {
         const bool valid = r < t.rows;
