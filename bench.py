@@ -142,6 +142,25 @@ def stage_bytes(w):
     return permute, combine
 
 
+def gemm1_traffic(workload):
+    """DRAM bytes per GEMM1 launch from the committed ncu summary
+    (profiles/gemm1_traffic_<workload>.txt), or None when there is none or the GEMM
+    source has changed since the counters were taken."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"gemm1_traffic_{workload}.txt")
+    if not os.path.exists(prof):
+        return None
+    fields = dict(l.split(None, 1) for l in open(prof).read().splitlines()
+                  if l.strip() and not l.startswith("#") and len(l.split(None, 1)) == 2)
+    src = os.path.join(ROOT, "ragged_grouped_gemm_topk_gb300", "csrc", "gemm.cu")
+    if fields.get("gemm_cu_sha256", "").strip() != hashlib.sha256(open(src, "rb").read()).hexdigest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 def run_ours(args, world, rank, local):
     import torch
     import ragged_grouped_gemm_topk_gb300 as pkg
@@ -235,10 +254,7 @@ def run_ours(args, world, rank, local):
     dtype_peak = pk["bf16_sus"] * (2.0 if w.dtype == "mxfp8" else (0.5 if w.dtype == "f32" else 1.0))
     perm_b, comb_b = stage_bytes(w)
     launches = layer.launches_per_forward() + (layer.launches_per_backward() if w.backward else 0)
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", f"gemm1_traffic_{w.name}.json")
-    if os.path.exists(prof):
-        traffic = json.load(open(prof)).get("dram_bytes_per_launch")
+    traffic = gemm1_traffic(w.name)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
