@@ -77,6 +77,7 @@ template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint8_t* __restrict__ yp, int T, int d, int k, const int32_t* __restrict__ dest_row,
     const float* __restrict__ topk_w, uint8_t* __restrict__ y, int32_t* status) {
+  pdl_begin();
   constexpr int N = Elt<Tin>::kN;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -135,6 +136,83 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
   }
 }
 
+// Same sum for a compile-time k in {1, 2, 4, 8}: a lane gathers U chunks of each
+// of the k source rows before it sums any of them, so that U*k = 8 or 16 16-byte
+// loads are in flight per lane (the runtime-k loop above has only k of them, too
+// few to cover HBM latency at k = 2).  Slot order and fp32 fmaf as above.
+constexpr int kFixedSlice = 256;   // 16-byte chunks per work item
+
+template <typename Tin, typename Tout, int K>
+__global__ void __launch_bounds__(kThreads) combine_fixed_kernel(
+    const uint8_t* __restrict__ yp, int T, int d, const int32_t* __restrict__ dest_row,
+    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int32_t* status) {
+  pdl_begin();
+  constexpr int N = Elt<Tin>::kN;
+  constexpr int U = (16 / K) < 8 ? (16 / K) : 8;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int M = T * K;
+  const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
+  const size_t out_row = static_cast<size_t>(d) * sizeof(Tout);
+  const int n16 = static_cast<int>(in_row / 16);
+  const int nslice = (n16 + kFixedSlice - 1) / kFixedSlice;
+  const long long tasks = static_cast<long long>(T) * nslice;
+  for (long long task = static_cast<long long>(blockIdx.x) * wpb + (threadIdx.x >> 5); task < tasks;
+       task += static_cast<long long>(gridDim.x) * wpb) {
+    const int t = static_cast<int>(task / nslice);
+    const int slice = static_cast<int>(task % nslice);
+    int src = -1;
+    float w = 0.f;
+    if (lane < K) {
+      const size_t p = static_cast<size_t>(t) * K + lane;
+      src = dest_row[p];
+      w = topk_w ? topk_w[p] : 1.f;
+      if (src < 0 || src >= M) {
+        if (slice == 0) flag_error(status, MOE_DEV_BAD_INDEX);
+        src = -1;
+      }
+    }
+    const Vec16* rows[K];
+    float wj[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const int sj = __shfl_sync(kFull, src, j);
+      wj[j] = __shfl_sync(kFull, w, j);
+      rows[j] = sj >= 0 ? reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * in_row) : nullptr;
+    }
+    const int c_end = min(n16, (slice + 1) * kFixedSlice);
+    for (int base = slice * kFixedSlice; base < c_end; base += 32 * U) {
+      Vec16 v[U][K];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int c = base + 32 * i + lane;
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+          if (c < c_end && rows[j] != nullptr) v[i][j] = rows[j][c];
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int c = base + 32 * i + lane;
+        if (c < c_end) {
+          float acc[N];
+#pragma unroll
+          for (int e = 0; e < N; ++e) acc[e] = 0.f;
+#pragma unroll
+          for (int j = 0; j < K; ++j) {
+            if (rows[j] != nullptr) {
+              float f[N];
+              Elt<Tin>::unpack(v[i][j], f);
+#pragma unroll
+              for (int e = 0; e < N; ++e) acc[e] = fmaf(wj[j], f[e], acc[e]);
+            }
+          }
+          store_out<Tout, N>(y + static_cast<size_t>(t) * out_row + static_cast<size_t>(c) * N * sizeof(Tout), acc);
+        }
+      }
+    }
+  }
+}
+
 // One warp per (token, slot): dyp[dest_row[t,j]] = w[t,j] dy[t] and
 // dw[t,j] = <dy[t], yp[dest_row[t,j]]> (warp reduction).  dy[t] is re-read by the
 // token's k warps, from L2.
@@ -143,6 +221,7 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
     const uint8_t* __restrict__ dy, const uint8_t* __restrict__ yp, int T, int d, int k,
     const int32_t* __restrict__ dest_row, const float* __restrict__ topk_w,
     uint8_t* __restrict__ dyp, float* __restrict__ dw, int32_t* status) {
+  pdl_begin();
   constexpr int N = Elt<Tin>::kN;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -187,6 +266,17 @@ int grid_for(long long tasks, int sms) {
   return static_cast<int>(g < 1 ? 1 : (g < cap ? g : cap));
 }
 
+template <typename Tin, typename Tout>
+void launch_fixed(int k, int grid, cudaStream_t stream, const uint8_t* a, int T, int d, const int32_t* dest_row,
+                  const float* topk_w, uint8_t* o, int32_t* dev_status) {
+  switch (k) {
+    case 1: launch_pdl(combine_fixed_kernel<Tin, Tout, 1>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
+    case 2: launch_pdl(combine_fixed_kernel<Tin, Tout, 2>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
+    case 4: launch_pdl(combine_fixed_kernel<Tin, Tout, 4>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
+    default: launch_pdl(combine_fixed_kernel<Tin, Tout, 8>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -213,17 +303,25 @@ extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype,
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (T == 0 || d == 0) return MOE_OK;
   const long long n16 = static_cast<long long>(d) * (dtype == MOE_BF16 ? 2 : 4) / 16;
-  const int grid = grid_for(static_cast<long long>(T) * ((n16 + kSliceChunks - 1) / kSliceChunks), sms);
   const uint8_t* a = static_cast<const uint8_t*>(yp);
   uint8_t* o = static_cast<uint8_t*>(y);
+  if (k == 1 || k == 2 || k == 4 || k == 8) {
+    const int grid = grid_for(static_cast<long long>(T) * ((n16 + kFixedSlice - 1) / kFixedSlice), sms);
+    if (dtype == MOE_BF16 && y_dtype == MOE_BF16) launch_fixed<uint16_t, uint16_t>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
+    else if (dtype == MOE_BF16) launch_fixed<uint16_t, float>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
+    else if (y_dtype == MOE_BF16) launch_fixed<float, uint16_t>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
+    else launch_fixed<float, float>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
+    return check_launch("moe_unpermute_combine");
+  }
+  const int grid = grid_for(static_cast<long long>(T) * ((n16 + kSliceChunks - 1) / kSliceChunks), sms);
   if (dtype == MOE_BF16 && y_dtype == MOE_BF16)
-    combine_kernel<uint16_t, uint16_t><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<uint16_t, uint16_t>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
   else if (dtype == MOE_BF16)
-    combine_kernel<uint16_t, float><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<uint16_t, float>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
   else if (y_dtype == MOE_BF16)
-    combine_kernel<float, uint16_t><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<float, uint16_t>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
   else
-    combine_kernel<float, float><<<grid, kThreads, 0, stream>>>(a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<float, float>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
   return check_launch("moe_unpermute_combine");
 }
 
@@ -253,8 +351,8 @@ extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp
   const uint8_t* b = static_cast<const uint8_t*>(yp);
   uint8_t* o = static_cast<uint8_t*>(dyp);
   if (dtype == MOE_BF16)
-    combine_bwd_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
+    launch_pdl(combine_bwd_kernel<uint16_t>, grid, kThreads, 0, stream, a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
   else
-    combine_bwd_kernel<float><<<grid, kThreads, 0, stream>>>(a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
+    launch_pdl(combine_bwd_kernel<float>, grid, kThreads, 0, stream, a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
   return check_launch("moe_unpermute_combine_bwd");
 }

@@ -33,6 +33,7 @@ constexpr int kScatterThreads = 256;
 __global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ local_rank,
     int32_t* __restrict__ block_hist, int32_t* status) {
+  pdl_begin();
   extern __shared__ uint32_t sm[];
   uint32_t* mask = sm;                                      // [8][E]
   int32_t* wbase = reinterpret_cast<int32_t*>(sm + 8 * E);  // [8][E]
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
                                                             int32_t* __restrict__ block_hist,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* status) {
+  pdl_begin();
   __shared__ int warp_sum[32];
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
   const int c = e < E ? counts[e] : 0;
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     const int32_t* local_rank, const int32_t* __restrict__ block_base,
     int32_t* dest_row, int32_t* __restrict__ src_pair, uint8_t* __restrict__ xp,
     uint8_t* __restrict__ xp_scales, int32_t* status) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
@@ -262,6 +265,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
     const uint8_t* __restrict__ in, int rows, int K, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   constexpr int EPL = Mx<Tin>::kEpl;
@@ -321,10 +325,10 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
     }
   }
   if (nblk > 0) {
-    permute_rank_kernel<<<nblk, kRankThreads, rank_smem, stream>>>(topk_idx, T, k, E, dest_row,
+    launch_pdl(permute_rank_kernel, nblk, kRankThreads, rank_smem, stream, topk_idx, T, k, E, dest_row,
                                                                    hist, dev_status);
   }
-  permute_scan_kernel<<<1, 1024, 0, stream>>>(counts, E, nblk, T * k, hist, offsets, dev_status);
+  launch_pdl(permute_scan_kernel, 1, 1024, 0, stream, counts, E, nblk, T * k, hist, offsets, dev_status);
   if (T == 0) return check_launch("moe_permute");
   const int grid = scatter_grid(T, sms);
   const uint8_t* xb = static_cast<const uint8_t*>(x);
@@ -333,16 +337,16 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
   // same element with the pair's final row (read and write by the same thread).
   if (xp_dtype == MOE_E4M3) {
     if (x_dtype == MOE_BF16)
-      permute_scatter_kernel<uint16_t, true><<<grid, kScatterThreads, 0, stream>>>(
+      launch_pdl(permute_scatter_kernel<uint16_t, true>, grid, kScatterThreads, 0, stream, 
           xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
     else
-      permute_scatter_kernel<float, true><<<grid, kScatterThreads, 0, stream>>>(
+      launch_pdl(permute_scatter_kernel<float, true>, grid, kScatterThreads, 0, stream, 
           xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
   } else if (x_dtype == MOE_BF16) {
-    permute_scatter_kernel<uint16_t, false><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(permute_scatter_kernel<uint16_t, false>, grid, kScatterThreads, 0, stream, 
         xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
   } else {
-    permute_scatter_kernel<float, false><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(permute_scatter_kernel<float, false>, grid, kScatterThreads, 0, stream, 
         xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
   }
   return check_launch("moe_permute");
@@ -443,10 +447,10 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
   if (rows == 0 || K == 0) return MOE_OK;
   const int grid = scatter_grid(rows, sms);
   if (in_dtype == MOE_BF16)
-    quantize_rowwise_kernel<uint16_t><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(quantize_rowwise_kernel<uint16_t>, grid, kScatterThreads, 0, stream, 
         static_cast<const uint8_t*>(in), rows, K, codes, scales);
   else
-    quantize_rowwise_kernel<float><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(quantize_rowwise_kernel<float>, grid, kScatterThreads, 0, stream, 
         static_cast<const uint8_t*>(in), rows, K, codes, scales);
   return check_launch("moe_quantize_mxfp8_grouped");
 }

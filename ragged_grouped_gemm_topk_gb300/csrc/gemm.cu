@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     tmem_relinquish();
     tc_fence_before();
   }
+  pdl_begin();             // the prologue above overlaps the preceding kernel
   build_tiles(s, g, p);   // contains __syncthreads
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
@@ -849,7 +850,7 @@ moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& 
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  kern<<<sms, threads_for<kKind, kMode>(), smem, stream>>>(ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
+  launch_pdl(kern, sms, threads_for<kKind, kMode>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
   return check_launch(what);
 }
 

@@ -18,6 +18,7 @@ constexpr int kRouteThreads = 256;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __global__ void zero_i32_kernel(int32_t* p, int n) {
+  pdl_begin();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
 }
 
@@ -34,6 +35,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renormalize,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ counts,
     int32_t* status) {
+  pdl_begin();
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_bwd_kernel(
     const float* __restrict__ dw, const float* __restrict__ topk_w,
     const int32_t* __restrict__ topk_idx, const float* __restrict__ logits, int T, int E, int k,
     int renormalize, float* __restrict__ dlogits, int32_t* status) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
@@ -169,7 +172,7 @@ void launch_route(const float* logits, int T, int E, int k, int renorm, int32_t*
   int grid = (T + wpb - 1) / wpb;
   grid = grid < sms * 4 ? grid : sms * 4;
   if (grid < 1) grid = 1;
-  route_topk_kernel<V><<<grid, kRouteThreads, E * sizeof(int), stream>>>(logits, T, E, k, renorm,
+  launch_pdl(route_topk_kernel<V>, grid, kRouteThreads, E * sizeof(int), stream, logits, T, E, k, renorm,
                                                                           idx, w, counts, status);
 }
 
@@ -192,7 +195,7 @@ extern "C" moe_status_t moe_route_topk(const float* logits, int T, int E, int k,
   }
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
-  zero_i32_kernel<<<(E + 255) / 256, 256, 0, stream>>>(counts, E);
+  launch_pdl(zero_i32_kernel, (E + 255) / 256, 256, 0, stream, counts, E);
   if (T > 0) {
     const int V = (E + 31) / 32;
     if (V <= 1) launch_route<1>(logits, T, E, k, renormalize, topk_idx, topk_w, counts, dev_status, stream, sms);
@@ -223,7 +226,7 @@ extern "C" moe_status_t moe_route_topk_bwd(const float* dw, const float* topk_w,
   const int wpb = kRouteThreads / 32;
   int grid = (T + wpb - 1) / wpb;
   grid = grid < sms * 8 ? grid : sms * 8;
-  route_topk_bwd_kernel<<<grid, kRouteThreads, 0, stream>>>(dw, topk_w, topk_idx, logits, T, E, k,
+  launch_pdl(route_topk_bwd_kernel, grid, kRouteThreads, 0, stream, dw, topk_w, topk_idx, logits, T, E, k,
                                                            renormalize, dlogits, dev_status);
   return check_launch("moe_route_topk_bwd");
 }

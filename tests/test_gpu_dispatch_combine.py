@@ -186,7 +186,31 @@ def test_combine(w):
     assert rel_l2(got, want) < 4e-3
 
 
-@pytest.mark.parametrize("k", [1, 2, 8])
+@pytest.mark.parametrize("k", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("d", [8, 2056])
+@pytest.mark.parametrize("dt_in,dt_out", [(torch.bfloat16, torch.bfloat16), (torch.bfloat16, torch.float32),
+                                          (torch.float32, torch.bfloat16), (torch.float32, torch.float32)],
+                         ids=["bf16-bf16", "bf16-f32", "f32-bf16", "f32-f32"])
+def test_combine_each_k_width_and_dtype(k, d, dt_in, dt_out):
+    """Every specialised k (1, 2, 4, 8) and the general loop (k=3), a one-chunk row
+    (d=8) and a row one chunk past a work item (d=2056 bf16), all dtype pairs."""
+    need_gpu()
+    T = 97
+    rng = np.random.default_rng(1000 + 10 * k + d)
+    dest = rng.permutation(T * k).reshape(T, k).astype(np.int64)
+    wts = rng.uniform(0.05, 1.0, size=(T, k))
+    yp = W.make_matrix(T * k, d, seed=79, dtype=dt_in, device="cuda")
+    got = f64(moe_gpu.moe_unpermute_combine(yp, torch.from_numpy(dest).to(torch.int32).cuda(),
+                                            torch.from_numpy(wts).float().cuda(), out_dtype=dt_out))
+    w32 = wts.astype(np.float32).astype(np.float64)
+    yp64 = f64(yp)
+    want = om.combine(yp64, dest, w32)
+    mag = _combine_bound(yp64, dest, w32) * 2.0 ** 8
+    ulp = 2.0 ** -8 if dt_out == torch.bfloat16 else 2.0 ** -23
+    assert (np.abs(got - want) <= (ulp + k * 2.0 ** -24) * mag + 1e-30).all()
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
 def test_combine_of_permute_identity_bit_exact(k):
     """k=1 with unit weights, or w = 1/k: combine(permute(x)) == x exactly."""
     need_gpu()
