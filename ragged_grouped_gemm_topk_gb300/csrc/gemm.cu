@@ -14,8 +14,10 @@
 //              commits each stage back to the producer and each tile to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (TMEM lane = tile row, one
 //              row per thread), the fused epilogue, release of the accumulator,
-//              then 16-byte stores masked at the group's last row and the matrix
-//              edge (wgrad: a shared-memory staging tile written by TMA store).
+//              then the stores: forward bf16 output by TMA store from a per-warp
+//              shared staging box (a warp whose rows cross the group's end stores
+//              its valid rows directly), wgrad likewise per 64-column dW box, other
+//              outputs by 16-byte stores masked at the group's end and the edge.
 // Tiles are enumerated on the device from `offsets`, so the host never learns the
 // per-expert sizes:
 //   forward / dgrad  expert e owns ceil(count_e / 128) row tiles x the column
@@ -52,7 +54,14 @@ constexpr int kBox = 8192;                        // one 64 x 64 bf16 MN-major b
 constexpr int kSfAStage = 2048;                   // MXFP8: raw A scale rows, 128 x 16 bytes
 constexpr int kSfBStage = 4096;                   // MXFP8: raw B scale rows, 256 x 16 bytes
 constexpr int kSfSlot = kSfAStage + kSfBStage;    // one raw scale slot (4 K-blocks' worth)
-constexpr int kAtoms = 2048;                      // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
+constexpr int kAtomBytes = 1536;                  // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
+constexpr int kEpiBox = 2048;                     // forward epilogue staging: 32 x 32 bf16 per warp
+// Forward kernels' extra shared memory (after the operand stages): the epilogue
+// staging boxes (1 KB aligned for the 64-byte swizzle), then for MXFP8 the scale
+// atoms of every stage and the two raw scale-row slots.
+constexpr int kEpiOff = 0;
+constexpr int kAtomOff = kEpiOff + 4 * kEpiBox;
+constexpr int kRawOff = kAtomOff + kStages * kAtomBytes;
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
@@ -83,7 +92,6 @@ struct Smem {
   int total_tiles;
   int nnz;                 // wgrad: experts with rows
   int prefix[kMaxE + 1];   // fwd/dgrad: tile prefix; wgrad: expert ids, non-empty then empty
-  int offs[kMaxE + 1];
 };
 
 // Per-kind configuration.  kind 0 = tf32, 1 = bf16: 6 warps.  kind 2 = MXFP8: a
@@ -92,23 +100,25 @@ struct Smem {
 template <int kKind>
 struct Cfg {
   static constexpr bool kMx = kKind == 2;
-  static constexpr int kStage = kStageBytes + (kMx ? kAtoms : 0);
+  static constexpr int kStage = kStageBytes;
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
 // wgrad: each epilogue warp stages kWgBoxes 64-column boxes of its 32 dW rows
-// (4 KB each) for the TMA store, and an 8 KB zero buffer feeds a 7th warp that
-// bulk-stores the dW of experts without rows; with one box per warp the 4-stage
-// operand ring still fits.
+// (4 KB each) for the TMA store (with one box per warp the 4-stage operand ring
+// still fits), and a 7th warp writes the dW of experts without rows.  Forward:
+// each epilogue warp stages one 32-row x 32-column bf16 box (2 KB) of its output
+// for the TMA store.
 constexpr int kWgBoxes = 1;
 constexpr int kWgStage = 4096 * kWgBoxes;
-constexpr int kZeroBuf = 8192;
 template <int kKind, int kMode>
 constexpr int stages_for() { return (kMode == kWgrad && kWgBoxes > 1) ? 3 : kStages; }
 template <int kKind, int kMode>
 constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
-constexpr size_t extra_smem() { return kMode == kWgrad ? 4 * kWgStage + kZeroBuf : (kKind == 2 ? 2 * kSfSlot : 0); }
+constexpr size_t extra_smem() {
+  return kMode == kWgrad ? 4 * kWgStage : (kMode == kFwd ? (kKind == 2 ? kRawOff + 2 * kSfSlot : kAtomOff) : 0);
+}
 template <int kKind, int kMode>
 constexpr size_t smem_for() {
   return 1024 + static_cast<size_t>(stages_for<kKind, kMode>()) * Cfg<kKind>::kStage +
@@ -185,7 +195,8 @@ struct Geo {
 };
 
 template <int kMode, int kEpi>
-__device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>& g, int tile, int E, int M) {
+__device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>& g, int tile, const Params& p) {
+  const int E = p.E, M = p.M;
   int lo = 0, local = 0;
   if (kMode == kWgrad) {
     // only experts with rows own tiles (in id order); empty ones are zero-filled
@@ -202,8 +213,8 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
   }
   Tile t;
   t.e = lo;
-  const int beg = s.offs[lo];
-  const int cnt = group_ok(beg, s.offs[lo + 1], M) ? s.offs[lo + 1] - beg : 0;
+  const int beg = __ldg(p.offsets + lo), end = __ldg(p.offsets + lo + 1);
+  const int cnt = group_ok(beg, end, M) ? end - beg : 0;
   if (kMode == kWgrad) {
     t.n0 = (local % g.nt) * kBM;
     t.col0 = (local / g.nt) * kBN;
@@ -226,8 +237,7 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
 // whose offsets are out of range is flagged and treated as empty.
 template <int kMode, int kEpi>
 __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p) {
-  for (int e = threadIdx.x; e <= p.E; e += blockDim.x) s.offs[e] = p.offsets[e];
-  __syncthreads();
+  const int32_t* offs = p.offsets;
   if (kMode == kWgrad) {
     // expert list: groups with rows in id order, then empty (or invalid) ones
     if (threadIdx.x < 32) {
@@ -237,9 +247,9 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
         const int e = base + lane;
         bool rows = false;
         if (e < p.E) {
-          const bool ok = group_ok(s.offs[e], s.offs[e + 1], p.M);
+          const bool ok = group_ok(offs[e], offs[e + 1], p.M);
           if (!ok && blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
-          rows = ok && s.offs[e + 1] > s.offs[e];
+          rows = ok && offs[e + 1] > offs[e];
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, rows);
         if (rows) s.prefix[nh + __popc(m & ((1u << lane) - 1u))] = e;
@@ -248,7 +258,7 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
       int nl = 0;
       for (int base = 0; base < p.E; base += 32) {
         const int e = base + lane;
-        const bool none = e < p.E && !(group_ok(s.offs[e], s.offs[e + 1], p.M) && s.offs[e + 1] > s.offs[e]);
+        const bool none = e < p.E && !(group_ok(offs[e], offs[e + 1], p.M) && offs[e + 1] > offs[e]);
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, none);
         if (none) s.prefix[nh + nl + __popc(m & ((1u << lane) - 1u))] = e;
         nl += __popc(m);
@@ -262,8 +272,8 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
     return;
   }
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    int cnt = s.offs[e + 1] - s.offs[e];
-    if (!group_ok(s.offs[e], s.offs[e + 1], p.M)) {
+    int cnt = offs[e + 1] - offs[e];
+    if (!group_ok(offs[e], offs[e + 1], p.M)) {
       if (blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
       cnt = 0;
     }
@@ -290,8 +300,11 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
   __syncthreads();
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g * __frcp_rn(1.f + __expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float g) { return __frcp_rn(1.f + __expf(-g)); }
+// silu(g) = g * sigmoid(g) with the fast exponential and division (the MXFP8 GEMM's
+// accumulator waits for this epilogue, so it must be short); for g < -88 the
+// exponential overflows and both give the exact limit 0.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
 
 // Store 32 consecutive fp32 values as OutT (16-byte stores).
 template <typename OutT>
@@ -334,10 +347,52 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
   }
 }
 
+// Write one warp's 32 tile rows of bf16 output (one row per lane in pk, two
+// columns per word).  A warp whose 32 rows all belong to the group sends
+// 32-column boxes through its 2 KB staging buffer (64-byte swizzle) by TMA store,
+// one box in flight; a warp whose rows cross the group's end (the next group's
+// rows follow) stores its valid rows directly.
+template <int kWords>
+__device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
+                                               int lane, uint16_t* out, int row0, int rows_valid, int col0,
+                                               int n_out) {
+  if (rows_valid >= 32) {
+#pragma unroll
+    for (int c = 0; c < kWords / 16; ++c) {
+      if (col0 + c * 32 >= n_out) break;
+      if (lane == 0) bulk_wait_read0();   // the previous box has left the buffer
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        *reinterpret_cast<uint4*>(stg + lane * 64 + ((h ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2], pk[c * 16 + 4 * h + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmD, stg, col0 + c * 32, row0);
+        bulk_commit();
+      }
+    }
+  } else if (lane < rows_valid) {
+#pragma unroll
+    for (int c = 0; c < kWords / 16; ++c) {
+      const int col = col0 + c * 32;
+      if (col < n_out) {
+        uint4* d4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + lane) * n_out + col);
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
+                             pk[c * 16 + 4 * h + 3]);
+      }
+    }
+  }
+}
+
 template <int kKind, int kMode, int kEpi, typename OutT>
 __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, const Params p) {
+    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+    const __grid_constant__ CUtensorMap tmD, const Params p) {
   using C = Cfg<kKind>;
   constexpr int NS = stages_for<kKind, kMode>();
   extern __shared__ uint8_t smem_raw[];
@@ -373,6 +428,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
+    if (kMode == kWgrad || (kMode == kFwd && sizeof(OutT) == 2)) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -391,12 +447,12 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       int stage = 0, ss = 0;
       uint32_t phase = 0, ss_phase = 0;
       for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-        const Tile t = tile_info(s, g, tile, p.E, p.M);
+        const Tile t = tile_info(s, g, tile, p);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (C::kMx && kMode == kFwd && kb % 4 == 0) {
             // raw E8M0 rows, 16 bytes per row = the scales of 4 K-blocks, into slot ss
             if (!mbar_wait(&s.sempty[ss], ss_phase ^ 1u, p.status, &s.abort)) break;
-            uint8_t* rsa = tiles + kStages * C::kStage + ss * kSfSlot;
+            uint8_t* rsa = tiles + NS * C::kStage + kRawOff + ss * kSfSlot;
             uint8_t* rsb = rsa + kSfAStage;
             const int sx = 16 * (kb / 4);
             const int brow = t.e * p.N;
@@ -448,7 +504,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      const Tile t = tile_info(s, g, tile, p);
       if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.status, &s.abort)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
@@ -459,7 +515,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (lane == 0) {
             const uint32_t sa = smem_u32(tiles + stage * C::kStage);
             const uint32_t sb = sa + kAStage;
-            const uint32_t ssa = sa + kStageBytes;       // this stage's scale atoms
+            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + kAtomOff + stage * kAtomBytes);  // atoms
             const uint32_t ssb = ssa + 512;
             // scale slot of this stage: A atom at +0 (4 columns), B atoms at +kSfB, +kSfB+4
             const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
@@ -531,11 +587,11 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     uint32_t phase = 0, ss_phase = 0;
     uint4 ra[4], rb[8];
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      const Tile t = tile_info(s, g, tile, p);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (kb % 4 == 0) {
           if (!mbar_wait(&s.sfull[ss], ss_phase, p.status, &s.abort)) break;
-          const uint8_t* rsa = tiles + kStages * C::kStage + ss * kSfSlot;
+          const uint8_t* rsa = tiles + NS * C::kStage + kRawOff + ss * kSfSlot;
           const uint8_t* rsb = rsa + kSfAStage;
 #pragma unroll
           for (int j = 0; j < 4; ++j) ra[j] = *reinterpret_cast<const uint4*>(rsa + (lane + 32 * j) * 16);
@@ -546,7 +602,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
-        uint8_t* at = tiles + stage * C::kStage + kStageBytes;
+        uint8_t* at = tiles + NS * C::kStage + kAtomOff + stage * kAtomBytes;
         const int w = kb % 4;
         auto word = [w](const uint4& v) { return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w)); };
         *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(word(ra[0]), word(ra[1]), word(ra[2]), word(ra[3]));
@@ -560,28 +616,22 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     }
   } else if (kMode == kWgrad && warp == 6) {
     // ------------------------------------------------------------------ wgrad zero fill
-    // Experts without rows own no tiles; their dW (exact zeros) is written here with
-    // bulk stores from a zeroed shared buffer, alongside the MMA work.  An expert's
-    // dW is N*K*2 bytes, a multiple of 2048 since N and K are multiples of 32.
-    uint8_t* zb = tiles + NS * C::kStage + 4 * kWgStage;
-    for (int i = lane; i < kZeroBuf / 16; i += 32) reinterpret_cast<uint4*>(zb)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const size_t per = static_cast<size_t>(p.N) * p.K * 2;
-      const uint32_t chunk = per % kZeroBuf == 0 ? kZeroBuf : 2048u;
-      const size_t cpe = per / chunk;
-      const size_t chunks = static_cast<size_t>(p.E - s.nnz) * cpe;
-      uint8_t* outb = static_cast<uint8_t*>(p.out);
-      for (size_t c = blockIdx.x; c < chunks && !s.abort; c += gridDim.x) {
-        const int e = s.prefix[s.nnz + static_cast<int>(c / cpe)];
-        bulk_store(outb + static_cast<size_t>(e) * per + (c % cpe) * chunk, zb, chunk);
-        bulk_commit();
-        bulk_wait_read8();
-      }
-      bulk_wait_all0();
+    // Experts without rows own no tiles; their dW (exact zeros) is written here,
+    // alongside the MMA work, with plain 16-byte stores (not through the TMA unit,
+    // which the operand loads need) marked evict-first in L2 (so the zeros do not
+    // push the operands out).  An expert's dW is N*K*2 bytes, a multiple of 2048
+    // since N and K are multiples of 32; a warp writes one 2 KB chunk per pass.
+    const uint64_t pol = l2_evict_first_policy();
+    const size_t per = static_cast<size_t>(p.N) * p.K * 2;
+    const size_t cpe = per / 2048;
+    const size_t chunks = static_cast<size_t>(p.E - s.nnz) * cpe;
+    uint8_t* outb = static_cast<uint8_t*>(p.out);
+    for (size_t c = blockIdx.x; c < chunks && !s.abort; c += gridDim.x) {
+      const int e = s.prefix[s.nnz + static_cast<int>(c / cpe)];
+      uint4* dst = reinterpret_cast<uint4*>(outb + static_cast<size_t>(e) * per + (c % cpe) * 2048);
+#pragma unroll
+      for (int i = lane; i < 128; i += 32) st_global_hint(dst + i, make_uint4(0, 0, 0, 0), pol);
     }
-    __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------------ epilogue
     // The accumulator is released (tempty) as soon as its last TMEM read is done;
@@ -593,7 +643,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-      const Tile t = tile_info(s, g, tile, p.E, p.M);
+      const Tile t = tile_info(s, g, tile, p);
       if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
@@ -632,7 +682,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (lane == 0) {
 #pragma unroll
             for (int j = 0; j < kWgBoxes; ++j)
-              tma_store_3d(&tmSA, stg + j * 4096, t.col0 + 64 * (round * kWgBoxes + j), t.n0 + 32 * q, t.e);
+              tma_store_3d(&tmD, stg + j * 4096, t.col0 + 64 * (round * kWgBoxes + j), t.n0 + 32 * q, t.e);
             bulk_commit();
           }
         }
@@ -656,19 +706,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          if (valid) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int col = t.col0 + c * 32;
-              if (col < g.n_out) {
-                uint4* d4 = reinterpret_cast<uint4*>(out + grow * g.n_out + col);
-#pragma unroll
-                for (int h = 0; h < 4; ++h)
-                  d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
-                                     pk[c * 16 + 4 * h + 3]);
-              }
-            }
-          }
+          epi_store_bf16(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+                         reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -738,7 +777,10 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          if (valid) {
+          if constexpr (kMode == kFwd) {
+            epi_store_bf16(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+                           reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+          } else if (valid) {
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
               const int col = t.col0 + c * 32;
@@ -773,8 +815,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       }
       if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
-    if constexpr (kMode == kWgrad) {
-      if (lane == 0) bulk_wait_all0();      // every dW store has landed
+    if constexpr (kMode == kWgrad || kMode == kFwd) {
+      if (lane == 0) bulk_wait_all0();      // every TMA store has landed
       __syncwarp();
     }
   }
@@ -844,13 +886,14 @@ bool ensure_smem(Kern k, size_t bytes) {
 template <int kKind, int kMode, int kEpi, typename OutT>
 moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t stream,
                     int sms, const char* what, const CUtensorMap* tsa = nullptr,
-                    const CUtensorMap* tsb = nullptr) {
+                    const CUtensorMap* tsb = nullptr, const CUtensorMap* td = nullptr) {
   using C = Cfg<kKind>;
   constexpr size_t smem = smem_for<kKind, kMode>();
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  launch_pdl(kern, sms, threads_for<kKind, kMode>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, p);
+  launch_pdl(kern, sms, threads_for<kKind, kMode>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
+             td ? *td : ta, p);
   return check_launch(what);
 }
 
@@ -924,6 +967,14 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   Params p{offsets, M, N, K, E, C, preact, nullptr, dev_status};
   const bool sw = epi == MOE_EPI_SWIGLU;
   const bool f32 = c_dtype == MOE_F32;
+  // bf16 C [M, n_out] is written by TMA from 32 x 32 staging boxes (64-byte swizzle)
+  CUtensorMap td = ta;
+  if (!f32) {
+    const uint64_t cdims[2] = {static_cast<uint64_t>(sw ? N / 2 : N), static_cast<uint64_t>(M)};
+    const uint32_t cbox[2] = {32, 32};
+    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MOE_ERR_INVALID_ARG;
+  }
   if (A->dtype == MOE_E4M3) {
     // E8M0 scales, [rows, K/32] bytes, read 16 bytes (4 stages' worth) per row
     CUtensorMap tsa, tsb;
@@ -934,20 +985,20 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
         !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
       return MOE_ERR_INVALID_ARG;
     if (sw) return f32 ? launch<2, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
-                       : launch<2, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+                       : launch<2, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
     return f32 ? launch<2, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
-               : launch<2, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+               : launch<2, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
   }
   if (A->dtype == MOE_F32) {
     if (sw) return f32 ? launch<0, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn)
-                       : launch<0, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn);
+                       : launch<0, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
     return f32 ? launch<0, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn)
-               : launch<0, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
+               : launch<0, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   }
   if (sw) return f32 ? launch<1, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn)
-                     : launch<1, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn);
+                     : launch<1, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   return f32 ? launch<1, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn)
-             : launch<1, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
+             : launch<1, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const moe_operand_t* B,
@@ -1011,5 +1062,5 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   const uint32_t dbox[3] = {64, 32, 1};
   if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox)) return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dB, nullptr, nullptr, dev_status};
-  return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &td, nullptr);
+  return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }

@@ -188,7 +188,7 @@ def _quantize(t):
 
 
 @pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
-@pytest.mark.parametrize("K,N", [(512, 256), (1024, 320), (2048, 64)])
+@pytest.mark.parametrize("K,N", [(512, 256), (1024, 320), (2048, 64), (512, 192), (512, 448)])
 def test_fwd_mxfp8_plain(counts, K, N):
     need_gpu()
     cnt = COUNTS[counts]
@@ -209,7 +209,7 @@ def test_fwd_mxfp8_plain(counts, K, N):
 
 
 @pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
-@pytest.mark.parametrize("K,f", [(512, 128), (1024, 256), (512, 96)])
+@pytest.mark.parametrize("K,f", [(512, 128), (1024, 256), (512, 96), (512, 288)])
 def test_fwd_mxfp8_swiglu(counts, K, f):
     need_gpu()
     cnt = COUNTS[counts]
@@ -222,6 +222,25 @@ def test_fwd_mxfp8_swiglu(counts, K, f):
     H = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi="swiglu", A_scales=As, B_scales=Bs)
     want = om.swiglu(om.grouped_gemm(A_deq, B_deq.reshape(E, 2 * f, K), off.cpu().numpy()))
     assert rel_l2(f64(H), want) < 1e-2
+
+
+@pytest.mark.parametrize("f", [96, 160])
+def test_fwd_mxfp8_swiglu_f32_out_and_preact(f):
+    """fp32 H and the pre-activation G|U store, across a partial last column tile."""
+    need_gpu()
+    cnt = COUNTS["mixed"]
+    E = len(cnt)
+    M, K = int(sum(cnt)), 512
+    A, B = _mats(M, K, 2 * f, E, torch.bfloat16, seed=f + 11)
+    Aq, As, A_deq = _quantize(A)
+    Bq, Bs, B_deq = _quantize(B)
+    off = ragged_offsets(cnt)
+    H, GU = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi="swiglu", A_scales=As, B_scales=Bs,
+                                         out_dtype=torch.float32, want_preact=True)
+    gu = om.grouped_gemm(A_deq, B_deq.reshape(E, 2 * f, K), off.cpu().numpy())
+    # same quantised inputs, fp32 out: only the tensor core's accumulation rounding
+    assert rel_l2(f64(GU), gu) < 1e-3
+    assert rel_l2(f64(H), om.swiglu(gu)) < 1e-3
 
 
 def test_fwd_mxfp8_requires_scales_and_k_multiple_of_512():
