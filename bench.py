@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -33,12 +34,15 @@ L2_BYTES = 129 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s of timed work; reference arm: 3)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of replays of the step captured in one CUDA graph")
     ap.add_argument("--T", type=int, default=None, help="override tokens (small profiling cases)")
     ap.add_argument("--f", type=int, default=None, help="override expert hidden dim (profiling)")
     ap.add_argument("--E", type=int, default=None, help="override expert count (profiling)")
@@ -142,6 +146,17 @@ def stage_bytes(w):
     return permute, combine
 
 
+def gemm1_bytes(w, e_used):
+    """Algorithmic HBM bytes of one GEMM1 launch: the W1 of every expert that
+    received tokens (and its E8M0 scales for MXFP8) and the permuted activations
+    read once, H (and, when training, the pre-activation G|U) written once."""
+    M, d, f, E = w.M, w.d, w.f, e_used
+    if w.dtype == "mxfp8":
+        return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * 2
+    s = 4 if w.dtype == "f32" else 2
+    return (E * 2 * f * d + M * d + M * f) * s + (M * 2 * f * s if w.backward else 0)
+
+
 def gemm1_traffic(workload):
     """DRAM bytes per GEMM1 launch from the committed ncu summary
     (profiles/gemm1_traffic_<workload>.txt), or None when there is none or the GEMM
@@ -219,19 +234,52 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    n_ev = 7 if w.backward else 6
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    # Headline: the whole step (no host reads, device-side counts) captured once in
+    # a CUDA graph and replayed; --eager times plain launches instead.
+    run_step = step
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            step()
+        run_step = graph.replay
+    for _ in range(args.warmup):
+        run_step()
+    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.steps is None:
+        # enough steps for ~1.5 s of timed work (several clock samples), same on every rank
+        t_a.record(stream)
+        run_step()
+        t_b.record(stream)
+        torch.cuda.synchronize()
+        est = max_over_ranks(t_a.elapsed_time(t_b), world)
+        args.steps = int(min(5000, max(20, math.ceil(1500.0 / max(est, 1e-3)))))
     clocks = Clocks(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(evs[i])
+    t_a.record(stream)
+    for _ in range(args.steps):
+        run_step()
+    t_b.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier(world)
     clk = clocks.stop()
+    # Per-stage breakdown: eager launches with events between the stages (a
+    # diagnostic pass after the timed region, at the clocks that load sustains).
+    n_ev = 7 if w.backward else 6
+    n_diag = min(args.steps or 20, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(n_diag)]
+    for i in range(n_diag):
+        step(evs[i])
+    torch.cuda.synchronize()
     if int(layer.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(layer.dev_status.item())}")
     per = {k: 0.0 for k in ("route", "dispatch", "gemm1", "gemm2", "combine", "backward", "step")}
@@ -244,14 +292,33 @@ def run_ours(args, world, rank, local):
         if w.backward:
             per["backward"] += e[5].elapsed_time(e[6])
         per["step"] += e[0].elapsed_time(e[-1])
-    per = {k: v / args.steps for k, v in per.items()}           # ms per step
-    ms = max_over_ranks(per["step"], world)
+    per = {k: v / n_diag for k, v in per.items()}               # ms per step (eager pass)
+    ms = max_over_ranks(t_a.elapsed_time(t_b) / args.steps, world)
     flops = w.fwd_flops * (3 if w.backward else 1)
     value = world * flops / (ms * 1e-3) / 1e12
     pk = peaks()
     g1_flops = 4.0 * w.M * w.d * w.f
     g1_tflops = g1_flops / (per["gemm1"] * 1e-3) / 1e12
     dtype_peak = pk["bf16_sus"] * (2.0 if w.dtype == "mxfp8" else (0.5 if w.dtype == "f32" else 1.0))
+    # the roofline that binds GEMM1: tensor time at the dtype's peak vs HBM time of
+    # its algorithmic bytes at the measured copy bandwidth
+    e_used = int((layer.counts > 0).sum().item())     # read after the timed region
+    g1_bytes = gemm1_bytes(w, e_used)
+    g1_s = per["gemm1"] * 1e-3
+    hbm_bound = g1_bytes / (pk["hbm"] * 1e9) > g1_flops / (dtype_peak * 1e12)
+    peak_src = (f"{pk['source']} bf16 sustained" + (" x2 (fp8 nominal ratio)" if w.dtype == "mxfp8" else "")
+                + (" x0.5 (tf32 nominal ratio)" if w.dtype == "f32" else ""))
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": round(g1_bytes / g1_s / 1e9, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(g1_bytes / g1_s / 1e9 / pk["hbm"], 4), "peak_source": f"{pk['source']} copy bandwidth",
+                "bytes_per_launch": round(g1_bytes), "experts_with_tokens": e_used,
+                "tensor_tflops": round(g1_tflops, 1),
+                "tensor_frac": round(g1_tflops / dtype_peak, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(g1_tflops, 1), "peak": round(dtype_peak, 1), "unit": "TFLOP/s",
+                "frac": round(g1_tflops / dtype_peak, 4), "peak_source": peak_src,
+                "hbm_gbs": round(g1_bytes / g1_s / 1e9, 1), "bytes_per_launch": round(g1_bytes),
+                "experts_with_tokens": e_used}
     perm_b, comb_b = stage_bytes(w)
     launches = layer.launches_per_forward() + (layer.launches_per_backward() if w.backward else 0)
     traffic = gemm1_traffic(w.name)
@@ -263,16 +330,13 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; no dataset or trained weights)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f,
                    "M_rows": w.M, "backward": w.backward,
+                   "timing": "eager launches" if args.eager else "whole step captured in one CUDA graph, replayed",
                    "l2": f"inputs larger than L2: {(W1.numel() + W2.numel()) * W1.element_size() / 1e9:.2f} GB of expert weights streamed per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "stages_ms": {k: round(v, 4) for k, v in per.items()},
+        "stages_ms": {k: round(v, 4) for k, v in per.items()},   # eager pass, events between stages
         "permute_gbs": round(perm_b / (per["dispatch"] * 1e-3) / 1e9, 1),
         "combine_gbs": round(comb_b / (per["combine"] * 1e-3) / 1e9, 1),
-        "roofline": {"kernel": "grouped GEMM1 (gate+up, fused SwiGLU)", "bound": "tensor",
-                     "achieved": round(g1_tflops, 1), "peak": round(dtype_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(g1_tflops / dtype_peak, 4),
-                     "peak_source": f"{pk['source']} bf16 sustained" + (" x2 (fp8 nominal ratio)" if w.dtype == "mxfp8" else "")
-                     + (" x0.5 (tf32 nominal ratio)" if w.dtype == "f32" else ""),
+        "roofline": {"kernel": "grouped GEMM1 (gate+up, fused SwiGLU)", **roof,
                      "traffic": traffic,
                      "hbm_frac_permute": round(perm_b / (per["dispatch"] * 1e-3) / 1e9 / pk["hbm"], 4),
                      "hbm_frac_combine": round(comb_b / (per["combine"] * 1e-3) / 1e9 / pk["hbm"], 4)},
@@ -444,6 +508,8 @@ def run_reference(args, world, rank):
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
+    if args.impl == "reference" and args.steps is None:
+        args.steps = 3
     if args.impl == "reference":
         line = run_reference(args, world, rank)
     else:
