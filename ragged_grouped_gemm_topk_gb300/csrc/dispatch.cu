@@ -13,8 +13,8 @@
 //   scan     one block: offsets = exclusive scan of counts, then for every expert
 //            an exclusive scan of the block totals down the blocks.
 //   scatter  one warp per token: dest_row / src_pair, then the token's row is
-//            copied with 16-byte loads and stores to its k rows, optionally
-//            quantised to MXFP8 on the way.
+//            copied with 16-byte loads (8 per lane in flight) and stores to its
+//            k rows, optionally quantised to MXFP8 on the way.
 //
 // MXFP8 follows the OCP Microscaling Formats v1.0 conversion (shared exponent
 // floor(log2 amax) - 8, clamped to [-127, 127]; E4M3 round-to-nearest-even with
@@ -196,6 +196,11 @@ __device__ __forceinline__ void mx_chunk(const Vec16& v, uint32_t (&codes)[2], u
   }
 }
 
+// One warp per token.  Each lane keeps kScatterU 16-byte chunks of the row in
+// flight (8 KB per warp), and the first batch is requested before the token's
+// destinations are resolved so that the two latencies overlap.
+constexpr int kScatterU = 8;
+
 template <typename Tin, bool kQuant>
 __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     const uint8_t* __restrict__ x, int T, int d, const int32_t* __restrict__ idx, int k, int E,
@@ -209,6 +214,20 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
   const size_t out_row = kQuant ? static_cast<size_t>(d) : in_row;
   const int n16 = static_cast<int>(in_row / 16);
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
+    Vec16 v[kScatterU];
+    auto load = [&](int base) {
+#pragma unroll
+      for (int i = 0; i < kScatterU; ++i) {
+        const int c = base + 32 * i + lane;
+        if (c < n16) {
+          v[i] = src[c];
+        } else {
+          v[i].w[0] = v[i].w[1] = v[i].w[2] = v[i].w[3] = 0;
+        }
+      }
+    };
+    if (xp != nullptr) load(0);
     int dest = -1;
     if (lane < k) {
       const size_t p = static_cast<size_t>(t) * k + lane;
@@ -224,37 +243,35 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
       if (dest >= 0) src_pair[dest] = static_cast<int32_t>(p);
     }
     if (xp == nullptr) continue;
-    const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
-    for (int base = 0; base < n16; base += 32) {
-      const int c = base + lane;
-      const bool active = c < n16;
-      Vec16 v;
-      if (active) {
-        v = src[c];
-      } else {
-        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0;
-      }
-      if constexpr (kQuant) {
-        uint32_t codes[2], sbyte;
-        mx_chunk<Tin>(v, codes, &sbyte);
-        constexpr int EPL = Mx<Tin>::kEpl;
-        for (int j = 0; j < k; ++j) {
-          const int dj = __shfl_sync(kFull, dest, j);
-          if (active && dj >= 0) {
-            uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * EPL;
-            if (EPL == 8)
-              *reinterpret_cast<uint2*>(orow) = make_uint2(codes[0], codes[1]);
-            else
-              *reinterpret_cast<uint32_t*>(orow) = codes[0];
-            if ((lane % Mx<Tin>::kLpb) == 0)
-              xp_scales[static_cast<size_t>(dj) * (d / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+    for (int base = 0; base < n16; base += 32 * kScatterU) {
+      if (base > 0) load(base);
+#pragma unroll
+      for (int i = 0; i < kScatterU; ++i) {
+        const int c = base + 32 * i + lane;
+        const bool active = c < n16;
+        if constexpr (kQuant) {
+          if (base + 32 * i >= n16) break;     // warp-uniform: no lane of this chunk row is active
+          uint32_t codes[2], sbyte;
+          mx_chunk<Tin>(v[i], codes, &sbyte);
+          constexpr int EPL = Mx<Tin>::kEpl;
+          for (int j = 0; j < k; ++j) {
+            const int dj = __shfl_sync(kFull, dest, j);
+            if (active && dj >= 0) {
+              uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * EPL;
+              if (EPL == 8)
+                *reinterpret_cast<uint2*>(orow) = make_uint2(codes[0], codes[1]);
+              else
+                *reinterpret_cast<uint32_t*>(orow) = codes[0];
+              if ((lane % Mx<Tin>::kLpb) == 0)
+                xp_scales[static_cast<size_t>(dj) * (d / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+            }
           }
-        }
-      } else {
-        for (int j = 0; j < k; ++j) {
-          const int dj = __shfl_sync(kFull, dest, j);
-          if (active && dj >= 0)
-            reinterpret_cast<Vec16*>(xp + static_cast<size_t>(dj) * out_row)[c] = v;
+        } else {
+          for (int j = 0; j < k; ++j) {
+            const int dj = __shfl_sync(kFull, dest, j);
+            if (active && dj >= 0)
+              reinterpret_cast<Vec16*>(xp + static_cast<size_t>(dj) * out_row)[c] = v[i];
+          }
         }
       }
     }
@@ -273,25 +290,33 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
   const int n16 = static_cast<int>(in_row / 16);
   for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
     const Vec16* src = reinterpret_cast<const Vec16*>(in + static_cast<size_t>(r) * in_row);
-    for (int base = 0; base < n16; base += 32) {
-      const int c = base + lane;
-      const bool active = c < n16;
-      Vec16 v;
-      if (active) {
-        v = src[c];
-      } else {
-        v.w[0] = v.w[1] = v.w[2] = v.w[3] = 0;
+    constexpr int U = kScatterU / 2;     // chunks per lane in flight
+    for (int base = 0; base < n16; base += 32 * U) {
+      Vec16 v[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int c = base + 32 * i + lane;
+        if (c < n16) {
+          v[i] = src[c];
+        } else {
+          v[i].w[0] = v[i].w[1] = v[i].w[2] = v[i].w[3] = 0;
+        }
       }
-      uint32_t q[2], sbyte;
-      mx_chunk<Tin>(v, q, &sbyte);
-      if (active) {
-        uint8_t* orow = codes + static_cast<size_t>(r) * K + static_cast<size_t>(c) * EPL;
-        if (EPL == 8)
-          *reinterpret_cast<uint2*>(orow) = make_uint2(q[0], q[1]);
-        else
-          *reinterpret_cast<uint32_t*>(orow) = q[0];
-        if ((lane % Mx<Tin>::kLpb) == 0)
-          scales[static_cast<size_t>(r) * (K / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        if (base + 32 * i >= n16) break;      // warp-uniform
+        const int c = base + 32 * i + lane;
+        uint32_t q[2], sbyte;
+        mx_chunk<Tin>(v[i], q, &sbyte);
+        if (c < n16) {
+          uint8_t* orow = codes + static_cast<size_t>(r) * K + static_cast<size_t>(c) * EPL;
+          if (EPL == 8)
+            *reinterpret_cast<uint2*>(orow) = make_uint2(q[0], q[1]);
+          else
+            *reinterpret_cast<uint32_t*>(orow) = q[0];
+          if ((lane % Mx<Tin>::kLpb) == 0)
+            scales[static_cast<size_t>(r) * (K / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+        }
       }
     }
   }

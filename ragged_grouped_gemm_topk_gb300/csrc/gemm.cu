@@ -55,13 +55,20 @@ constexpr int kSfAStage = 2048;                   // MXFP8: raw A scale rows, 12
 constexpr int kSfBStage = 4096;                   // MXFP8: raw B scale rows, 256 x 16 bytes
 constexpr int kSfSlot = kSfAStage + kSfBStage;    // one raw scale slot (4 K-blocks' worth)
 constexpr int kAtomBytes = 1536;                  // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
-constexpr int kEpiBox = 2048;                     // forward epilogue staging: 32 x 32 bf16 per warp
-// Forward kernels' extra shared memory (after the operand stages): the epilogue
-// staging boxes (1 KB aligned for the 64-byte swizzle), then for MXFP8 the scale
-// atoms of every stage and the two raw scale-row slots.
+// Forward kernels' extra shared memory (after the operand stages): one epilogue
+// staging box per epilogue warp (32 rows x epi_cols bf16; 1 KB aligned for the
+// swizzle), then for MXFP8 the scale atoms of every stage and the two raw
+// scale-row slots.  32-column boxes measured faster than 64-column ones for bf16
+// too (and MXFP8 has room for no more).
+template <int kKind>
+constexpr int epi_cols() { return 32; }
+template <int kKind>
+constexpr int epi_box() { return 32 * epi_cols<kKind>() * 2; }
 constexpr int kEpiOff = 0;
-constexpr int kAtomOff = kEpiOff + 4 * kEpiBox;
-constexpr int kRawOff = kAtomOff + kStages * kAtomBytes;
+template <int kKind>
+constexpr int atom_off() { return kEpiOff + 4 * epi_box<kKind>(); }
+template <int kKind>
+constexpr int raw_off() { return atom_off<kKind>() + kStages * kAtomBytes; }
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
@@ -117,7 +124,8 @@ template <int kKind, int kMode>
 constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
 constexpr size_t extra_smem() {
-  return kMode == kWgrad ? 4 * kWgStage : (kMode == kFwd ? (kKind == 2 ? kRawOff + 2 * kSfSlot : kAtomOff) : 0);
+  return kMode == kWgrad ? 4 * kWgStage
+                        : (kMode == kFwd ? (kKind == 2 ? raw_off<kKind>() + 2 * kSfSlot : atom_off<kKind>()) : 0);
 }
 template <int kKind, int kMode>
 constexpr size_t smem_for() {
@@ -349,27 +357,33 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 
 // Write one warp's 32 tile rows of bf16 output (one row per lane in pk, two
 // columns per word).  A warp whose 32 rows all belong to the group sends
-// 32-column boxes through its 2 KB staging buffer (64-byte swizzle) by TMA store,
-// one box in flight; a warp whose rows cross the group's end (the next group's
-// rows follow) stores its valid rows directly.
-template <int kWords>
+// kCols-column boxes through its staging buffer by TMA store, one box in flight
+// (rows of kCols * 2 bytes, 64- or 128-byte swizzle: 16-byte chunk h of row r sits
+// at chunk h ^ ((r >> 1) & 3), resp. h ^ (r & 7)); a warp whose rows cross the
+// group's end (the next group's rows follow) stores its valid rows directly.
+template <int kCols, int kWords>
 __device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
                                                int lane, uint16_t* out, int row0, int rows_valid, int col0,
                                                int n_out) {
+  static_assert(kCols == 32 || kCols == 64, "box width");
+  constexpr int kChunks = kCols / 8;                  // 16-byte chunks per row
   if (rows_valid >= 32) {
 #pragma unroll
-    for (int c = 0; c < kWords / 16; ++c) {
-      if (col0 + c * 32 >= n_out) break;
+    for (int c = 0; c < kWords / (kCols / 2); ++c) {
+      if (col0 + c * kCols >= n_out) break;
       if (lane == 0) bulk_wait_read0();   // the previous box has left the buffer
       __syncwarp();
+      const int sw = kCols == 32 ? (lane >> 1) & 3 : lane & 7;
 #pragma unroll
-      for (int h = 0; h < 4; ++h)
-        *reinterpret_cast<uint4*>(stg + lane * 64 + ((h ^ ((lane >> 1) & 3)) * 16)) =
-            make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2], pk[c * 16 + 4 * h + 3]);
+      for (int h = 0; h < kChunks; ++h) {
+        const int w0 = c * (kCols / 2) + 4 * h;
+        *reinterpret_cast<uint4*>(stg + lane * (kCols * 2) + ((h ^ sw) * 16)) =
+            make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tmD, stg, col0 + c * 32, row0);
+        tma_store_2d(tmD, stg, col0 + c * kCols, row0);
         bulk_commit();
       }
     }
@@ -452,7 +466,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (C::kMx && kMode == kFwd && kb % 4 == 0) {
             // raw E8M0 rows, 16 bytes per row = the scales of 4 K-blocks, into slot ss
             if (!mbar_wait(&s.sempty[ss], ss_phase ^ 1u, p.status, &s.abort)) break;
-            uint8_t* rsa = tiles + NS * C::kStage + kRawOff + ss * kSfSlot;
+            uint8_t* rsa = tiles + NS * C::kStage + raw_off<kKind>() + ss * kSfSlot;
             uint8_t* rsb = rsa + kSfAStage;
             const int sx = 16 * (kb / 4);
             const int brow = t.e * p.N;
@@ -515,7 +529,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (lane == 0) {
             const uint32_t sa = smem_u32(tiles + stage * C::kStage);
             const uint32_t sb = sa + kAStage;
-            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + kAtomOff + stage * kAtomBytes);  // atoms
+            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + atom_off<kKind>() + stage * kAtomBytes);  // atoms
             const uint32_t ssb = ssa + 512;
             // scale slot of this stage: A atom at +0 (4 columns), B atoms at +kSfB, +kSfB+4
             const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
@@ -591,7 +605,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (kb % 4 == 0) {
           if (!mbar_wait(&s.sfull[ss], ss_phase, p.status, &s.abort)) break;
-          const uint8_t* rsa = tiles + NS * C::kStage + kRawOff + ss * kSfSlot;
+          const uint8_t* rsa = tiles + NS * C::kStage + raw_off<kKind>() + ss * kSfSlot;
           const uint8_t* rsb = rsa + kSfAStage;
 #pragma unroll
           for (int j = 0; j < 4; ++j) ra[j] = *reinterpret_cast<const uint4*>(rsa + (lane + 32 * j) * 16);
@@ -602,7 +616,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
-        uint8_t* at = tiles + NS * C::kStage + kAtomOff + stage * kAtomBytes;
+        uint8_t* at = tiles + NS * C::kStage + atom_off<kKind>() + stage * kAtomBytes;
         const int w = kb % 4;
         auto word = [w](const uint4& v) { return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w)); };
         *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(word(ra[0]), word(ra[1]), word(ra[2]), word(ra[3]));
@@ -706,7 +720,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          epi_store_bf16(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+          epi_store_bf16<epi_cols<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_box<kKind>(), pk, lane,
                          reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
@@ -778,7 +792,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           mbar_arrive(&s.tempty[acc]);
           released = true;
           if constexpr (kMode == kFwd) {
-            epi_store_bf16(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+            epi_store_bf16<epi_cols<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_box<kKind>(), pk, lane,
                            reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
 #pragma unroll
@@ -967,12 +981,16 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   Params p{offsets, M, N, K, E, C, preact, nullptr, dev_status};
   const bool sw = epi == MOE_EPI_SWIGLU;
   const bool f32 = c_dtype == MOE_F32;
-  // bf16 C [M, n_out] is written by TMA from 32 x 32 staging boxes (64-byte swizzle)
+  // bf16 C [M, n_out] is written by TMA from 32-row staging boxes: 32 columns with
+  // 64-byte swizzle (MXFP8) or 64 columns with 128-byte swizzle (tf32 / bf16)
   CUtensorMap td = ta;
   if (!f32) {
+    const bool mx = A->dtype == MOE_E4M3;
     const uint64_t cdims[2] = {static_cast<uint64_t>(sw ? N / 2 : N), static_cast<uint64_t>(M)};
-    const uint32_t cbox[2] = {32, 32};
-    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    const int cols = mx ? epi_cols<2>() : epi_cols<1>();
+    const uint32_t cbox[2] = {static_cast<uint32_t>(cols), 32};
+    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox,
+                  cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_INVALID_ARG;
   }
   if (A->dtype == MOE_E4M3) {
