@@ -149,10 +149,11 @@ def stage_bytes(w):
 def gemm1_bytes(w, e_used):
     """Algorithmic HBM bytes of one GEMM1 launch: the W1 of every expert that
     received tokens (and its E8M0 scales for MXFP8) and the permuted activations
-    read once, H (and, when training, the pre-activation G|U) written once."""
+    read once, H (MXFP8: its codes and scales; when training also the
+    pre-activation G|U) written once."""
     M, d, f, E = w.M, w.d, w.f, e_used
     if w.dtype == "mxfp8":
-        return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * 2
+        return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * (1 + 1 / 32)   # H as MXFP8
     s = 4 if w.dtype == "f32" else 2
     return (E * 2 * f * d + M * d + M * f) * s + (M * 2 * f * s if w.backward else 0)
 
@@ -216,10 +217,10 @@ def run_ours(args, world, rank, local):
             pkg.moe_grouped_gemm_fwd(layer.h, layer.W2, layer.offsets, out=layer.yp,
                                      dev_status=layer.dev_status)
         elif ev is not None:
-            pkg.moe_grouped_gemm_fwd(layer.xq, layer.W1q, layer.offsets, epi="swiglu", A_scales=layer.xs,
-                                     B_scales=layer.W1s, out=layer.h, dev_status=layer.dev_status)
+            pkg.moe_grouped_gemm_fwd_mxfp8_out(layer.xq, layer.W1q, layer.offsets, epi="swiglu",
+                                               A_scales=layer.xs, B_scales=layer.W1s, codes=layer.hq,
+                                               scales=layer.hs, dev_status=layer.dev_status)
             mark(3)
-            pkg.moe_quantize_mxfp8_grouped(layer.h, codes=layer.hq, scales=layer.hs)
             pkg.moe_grouped_gemm_fwd(layer.hq, layer.W2q, layer.offsets, A_scales=layer.hs,
                                      B_scales=layer.W2s, out=layer.yp, dev_status=layer.dev_status)
         else:

@@ -190,6 +190,21 @@ moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_operand_t* B
                                   moe_epilogue_t epi, void* C, moe_dtype_t c_dtype,
                                   void* preact, int32_t* dev_status, cudaStream_t stream);
 
+/* Forward with MXFP8 output ([1] lists quantisation fused with the GEMM as
+ * planned work; this is that fusion): as moe_grouped_gemm_fwd with E4M3 operands,
+ * but the result (SWIGLU: H [M, f]; NONE: C [M, N]) leaves the epilogue quantised
+ * row-wise to MXFP8, ready to be the A operand of the next forward GEMM.  Each
+ * value is rounded to bf16 first, so codes and scales equal those of a bf16
+ * result passed through moe_quantize_mxfp8_grouped.
+ *   c_codes  [M, n_out] uint8 (E4M3), 16-byte aligned; c_scales [M, n_out / 32]
+ *            uint8 (E8M0).  Rows outside every group are not written.
+ * Limits as moe_grouped_gemm_fwd; A and B must be MOE_E4M3 (MOE_ERR_UNSUPPORTED
+ * otherwise). */
+moe_status_t moe_grouped_gemm_fwd_mxfp8_out(const moe_operand_t* A, const moe_operand_t* B,
+                                            const int32_t* offsets, int M, int N, int K, int E,
+                                            moe_epilogue_t epi, uint8_t* c_codes, uint8_t* c_scales,
+                                            int32_t* dev_status, cudaStream_t stream);
+
 /* Data gradient: dA[r, :] = dC[r, :] . B[e] for r in expert e's rows.
  *   dC [M, N], B [E, N, K] (both MOE_BF16 or both MOE_F32) -> dA [M, K] in dA_dtype.
  *   epi == MOE_EPI_DSWIGLU fuses the SwiGLU backward: the product is dH [M, K]

@@ -125,6 +125,25 @@ def moe_grouped_gemm_fwd(A, B, offsets, *, epi="none", A_scales=None, B_scales=N
     return (out, preact) if want_preact or preact is not None else out
 
 
+def moe_grouped_gemm_fwd_mxfp8_out(A, B, offsets, *, epi="none", A_scales=None, B_scales=None, codes=None,
+                                   scales=None, dev_status=None):
+    """As moe_grouped_gemm_fwd on MXFP8 operands, with the result quantised to MXFP8
+    in the epilogue: returns (codes [M, n_out] uint8, scales [M, n_out/32] uint8)."""
+    M, K = A.shape
+    E, N, K2 = B.shape
+    if K2 != K:
+        raise ValueError("A and B disagree on K")
+    n_out = N // 2 if epi == "swiglu" else N
+    if codes is None:
+        codes = torch.empty(M, n_out, dtype=torch.uint8, device=A.device)
+    if scales is None:
+        scales = torch.empty(M, n_out // 32, dtype=torch.uint8, device=A.device)
+    a, b = _operand(A, A_scales), _operand(B, B_scales)
+    _lib.call("moe_grouped_gemm_fwd_mxfp8_out", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E, _EPI[epi],
+              _ptr(codes), _ptr(scales), _ptr(dev_status), _stream())
+    return codes, scales
+
+
 def moe_grouped_gemm_dgrad(dC, B, offsets, *, epi="none", preact=None, out_dtype=torch.bfloat16,
                            out=None, dev_status=None):
     """dA = ragged dC [M,N] . B[e] with B [E,N,K]; epi "dswiglu" (with preact [M,2K])

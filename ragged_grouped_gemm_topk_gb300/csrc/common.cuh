@@ -59,6 +59,22 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// MXFP8 shared-exponent rule (OCP Microscaling Formats v1.0): X = floor(log2 amax)
+// - 8 (8 = E4M3's largest exponent), clamped at -127, stored as the E8M0 byte
+// X + 127; an all-zero block gets byte 127.  Returns the byte and the exact power
+// of two 2^-X to multiply the block by before the E4M3 conversion.
+__device__ __forceinline__ void mx_scale(float amax, uint32_t* sbyte, float* inv) {
+  if (amax == 0.f) {
+    *sbyte = 127u;
+    *inv = 1.f;
+    return;
+  }
+  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent
+  const int s = eb - 8 > 0 ? eb - 8 : 0;                                     // X + 127
+  *sbyte = static_cast<uint32_t>(s);
+  *inv = __uint_as_float(static_cast<uint32_t>(254 - s) << 23);              // 2^(127 - s)
+}
+
 // ----------------------------------------------------------------------------- dependent launch
 
 // Every kernel of the library starts with pdl_begin(): wait until the preceding

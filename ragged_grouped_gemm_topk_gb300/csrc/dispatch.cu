@@ -162,19 +162,6 @@ struct Mx<float> {  // f32: 4 elements per lane, 8 lanes per block
   }
 };
 
-// Shared-exponent rule: scale byte and the exact power of two 2^-X to multiply by.
-__device__ __forceinline__ void mx_scale(float amax, uint32_t* sbyte, float* inv) {
-  if (amax == 0.f) {
-    *sbyte = 127u;
-    *inv = 1.f;
-    return;
-  }
-  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);  // biased exponent
-  const int s = eb - 8 > 0 ? eb - 8 : 0;                                     // X + 127
-  *sbyte = static_cast<uint32_t>(s);
-  *inv = __uint_as_float(static_cast<uint32_t>(254 - s) << 23);              // 2^(127 - s)
-}
-
 // Quantise one lane's chunk; all 32 lanes must call (inactive lanes pass zeros).
 template <typename Tin>
 __device__ __forceinline__ void mx_chunk(const Vec16& v, uint32_t (&codes)[2], uint32_t* sbyte) {

@@ -56,17 +56,15 @@ constexpr int kSfBStage = 4096;                   // MXFP8: raw B scale rows, 25
 constexpr int kSfSlot = kSfAStage + kSfBStage;    // one raw scale slot (4 K-blocks' worth)
 constexpr int kAtomBytes = 1536;                  // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
 // Forward kernels' extra shared memory (after the operand stages): one epilogue
-// staging box per epilogue warp (32 rows x epi_cols bf16; 1 KB aligned for the
-// swizzle), then for MXFP8 the scale atoms of every stage and the two raw
-// scale-row slots.  32-column boxes measured faster than 64-column ones for bf16
-// too (and MXFP8 has room for no more).
-template <int kKind>
-constexpr int epi_cols() { return 32; }
-template <int kKind>
-constexpr int epi_box() { return 32 * epi_cols<kKind>() * 2; }
+// staging box per epilogue warp (32 rows x 64 bytes: 32 bf16 or 64 E4M3 columns;
+// 1 KB aligned for the 64-byte swizzle), then for MXFP8 the scale atoms of every
+// stage and the two raw scale-row slots.  64-byte boxes measured faster than
+// 128-byte ones for bf16 too (and MXFP8 has room for no more).
+constexpr int kEpiRowBytes = 64;
+constexpr int kEpiBox = 32 * kEpiRowBytes;
 constexpr int kEpiOff = 0;
 template <int kKind>
-constexpr int atom_off() { return kEpiOff + 4 * epi_box<kKind>(); }
+constexpr int atom_off() { return kEpiOff + 4 * kEpiBox; }
 template <int kKind>
 constexpr int raw_off() { return atom_off<kKind>() + kStages * kAtomBytes; }
 constexpr int kTmemCols = 512;
@@ -159,6 +157,7 @@ struct Params {
   void* out;               // C / dA / dB
   void* preact_out;        // forward SwiGLU: G|U store (may be null)
   const void* preact_in;   // dgrad dSwiGLU: G|U input
+  uint8_t* out_scales;     // forward with MXFP8 output: E8M0 [M, n_out / 32]
   int32_t* status;
 };
 
@@ -355,49 +354,49 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
   }
 }
 
-// Write one warp's 32 tile rows of bf16 output (one row per lane in pk, two
-// columns per word).  A warp whose 32 rows all belong to the group sends
-// kCols-column boxes through its staging buffer by TMA store, one box in flight
-// (rows of kCols * 2 bytes, 64- or 128-byte swizzle: 16-byte chunk h of row r sits
-// at chunk h ^ ((r >> 1) & 3), resp. h ^ (r & 7)); a warp whose rows cross the
+// Write one warp's 32 tile rows of output, held one row per lane as 32-bit words
+// (two bf16 or four E4M3 values each).  A warp whose 32 rows all belong to the
+// group sends 64-byte-wide boxes (16 words per row; kBoxElems elements) through its
+// 2 KB staging buffer by TMA store, one box in flight; 16-byte chunk h of row r sits
+// at chunk h ^ ((r >> 1) & 3) (64-byte swizzle).  A warp whose rows cross the
 // group's end (the next group's rows follow) stores its valid rows directly.
-template <int kCols, int kWords>
-__device__ __forceinline__ void epi_store_bf16(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
-                                               int lane, uint16_t* out, int row0, int rows_valid, int col0,
+template <int kBoxElems, int kWords>
+__device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
+                                               int lane, uint8_t* out, int row0, int rows_valid, int col0,
                                                int n_out) {
-  static_assert(kCols == 32 || kCols == 64, "box width");
-  constexpr int kChunks = kCols / 8;                  // 16-byte chunks per row
+  constexpr int kElemBytes = kEpiRowBytes / kBoxElems;
+  const size_t row_bytes = static_cast<size_t>(n_out) * kElemBytes;
   if (rows_valid >= 32) {
 #pragma unroll
-    for (int c = 0; c < kWords / (kCols / 2); ++c) {
-      if (col0 + c * kCols >= n_out) break;
+    for (int c = 0; c < kWords / 16; ++c) {
+      if (col0 + c * kBoxElems >= n_out) break;
       if (lane == 0) bulk_wait_read0();   // the previous box has left the buffer
       __syncwarp();
-      const int sw = kCols == 32 ? (lane >> 1) & 3 : lane & 7;
+      const int sw = (lane >> 1) & 3;
 #pragma unroll
-      for (int h = 0; h < kChunks; ++h) {
-        const int w0 = c * (kCols / 2) + 4 * h;
-        *reinterpret_cast<uint4*>(stg + lane * (kCols * 2) + ((h ^ sw) * 16)) =
+      for (int h = 0; h < 4; ++h) {
+        const int w0 = c * 16 + 4 * h;
+        *reinterpret_cast<uint4*>(stg + lane * kEpiRowBytes + ((h ^ sw) * 16)) =
             make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tmD, stg, col0 + c * kCols, row0);
+        tma_store_2d(tmD, stg, col0 + c * kBoxElems, row0);
         bulk_commit();
       }
     }
   } else if (lane < rows_valid) {
 #pragma unroll
     for (int c = 0; c < kWords / 16; ++c) {
-      const int col = col0 + c * 32;
-      if (col < n_out) {
-        uint4* d4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + lane) * n_out + col);
+      const int col = col0 + c * kBoxElems;
+      uint4* d4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + lane) * row_bytes +
+                                           static_cast<size_t>(col) * kElemBytes);
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+      for (int h = 0; h < 4; ++h)   // n_out is a multiple of 16 bytes' worth: check per chunk
+        if (col + h * (16 / kElemBytes) < n_out)
           d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
                              pk[c * 16 + 4 * h + 3]);
-      }
     }
   }
 }
@@ -442,7 +441,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (kMode == kWgrad || (kMode == kFwd && sizeof(OutT) == 2)) tma_prefetch_desc(&tmD);
+    if (kMode == kWgrad || (kMode == kFwd && sizeof(OutT) <= 2)) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -700,6 +699,65 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             bulk_commit();
           }
         }
+      } else if constexpr (sizeof(OutT) == 1) {
+        // MXFP8 output: the 32 consecutive columns a thread holds of its row are one
+        // 32-element block.  The values are rounded to bf16 while the accumulator is
+        // read (so the result equals a bf16 store followed by row-wise quantisation);
+        // after its release, each block's shared exponent comes from its amax and the
+        // codes are E4M3 with round-to-nearest-even and saturation.
+        constexpr int NB = (kEpi == kEpiSwiglu ? BN / 2 : BN) / 32;   // blocks per tile row
+        uint32_t pk[NB * 16];
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          if constexpr (kEpi == kEpiSwiglu) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tb + c * 32, gv);
+            tmem_ld32(tb + BN / 2 + c * 32, uv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[c * 16 + i] = pack_bf16x2(silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]),
+                                           silu_f(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]));
+          } else {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+        released = true;
+        uint32_t cw[NB * 8];
+        uint32_t sb[NB];
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(static_cast<uint16_t>(pk[c * 16 + i] & 0xFFFFu))),
+                                     fabsf(bf16_to_f32(static_cast<uint16_t>(pk[c * 16 + i] >> 16)))));
+          float inv;
+          mx_scale(amax, &sb[c], &inv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t w0 = pk[c * 16 + 2 * i], w1 = pk[c * 16 + 2 * i + 1];
+            cw[c * 8 + i] =
+                static_cast<uint32_t>(f32x2_to_e4m3x2(bf16_to_f32(static_cast<uint16_t>(w0 & 0xFFFFu)) * inv,
+                                                      bf16_to_f32(static_cast<uint16_t>(w0 >> 16)) * inv)) |
+                (static_cast<uint32_t>(f32x2_to_e4m3x2(bf16_to_f32(static_cast<uint16_t>(w1 & 0xFFFFu)) * inv,
+                                                       bf16_to_f32(static_cast<uint16_t>(w1 >> 16)) * inv)) << 16);
+          }
+        }
+        epi_store_rows<64>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, cw, lane,
+                           reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+        if (r < t.rows) {
+          uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
+#pragma unroll
+          for (int c = 0; c < NB; ++c)
+            if (t.col0 + 32 * c < g.n_out) srow[t.col0 / 32 + c] = static_cast<uint8_t>(sb[c]);
+        }
       } else if constexpr (kEpi == kEpiSwiglu) {
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
@@ -720,8 +778,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          epi_store_bf16<epi_cols<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_box<kKind>(), pk, lane,
-                         reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+          epi_store_rows<32>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+                             reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -792,8 +850,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           mbar_arrive(&s.tempty[acc]);
           released = true;
           if constexpr (kMode == kFwd) {
-            epi_store_bf16<epi_cols<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_box<kKind>(), pk, lane,
-                           reinterpret_cast<uint16_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+            epi_store_rows<32>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+                               reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
@@ -978,19 +1036,16 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   if (!make_map(&ta, map_type(A->dtype), eb, A->ptr, 2, adims, abox) ||
       !make_map(&tb, map_type(A->dtype), eb, B->ptr, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
-  Params p{offsets, M, N, K, E, C, preact, nullptr, dev_status};
+  Params p{offsets, M, N, K, E, C, preact, nullptr, nullptr, dev_status};
   const bool sw = epi == MOE_EPI_SWIGLU;
   const bool f32 = c_dtype == MOE_F32;
-  // bf16 C [M, n_out] is written by TMA from 32-row staging boxes: 32 columns with
-  // 64-byte swizzle (MXFP8) or 64 columns with 128-byte swizzle (tf32 / bf16)
+  // bf16 C [M, n_out] is written by TMA from 32-row x 32-column staging boxes
+  // (64-byte rows, 64-byte swizzle)
   CUtensorMap td = ta;
   if (!f32) {
-    const bool mx = A->dtype == MOE_E4M3;
     const uint64_t cdims[2] = {static_cast<uint64_t>(sw ? N / 2 : N), static_cast<uint64_t>(M)};
-    const int cols = mx ? epi_cols<2>() : epi_cols<1>();
-    const uint32_t cbox[2] = {static_cast<uint32_t>(cols), 32};
-    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox,
-                  cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint32_t cbox[2] = {kEpiRowBytes / 2, 32};
+    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
       return MOE_ERR_INVALID_ARG;
   }
   if (A->dtype == MOE_E4M3) {
@@ -1017,6 +1072,52 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
                      : launch<1, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   return f32 ? launch<1, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn)
              : launch<1, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
+}
+
+extern "C" moe_status_t moe_grouped_gemm_fwd_mxfp8_out(const moe_operand_t* A, const moe_operand_t* B,
+                                                       const int32_t* offsets, int M, int N, int K, int E,
+                                                       moe_epilogue_t epi, uint8_t* c_codes, uint8_t* c_scales,
+                                                       int32_t* dev_status, cudaStream_t stream) {
+  const char* fn = "moe_grouped_gemm_fwd_mxfp8_out";
+  int sms = 0;
+  moe_status_t st = common_checks(fn, A, B, offsets, M, N, K, E, c_codes, &sms);
+  if (st != MOE_OK) return st;
+  if ((epi != MOE_EPI_NONE && epi != MOE_EPI_SWIGLU) || (epi == MOE_EPI_SWIGLU && N % 64) ||
+      (M > 0 && !c_scales)) {
+    set_error("%s: epi NONE|SWIGLU (SWIGLU: N %% 64 == 0) and an output scale buffer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (A->dtype != MOE_E4M3) {
+    set_error("%s: MXFP8 (E4M3) operands only", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (!A->scales || !B->scales || K % 512 || !aligned16(A->scales) || !aligned16(B->scales)) {
+    set_error("%s: MXFP8 needs 16-byte aligned A and B scales and K %% 512 == 0", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M == 0) return MOE_OK;
+  const bool sw = epi == MOE_EPI_SWIGLU;
+  const int n_out = sw ? N / 2 : N;
+  CUtensorMap ta, tb, tsa, tsb, td;
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint32_t abox[2] = {kBKBytes, kBM};
+  const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+  const uint32_t bbox[3] = {kBKBytes, static_cast<uint32_t>(sw ? kBN / 2 : kBN), 1};
+  const uint64_t sadims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M)};
+  const uint64_t sbdims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(N) * static_cast<uint64_t>(E)};
+  const uint32_t sbox[2] = {16, kBM};
+  // codes [M, n_out] are written by TMA from 32-row x 64-column staging boxes
+  const uint64_t cdims[2] = {static_cast<uint64_t>(n_out), static_cast<uint64_t>(M)};
+  const uint32_t cbox[2] = {kEpiRowBytes, 32};
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->ptr, 2, adims, abox) ||
+      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->ptr, 3, bdims, bbox) ||
+      !make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, c_codes, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_INVALID_ARG;
+  Params p{offsets, M, N, K, E, c_codes, nullptr, nullptr, c_scales, dev_status};
+  if (sw) return launch<2, kFwd, kEpiSwiglu, uint8_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
+  return launch<2, kFwd, kEpiNone, uint8_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const moe_operand_t* B,
@@ -1046,7 +1147,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC->ptr, 2, adims, abox) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B->ptr, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
-  Params p{offsets, M, N, K, E, dA, nullptr, preact, dev_status};
+  Params p{offsets, M, N, K, E, dA, nullptr, preact, nullptr, dev_status};
   if (epi == MOE_EPI_DSWIGLU) return launch<1, kDgrad, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn);
   return launch<1, kDgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
 }
@@ -1079,6 +1180,6 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint32_t dbox[3] = {64, 32, 1};
   if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox)) return MOE_ERR_INVALID_ARG;
-  Params p{offsets, M, N, K, E, dB, nullptr, nullptr, dev_status};
+  Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status};
   return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }

@@ -45,7 +45,8 @@ class MoELayer:
         self.src_pair = torch.empty(M, **i32)
         self.workspace = torch.empty(B.moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
         self.dev_status = torch.zeros(1, **i32)
-        self.h = torch.empty(M, f, dtype=store, device=dev)
+        # MXFP8: GEMM1 writes H straight as MXFP8 codes + scales (hq, hs)
+        self.h = torch.empty(M, f, dtype=store, device=dev) if dtype != "mxfp8" or training else None
         self.yp = torch.empty(M, d, dtype=store, device=dev)
         self.y = torch.empty(T, d, dtype=store, device=dev)
         self.gu = torch.empty(M, 2 * f, dtype=store, device=dev) if training else None
@@ -88,9 +89,9 @@ class MoELayer:
 
     def expert_mlp(self):
         if self.dtype == "mxfp8":
-            B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
-                                   B_scales=self.W1s, out=self.h, dev_status=self.dev_status)
-            B.moe_quantize_mxfp8_grouped(self.h, self.offsets, self.E, codes=self.hq, scales=self.hs)
+            B.moe_grouped_gemm_fwd_mxfp8_out(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
+                                             B_scales=self.W1s, codes=self.hq, scales=self.hs,
+                                             dev_status=self.dev_status)
             B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
                                    out=self.yp, dev_status=self.dev_status)
         else:
@@ -113,8 +114,8 @@ class MoELayer:
 
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
-        scan, scatter), GEMM1, [MXFP8 quantise of H], GEMM2, combine."""
-        return 2 + 3 + 2 + (1 if self.dtype == "mxfp8" else 0) + 1
+        scan, scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine."""
+        return 2 + 3 + 2 + 1
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd."""

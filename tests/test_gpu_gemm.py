@@ -243,6 +243,46 @@ def test_fwd_mxfp8_swiglu_f32_out_and_preact(f):
     assert rel_l2(f64(H), om.swiglu(gu)) < 1e-3
 
 
+@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
+@pytest.mark.parametrize("epi,K,N", [("swiglu", 512, 256), ("swiglu", 1024, 576), ("none", 512, 320),
+                                     ("none", 512, 64)], ids=["swiglu-f128", "swiglu-f288", "none-N320", "none-N64"])
+def test_fwd_mxfp8_out(counts, epi, K, N):
+    """GEMM with the result quantised to MXFP8 in its epilogue: codes and scales
+    equal, bit for bit, the bf16 result of the same GEMM passed through the row-wise
+    quantiser (itself pinned bit-exactly against the oracle's quantiser); the
+    decoded values match the oracle's result on the same quantised operands."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 2
+    rows = int(sum(cnt))
+    A, B = _mats(M, K, N, E, torch.bfloat16, seed=K + N + 13)
+    Aq, As, A_deq = _quantize(A)
+    Bq, Bs, B_deq = _quantize(B)
+    off = ragged_offsets(cnt)
+    n_out = N // 2 if epi == "swiglu" else N
+    codes = torch.full((M, n_out), 0xAB, dtype=torch.uint8, device="cuda")
+    scales = torch.full((M, n_out // 32), 0xCD, dtype=torch.uint8, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd_mxfp8_out(Aq, Bq, off, epi=epi, A_scales=As, B_scales=Bs, codes=codes,
+                                           scales=scales)
+    C = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi=epi, A_scales=As, B_scales=Bs)
+    cq, cs = moe_gpu.moe_quantize_mxfp8_grouped(C[:rows].contiguous())
+    assert torch.equal(codes[:rows], cq) and torch.equal(scales[:rows], cs)
+    assert (codes[rows:] == 0xAB).all() and (scales[rows:] == 0xCD).all()     # rows outside every group
+    want = om.grouped_gemm(A_deq, B_deq.reshape(E, N, K), off.cpu().numpy())
+    if epi == "swiglu":
+        want = om.swiglu(want)
+    got = omx.dequantize_rowwise(codes[:rows].cpu().numpy(), scales[:rows].cpu().numpy())
+    assert rel_l2(got, want[:rows]) < TOL_MXFP8
+
+
+def test_fwd_mxfp8_out_rejects_bf16_operands():
+    need_gpu()
+    A, B = _mats(64, 512, 64, 2, torch.bfloat16, seed=3)
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_grouped_gemm_fwd_mxfp8_out(A, B, ragged_offsets([32, 32]))
+
+
 def test_fwd_mxfp8_requires_scales_and_k_multiple_of_512():
     need_gpu()
     A, B = _mats(64, 256, 64, 2, torch.bfloat16, seed=1)

@@ -17,6 +17,7 @@ import torch
 import ragged_grouped_gemm_topk_gb300 as moe_gpu
 from ragged_grouped_gemm_topk_gb300 import workloads as W
 from oracle import moe as om
+from oracle import mxfp8 as omx
 from _parity import TOL_BF16, TOL_MXFP8, f64, i64, logits_dev, need_gpu, rel_l2
 
 pytestmark = pytest.mark.gpu
@@ -57,6 +58,13 @@ def _sample_experts(counts, rng, n_random=2):
     return sorted(picks)
 
 
+def _h_values(layer):
+    """H as the layer holds it: bf16, or (MXFP8) decoded from its codes and scales."""
+    if layer.dtype != "mxfp8":
+        return f64(layer.h)
+    return omx.dequantize_rowwise(layer.hq.cpu().numpy(), layer.hs.cpu().numpy())
+
+
 def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=6, rows_per_expert=12, seed=0):
     """Full integer parity + sampled float parity for a large workload."""
     rng = np.random.default_rng(seed)
@@ -90,8 +98,8 @@ def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=6, rows_per_expert=12,
         h = om.swiglu(xr @ w1.T)
         yp = (om.mx_roundtrip(h) if mx else h) @ w2.T
         r = torch.from_numpy(rows).cuda()
-        h_got.append(f64(layer.h[r]))
-        h_want.append(h)
+        h_got.append(_h_values(layer)[rows] if mx else f64(layer.h[r]))
+        h_want.append(om.mx_roundtrip(h) if mx else h)
         y_got.append(f64(layer.yp[r]))
         y_want.append(yp)
     assert rel_l2(np.concatenate(h_got), np.concatenate(h_want)) < tol
@@ -197,7 +205,9 @@ def test_mxfp8_layer_scaled_full():
     assert int(layer.dev_status.item()) == 0
     ref = om.layer_forward(f64(x), lg.cpu().numpy(), f64(W1), f64(W2), w.k, mxfp8_operands=True)
     assert (i64(layer.src_pair) == ref["src_pair"]).all()
-    assert rel_l2(f64(layer.h), ref["H"]) < TOL_MXFP8
+    # GEMM1 writes H as MXFP8: compare its dequantised values with the oracle's H
+    # after the oracle's own MXFP8 round trip (what the oracle feeds GEMM2)
+    assert rel_l2(_h_values(layer), om.mx_roundtrip(ref["H"])) < TOL_MXFP8
     assert rel_l2(f64(y), ref["y"]) < TOL_MXFP8
 
 
