@@ -156,10 +156,19 @@ moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, int T, int 
  * codes = round-to-nearest-even(v / 2^X) to E4M3, saturated to +-448.
  *
  * in     [rows, K] MOE_BF16 or MOE_F32; K % 32 == 0.
- * codes  [rows, K] uint8 out; scales [rows, K/32] uint8 out.
- * offsets/E: the expert groups of the rows.  Row-wise blocks lie inside one row
- *        and so inside one group by construction; offsets may be NULL.
- * axis   0 = row-wise (the only axis built; others return MOE_ERR_UNSUPPORTED).
+ * codes  [rows, K] uint8 out (both axes).
+ * axis   0 = row-wise: blocks of 32 along a row (the forward operands);
+ *        scales [rows, K/32] uint8 out.  Row-wise blocks lie inside one row and so
+ *        inside one group; offsets may be NULL.
+ *        1 = column-wise, group-aware (the operands that contract over rows, as in
+ *        the weight gradient): blocks of 32 consecutive rows of one column that
+ *        restart at every group start ([1] "grouped quantisation"); a group's last
+ *        partial block is zero-padded (the padding has no codes).  offsets [E+1]
+ *        (device, as from moe_permute) and 1 <= E <= 1024 required.  scales
+ *        [n_blocks, K] uint8 out with group e's blocks from row sum over e' < e of
+ *        ceil(count_e' / 32); the caller's buffer must hold ceil(rows/32) + E rows
+ *        (the bound on n_blocks); rows past n_blocks are not written.
+ * MOE_ERR_UNSUPPORTED for any other axis.
  */
 moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows, int K,
                                         const int32_t* offsets, int E, int axis,

@@ -96,12 +96,17 @@ def moe_permute(x, topk_idx, counts, E, *, xp_dtype=None, rows=True, offsets=Non
     return dict(offsets=offsets, dest_row=dest_row, src_pair=src_pair, xp=xp, xp_scales=xp_scales)
 
 
-def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=None):
-    """Row-wise MXFP8 of inp [rows,K] (bf16/fp32) -> (codes u8 [rows,K], scales u8 [rows,K/32])."""
+def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=None, axis=0):
+    """MXFP8 of inp [rows,K] (bf16/fp32) -> (codes u8 [rows,K], scales u8).
+    axis 0: row-wise, scales [rows, K/32].  axis 1: column-wise and group-aware
+    (offsets [E+1] required), scales [ceil(rows/32) + E, K] of which the first
+    sum_e ceil(count_e/32) rows are written."""
     rows, K = inp.shape
     codes = codes if codes is not None else torch.empty(rows, K, dtype=torch.uint8, device=inp.device)
-    scales = scales if scales is not None else torch.empty(rows, K // 32, dtype=torch.uint8, device=inp.device)
-    _lib.call("moe_quantize_mxfp8_grouped", _ptr(inp), _dt(inp), rows, K, _ptr(offsets), E, 0,
+    if scales is None:
+        shape = (rows, K // 32) if axis == 0 else ((rows + 31) // 32 + E, K)
+        scales = torch.empty(*shape, dtype=torch.uint8, device=inp.device)
+    _lib.call("moe_quantize_mxfp8_grouped", _ptr(inp), _dt(inp), rows, K, _ptr(offsets), E, axis,
               _ptr(codes), _ptr(scales), _stream())
     return codes, scales
 

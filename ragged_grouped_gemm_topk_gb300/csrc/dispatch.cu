@@ -309,6 +309,141 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
   }
 }
 
+// Column-wise, group-aware MXFP8: a block is 32 consecutive rows of one column,
+// blocks restart at every group start, and the rows of a group's last block past
+// its end count as zeros (they never change the amax and get no codes).  Block
+// rows are numbered group by group: group e's first is sum over e' < e of
+// ceil(count_e' / 32).  One work item = (block row, strip of columns); each thread
+// owns 4 adjacent columns (an 8- or 16-byte chunk) and keeps the block's 32 rows of
+// them in registers (32 loads in flight), so reads and writes stay row-contiguous
+// across the warp.
+constexpr int kColThreads = 128;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
+    const uint8_t* __restrict__ in, int rows, int K, const int32_t* __restrict__ offsets, int E,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  pdl_begin();
+  constexpr int EB = sizeof(Tin);
+  constexpr int CPT = 4;                       // columns per thread
+  constexpr int NW = CPT * EB / 4;             // 32-bit words per chunk
+  constexpr int kStrip = kColThreads * CPT;
+  __shared__ int bpre[1025];                   // block-row prefix per group
+  __shared__ int part[kColThreads];
+  // blocks per group (invalid groups count as empty), then an exclusive scan
+  constexpr int G = 1024 / kColThreads;        // groups per thread (E <= 1024)
+  int cnt[G], sum = 0;
+#pragma unroll
+  for (int u = 0; u < G; ++u) {
+    const int e = threadIdx.x * G + u;
+    int c = 0;
+    if (e < E) {
+      const int lo = offsets[e], hi = offsets[e + 1];
+      if (lo >= 0 && hi >= lo && hi <= rows) c = (hi - lo + 31) / 32;
+    }
+    cnt[u] = c;
+    sum += c;
+  }
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int base = 0; base < kColThreads; base += 32) {
+      int v = part[base + threadIdx.x];
+      const int own = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int w = __shfl_up_sync(kFull, v, off);
+        if (static_cast<int>(threadIdx.x) >= off) v += w;
+      }
+      part[base + threadIdx.x] = carry + v - own;   // exclusive
+      carry += __shfl_sync(kFull, v, 31);
+    }
+  }
+  __syncthreads();
+  {
+    int run = part[threadIdx.x];
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const int e = threadIdx.x * G + u;
+      if (e < E) bpre[e] = run;
+      run += cnt[u];
+    }
+    if (threadIdx.x == kColThreads - 1) bpre[E] = run;   // every block row
+  }
+  __syncthreads();
+  const int total = bpre[E];
+  const int nstrip = (K + kStrip - 1) / kStrip;
+  const size_t in_row = static_cast<size_t>(K) * EB;
+  for (long long task = blockIdx.x; task < static_cast<long long>(total) * nstrip; task += gridDim.x) {
+    const int br = static_cast<int>(task / nstrip);
+    const int strip = static_cast<int>(task % nstrip);
+    int lo_e = 0, hi_e = E - 1;                 // last group whose first block row <= br
+    while (lo_e < hi_e) {
+      const int mid = (lo_e + hi_e + 1) >> 1;
+      if (bpre[mid] <= br) lo_e = mid; else hi_e = mid - 1;
+    }
+    const int r0 = offsets[lo_e] + (br - bpre[lo_e]) * 32;
+    const int n = min(32, offsets[lo_e + 1] - r0);
+    const int col = strip * kStrip + CPT * threadIdx.x;   // K % 32 == 0: a chunk is all in or all out
+    if (col >= K) continue;
+    uint32_t raw[32][NW];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint8_t* src = in + static_cast<size_t>(r0 + i) * in_row + static_cast<size_t>(col) * EB;
+      if constexpr (NW == 2) {
+        const uint2 u = i < n ? *reinterpret_cast<const uint2*>(src) : make_uint2(0u, 0u);
+        raw[i][0] = u.x;
+        raw[i][1] = u.y;
+      } else {
+        const uint4 u = i < n ? *reinterpret_cast<const uint4*>(src) : make_uint4(0u, 0u, 0u, 0u);
+        raw[i][0] = u.x;
+        raw[i][1] = u.y;
+        raw[i][2] = u.z;
+        raw[i][3] = u.w;
+      }
+    }
+    auto decode = [](const uint32_t (&w)[NW], float (&f)[CPT]) {
+      if constexpr (NW == 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          f[2 * j] = bf16_to_f32(static_cast<uint16_t>(w[j] & 0xFFFFu));
+          f[2 * j + 1] = bf16_to_f32(static_cast<uint16_t>(w[j] >> 16));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = __uint_as_float(w[j]);
+      }
+    };
+    float amax[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) amax[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float f[CPT];
+      decode(raw[i], f);
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) amax[j] = fmaxf(amax[j], fabsf(f[j]));
+    }
+    uint32_t sb[CPT];
+    float inv[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) mx_scale(amax[j], &sb[j], &inv[j]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < n) {
+        float f[CPT];
+        decode(raw[i], f);
+        *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r0 + i) * K + col) =
+            static_cast<uint32_t>(f32x2_to_e4m3x2(f[0] * inv[0], f[1] * inv[1])) |
+            (static_cast<uint32_t>(f32x2_to_e4m3x2(f[2] * inv[2], f[3] * inv[3])) << 16);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(scales + static_cast<size_t>(br) * K + col) =
+        sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+  }
+}
+
 int scatter_grid(int T, int sms) {
   const int wpb = kScatterThreads / 32;
   int g = (T + wpb - 1) / wpb;
@@ -440,11 +575,13 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
                                                    int K, const int32_t* offsets, int E, int axis,
                                                    uint8_t* codes, uint8_t* scales,
                                                    cudaStream_t stream) {
-  (void)offsets;
-  (void)E;
-  if (axis != 0) {
-    set_error("moe_quantize_mxfp8_grouped: only axis 0 (row-wise) is built");
+  if (axis != 0 && axis != 1) {
+    set_error("moe_quantize_mxfp8_grouped: axis 0 (row-wise) or 1 (column-wise)");
     return MOE_ERR_UNSUPPORTED;
+  }
+  if (axis == 1 && (!offsets || E < 1 || E > 1024)) {
+    set_error("moe_quantize_mxfp8_grouped: column-wise needs offsets and 1 <= E <= 1024");
+    return MOE_ERR_INVALID_ARG;
   }
   if (rows < 0 || K < 0 || K % 32 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
     set_error("moe_quantize_mxfp8_grouped: need rows >= 0, K %% 32 == 0, BF16/F32 input");
@@ -457,6 +594,18 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (rows == 0 || K == 0) return MOE_OK;
+  if (axis == 1) {
+    const int strip = kColThreads * 4;
+    const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
+    const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
+    if (in_dtype == MOE_BF16)
+      launch_pdl(quantize_colwise_kernel<uint16_t>, grid, kColThreads, 0, stream,
+                 static_cast<const uint8_t*>(in), rows, K, offsets, E, codes, scales);
+    else
+      launch_pdl(quantize_colwise_kernel<float>, grid, kColThreads, 0, stream,
+                 static_cast<const uint8_t*>(in), rows, K, offsets, E, codes, scales);
+    return check_launch("moe_quantize_mxfp8_grouped");
+  }
   const int grid = scatter_grid(rows, sms);
   if (in_dtype == MOE_BF16)
     launch_pdl(quantize_rowwise_kernel<uint16_t>, grid, kScatterThreads, 0, stream, 

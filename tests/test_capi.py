@@ -68,7 +68,9 @@ def test_bad_arguments_rejected_before_any_launch():
     st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 48, None, 0, 0, None, None, None)
     assert st == _lib.MOE_ERR_INVALID_ARG
     st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 1, None, None, None)
-    assert st == _lib.MOE_ERR_UNSUPPORTED
+    assert st == _lib.MOE_ERR_INVALID_ARG                                      # column-wise without groups
+    st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 2, None, None, None)
+    assert st == _lib.MOE_ERR_UNSUPPORTED                                      # no such axis
 
 
 def test_no_cpu_fallback_in_product_package():

@@ -160,6 +160,44 @@ def test_quantize_rowwise_bit_exact(dtype):
     assert (scales.cpu().numpy() == s).all()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("counts,K", [([0, 1, 130, 257, 3, 128, 0, 64], 2048),   # empty, single, partial blocks
+                                      ([33] * 5, 544),                            # strip tail (544 = 512 + 32)
+                                      ([0, 0, 700], 32),                          # leading empty groups
+                                      ([31, 32, 0, 65, 1], 96),
+                                      ([1] * 300, 64)],                           # many one-row groups
+                         ids=["mixed", "K544", "lead-empty", "edges", "singles"])
+def test_quantize_colwise_grouped_bit_exact(dtype, counts, K):
+    """Column-wise group-aware MXFP8 (blocks of 32 rows restarting per group, the
+    last one zero-padded) against the oracle: codes and every written scale row
+    bit-exact; scale rows past the blocks untouched."""
+    need_gpu()
+    rows = int(sum(counts))
+    a = W.make_matrix(rows, K, seed=len(counts) + K, dtype=dtype, device="cuda")
+    if rows > 40:
+        a[3:6, :] = 0                                     # zero rows inside a block
+        a[40, 0] = 448.0 * 2.0 ** 20                      # saturation boundary
+        a[41, 1] = -0.0
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    E = len(counts)
+    cap = (rows + 31) // 32 + E
+    codes = torch.full((rows, K), 0x5A, dtype=torch.uint8, device="cuda")
+    scales = torch.full((cap, K), 0xA5, dtype=torch.uint8, device="cuda")
+    moe_gpu.moe_quantize_mxfp8_grouped(a, off, E, codes=codes, scales=scales, axis=1)
+    c, sc = omx.quantize_colwise_grouped(f64(a), off.cpu().numpy())
+    assert (codes.cpu().numpy() == c).all()
+    n = sc.shape[0]
+    assert (scales[:n].cpu().numpy() == sc).all()
+    assert (scales[n:] == 0xA5).all()
+
+
+def test_quantize_colwise_needs_offsets():
+    need_gpu()
+    a = W.make_matrix(64, 64, seed=1, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_quantize_mxfp8_grouped(a, None, 0, axis=1)
+
+
 def _combine_bound(yp64, dest, w):
     """|fp32 sum of k products rounded once to bf16 - exact| <= 2^-8 * sum_j |w_j yp_j|."""
     T, k = dest.shape
