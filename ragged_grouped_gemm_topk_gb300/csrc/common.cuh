@@ -217,6 +217,13 @@ __device__ __forceinline__ void st_global_hint(void* dst, uint4 v, uint64_t pol)
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Allow at most N of this thread's committed bulk store groups to be still
+// reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Wait until this thread's committed bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

@@ -109,15 +109,15 @@ struct Cfg {
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
-// wgrad: each epilogue warp stages kWgBoxes 64-column boxes of its 32 dW rows
-// (4 KB each) for the TMA store (with one box per warp the 4-stage operand ring
-// still fits), and a 7th warp writes the dW of experts without rows.  Forward:
+// wgrad: each epilogue warp stages its 32 dW rows in kWgBufs rotating 2 KB boxes of
+// 32 columns for the TMA store (so the 4-stage operand ring still fits), and a 7th
+// warp writes the dW of experts without rows.  Forward:
 // each epilogue warp stages one 32-row x 32-column bf16 box (2 KB) of its output
 // for the TMA store.
-constexpr int kWgBoxes = 1;
-constexpr int kWgStage = 4096 * kWgBoxes;
+constexpr int kWgBufs = 3;                        // 2 KB staging boxes per epilogue warp
+constexpr int kWgStage = 2048 * kWgBufs;
 template <int kKind, int kMode>
-constexpr int stages_for() { return (kMode == kWgrad && kWgBoxes > 1) ? 3 : kStages; }
+constexpr int stages_for() { return kStages; }
 template <int kKind, int kMode>
 constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
@@ -662,40 +662,38 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       bool released = false;
       if constexpr (kMode == kWgrad) {
-        // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns, written by TMA (clipped
-        // at N and K) in rounds of kWgBoxes 64-column, 128-byte-swizzled boxes staged
-        // in this warp's shared buffer.
+        // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns: the accumulator is read
+        // whole into registers and released, then written by TMA (clipped at N and K) in
+        // 32-column boxes (64-byte swizzle) through the warp's kWgBufs rotating 2 KB
+        // staging buffers, so boxes are staged while earlier ones are still read.
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        }
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+        released = true;
         uint8_t* stg = tiles + NS * C::kStage + q * kWgStage;
-#pragma unroll 1
-        for (int round = 0; round < 4 / kWgBoxes; ++round) {
-          if (lane == 0) bulk_wait_read0();   // the previous round's stores have read stg
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          if (t.col0 + 32 * c >= p.K) break;      // warp-uniform: past the last dW column
+          uint8_t* buf = stg + (c % kWgBufs) * 2048;
+          if (lane == 0) bulk_wait_read<kWgBufs - 1>();   // the box that last used buf is read
           __syncwarp();
-#pragma unroll 1
-          for (int cc = 0; cc < 2 * kWgBoxes; ++cc) {
-            uint32_t v[32], pk[16];
-            tmem_ld32(tb + (round * 2 * kWgBoxes + cc) * 32, v);
-            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            uint8_t* box = stg + (cc >> 1) * 4096 + lane * 128;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const int chunk = (cc & 1) * 4 + h;
-              *reinterpret_cast<uint4*>(box + ((chunk ^ (lane & 7)) * 16)) =
-                  make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
-            }
-          }
-          if (round == 4 / kWgBoxes - 1) {
-            tc_fence_before();
-            mbar_arrive(&s.tempty[acc]);
-            released = true;
-          }
+          for (int h = 0; h < 4; ++h)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((h ^ sw) * 16)) =
+                make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2], pk[c * 16 + 4 * h + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < kWgBoxes; ++j)
-              tma_store_3d(&tmD, stg + j * 4096, t.col0 + 64 * (round * kWgBoxes + j), t.n0 + 32 * q, t.e);
+            tma_store_3d(&tmD, buf, t.col0 + 32 * c, t.n0 + 32 * q, t.e);
             bulk_commit();
           }
         }
@@ -1175,11 +1173,12 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cptr, 2, cdims, box) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aptr, 2, adims, box))
     return MOE_ERR_INVALID_ARG;
-  // dB [E, N, K] is written by TMA from 64-column x 32-row staging boxes
+  // dB [E, N, K] is written by TMA from 32-column x 32-row staging boxes (64-byte swizzle)
   CUtensorMap td;
   const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
-  const uint32_t dbox[3] = {64, 32, 1};
-  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox)) return MOE_ERR_INVALID_ARG;
+  const uint32_t dbox[3] = {32, 32, 1};
+  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status};
   return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }
