@@ -10,11 +10,12 @@
 //            a pair's rank among earlier tokens of the same expert is a popcount;
 //            per-warp counts are scanned inside the block and the block's
 //            per-expert totals go to the workspace.
-//   scan     one block: offsets = exclusive scan of counts, then for every expert
-//            an exclusive scan of the block totals down the blocks.
-//   scatter  one warp per token: dest_row / src_pair, then the token's row is
-//            copied with 16-byte loads (8 per lane in flight) and stores to its
-//            k rows, optionally quantised to MXFP8 on the way.
+//   scatter  every CTA scans the routed counts into offsets (CTA 0 publishes
+//            them and checks them against the rank pass); one warp per token
+//            adds the counts of its expert in the earlier rank blocks (a warp
+//            reduction) to get dest_row / src_pair, then copies the token's row
+//            with 16-byte loads (8 per lane in flight) and stores to its k rows,
+//            optionally quantised to MXFP8 on the way.
 //
 // MXFP8 follows the OCP Microscaling Formats v1.0 conversion (shared exponent
 // floor(log2 amax) - 8, clamped to [-127, 127]; E4M3 round-to-nearest-even with
@@ -71,63 +72,6 @@ __global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
       local_rank[static_cast<size_t>(t) * k + j] = r;
     }
   }
-}
-
-// Single block of 1024 threads; thread e owns expert e.
-__global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ counts,
-                                                            int E, int nblk, int total,
-                                                            int32_t* __restrict__ block_hist,
-                                                            int32_t* __restrict__ offsets,
-                                                            int32_t* status) {
-  pdl_begin();
-  __shared__ int warp_sum[32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  const int c = e < E ? counts[e] : 0;
-  int incl = c;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(kFull, incl, off);
-    if (lane >= off) incl += v;
-  }
-  if (lane == 31) warp_sum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int s = warp_sum[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(kFull, s, off);
-      if (lane >= off) s += v;
-    }
-    warp_sum[lane] = s;  // inclusive over warps
-  }
-  __syncthreads();
-  const int excl = incl - c + (warp > 0 ? warp_sum[warp - 1] : 0);
-  if (e < E) {
-    offsets[e] = excl;
-    if (e == E - 1) {
-      offsets[E] = excl + c;
-      if (excl + c != total) flag_error(status, MOE_DEV_BAD_INDEX);
-    }
-    int run = excl;
-    int b = 0;
-    for (; b + 8 <= nblk; b += 8) {
-      int h[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) h[u] = block_hist[static_cast<size_t>(b + u) * E + e];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        block_hist[static_cast<size_t>(b + u) * E + e] = run;
-        run += h[u];
-      }
-    }
-    for (; b < nblk; ++b) {
-      const int h = block_hist[static_cast<size_t>(b) * E + e];
-      block_hist[static_cast<size_t>(b) * E + e] = run;
-      run += h;
-    }
-    if (run != excl + c) flag_error(status, MOE_DEV_BAD_INDEX);
-  }
-  if (E == 0 && e == 0) offsets[0] = 0;
 }
 
 struct alignas(16) Vec16 {
@@ -191,12 +135,54 @@ constexpr int kScatterU = 8;
 template <typename Tin, bool kQuant>
 __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     const uint8_t* __restrict__ x, int T, int d, const int32_t* __restrict__ idx, int k, int E,
-    const int32_t* local_rank, const int32_t* __restrict__ block_base,
-    int32_t* dest_row, int32_t* __restrict__ src_pair, uint8_t* __restrict__ xp,
-    uint8_t* __restrict__ xp_scales, int32_t* status) {
+    const int32_t* __restrict__ counts, const int32_t* local_rank, const int32_t* __restrict__ block_hist,
+    int nblk, int32_t* __restrict__ offsets, int32_t* dest_row, int32_t* __restrict__ src_pair,
+    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_scales, int32_t* status) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
+  // offsets = exclusive scan of the routed counts, in every CTA (E <= 1024)
+  __shared__ int s_off[1025];
+  __shared__ int s_part[kScatterThreads / 32];
+  {
+    constexpr int G = 1024 / kScatterThreads;
+    int c[G], sum = 0;
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const int e = threadIdx.x * G + u;
+      c[u] = e < E ? counts[e] : 0;
+      sum += c[u];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int w = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += w;
+    }
+    if (lane == 31) s_part[threadIdx.x >> 5] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < static_cast<int>(threadIdx.x >> 5); ++w) before += s_part[w];
+    int run = before + incl - sum;
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const int e = threadIdx.x * G + u;
+      if (e <= E) s_off[e] = run;
+      run += c[u];
+    }
+    __syncthreads();
+  }
+  if (blockIdx.x == 0) {
+    // publish offsets; the routed counts must cover every pair and agree with the
+    // per-block histograms of the rank pass
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    if (threadIdx.x == 0 && s_off[E] != T * k) flag_error(status, MOE_DEV_BAD_INDEX);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int col = 0;
+      for (int b = 0; b < nblk; ++b) col += block_hist[static_cast<size_t>(b) * E + e];
+      if (col != s_off[e + 1] - s_off[e]) flag_error(status, MOE_DEV_BAD_INDEX);
+    }
+  }
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
   const size_t out_row = kQuant ? static_cast<size_t>(d) : in_row;
   const int n16 = static_cast<int>(in_row / 16);
@@ -215,13 +201,29 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
       }
     };
     if (xp != nullptr) load(0);
+    // destination of slot j (lane j): offsets[e] + the pairs of expert e in the rank
+    // blocks before this token's (summed by the warp) + the rank inside its block
+    const int blk = t / kTokensPerRankBlock;
+    int e_l = -1, r_l = -1;
+    if (lane < k) {
+      const size_t p = static_cast<size_t>(t) * k + lane;
+      e_l = idx[p];
+      r_l = local_rank[p];
+    }
+    int before = 0;
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(kFull, e_l, j);
+      int part = 0;
+      if (e >= 0 && e < E)
+        for (int b = lane; b < blk; b += 32) part += block_hist[static_cast<size_t>(b) * E + e];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+      if (lane == j) before = part;
+    }
     int dest = -1;
     if (lane < k) {
       const size_t p = static_cast<size_t>(t) * k + lane;
-      const int e = idx[p];
-      const int r = local_rank[p];
-      if (e >= 0 && e < E && r >= 0)
-        dest = block_base[static_cast<size_t>(t / kTokensPerRankBlock) * E + e] + r;
+      if (e_l >= 0 && e_l < E && r_l >= 0) dest = s_off[e_l] + before + r_l;
       if (dest >= T * k) {
         flag_error(status, MOE_DEV_BAD_INDEX);
         dest = -1;
@@ -475,8 +477,7 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
     launch_pdl(permute_rank_kernel, nblk, kRankThreads, rank_smem, stream, topk_idx, T, k, E, dest_row,
                                                                    hist, dev_status);
   }
-  launch_pdl(permute_scan_kernel, 1, 1024, 0, stream, counts, E, nblk, T * k, hist, offsets, dev_status);
-  if (T == 0) return check_launch("moe_permute");
+  // the scatter also publishes offsets (so it runs even for T == 0)
   const int grid = scatter_grid(T, sms);
   const uint8_t* xb = static_cast<const uint8_t*>(x);
   uint8_t* xpb = static_cast<uint8_t*>(xp);
@@ -485,16 +486,20 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
   if (xp_dtype == MOE_E4M3) {
     if (x_dtype == MOE_BF16)
       launch_pdl(permute_scatter_kernel<uint16_t, true>, grid, kScatterThreads, 0, stream, 
-          xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
+          xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales,
+          dev_status);
     else
       launch_pdl(permute_scatter_kernel<float, true>, grid, kScatterThreads, 0, stream, 
-          xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, xp_scales, dev_status);
+          xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales,
+          dev_status);
   } else if (x_dtype == MOE_BF16) {
     launch_pdl(permute_scatter_kernel<uint16_t, false>, grid, kScatterThreads, 0, stream, 
-        xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
+        xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, nullptr,
+        dev_status);
   } else {
     launch_pdl(permute_scatter_kernel<float, false>, grid, kScatterThreads, 0, stream, 
-        xb, T, d, topk_idx, k, E, dest_row, hist, dest_row, src_pair, xpb, nullptr, dev_status);
+        xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, nullptr,
+        dev_status);
   }
   return check_launch("moe_permute");
 }

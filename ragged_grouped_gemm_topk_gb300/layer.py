@@ -114,8 +114,8 @@ class MoELayer:
 
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
-        scan, scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine."""
-        return 2 + 3 + 2 + 1
+        scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine."""
+        return 2 + 2 + 2 + 1
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd."""
