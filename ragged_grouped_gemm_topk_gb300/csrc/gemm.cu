@@ -37,6 +37,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -668,12 +670,16 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         // staging buffers, so boxes are staged while earlier ones are still read.
         uint32_t pk[kBN / 2];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
+        for (int c = 0; c < kBN / 32; c += 2) {   // two loads per wait
+          uint32_t v[2][32];
+          tmem_ld32(tb + c * 32, v[0]);
+          tmem_ld32(tb + (c + 1) * 32, v[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[(c + h) * 16 + i] = pack_bf16x2(__uint_as_float(v[h][2 * i]), __uint_as_float(v[h][2 * i + 1]));
         }
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
@@ -943,12 +949,40 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const vo
   return true;
 }
 
+}  // namespace gemm
+namespace {
+// Kernels whose shared-memory attribute is set, per device.  Internal linkage on
+// purpose: a function-local static in a template would be merged across every
+// copy of this library loaded into one process.
+struct SmemSet {
+  const void* fn;
+  uint64_t devs;
+};
+SmemSet g_smem_set[64];
+std::mutex g_smem_mu;
+}  // namespace
+namespace gemm {
+
 template <typename Kern>
 bool ensure_smem(Kern k, size_t bytes) {
+  // once per kernel and device: the attribute sticks, and setting it costs a driver call
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 63;
+  const uint64_t bit = 1ull << dev;
+  const void* fn = reinterpret_cast<const void*>(k);
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  int slot = -1;
+  for (int i = 0; i < 64 && slot < 0; ++i)
+    if (g_smem_set[i].fn == fn || g_smem_set[i].fn == nullptr) slot = i;
+  if (slot >= 0 && g_smem_set[slot].fn == fn && (g_smem_set[slot].devs & bit)) return true;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) {
     set_error("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     return false;
+  }
+  if (slot >= 0) {
+    g_smem_set[slot].fn = fn;
+    g_smem_set[slot].devs |= bit;
   }
   return true;
 }
