@@ -65,8 +65,14 @@ constexpr int kAtomBytes = 1536;                  // MXFP8 per-stage atoms: A 51
 constexpr int kEpiRowBytes = 64;
 constexpr int kEpiBox = 32 * kEpiRowBytes;
 constexpr int kEpiOff = 0;
+// staging boxes per epilogue warp (rotating: a box is staged while the previous
+// ones are still being read by their TMA stores) and raw scale-row slots (MXFP8)
 template <int kKind>
-constexpr int atom_off() { return kEpiOff + 4 * kEpiBox; }
+constexpr int epi_bufs() { return kKind == 2 ? 1 : 2; }
+template <int kKind>
+constexpr int raw_slots() { return 2; }
+template <int kKind>
+constexpr int atom_off() { return kEpiOff + 4 * epi_bufs<kKind>() * kEpiBox; }
 template <int kKind>
 constexpr int raw_off() { return atom_off<kKind>() + kStages * kAtomBytes; }
 constexpr int kTmemCols = 512;
@@ -125,7 +131,9 @@ constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192
 template <int kKind, int kMode>
 constexpr size_t extra_smem() {
   return kMode == kWgrad ? 4 * kWgStage
-                        : (kMode == kFwd ? (kKind == 2 ? raw_off<kKind>() + 2 * kSfSlot : atom_off<kKind>()) : 0);
+                        : (kMode == kFwd ? (kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
+                                                       : atom_off<kKind>())
+                                         : 0);
 }
 template <int kKind, int kMode>
 constexpr size_t smem_for() {
@@ -359,10 +367,10 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 // Write one warp's 32 tile rows of output, held one row per lane as 32-bit words
 // (two bf16 or four E4M3 values each).  A warp whose 32 rows all belong to the
 // group sends 64-byte-wide boxes (16 words per row; kBoxElems elements) through its
-// 2 KB staging buffer by TMA store, one box in flight; 16-byte chunk h of row r sits
+// kBufs rotating 2 KB staging buffers by TMA store; 16-byte chunk h of row r sits
 // at chunk h ^ ((r >> 1) & 3) (64-byte swizzle).  A warp whose rows cross the
 // group's end (the next group's rows follow) stores its valid rows directly.
-template <int kBoxElems, int kWords>
+template <int kBoxElems, int kBufs, int kWords>
 __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
                                                int lane, uint8_t* out, int row0, int rows_valid, int col0,
                                                int n_out) {
@@ -372,19 +380,20 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
 #pragma unroll
     for (int c = 0; c < kWords / 16; ++c) {
       if (col0 + c * kBoxElems >= n_out) break;
-      if (lane == 0) bulk_wait_read0();   // the previous box has left the buffer
+      uint8_t* buf = stg + (c % kBufs) * kEpiBox;
+      if (lane == 0) bulk_wait_read<kBufs - 1>();   // the box that last used buf has been read
       __syncwarp();
       const int sw = (lane >> 1) & 3;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const int w0 = c * 16 + 4 * h;
-        *reinterpret_cast<uint4*>(stg + lane * kEpiRowBytes + ((h ^ sw) * 16)) =
+        *reinterpret_cast<uint4*>(buf + lane * kEpiRowBytes + ((h ^ sw) * 16)) =
             make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(tmD, stg, col0 + c * kBoxElems, row0);
+        tma_store_2d(tmD, buf, col0 + c * kBoxElems, row0);
         bulk_commit();
       }
     }
@@ -480,7 +489,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
               tma_load_2d(rsb, &tmSB, &s.sfull[ss], sx, brow + t.col0);
               tma_load_2d(rsb + kSfBStage / 2, &tmSB, &s.sfull[ss], sx, brow + t.col0 + kBM);
             }
-            if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
+            if (++ss == raw_slots<kKind>()) { ss = 0; ss_phase ^= 1u; }
           }
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.status, &s.abort)) break;
           uint8_t* sa = tiles + stage * C::kStage;
@@ -614,7 +623,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           for (int j = 0; j < 8; ++j) rb[j] = *reinterpret_cast<const uint4*>(rsb + (lane + 32 * j) * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&s.sempty[ss]);
-          if (++ss == 2) { ss = 0; ss_phase ^= 1u; }
+          if (++ss == raw_slots<kKind>()) { ss = 0; ss_phase ^= 1u; }
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
         uint8_t* at = tiles + NS * C::kStage + atom_off<kKind>() + stage * kAtomBytes;
@@ -754,7 +763,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
                                                        bf16_to_f32(static_cast<uint16_t>(w1 >> 16)) * inv)) << 16);
           }
         }
-        epi_store_rows<64>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, cw, lane,
+        epi_store_rows<64, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, cw, lane,
                            reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         if (r < t.rows) {
           uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
@@ -782,7 +791,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          epi_store_rows<32>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+          epi_store_rows<32, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, pk, lane,
                              reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
@@ -854,7 +863,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           mbar_arrive(&s.tempty[acc]);
           released = true;
           if constexpr (kMode == kFwd) {
-            epi_store_rows<32>(&tmD, tiles + NS * C::kStage + kEpiOff + q * kEpiBox, pk, lane,
+            epi_store_rows<32, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, pk, lane,
                                reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
 #pragma unroll
