@@ -77,6 +77,13 @@ typedef struct {
 int moe_version(void);                    /* (major << 16) | (minor << 8) | patch */
 const char* moe_last_error_string(void);  /* message of this thread's last error */
 
+/* Diagnostic with no counterpart in the pages: exercises the failure path of the
+ * bounded pipeline wait that every GEMM stage uses.  One CTA waits on a barrier
+ * nothing arrives at; after limit_us microseconds (1 .. 2e6) the wait gives up,
+ * ORs MOE_DEV_TIMEOUT into *dev_status and the kernel returns, leaving the CUDA
+ * context usable.  Asynchronous on `stream`. */
+moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- route ----
  * Top-k expert selection with softmax routing weights ([1] opening section: a
  * learnable router activates the top-K experts of each token; [1] "Optimisation

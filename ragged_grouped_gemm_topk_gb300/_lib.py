@@ -31,6 +31,7 @@ OP = C.POINTER(Operand)
 SIGNATURES = {
     "moe_version": (C.c_int, []),
     "moe_last_error_string": (C.c_char_p, []),
+    "moe_check_wait_timeout": (st, [vp, i32, vp]),
     "moe_route_topk": (st, [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "moe_permute_workspace_size": (sz, [i32, i32, i32]),
     "moe_permute": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz,

@@ -96,6 +96,15 @@ def moe_permute(x, topk_idx, counts, E, *, xp_dtype=None, rows=True, offsets=Non
     return dict(offsets=offsets, dest_row=dest_row, src_pair=src_pair, xp=xp, xp_scales=xp_scales)
 
 
+def moe_check_wait_timeout(limit_us, dev_status=None):
+    """Run the bounded-wait failure path: returns the device status word (int32
+    tensor) after a barrier wait of limit_us microseconds has given up."""
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=torch.cuda.current_device())
+    _lib.call("moe_check_wait_timeout", _ptr(dev_status), int(limit_us), _stream())
+    return dev_status
+
+
 def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=None, axis=0):
     """MXFP8 of inp [rows,K] (bf16/fp32) -> (codes u8 [rows,K], scales u8).
     axis 0: row-wise, scales [rows, K/32].  axis 1: column-wise and group-aware

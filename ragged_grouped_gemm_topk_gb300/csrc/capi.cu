@@ -65,3 +65,36 @@ bool device_is_sm103(int* sm_count) {
 extern "C" int moe_version(void) { return (0 << 16) | (1 << 8) | 0; }
 
 extern "C" const char* moe_last_error_string(void) { return moe::g_err; }
+
+namespace moe {
+namespace {
+
+// One CTA waits on an mbarrier that nothing ever arrives at, through the same
+// bounded wait every pipeline stage of the GEMM uses, with a caller-chosen limit.
+__global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
+  pdl_begin();
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status, &abort_flag, limit_ns);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us, cudaStream_t stream) {
+  using namespace moe;
+  if (!dev_status || limit_us < 1 || limit_us > 2000000) {
+    set_error("moe_check_wait_timeout: need a status word and 1 <= limit_us <= 2000000");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  launch_pdl(wait_timeout_kernel, 1, 32, 0, stream, dev_status, static_cast<uint64_t>(limit_us) * 1000ull);
+  return check_launch("moe_check_wait_timeout");
+}
