@@ -175,12 +175,31 @@ moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, int T, int 
  *        [n_blocks, K] uint8 out with group e's blocks from row sum over e' < e of
  *        ceil(count_e' / 32); the caller's buffer must hold ceil(rows/32) + E rows
  *        (the bound on n_blocks); rows past n_blocks are not written.
+ *        2 = column-wise as axis 1 (same codes, same scale values), the scales laid
+ *        out for the MXFP8 weight-gradient GEMM, which copies them into tensor
+ *        memory as they are: group e's blocks taken four at a time (quads of 128
+ *        rows), quad q of group e numbered Q = floor(offsets[e] / 128) + e + q; the
+ *        scales of quad Q and columns [128c, 128c + 128) are one 512-byte tile at
+ *        byte ((Q * K/128) + c) * 512, column m of the 128 and block j of the quad
+ *        at (m % 32) * 16 + (m / 32) * 4 + j.  K % 128 == 0; the buffer must hold
+ *        (ceil(rows/128) + E) * K/128 tiles; bytes of blocks past a group's last
+ *        one are not written.
  * MOE_ERR_UNSUPPORTED for any other axis.
  */
 moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows, int K,
                                         const int32_t* offsets, int E, int axis,
                                         uint8_t* codes, uint8_t* scales,
                                         cudaStream_t stream);
+
+/* Transposed row-wise MXFP8 of a batch of matrices, for weights that a gradient
+ * contracts along their first dim (the data gradient contracts B [E, N, K] over N):
+ *   in     [G, R, C] MOE_BF16 or MOE_F32, 16-byte aligned; R % 32 == 0, C % 8 == 0.
+ *   codes  [G, C, R] uint8 out (E4M3): codes[g, c, r] encodes in[g, r, c].
+ *   scales [G * C, R / 32] uint8 out (E8M0), blocks of 32 along R.
+ * The result equals moe_quantize_mxfp8_grouped (axis 0) of each in[g]^T, bit for bit.
+ * Stateless: no workspace; G, R or C == 0 is a no-op. */
+moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype, int G, int R, int C,
+                                           uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- grouped GEMM
  * Ragged grouped GEMM ([1] "Optimisation 1": one kernel launch covers every
@@ -234,9 +253,28 @@ moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const moe_operand_t
                                     void* dA, moe_dtype_t dA_dtype,
                                     int32_t* dev_status, cudaStream_t stream);
 
+/* MXFP8 data gradient ([1] "Optimisation 1" with block-scaled operands; the
+ * backward of the MXFP8 forward): dA[r, :] = dC[r, :] . B[e] for r in expert e's
+ * rows, with both operands quantised along the contraction dim N.
+ *   dC  MOE_E4M3 codes [M, N], scales [M, N/32] (moe_quantize_mxfp8_grouped, axis 0).
+ *   BT  MOE_E4M3 codes [E, K, N] = B^T, scales [E*K, N/32]
+ *       (moe_quantize_mxfp8_transposed of B [E, N, K]).
+ *   dA  bf16 [M, K] (NONE) or [M, 2K] = [dG | dU] (DSWIGLU, with `preact` the
+ *       bf16 forward pre-activations [M, 2K], formula as moe_grouped_gemm_dgrad).
+ * Limits: N % 512 == 0, K % 32 == 0, E <= 1024, 16-byte aligned pointers and
+ * scales; MOE_ERR_UNSUPPORTED unless both operands are MOE_E4M3. */
+moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, const moe_operand_t* BT,
+                                          const int32_t* offsets, int M, int N, int K, int E,
+                                          moe_epilogue_t epi, const void* preact, void* dA,
+                                          int32_t* dev_status, cudaStream_t stream);
+
 /* Weight gradient: dB[e] = dC[R_e]^T . A[R_e], a contraction over the ragged rows
  * R_e of each expert; an expert with no rows gets an exact zero gradient.
- *   A [M, K], dC [M, N] (both MOE_BF16 or both MOE_F32) -> dB [E, N, K] in dB_dtype.
+ *   A [M, K], dC [M, N], both MOE_BF16 -> dB [E, N, K] in dB_dtype (MOE_BF16).
+ *   Or both MOE_E4M3 ([1] "grouped quantisation": the blocks of 32 run down the
+ *   contraction, restarting at each group): codes and tiled scales from
+ *   moe_quantize_mxfp8_grouped axis 2 of A and of dC (scales required);
+ *   N % 128 == 0 and K % 128 == 0.
  * Limits as the forward. */
 moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
                                     const int32_t* offsets, int M, int N, int K, int E,

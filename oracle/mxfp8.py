@@ -30,7 +30,8 @@ Readings taken where the definition is silent (each listed in the design doc):
 
 parity pinned: tests/test_oracle_mxfp8.py (format table from the definition,
 torch.float8_e4m3fn casts of in-range values, idempotence, closed-form scales,
-golden points in tests/golden/e4m3_points.txt).
+golden points in tests/golden/e4m3_points.txt; the column-wise round trip against
+the row-wise one of the transpose, and group separation under the E4M3 bound).
 """
 
 from __future__ import annotations
@@ -147,3 +148,22 @@ def quantize_colwise_grouped(a: np.ndarray, offsets: np.ndarray):
             scales[brow, :] = (X + E8M0_BIAS).astype(np.uint8)
             brow += 1
     return codes, scales
+
+
+def dequantize_colwise_grouped(codes: np.ndarray, scales: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+    """Exact float64 values of a column-wise group-aware quantisation: row r of
+    group e, column c decodes as code * 2^(scale[block row of r, c] - 127), the
+    block rows numbered as in ``quantize_colwise_grouped``."""
+    codes = np.asarray(codes)
+    rows, K = codes.shape
+    offsets = np.asarray(offsets, dtype=np.int64)
+    out = np.zeros((rows, K), dtype=np.float64)
+    brow = 0
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for r0 in range(lo, hi, BLOCK):
+            r1 = min(r0 + BLOCK, hi)
+            mult = np.exp2(scales[brow].astype(np.float64) - E8M0_BIAS)
+            out[r0:r1] = E4M3_ALL[codes[r0:r1].astype(np.int64)] * mult[None, :]
+            brow += 1
+    return out

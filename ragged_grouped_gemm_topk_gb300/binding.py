@@ -109,14 +109,26 @@ def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=Non
     """MXFP8 of inp [rows,K] (bf16/fp32) -> (codes u8 [rows,K], scales u8).
     axis 0: row-wise, scales [rows, K/32].  axis 1: column-wise and group-aware
     (offsets [E+1] required), scales [ceil(rows/32) + E, K] of which the first
-    sum_e ceil(count_e/32) rows are written."""
+    sum_e ceil(count_e/32) rows are written.  axis 2: as axis 1 with the scales in
+    the weight-gradient GEMM's tiled layout, [(ceil(rows/128) + E) * K/128, 512]."""
     rows, K = inp.shape
     codes = codes if codes is not None else torch.empty(rows, K, dtype=torch.uint8, device=inp.device)
     if scales is None:
-        shape = (rows, K // 32) if axis == 0 else ((rows + 31) // 32 + E, K)
+        shape = {0: (rows, K // 32), 1: ((rows + 31) // 32 + E, K),
+                 2: (((rows + 127) // 128 + E) * (K // 128), 512)}[axis]
         scales = torch.empty(*shape, dtype=torch.uint8, device=inp.device)
     _lib.call("moe_quantize_mxfp8_grouped", _ptr(inp), _dt(inp), rows, K, _ptr(offsets), E, axis,
               _ptr(codes), _ptr(scales), _stream())
+    return codes, scales
+
+
+def moe_quantize_mxfp8_transposed(inp, *, codes=None, scales=None):
+    """Row-wise MXFP8 of each inp[g]^T for inp [G,R,C] (bf16/fp32) -> (codes u8
+    [G,C,R], scales u8 [G*C, R/32])."""
+    G, R, Cc = inp.shape
+    codes = codes if codes is not None else torch.empty(G, Cc, R, dtype=torch.uint8, device=inp.device)
+    scales = scales if scales is not None else torch.empty(G * Cc, R // 32, dtype=torch.uint8, device=inp.device)
+    _lib.call("moe_quantize_mxfp8_transposed", _ptr(inp), _dt(inp), G, R, Cc, _ptr(codes), _ptr(scales), _stream())
     return codes, scales
 
 
@@ -175,15 +187,35 @@ def moe_grouped_gemm_dgrad(dC, B, offsets, *, epi="none", preact=None, out_dtype
     return out
 
 
-def moe_grouped_gemm_wgrad(A, dC, offsets, E, *, out_dtype=torch.bfloat16, out=None, dev_status=None):
-    """dB[e] = dC[R_e]^T . A[R_e] -> [E, N, K]."""
+def moe_grouped_gemm_dgrad_mxfp8(dC, BT, offsets, *, dC_scales, BT_scales, epi="none", preact=None, out=None,
+                                 dev_status=None):
+    """dA = ragged dC . B[e] on MXFP8 operands: dC codes [M,N], BT codes [E,K,N]
+    (= B^T quantised along N); bf16 result [M,K], or [M,2K] = [dG | dU] with
+    epi "dswiglu" and preact [M,2K]."""
+    M, N = dC.shape
+    E, K, N2 = BT.shape
+    if N2 != N:
+        raise ValueError("dC and BT disagree on N")
+    width = 2 * K if epi == "dswiglu" else K
+    if out is None:
+        out = torch.empty(M, width, dtype=torch.bfloat16, device=dC.device)
+    a, b = _operand(dC, dC_scales), _operand(BT, BT_scales)
+    _lib.call("moe_grouped_gemm_dgrad_mxfp8", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E, _EPI[epi],
+              _ptr(preact), _ptr(out), _ptr(dev_status), _stream())
+    return out
+
+
+def moe_grouped_gemm_wgrad(A, dC, offsets, E, *, A_scales=None, dC_scales=None, out_dtype=torch.bfloat16,
+                           out=None, dev_status=None):
+    """dB[e] = dC[R_e]^T . A[R_e] -> [E, N, K].  MXFP8: A and dC are codes from the
+    tiled column-wise quantiser (axis 2), with their scale buffers."""
     M, K = A.shape
     M2, N = dC.shape
     if M2 != M:
         raise ValueError("A and dC disagree on M")
     if out is None:
         out = torch.empty(E, N, K, dtype=out_dtype, device=A.device)
-    a, b = _operand(A), _operand(dC)
+    a, b = _operand(A, A_scales), _operand(dC, dC_scales)
     _lib.call("moe_grouped_gemm_wgrad", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E,
               _ptr(out), _dt(out), _ptr(dev_status), _stream())
     return out

@@ -319,9 +319,18 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
 // owns 4 adjacent columns (an 8- or 16-byte chunk) and keeps the block's 32 rows of
 // them in registers (32 loads in flight), so reads and writes stay row-contiguous
 // across the warp.
+//
+// kTiled: the scales leave in the layout the block-scaled weight-gradient GEMM reads
+// straight into its tensor-memory scale slots.  Group e's 32-row blocks are taken
+// four at a time (a quad: 128 rows); quad q of group e has index
+// Q = floor(offsets[e] / 128) + e + q (distinct for every group and quad, and below
+// ceil(rows / 128) + E).  The scales of quad Q and columns [128c, 128c + 128) form
+// one 512-byte tile at ((Q * K / 128) + c) * 512, where column m of the 128 and block
+// j of the quad sit at byte (m % 32) * 16 + (m / 32) * 4 + j.  Bytes of blocks past a
+// group's last one are not written.
 constexpr int kColThreads = 128;
 
-template <typename Tin>
+template <typename Tin, bool kTiled>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const uint8_t* __restrict__ in, int rows, int K, const int32_t* __restrict__ offsets, int E,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
@@ -441,8 +450,131 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
             (static_cast<uint32_t>(f32x2_to_e4m3x2(f[2] * inv[2], f[3] * inv[3])) << 16);
       }
     }
-    *reinterpret_cast<uint32_t*>(scales + static_cast<size_t>(br) * K + col) =
-        sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+    if constexpr (kTiled) {
+      const int b = br - bpre[lo_e];                         // block within the group
+      const size_t quad = static_cast<size_t>(offsets[lo_e] / 128 + lo_e + b / 4);
+      uint8_t* tile = scales + (quad * (K / 128) + col / 128) * 512 + (b % 4);
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const int m = col % 128 + j;
+        tile[(m % 32) * 16 + (m / 32) * 4] = static_cast<uint8_t>(sb[j]);
+      }
+    } else {
+      *reinterpret_cast<uint32_t*>(scales + static_cast<size_t>(br) * K + col) =
+          sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+    }
+  }
+}
+
+// Transposed row-wise MXFP8 of a batch of matrices: in [G, R, C] -> codes [G, C, R]
+// and scales [G, C, R / 32], blocks of 32 along R (so the transposed matrix is
+// quantised row-wise along its rows).  For weights read along their output dim: the
+// data gradient contracts B [E, N, K] over N, so it needs B^T [E, K, N] with scales
+// along N.  A CTA task is one matrix, kTrCols(Tin) columns (512 bytes of a row) and
+// kTrRb 32-row blocks.  Thread j owns column j: per block it quantises the 32
+// values of its column (read back from shared memory) and writes them as one
+// 32-byte run of the transposed row; its kTrRb scale bytes leave as one 16-byte
+// store at the end, so scale writes fill whole sectors.  Row blocks stream through
+// two shared-memory buffers with cp.async, the next block loading while this one
+// is encoded.
+constexpr int kTrRb = 16;
+template <typename Tin>
+constexpr int tr_cols() { return 512 / static_cast<int>(sizeof(Tin)); }
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <typename Tin>
+__global__ void __launch_bounds__(tr_cols<Tin>(), 4) quantize_transposed_kernel(
+    const uint8_t* __restrict__ in, int G, int R, int C, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
+  pdl_begin();
+  constexpr int EB = sizeof(Tin);
+  constexpr int COLS = tr_cols<Tin>();
+  constexpr int kChunks = COLS * EB / 16;                    // 16-byte chunks per tile row (32)
+  __shared__ __align__(16) Tin tile[2][32][COLS];
+  const int nrb = R / 32, ncb = (C + COLS - 1) / COLS, nrg = (nrb + kTrRb - 1) / kTrRb;
+  const long long tasks = static_cast<long long>(G) * ncb * nrg;
+  const bool vec_scales = nrb % kTrRb == 0;                   // 16-byte aligned scale runs
+  for (long long task = blockIdx.x; task < tasks; task += gridDim.x) {
+    const int g = static_cast<int>(task / (static_cast<long long>(ncb) * nrg));
+    const int rem = static_cast<int>(task % (static_cast<long long>(ncb) * nrg));
+    const int rg = rem / ncb, c0 = (rem % ncb) * COLS;
+    const int rb0 = rg * kTrRb, nb = min(kTrRb, nrb - rb0);
+    const uint8_t* src = in + static_cast<size_t>(g) * R * C * EB;
+    auto load = [&](int rb, int buf) {
+#pragma unroll
+      for (int i = threadIdx.x; i < 32 * kChunks; i += COLS) {
+        const int r = i / kChunks, ch = i % kChunks;
+        const int c = c0 + ch * (16 / EB);
+        const bool ok = c < C;
+        const uint8_t* gp = src + (static_cast<size_t>(rb * 32 + r) * C + (ok ? c : 0)) * EB;
+        cp_async16(&tile[buf][r][ch * (16 / EB)], gp, ok);
+      }
+      cp_async_commit();
+    };
+    load(rb0, 0);
+    const int c = c0 + threadIdx.x;
+    uint32_t sc[kTrRb / 4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < kTrRb; ++i) {
+      if (i < nb) {
+        if (i + 1 < nb) {
+          load(rb0 + i + 1, (i + 1) & 1);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+        __syncthreads();
+        if (c < C) {
+          const Tin* col = &tile[i & 1][0][threadIdx.x];
+          float amax = 0.f;
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            float v;
+            if constexpr (EB == 2) v = bf16_to_f32(static_cast<uint16_t>(col[r * COLS]));
+            else v = static_cast<float>(col[r * COLS]);
+            amax = fmaxf(amax, fabsf(v));
+          }
+          uint32_t sb;
+          float inv;
+          mx_scale(amax, &sb, &inv);
+          uint32_t w[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if constexpr (EB == 2) v[u] = bf16_to_f32(static_cast<uint16_t>(col[(4 * q + u) * COLS]));
+              else v[u] = static_cast<float>(col[(4 * q + u) * COLS]);
+            }
+            w[q] = static_cast<uint32_t>(f32x2_to_e4m3x2(v[0] * inv, v[1] * inv)) |
+                   (static_cast<uint32_t>(f32x2_to_e4m3x2(v[2] * inv, v[3] * inv)) << 16);
+          }
+          uint8_t* dst = codes + (static_cast<size_t>(g) * C + c) * R + static_cast<size_t>(rb0 + i) * 32;
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          sc[i / 4] |= sb << (8 * (i % 4));
+        }
+        __syncthreads();                  // the buffer is reloaded two blocks on
+      }
+    }
+    if (c < C) {
+      uint8_t* sdst = scales + (static_cast<size_t>(g) * C + c) * nrb + rb0;
+      if (vec_scales) {
+        *reinterpret_cast<uint4*>(sdst) = make_uint4(sc[0], sc[1], sc[2], sc[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTrRb; ++i)
+          if (i < nb) sdst[i] = static_cast<uint8_t>(sc[i / 4] >> (8 * (i % 4)));
+      }
+    }
   }
 }
 
@@ -580,12 +712,16 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
                                                    int K, const int32_t* offsets, int E, int axis,
                                                    uint8_t* codes, uint8_t* scales,
                                                    cudaStream_t stream) {
-  if (axis != 0 && axis != 1) {
-    set_error("moe_quantize_mxfp8_grouped: axis 0 (row-wise) or 1 (column-wise)");
+  if (axis != 0 && axis != 1 && axis != 2) {
+    set_error("moe_quantize_mxfp8_grouped: axis 0 (row-wise), 1 (column-wise) or 2 (column-wise, tiled scales)");
     return MOE_ERR_UNSUPPORTED;
   }
-  if (axis == 1 && (!offsets || E < 1 || E > 1024)) {
+  if (axis >= 1 && (!offsets || E < 1 || E > 1024)) {
     set_error("moe_quantize_mxfp8_grouped: column-wise needs offsets and 1 <= E <= 1024");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (axis == 2 && K % 128) {
+    set_error("moe_quantize_mxfp8_grouped: tiled column-wise scales need K %% 128 == 0");
     return MOE_ERR_INVALID_ARG;
   }
   if (rows < 0 || K < 0 || K % 32 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
@@ -599,16 +735,18 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (rows == 0 || K == 0) return MOE_OK;
-  if (axis == 1) {
+  if (axis >= 1) {
     const int strip = kColThreads * 4;
     const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
     const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
-    if (in_dtype == MOE_BF16)
-      launch_pdl(quantize_colwise_kernel<uint16_t>, grid, kColThreads, 0, stream,
-                 static_cast<const uint8_t*>(in), rows, K, offsets, E, codes, scales);
-    else
-      launch_pdl(quantize_colwise_kernel<float>, grid, kColThreads, 0, stream,
-                 static_cast<const uint8_t*>(in), rows, K, offsets, E, codes, scales);
+    const uint8_t* src = static_cast<const uint8_t*>(in);
+    if (in_dtype == MOE_BF16) {
+      if (axis == 2) launch_pdl(quantize_colwise_kernel<uint16_t, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
+      else launch_pdl(quantize_colwise_kernel<uint16_t, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
+    } else {
+      if (axis == 2) launch_pdl(quantize_colwise_kernel<float, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
+      else launch_pdl(quantize_colwise_kernel<float, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
+    }
     return check_launch("moe_quantize_mxfp8_grouped");
   }
   const int grid = scatter_grid(rows, sms);
@@ -619,4 +757,34 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
     launch_pdl(quantize_rowwise_kernel<float>, grid, kScatterThreads, 0, stream, 
         static_cast<const uint8_t*>(in), rows, K, codes, scales);
   return check_launch("moe_quantize_mxfp8_grouped");
+}
+
+extern "C" moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype, int G, int R,
+                                                      int C, uint8_t* codes, uint8_t* scales,
+                                                      cudaStream_t stream) {
+  if (G < 0 || R < 0 || C < 0 || R % 32 || C % 8 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
+    set_error("moe_quantize_mxfp8_transposed: need G, R, C >= 0, R %% 32 == 0, C %% 8 == 0, BF16/F32 input");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (G > 0 && R > 0 && C > 0 && (!in || !codes || !scales || !aligned16(in) || !aligned16(codes))) {
+    set_error("moe_quantize_mxfp8_transposed: null or misaligned pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (G == 0 || R == 0 || C == 0) return MOE_OK;
+  if (in_dtype == MOE_BF16) {
+    const long long items = static_cast<long long>(G) * ((R / 32 + kTrRb - 1) / kTrRb) *
+                            ((C + tr_cols<uint16_t>() - 1) / tr_cols<uint16_t>());
+    const int grid = static_cast<int>(items < static_cast<long long>(sms) * 4 ? items : sms * 4);
+    launch_pdl(quantize_transposed_kernel<uint16_t>, grid, tr_cols<uint16_t>(), 0, stream,
+               static_cast<const uint8_t*>(in), G, R, C, codes, scales);
+  } else {
+    const long long items = static_cast<long long>(G) * ((R / 32 + kTrRb - 1) / kTrRb) *
+                            ((C + tr_cols<float>() - 1) / tr_cols<float>());
+    const int grid = static_cast<int>(items < static_cast<long long>(sms) * 6 ? items : sms * 6);
+    launch_pdl(quantize_transposed_kernel<float>, grid, tr_cols<float>(), 0, stream,
+               static_cast<const uint8_t*>(in), G, R, C, codes, scales);
+  }
+  return check_launch("moe_quantize_mxfp8_transposed");
 }

@@ -117,20 +117,27 @@ struct Cfg {
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
-// wgrad: each epilogue warp stages its 32 dW rows in kWgBufs rotating 2 KB boxes of
+// wgrad: each epilogue warp stages its 32 dW rows in wg_bufs rotating 2 KB boxes of
 // 32 columns for the TMA store (so the 4-stage operand ring still fits), and a 7th
-// warp writes the dW of experts without rows.  Forward:
+// warp writes the dW of experts without rows.  MXFP8 wgrad keeps two boxes per warp
+// to make room for each stage's 1.5 KB of scale atoms, which arrive ready-made (the
+// tiled column-wise scale layout) by bulk copy with the stage's operands.  Forward:
 // each epilogue warp stages one 32-row x 32-column bf16 box (2 KB) of its output
 // for the TMA store.
-constexpr int kWgBufs = 3;                        // 2 KB staging boxes per epilogue warp
-constexpr int kWgStage = 2048 * kWgBufs;
+template <int kKind>
+constexpr int wg_bufs() { return kKind == 2 ? 2 : 3; }   // 2 KB staging boxes per epilogue warp
+template <int kKind>
+constexpr int wg_stage() { return 2048 * wg_bufs<kKind>(); }
+template <int kKind>
+constexpr int wg_atom_off() { return 4 * wg_stage<kKind>(); }
+constexpr int kMxWgRows = 128;                    // MXFP8 wgrad: contraction rows per stage (4 blocks)
 template <int kKind, int kMode>
 constexpr int stages_for() { return kStages; }
 template <int kKind, int kMode>
 constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
 constexpr size_t extra_smem() {
-  return kMode == kWgrad ? 4 * kWgStage
+  return kMode == kWgrad ? wg_atom_off<kKind>() + (kKind == 2 ? kStages * kAtomBytes : 0)
                         : (kMode == kFwd ? (kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
                                                        : atom_off<kKind>())
                                          : 0);
@@ -169,6 +176,8 @@ struct Params {
   const void* preact_in;   // dgrad dSwiGLU: G|U input
   uint8_t* out_scales;     // forward with MXFP8 output: E8M0 [M, n_out / 32]
   int32_t* status;
+  const uint8_t* sfa;      // MXFP8 wgrad: tiled column-wise scales of dC (the MMA's A) ...
+  const uint8_t* sfb;      // ... and of A (the MMA's B)
 };
 
 struct Tile {
@@ -189,7 +198,9 @@ struct Geo {
   int n_out;    // output columns (fwd/dgrad)
   int bn_out;   // output columns per tile
   int kb_fixed; // contraction blocks (fwd/dgrad)
+  int mn_rows;  // wgrad: contraction rows per stage
   __device__ Geo(const Params& p, int elem_bytes, int bn) {
+    mn_rows = elem_bytes == 1 ? kMxWgRows : kMnRows;
     if (kMode == kWgrad) {
       nt = (p.N + kBM - 1) / kBM;
       nt2 = (p.K + kBN - 1) / kBN;
@@ -237,7 +248,7 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
     t.col0 = (local / g.nt) * kBN;
     t.row0 = cnt > 0 ? beg : 0;
     t.rows = cnt;
-    t.kblocks = (cnt + kMnRows - 1) / kMnRows;
+    t.kblocks = (cnt + g.mn_rows - 1) / g.mn_rows;
   } else {
     const int mt = (cnt + kBM - 1) / kBM;   // >= 1: only non-empty groups own tiles
     t.row0 = beg + (local % mt) * kBM;
@@ -495,7 +506,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           uint8_t* sa = tiles + stage * C::kStage;
           uint8_t* sb = sa + kAStage;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, kStageBytes);
+          mbar_arrive_expect_tx(bar, kStageBytes + (C::kMx && kMode == kWgrad ? kAtomBytes : 0));
           if (kMode == kFwd) {
             const int kx = kb * (kBKBytes / eb);
             tma_load_2d(sa, &tmA, bar, kx, t.row0);
@@ -510,6 +521,17 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             tma_load_2d(sa, &tmA, bar, nx, t.row0);
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j) tma_load_3d(sb + j * kBox, &tmB, bar, t.col0 + 64 * j, nx, t.e);
+          } else if constexpr (C::kMx) {
+            // 128 rows of the group: one 128-column box of dC^T, two of A, and the
+            // quad's scale tiles (dC: 512 B for rows n0.., A: 1 KB for columns col0..)
+            const int r = t.row0 + kb * kMxWgRows;
+            tma_load_2d(sa, &tmA, bar, t.n0, r);
+            tma_load_2d(sb, &tmB, bar, t.col0, r);
+            tma_load_2d(sb + kBStage / 2, &tmB, bar, t.col0 + 128, r);
+            const size_t quad = static_cast<size_t>(t.row0 / 128 + t.e + kb);
+            uint8_t* at = tiles + NS * C::kStage + wg_atom_off<kKind>() + stage * kAtomBytes;
+            bulk_load(at, p.sfa + (quad * (p.N / 128) + t.n0 / 128) * 512, 512, bar);
+            bulk_load(at + 512, p.sfb + (quad * (p.K / 128) + t.col0 / 128) * 512, 1024, bar);
           } else {
             const int r = t.row0 + kb * kMnRows;          // contraction index (rows of the group)
 #pragma unroll
@@ -523,7 +545,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, BN)
+    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, BN) | (kMode == kWgrad ? (3u << 15) : 0u)
                                       : make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -533,6 +555,44 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       tc_fence_after();
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (C::kMx && kMode == kWgrad) {
+          // Both operands MN-major (A = dC^T, B = A), 128 contraction rows per stage.
+          // Last block of the group: zero rows [valid, 32*steps) of dC^T and skip
+          // 32-row steps wholly past the group (their scales are never read).
+          if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
+          tc_fence_after();
+          uint8_t* sa_ptr = tiles + stage * C::kStage;
+          const int valid = t.rows - kb * kMxWgRows;
+          int steps = 4;
+          if (valid < kMxWgRows) {
+            steps = (valid + 31) / 32;
+            const int zrows = steps * 32 - valid;
+            for (int i = lane; i < zrows * 8; i += 32)
+              *reinterpret_cast<uint4*>(sa_ptr + (valid + i / 8) * 128 + (i % 8) * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(sa_ptr);
+            const uint32_t sb = sa + kAStage;
+            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + wg_atom_off<kKind>() + stage * kAtomBytes);
+            const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
+            tc_cp_32x128b_warpx4(slot, make_sdesc(ssa, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + TL::kSfB, make_sdesc(ssa + 512, 0, 128, 0));
+            tc_cp_32x128b_warpx4(slot + TL::kSfB + 4, make_sdesc(ssa + 1024, 0, 128, 0));
+            for (int kk = 0; kk < steps; ++kk) {
+              // 32 rows x 128 bytes per step; 128-column atoms 16 KB apart, 8-row groups 1 KB apart
+              const uint64_t ad = make_sdesc(sa + kk * 4096, kBStage / 2, 1024, 2);
+              const uint64_t bd = make_sdesc(sb + kk * 4096, kBStage / 2, 1024, 2);
+              const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
+              tc_mma_mxf8(d_tmem, ad, bd, id, slot, slot + TL::kSfB, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(&s.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+          continue;
+        }
         if (C::kMx) {
           if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
           tc_fence_after();
@@ -600,7 +660,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       __syncwarp();
       if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
-  } else if (C::kMx && warp == 6) {
+  } else if (C::kMx && kMode == kFwd && warp == 6) {
     // ------------------------------------------------------------------ MXFP8 scale layout
     // Every 4 K-blocks: take the raw scale rows of the slot (row r: 16 bytes, the
     // scales of 4 K-blocks) into registers and free the slot.  Every K-block: write
@@ -675,7 +735,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       if constexpr (kMode == kWgrad) {
         // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns: the accumulator is read
         // whole into registers and released, then written by TMA (clipped at N and K) in
-        // 32-column boxes (64-byte swizzle) through the warp's kWgBufs rotating 2 KB
+        // 32-column boxes (64-byte swizzle) through the warp's wg_bufs rotating 2 KB
         // staging buffers, so boxes are staged while earlier ones are still read.
         uint32_t pk[kBN / 2];
 #pragma unroll
@@ -693,7 +753,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
         released = true;
-        uint8_t* stg = tiles + NS * C::kStage + q * kWgStage;
+        constexpr int kWgBufs = wg_bufs<kKind>();
+        uint8_t* stg = tiles + NS * C::kStage + q * wg_stage<kKind>();
         const int sw = (lane >> 1) & 3;
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
@@ -820,11 +881,11 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           }
         }
       } else if constexpr (kEpi == kEpiDswiglu) {
-        // the product is dH [M, K]; preact (G | U) is [M, 2K]; output [dG | dU]
+        // the product is dH [M, f]; preact (G | U) is [M, 2f]; output [dG | dU]
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
         const OutT* pre = static_cast<const OutT*>(p.preact_in);
-        const int f = p.K;
+        const int f = g.n_out;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -1193,6 +1254,49 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
   return launch<1, kDgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
 }
 
+extern "C" moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, const moe_operand_t* BT,
+                                                     const int32_t* offsets, int M, int N, int K, int E,
+                                                     moe_epilogue_t epi, const void* preact, void* dA,
+                                                     int32_t* dev_status, cudaStream_t stream) {
+  // dA[R_e] = dC[R_e] @ B[e] with both operands quantised along the contraction dim N:
+  // dC codes [M, N] (scales [M, N/32]) and B^T codes [E, K, N] (scales [E*K, N/32]).
+  // That is the forward problem with N and K swapped, so the forward MXFP8 kernel runs it.
+  const char* fn = "moe_grouped_gemm_dgrad_mxfp8";
+  int sms = 0;
+  moe_status_t st = common_checks(fn, dC, BT, offsets, M, N, K, E, dA, &sms);
+  if (st != MOE_OK) return st;
+  if (dC->dtype != MOE_E4M3) {
+    set_error("%s: MXFP8 (E4M3) operands only", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if ((epi != MOE_EPI_NONE && epi != MOE_EPI_DSWIGLU) ||
+      (epi == MOE_EPI_DSWIGLU && (!preact || !aligned16(preact))) || N % 512 || !dC->scales || !BT->scales ||
+      !aligned16(dC->scales) || !aligned16(BT->scales)) {
+    set_error("%s: epi NONE|DSWIGLU (DSWIGLU needs an aligned preact [M, 2K]), N %% 512 == 0, aligned scales", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (M == 0) return MOE_OK;
+  CUtensorMap ta, tb, tsa, tsb, td;
+  const uint64_t adims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const uint32_t abox[2] = {kBKBytes, kBM};
+  const uint64_t bdims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K), static_cast<uint64_t>(E)};
+  const uint32_t bbox[3] = {kBKBytes, kBN, 1};
+  const uint64_t sadims[2] = {static_cast<uint64_t>(N / 32), static_cast<uint64_t>(M)};
+  const uint64_t sbdims[2] = {static_cast<uint64_t>(N / 32), static_cast<uint64_t>(K) * static_cast<uint64_t>(E)};
+  const uint32_t sbox[2] = {16, kBM};
+  const uint64_t cdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint32_t cbox[2] = {kEpiRowBytes / 2, 32};
+  if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dC->ptr, 2, adims, abox) ||
+      !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BT->ptr, 3, bdims, bbox) ||
+      !make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dC->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BT->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dA, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_INVALID_ARG;
+  Params p{offsets, M, K, N, E, dA, nullptr, preact, nullptr, dev_status};
+  if (epi == MOE_EPI_DSWIGLU) return launch<2, kFwd, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
+  return launch<2, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
+}
+
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
                                                const int32_t* offsets, int M, int N, int K, int E,
                                                void* dB, moe_dtype_t dB_dtype, int32_t* dev_status,
@@ -1201,9 +1305,36 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   int sms = 0;
   moe_status_t st = common_checks(fn, A, dC, offsets, M, N, K, E, dB, &sms);
   if (st != MOE_OK) return st;
-  if (A->dtype != MOE_BF16 || dB_dtype != MOE_BF16) {
-    set_error("%s: BF16 operands and output only", fn);
+  if ((A->dtype != MOE_BF16 && A->dtype != MOE_E4M3) || dB_dtype != MOE_BF16) {
+    set_error("%s: BF16 or MXFP8 (E4M3) operands, BF16 output", fn);
     return MOE_ERR_UNSUPPORTED;
+  }
+  // dB [E, N, K] is written by TMA from 32-column x 32-row staging boxes (64-byte swizzle)
+  CUtensorMap td;
+  const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+  const uint32_t dbox[3] = {32, 32, 1};
+  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_INVALID_ARG;
+  if (A->dtype == MOE_E4M3) {
+    // Both operands quantised column-wise (group-aware, along the rows), scales in
+    // the tiled layout; read as 128 x 128 MN-major boxes (128-byte swizzle).
+    if (N % 128 || K % 128 || (M > 0 && (!A->scales || !dC->scales)) || !aligned16(A->scales) ||
+        !aligned16(dC->scales)) {
+      set_error("%s: MXFP8 needs N %% 128 == 0, K %% 128 == 0 and 16-byte aligned tiled scales", fn);
+      return MOE_ERR_INVALID_ARG;
+    }
+    CUtensorMap ta, tb;
+    const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M > 0 ? M : 1)};
+    const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M > 0 ? M : 1)};
+    const uint32_t box[2] = {128, kMxWgRows};
+    const void* cptr = dC->ptr ? dC->ptr : dB;
+    const void* aptr = A->ptr ? A->ptr : dB;
+    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, cptr, 2, cdims, box) ||
+        !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, aptr, 2, adims, box))
+      return MOE_ERR_INVALID_ARG;
+    Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status,
+             static_cast<const uint8_t*>(dC->scales), static_cast<const uint8_t*>(A->scales)};
+    return launch<2, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   }
   CUtensorMap ta, tb;
   // The MMA's A operand is dC^T (rows n, contraction over the group's rows); its
@@ -1215,12 +1346,6 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
   const void* aptr = A->ptr ? A->ptr : dB;
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cptr, 2, cdims, box) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aptr, 2, adims, box))
-    return MOE_ERR_INVALID_ARG;
-  // dB [E, N, K] is written by TMA from 32-column x 32-row staging boxes (64-byte swizzle)
-  CUtensorMap td;
-  const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
-  const uint32_t dbox[3] = {32, 32, 1};
-  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox, CU_TENSOR_MAP_SWIZZLE_64B))
     return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status};
   return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);

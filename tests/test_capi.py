@@ -70,6 +70,8 @@ def test_bad_arguments_rejected_before_any_launch():
     st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 1, None, None, None)
     assert st == _lib.MOE_ERR_INVALID_ARG                                      # column-wise without groups
     st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 2, None, None, None)
+    assert st == _lib.MOE_ERR_INVALID_ARG                                      # tiled column-wise without groups
+    st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 3, None, None, None)
     assert st == _lib.MOE_ERR_UNSUPPORTED                                      # no such axis
 
 

@@ -191,6 +191,47 @@ def test_quantize_colwise_grouped_bit_exact(dtype, counts, K):
     assert (scales[n:] == 0xA5).all()
 
 
+def tiled_scale_index(offsets, K):
+    """Byte index, in the tiled column-wise scale layout, of every (block row, column)
+    of the compact layout, block rows numbered group by group."""
+    idx = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for b in range((hi - lo + 31) // 32):
+            quad = lo // 128 + e + b // 4
+            m = np.arange(K)
+            idx.append((quad * (K // 128) + m // 128) * 512 + (m % 32) * 16 + ((m % 128) // 32) * 4 + b % 4)
+    return np.array(idx, dtype=np.int64).reshape(-1, K)
+
+
+@pytest.mark.parametrize("counts,K", [([0, 1, 130, 257, 3, 128, 0, 64], 256),
+                                      ([1] * 300, 128),
+                                      ([0, 0, 700], 384),
+                                      ([127, 129, 0, 256, 31], 512)],
+                         ids=["mixed", "singles", "lead-empty", "quad-edges"])
+def test_quantize_colwise_tiled_scales(counts, K):
+    """Axis 2: the codes of axis 1, and each scale byte at its place in the tiled
+    layout equal to the oracle's; bytes outside every group's blocks untouched."""
+    need_gpu()
+    rows = int(sum(counts))
+    a = W.make_matrix(rows, K, seed=len(counts) + K + 1, dtype=torch.bfloat16, device="cuda")
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32, device="cuda")
+    E = len(counts)
+    codes = torch.full((rows, K), 0x5A, dtype=torch.uint8, device="cuda")
+    tiles = ((rows + 127) // 128 + E) * (K // 128)
+    scales = torch.full((tiles, 512), 0xA5, dtype=torch.uint8, device="cuda")
+    moe_gpu.moe_quantize_mxfp8_grouped(a, off, E, codes=codes, scales=scales, axis=2)
+    c, sc = omx.quantize_colwise_grouped(f64(a), off.cpu().numpy())
+    assert (codes.cpu().numpy() == c).all()
+    idx = tiled_scale_index(off.cpu().numpy(), K)
+    flat = scales.cpu().numpy().reshape(-1)
+    assert len(np.unique(idx)) == idx.size and idx.max() < flat.size      # distinct places, in the buffer
+    assert (flat[idx] == sc).all()
+    rest = np.ones(flat.size, dtype=bool)
+    rest[idx.reshape(-1)] = False
+    assert (flat[rest] == 0xA5).all()
+
+
 def test_quantize_colwise_needs_offsets():
     need_gpu()
     a = W.make_matrix(64, 64, seed=1, dtype=torch.bfloat16, device="cuda")

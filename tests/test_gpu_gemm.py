@@ -290,3 +290,147 @@ def test_fwd_mxfp8_requires_scales_and_k_multiple_of_512():
     Bq, Bs, _ = _quantize(B)
     with pytest.raises(moe_gpu.binding.MoeError, match="512"):
         moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, ragged_offsets([32, 32]), A_scales=As, B_scales=Bs)
+
+
+# ----------------------------------------------------------------------------- MXFP8 data gradient
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("G,R,C", [(3, 64, 40), (2, 512, 264), (1, 32, 8), (4, 96, 1024)])
+def test_quantize_transposed(dtype, G, R, C):
+    """Codes and scales of B^T equal the oracle's row-wise quantiser on each B[g]^T,
+    bit for bit (C spans several 256-column tiles and a partial one)."""
+    need_gpu()
+    x = W.make_matrix(G * R, C, seed=G + R + C, dtype=dtype, device="cuda", scale=3.0).view(G, R, C)
+    codes, scales = moe_gpu.moe_quantize_mxfp8_transposed(x)
+    assert codes.shape == (G, C, R) and scales.shape == (G * C, R // 32)
+    xt = f64(x).transpose(0, 2, 1).reshape(G * C, R)
+    c, s = omx.quantize_rowwise(xt)
+    assert (codes.cpu().numpy().reshape(G * C, R) == c).all()
+    assert (scales.cpu().numpy() == s).all()
+
+
+def test_quantize_transposed_rejects_bad_shapes():
+    need_gpu()
+    x = torch.zeros(2, 48, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_quantize_mxfp8_transposed(x)          # R % 32 != 0
+
+
+def _dgrad_mx_operands(M, N, K, E, seed):
+    """dC [M,N] and B [E,N,K] in bf16, their MXFP8 forms along N, and the values
+    the quantised operands decode to."""
+    dC = W.make_matrix(M, N, seed=seed, dtype=torch.bfloat16, device="cuda")
+    B = W.make_matrix(E * N, K, seed=seed + 1, dtype=torch.bfloat16, device="cuda", scale=N ** -0.5).view(E, N, K)
+    dCq, dCs, dC_deq = _quantize(dC)
+    BTq, BTs = moe_gpu.moe_quantize_mxfp8_transposed(B)
+    c, s = omx.quantize_rowwise(f64(B).transpose(0, 2, 1).reshape(E * K, N))
+    assert (BTq.cpu().numpy().reshape(E * K, N) == c).all() and (BTs.cpu().numpy() == s).all()
+    B_deq = omx.dequantize_rowwise(c, s).reshape(E, K, N).transpose(0, 2, 1)   # [E, N, K]
+    return dCq, dCs, dC_deq, BTq, BTs, B_deq
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "all-in-last"], ids=str)
+@pytest.mark.parametrize("N,K", [(512, 256), (1024, 96), (512, 320)])
+def test_dgrad_mxfp8_plain(counts, N, K):
+    """dA = dC . B[e] on MXFP8 operands quantised along N; rows outside every group
+    untouched."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 3
+    rows = int(sum(cnt))
+    dCq, dCs, dC_deq, BTq, BTs, B_deq = _dgrad_mx_operands(M, N, K, E, seed=N + K + 21)
+    off = ragged_offsets(cnt)
+    dA = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_dgrad_mxfp8(dCq, BTq, off, dC_scales=dCs, BT_scales=BTs, out=dA)
+    want = om.grouped_gemm_dgrad(dC_deq, B_deq, off.cpu().numpy())
+    got = f64(dA)
+    assert np.isnan(got[rows:]).all()
+    err = rel_l2(got[:rows], want[:rows])
+    assert err < TOL_MXFP8 and err < 1e-2, err        # same quantised inputs: only fp32/bf16 rounding
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+@pytest.mark.parametrize("d,f", [(512, 256), (1024, 96), (512, 288)])
+def test_dgrad_mxfp8_dswiglu(counts, d, f):
+    """GEMM2 data gradient on MXFP8 operands with the SwiGLU backward fused."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt))
+    dCq, dCs, dC_deq, BTq, BTs, B_deq = _dgrad_mx_operands(M, d, f, E, seed=d + f + 23)
+    GU = W.make_matrix(M, 2 * f, seed=d + f + 25, dtype=torch.bfloat16, device="cuda", scale=2.0)
+    off = ragged_offsets(cnt)
+    dGU = moe_gpu.moe_grouped_gemm_dgrad_mxfp8(dCq, BTq, off, dC_scales=dCs, BT_scales=BTs, epi="dswiglu",
+                                               preact=GU)
+    dH = om.grouped_gemm_dgrad(dC_deq, B_deq, off.cpu().numpy())
+    want = om.dswiglu(dH, f64(GU))
+    assert dGU.shape == (M, 2 * f)
+    assert rel_l2(f64(dGU), want) < 1e-2
+
+
+def test_dgrad_mxfp8_rejects_bad_args():
+    need_gpu()
+    dCq, dCs, _, BTq, BTs, _ = _dgrad_mx_operands(64, 512, 64, 2, seed=5)
+    off = ragged_offsets([32, 32])
+    with pytest.raises(moe_gpu.binding.MoeError, match="512"):     # N % 512
+        moe_gpu.moe_grouped_gemm_dgrad_mxfp8(dCq[:, :256].contiguous(), BTq[:, :, :256].contiguous(), off,
+                                             dC_scales=dCs[:, :8].contiguous(), BT_scales=BTs[:, :8].contiguous())
+    with pytest.raises(moe_gpu.binding.MoeError):                  # bf16 operands
+        dC = torch.zeros(64, 512, dtype=torch.bfloat16, device="cuda")
+        B = torch.zeros(2, 64, 512, dtype=torch.bfloat16, device="cuda")
+        moe_gpu.moe_grouped_gemm_dgrad_mxfp8(dC, B, off, dC_scales=None, BT_scales=None)
+
+
+# ----------------------------------------------------------------------------- MXFP8 weight gradient
+
+def _colwise_tiled(t, off, E):
+    """Tiled column-wise MXFP8 of t on the GPU and the values the oracle's own
+    column-wise quantisation of t decodes to (codes bit-exact with the oracle)."""
+    codes, scales = moe_gpu.moe_quantize_mxfp8_grouped(t, off, E, axis=2)
+    c, sc = omx.quantize_colwise_grouped(f64(t), off.cpu().numpy())
+    rows = int(off[-1])                       # rows no group owns get no codes
+    assert (codes[:rows].cpu().numpy() == c[:rows]).all()
+    return codes, scales, omx.dequantize_colwise_grouped(c, sc, off.cpu().numpy())
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "all-in-last", "one-expert"], ids=str)
+@pytest.mark.parametrize("N,K", [(256, 512), (128, 384), (384, 128)])
+def test_wgrad_mxfp8(counts, N, K):
+    """dB[e] = dC[R_e]^T A[R_e] on column-wise group-aware MXFP8 operands (blocks of
+    32 down the contraction, restarting at each group): the oracle's result on the
+    same quantised values; empty groups exact zeros; rows no group owns never read."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    rows = int(sum(cnt))
+    M = rows + 7
+    A = W.make_matrix(M, K, seed=N + K + 31, dtype=torch.bfloat16, device="cuda")
+    dC = W.make_matrix(M, N, seed=N + K + 33, dtype=torch.bfloat16, device="cuda")
+    off = ragged_offsets(cnt)
+    Aq, As, A_deq = _colwise_tiled(A, off, E)
+    Cq, Cs, C_deq = _colwise_tiled(dC, off, E)
+    Aq[rows:] = 0x7E                          # poison the rows no group owns (448)
+    dB = torch.full((E, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_wgrad(Aq, Cq, off, E, A_scales=As, dC_scales=Cs, out=dB)
+    want = om.grouped_gemm_wgrad(A_deq, C_deq, off.cpu().numpy(), E)
+    got = f64(dB)
+    for e in range(E):
+        if cnt[e] == 0:
+            assert (got[e] == 0).all() and not np.signbit(got[e]).any(), f"expert {e} not exactly zero"
+    assert not np.isnan(got).any()
+    err = rel_l2(got, want)
+    assert err < TOL_MXFP8 and err < 1e-2, err       # same quantised inputs: only fp32/bf16 rounding
+
+
+def test_wgrad_mxfp8_rejects_bad_shapes_and_missing_scales():
+    need_gpu()
+    off = ragged_offsets([32, 32])
+    A = torch.zeros(64, 96, dtype=torch.uint8, device="cuda")
+    dC = torch.zeros(64, 128, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe_gpu.binding.MoeError, match="128"):                 # K % 128
+        moe_gpu.moe_grouped_gemm_wgrad(A, dC, off, 2, A_scales=s, dC_scales=s)
+    A = torch.zeros(64, 128, dtype=torch.uint8, device="cuda")
+    with pytest.raises(moe_gpu.binding.MoeError):                             # no scales
+        moe_gpu.moe_grouped_gemm_wgrad(A, dC, off, 2)

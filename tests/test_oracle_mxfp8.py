@@ -128,3 +128,30 @@ def test_colwise_grouped_blocks_restart_per_group():
         c_t, s_t = mxfp8.quantize_rowwise(pad.T.copy())
         assert (scales[b] == s_t[:, 0]).all()
         assert (codes[r0:r1].T == c_t[:, :r1 - r0]).all()
+
+
+def test_colwise_dequantize_matches_transposed_rowwise():
+    """One group whose size is a multiple of 32: the column-wise round trip equals
+    the row-wise round trip of the transpose (already pinned above)."""
+    rng = np.random.default_rng(11)
+    a = rng.standard_normal((96, 64)) * np.exp2(rng.integers(-6, 6, size=(96, 1)))
+    codes, scales = mxfp8.quantize_colwise_grouped(a, np.array([0, 96]))
+    got = mxfp8.dequantize_colwise_grouped(codes, scales, np.array([0, 96]))
+    c_t, s_t = mxfp8.quantize_rowwise(a.T.copy())
+    assert np.array_equal(got, mxfp8.dequantize_rowwise(c_t, s_t).T)
+
+
+def test_colwise_dequantize_keeps_groups_apart():
+    """Neighbouring groups of very different magnitude: each element comes back
+    within the E4M3 half-ulp bound of its own group's block (a scale taken from
+    the wrong group would flush the small group to zero or saturate it).  Values
+    lie in [1, 1.5) times a power of two per group: normal range, no saturation."""
+    rng = np.random.default_rng(12)
+    offsets = np.array([0, 7, 7, 40, 41, 75])
+    a = rng.uniform(1.0, 1.5, size=(75, 32)) * rng.choice([-1.0, 1.0], size=(75, 32))
+    a[7:40] *= 2.0 ** 12
+    a[41:75] *= 2.0 ** -12
+    codes, scales = mxfp8.quantize_colwise_grouped(a, offsets)
+    got = mxfp8.dequantize_colwise_grouped(codes, scales, offsets)
+    assert (np.abs(got - a) <= np.abs(a) * 2.0 ** -4 + 1e-300).all()
+    assert (got != 0).all()
