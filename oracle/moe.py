@@ -275,17 +275,45 @@ def route_bwd(dw, w, idx, logits, renormalize=True):
     return dl
 
 
-def layer_backward(fwd, dy, x, logits, W1, W2, k, renormalize=True):
-    """The full backward of ``layer_forward`` (bf16/fp32 operands), returning
-    dx, dlogits, dW1, dW2 and the intermediates dYp, dw, dGU, dXp."""
+def mx_roundtrip_dim1(W: np.ndarray) -> np.ndarray:
+    """Values of a weight stack W [E, R, C] quantised along R (its output dim), as
+    the data gradient reads it: blocks of 32 consecutive rows of one column."""
+    Wt = np.ascontiguousarray(np.asarray(W, dtype=np.float64).transpose(0, 2, 1))
+    return mx_roundtrip(Wt).transpose(0, 2, 1)
+
+
+def mx_roundtrip_colwise(a: np.ndarray, offsets: np.ndarray) -> np.ndarray:
+    """Values of a [rows, K] operand quantised column-wise and group-aware, as the
+    weight gradient reads it (blocks of 32 rows restarting at each group)."""
+    c, s = mxfp8.quantize_colwise_grouped(a, offsets)
+    return mxfp8.dequantize_colwise_grouped(c, s, offsets)
+
+
+def layer_backward(fwd, dy, x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False):
+    """The full backward of ``layer_forward``, returning dx, dlogits, dW1, dW2 and
+    the intermediates dYp, dw, dGU, dXp.
+
+    With ``mxfp8_operands`` every backward GEMM takes MXFP8 operands quantised
+    along its own contraction dim ([1] "grouped quantisation"): the data
+    gradients read dYp / dGU row-wise and W2 / W1 along their output dim; the
+    weight gradients read H, dYp, Xp and dGU column-wise, group-aware."""
     E = W1.shape[0]
     offsets, dest_row = fwd["offsets"], fwd["dest_row"]
     dYp, dw = combine_bwd(dy, fwd["Yp"], dest_row, fwd["w"])
-    dH = grouped_gemm_dgrad(dYp, W2, offsets)
-    dGU = dswiglu(dH, fwd["GU"])
-    dW2 = grouped_gemm_wgrad(fwd["H"], dYp, offsets, E)
-    dXp = grouped_gemm_dgrad(dGU, W1, offsets)
-    dW1 = grouped_gemm_wgrad(fwd["Xp"], dGU, offsets, E)
+    if mxfp8_operands:
+        dH = grouped_gemm_dgrad(mx_roundtrip(dYp), mx_roundtrip_dim1(W2), offsets)
+        dGU = dswiglu(dH, fwd["GU"])
+        dW2 = grouped_gemm_wgrad(mx_roundtrip_colwise(fwd["H"], offsets), mx_roundtrip_colwise(dYp, offsets),
+                                 offsets, E)
+        dXp = grouped_gemm_dgrad(mx_roundtrip(dGU), mx_roundtrip_dim1(W1), offsets)
+        dW1 = grouped_gemm_wgrad(mx_roundtrip_colwise(fwd["Xp"], offsets), mx_roundtrip_colwise(dGU, offsets),
+                                 offsets, E)
+    else:
+        dH = grouped_gemm_dgrad(dYp, W2, offsets)
+        dGU = dswiglu(dH, fwd["GU"])
+        dW2 = grouped_gemm_wgrad(fwd["H"], dYp, offsets, E)
+        dXp = grouped_gemm_dgrad(dGU, W1, offsets)
+        dW1 = grouped_gemm_wgrad(fwd["Xp"], dGU, offsets, E)
     dx = combine(dXp, dest_row, None)
     dlogits = route_bwd(dw, fwd["w"], fwd["idx"], logits, renormalize)
     return dict(dYp=dYp, dw=dw, dH=dH, dGU=dGU, dW2=dW2, dXp=dXp, dW1=dW1, dx=dx,

@@ -22,13 +22,18 @@ class MoELayer:
     W1 [E, 2f, d] (gate rows then up rows) and W2 [E, d, f] in the compute dtype
     ("f32", "bf16"; "mxfp8" keeps bf16 master weights and quantises them once,
     at construction, to MXFP8 codes + E8M0 scales along the contraction dim).
+
+    MXFP8 training quantises every GEMM operand along that GEMM's contraction:
+    the forward and the data gradients read activations and gradients row-wise
+    (the weights along d for GEMM1, along f for GEMM2, and along their output dim
+    for the data gradients); the weight gradients read Xp, H, dYp and dGU
+    column-wise, group-aware, with scales in the weight-gradient GEMM's tiled
+    layout.  Activations and gradients are kept in bf16 between the GEMMs.
     """
 
     def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False):
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.dtype, self.renormalize, self.training = dtype, renormalize, training
-        if training and dtype == "mxfp8":
-            raise NotImplementedError("the MXFP8 backward is not built")
         dev = W1.device
         self.device = dev
         M = T * k
@@ -50,18 +55,35 @@ class MoELayer:
         self.yp = torch.empty(M, d, dtype=store, device=dev)
         self.y = torch.empty(T, d, dtype=store, device=dev)
         self.gu = torch.empty(M, 2 * f, dtype=store, device=dev) if training else None
+        u8 = dict(dtype=torch.uint8, device=dev)
         if dtype == "mxfp8":
-            self.xq = torch.empty(M, d, dtype=torch.uint8, device=dev)
-            self.xs = torch.empty(M, d // 32, dtype=torch.uint8, device=dev)
-            self.hq = torch.empty(M, f, dtype=torch.uint8, device=dev)
-            self.hs = torch.empty(M, f // 32, dtype=torch.uint8, device=dev)
+            self.xq = torch.empty(M, d, **u8)
+            self.xs = torch.empty(M, d // 32, **u8)
+            self.hq = torch.empty(M, f, **u8)
+            self.hs = torch.empty(M, f // 32, **u8)
             self.W1q, self.W1s = B.moe_quantize_mxfp8_grouped(W1.reshape(E * 2 * f, d))
             self.W2q, self.W2s = B.moe_quantize_mxfp8_grouped(W2.reshape(E * d, f))
             self.W1q, self.W1s = self.W1q.view(E, 2 * f, d), self.W1s.view(E, 2 * f, d // 32)
             self.W2q, self.W2s = self.W2q.view(E, d, f), self.W2s.view(E, d, f // 32)
-            self.xp = None
+            self.xp = torch.empty(M, d, dtype=store, device=dev) if training else None
         else:
             self.xp = torch.empty(M, d, dtype=store, device=dev)
+        if dtype == "mxfp8" and training:
+            # data gradients: the weights quantised along their output dim (W^T row-wise)
+            self.W1t, self.W1ts = B.moe_quantize_mxfp8_transposed(W1)          # [E, d, 2f]
+            self.W2t, self.W2ts = B.moe_quantize_mxfp8_transposed(W2)          # [E, f, d]
+
+            def colwise(width):
+                tiles = ((M + 127) // 128 + E) * (width // 128)
+                return torch.empty(M, width, **u8), torch.empty(tiles, 512, **u8)
+            # weight gradients: column-wise, group-aware operands (tiled scales)
+            self.xcq, self.xcs = colwise(d)
+            self.hcq, self.hcs = colwise(f)
+            self.dycq, self.dycs = colwise(d)
+            self.dgcq, self.dgcs = colwise(2 * f)
+            # data gradients: row-wise dYp and dGU
+            self.dyq, self.dys = torch.empty(M, d, **u8), torch.empty(M, d // 32, **u8)
+            self.dgq, self.dgs = torch.empty(M, 2 * f, **u8), torch.empty(M, 2 * f // 32, **u8)
         if training:
             self.dyp = torch.empty(M, d, dtype=store, device=dev)
             self.dw = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -78,7 +100,14 @@ class MoELayer:
                          topk_w=self.topk_w, counts=self.counts, dev_status=self.dev_status)
 
     def dispatch(self, x):
-        if self.dtype == "mxfp8":
+        if self.dtype == "mxfp8" and self.training:
+            # bf16 Xp (kept for the weight gradient), then both MXFP8 forms of it
+            B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
+                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
+                          workspace=self.workspace, dev_status=self.dev_status)
+            B.moe_quantize_mxfp8_grouped(self.xp, codes=self.xq, scales=self.xs)
+            B.moe_quantize_mxfp8_grouped(self.xp, self.offsets, self.E, codes=self.xcq, scales=self.xcs, axis=2)
+        elif self.dtype == "mxfp8":
             B.moe_permute(x, self.topk_idx, self.counts, self.E, xp_dtype="mxfp8", offsets=self.offsets,
                           dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xq,
                           xp_scales=self.xs, workspace=self.workspace, dev_status=self.dev_status)
@@ -88,7 +117,15 @@ class MoELayer:
                           workspace=self.workspace, dev_status=self.dev_status)
 
     def expert_mlp(self):
-        if self.dtype == "mxfp8":
+        if self.dtype == "mxfp8" and self.training:
+            # GEMM1 keeps H and the pre-activations in bf16 for the backward
+            B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
+                                   B_scales=self.W1s, out=self.h, preact=self.gu, dev_status=self.dev_status)
+            B.moe_quantize_mxfp8_grouped(self.h, codes=self.hq, scales=self.hs)
+            B.moe_quantize_mxfp8_grouped(self.h, self.offsets, self.E, codes=self.hcq, scales=self.hcs, axis=2)
+            B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
+                                   out=self.yp, dev_status=self.dev_status)
+        elif self.dtype == "mxfp8":
             B.moe_grouped_gemm_fwd_mxfp8_out(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
                                              B_scales=self.W1s, codes=self.hq, scales=self.hs,
                                              dev_status=self.dev_status)
@@ -114,12 +151,14 @@ class MoELayer:
 
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
-        scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine."""
-        return 2 + 2 + 2 + 1
+        scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
+        MXFP8 training adds the row- and column-wise quantisation of Xp and of H."""
+        return 2 + 2 + 2 + 1 + (4 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:
-        """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd."""
-        return 7
+        """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd;
+        MXFP8 adds the row- and column-wise quantisation of dYp and of dGU."""
+        return 7 + (4 if self.dtype == "mxfp8" else 0)
 
     # ------------------------------------------------------------------ backward
     def backward(self, dy, logits=None, dx_out=None):
@@ -130,11 +169,26 @@ class MoELayer:
         st = self.dev_status
         B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
                                     dev_status=st)
-        B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
-                                 out=self.dgu, dev_status=st)
-        B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
-        B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
-        B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
+        if self.dtype == "mxfp8":
+            off, E = self.offsets, self.E
+            B.moe_quantize_mxfp8_grouped(self.dyp, codes=self.dyq, scales=self.dys)
+            B.moe_quantize_mxfp8_grouped(self.dyp, off, E, codes=self.dycq, scales=self.dycs, axis=2)
+            B.moe_grouped_gemm_dgrad_mxfp8(self.dyq, self.W2t, off, dC_scales=self.dys, BT_scales=self.W2ts,
+                                           epi="dswiglu", preact=self.gu, out=self.dgu, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.hcq, self.dycq, off, E, A_scales=self.hcs, dC_scales=self.dycs,
+                                     out=self.dW2, dev_status=st)
+            B.moe_quantize_mxfp8_grouped(self.dgu, codes=self.dgq, scales=self.dgs)
+            B.moe_quantize_mxfp8_grouped(self.dgu, off, E, codes=self.dgcq, scales=self.dgcs, axis=2)
+            B.moe_grouped_gemm_dgrad_mxfp8(self.dgq, self.W1t, off, dC_scales=self.dgs, BT_scales=self.W1ts,
+                                           out=self.dxp, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.xcq, self.dgcq, off, E, A_scales=self.xcs, dC_scales=self.dgcs,
+                                     out=self.dW1, dev_status=st)
+        else:
+            B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
+                                     out=self.dgu, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
+            B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
         dx = self.dx if dx_out is None else dx_out
         B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=dx, dev_status=st)
         B.moe_route_topk_bwd(self.dw, self.topk_w, self.topk_idx, self.E, logits=logits,

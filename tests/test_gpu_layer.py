@@ -211,6 +211,34 @@ def test_mxfp8_layer_scaled_full():
     assert rel_l2(f64(y), ref["y"]) < TOL_MXFP8
 
 
+@pytest.mark.parametrize("w", [W.BY_NAME["dsv3-mxfp8"].scaled(T=256, d=512, f=512, name="dsv3-mx-train-small"),
+                               W.BY_NAME["dsv3-mxfp8"].scaled(T=600, E=16, d=512, f=512, name="mx-train-E16")],
+                         ids=lambda w: w.name)
+def test_mxfp8_backward_scaled_full(w):
+    """MXFP8 training step (forward and backward, every GEMM on MXFP8 operands
+    quantised along its own contraction) against the oracle's MXFP8 chain, every
+    element; experts without rows get exact zero weight gradients."""
+    need_gpu()
+    layer, x, W1, W2, lg = _build(w, training=True)
+    dy = W.make_dy(w, "cuda")
+    layer.forward(x, lg)
+    dx, dlogits, dW1, dW2 = layer.backward(dy, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    lg_h = lg.cpu().numpy()
+    ref = om.layer_forward(f64(x), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=True)
+    bwd = om.layer_backward(ref, f64(dy), f64(x), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=True)
+    assert (i64(layer.src_pair) == ref["src_pair"]).all()
+    assert rel_l2(f64(layer.gu), ref["GU"]) < TOL_MXFP8
+    assert rel_l2(f64(layer.h), ref["H"]) < TOL_MXFP8
+    for name, got in (("dYp", layer.dyp), ("dGU", layer.dgu), ("dXp", layer.dxp), ("dW2", dW2), ("dW1", dW1),
+                      ("dx", dx), ("dlogits", dlogits)):
+        err = rel_l2(f64(got), bwd[name])
+        assert err < TOL_MXFP8, (name, err)
+    for e in np.nonzero(ref["counts"] == 0)[0]:
+        assert (f64(dW1[e]) == 0).all() and (f64(dW2[e]) == 0).all()
+
+
 def test_mxfp8_layer_full_size_sampled():
     need_gpu()
     w = W.BY_NAME["dsv3-mxfp8"]

@@ -193,3 +193,68 @@ def test_expert_wgrad_sampled_matches_full_wgrad():
         dw1, dw2 = moe.expert_wgrad_sampled(fwd["Xp"][lo:hi], bwd["dYp"][lo:hi], W1[e], W2[e], rows, cols)
         np.testing.assert_allclose(dw1, bwd["dW1"][e][rows], rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(dw2, bwd["dW2"][e][:, cols], rtol=1e-11, atol=1e-13)
+
+
+def _block_values(v, lo, hi):
+    """Values of v[lo:hi] (one column of one group) under blocks of 32 starting at
+    lo, each quantised by the row-wise quantiser as one zero-padded row."""
+    from oracle import mxfp8
+    out = np.zeros(hi - lo)
+    for r0 in range(lo, hi, 32):
+        r1 = min(r0 + 32, hi)
+        blk = np.zeros((1, 32))
+        blk[0, :r1 - r0] = v[r0:r1]
+        out[r0 - lo:r1 - lo] = mxfp8.dequantize_rowwise(*mxfp8.quantize_rowwise(blk))[0, :r1 - r0]
+    return out
+
+
+def _row_values(v):
+    from oracle import mxfp8
+    return mxfp8.dequantize_rowwise(*mxfp8.quantize_rowwise(np.asarray(v, dtype=np.float64)[None, :]))[0]
+
+
+def test_mxfp8_backward_elements_from_blockwise_quantisation():
+    """Each MXFP8 backward GEMM, element by element: operands quantised along that
+    GEMM's own contraction, built here one block at a time through the row-wise
+    quantiser (pinned on its own) rather than through the layer's helpers."""
+    T, d, E, k, f = 48, 64, 3, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=71)
+    dy = np.random.default_rng(72).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=True)
+    bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k, mxfp8_operands=True)
+    off = fwd["offsets"]
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi - lo < 2:
+            continue
+        for i, j in ((0, 0), (d - 1, 5), (17, f - 1)):          # dW2[e][i, j]: contraction over the group's rows
+            want = _block_values(bwd["dYp"][:, i], lo, hi) @ _block_values(fwd["H"][:, j], lo, hi)
+            np.testing.assert_allclose(bwd["dW2"][e][i, j], want, rtol=1e-12, atol=1e-14)
+        for m, c in ((0, 0), (2 * f - 1, d - 1), (f, 9)):       # dW1[e][m, c]
+            want = _block_values(bwd["dGU"][:, m], lo, hi) @ _block_values(fwd["Xp"][:, c], lo, hi)
+            np.testing.assert_allclose(bwd["dW1"][e][m, c], want, rtol=1e-12, atol=1e-14)
+        for r in (lo, hi - 1):                                  # data gradients: contraction over d / 2f
+            for j in (0, f - 1):
+                want = _row_values(bwd["dYp"][r]) @ _row_values(W2[e][:, j])
+                np.testing.assert_allclose(bwd["dH"][r, j], want, rtol=1e-12, atol=1e-14)
+            for c in (0, d - 1):
+                want = _row_values(bwd["dGU"][r]) @ _row_values(W1[e][:, c])
+                np.testing.assert_allclose(bwd["dXp"][r, c], want, rtol=1e-12, atol=1e-14)
+
+
+def test_mxfp8_backward_close_to_exact():
+    """The MXFP8 gradients stay within the format's error of the exact ones: E4M3
+    keeps 3 mantissa bits (about 3.6% rms relative error per quantised operand),
+    and dx passes through two quantised data gradients, each with both operands
+    quantised, after a quantised forward; a transposed operand or a wrong group
+    would be off by order one."""
+    T, d, E, k, f = 64, 64, 4, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=81)
+    dy = np.random.default_rng(82).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k)
+    exact = moe.layer_backward(fwd, dy, x, lg, W1, W2, k)
+    fwd_mx = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=True)
+    mx = moe.layer_backward(fwd_mx, dy, x, lg, W1, W2, k, mxfp8_operands=True)
+    for name in ("dx", "dW1", "dW2", "dlogits"):
+        err = np.linalg.norm(mx[name] - exact[name]) / np.linalg.norm(exact[name])
+        assert 0 < err < 0.2, (name, err)
