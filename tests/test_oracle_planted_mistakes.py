@@ -94,3 +94,26 @@ def test_pins_catch_scale_exponent_off_by_one(monkeypatch):
         mx_pins.test_shared_exponent_closed_form(1.0, 119)
     with pytest.raises(AssertionError):
         mx_pins.test_quantize_rowwise_properties()
+
+
+def _dequant_colwise_next_scale(codes, scales, offsets):
+    """Each block decoded with the scale row of the block after it."""
+    rolled = np.concatenate([scales[1:], scales[:1]], axis=0)
+    return _real_dequant_colwise(codes, rolled, offsets)
+
+
+_real_dequant_colwise = mxfp8.dequantize_colwise_grouped
+
+
+@pytest.mark.parametrize("target,attr,fake,check", [
+    (moe, "mx_roundtrip_colwise", lambda a, offsets: moe.mx_roundtrip(a),
+     lambda: ffn_pins.test_mxfp8_backward_elements_from_blockwise_quantisation()),
+    (moe, "mx_roundtrip_dim1", lambda W: moe.mx_roundtrip(W),
+     lambda: ffn_pins.test_mxfp8_backward_elements_from_blockwise_quantisation()),
+    (mxfp8, "dequantize_colwise_grouped", _dequant_colwise_next_scale,
+     lambda: mx_pins.test_colwise_dequantize_matches_transposed_rowwise()),
+], ids=["wgrad-operands-row-wise", "dgrad-weights-wrong-dim", "colwise-scale-row"])
+def test_mxfp8_backward_pins_catch_planted_mistake(monkeypatch, target, attr, fake, check):
+    monkeypatch.setattr(target, attr, fake)
+    with pytest.raises(AssertionError):
+        check()
