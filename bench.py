@@ -137,11 +137,18 @@ class Clocks:
 # ----------------------------------------------------------------------------- our arm
 
 def stage_bytes(w):
-    """Algorithmic bytes of the bandwidth stages (each moved once)."""
+    """Algorithmic bytes of the bandwidth stages (each moved once).  The MXFP8
+    training dispatch writes Xp in bf16 and in both MXFP8 forms (row-wise codes +
+    scales, column-wise codes + scales): x read once, the three outputs written
+    once."""
     s = 4 if w.dtype == "f32" else 2
-    xp_s = 1 if w.dtype == "mxfp8" else s
-    permute = w.T * w.d * s + w.M * w.d * xp_s + (w.M * w.d // 32 if w.dtype == "mxfp8" else 0) \
-        + w.T * w.k * 4 * 3 + w.M * 4
+    if w.dtype == "mxfp8" and w.backward:
+        xp_out = w.M * w.d * (2 + 2 * (1 + 1 / 32))
+    elif w.dtype == "mxfp8":
+        xp_out = w.M * w.d * (1 + 1 / 32)
+    else:
+        xp_out = w.M * w.d * s
+    permute = w.T * w.d * s + xp_out + w.T * w.k * 4 * 3 + w.M * 4
     combine = w.M * w.d * s + w.T * w.d * s + w.T * w.k * 8
     return permute, combine
 
@@ -152,6 +159,8 @@ def gemm1_bytes(w, e_used):
     read once, H (MXFP8: its codes and scales; when training also the
     pre-activation G|U) written once."""
     M, d, f, E = w.M, w.d, w.f, e_used
+    if w.dtype == "mxfp8" and w.backward:       # H and G|U in bf16 for the backward
+        return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * 2 + M * 2 * f * 2
     if w.dtype == "mxfp8":
         return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * (1 + 1 / 32)   # H as MXFP8
     s = 4 if w.dtype == "f32" else 2
@@ -216,6 +225,17 @@ def run_ours(args, world, rank, local):
             mark(3)
             pkg.moe_grouped_gemm_fwd(layer.h, layer.W2, layer.offsets, out=layer.yp,
                                      dev_status=layer.dev_status)
+        elif ev is not None and w.backward:
+            # MXFP8 training: GEMM1 (bf16 H and G|U) with H's two quantisations, then GEMM2
+            pkg.moe_grouped_gemm_fwd(layer.xq, layer.W1q, layer.offsets, epi="swiglu", A_scales=layer.xs,
+                                     B_scales=layer.W1s, out=layer.h, preact=layer.gu,
+                                     dev_status=layer.dev_status)
+            pkg.moe_quantize_mxfp8_grouped(layer.h, codes=layer.hq, scales=layer.hs)
+            pkg.moe_quantize_mxfp8_grouped(layer.h, layer.offsets, layer.E, codes=layer.hcq, scales=layer.hcs,
+                                           axis=2)
+            mark(3)
+            pkg.moe_grouped_gemm_fwd(layer.hq, layer.W2q, layer.offsets, A_scales=layer.hs,
+                                     B_scales=layer.W2s, out=layer.yp, dev_status=layer.dev_status)
         elif ev is not None:
             pkg.moe_grouped_gemm_fwd_mxfp8_out(layer.xq, layer.W1q, layer.offsets, epi="swiglu",
                                                A_scales=layer.xs, B_scales=layer.W1s, codes=layer.hq,
@@ -460,7 +480,7 @@ def cpu_baseline(w, budget_s=12.0):
         fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8")
         if w.backward:
             dy = x * 0 + 1.0
-            om.layer_backward(fwd, dy, x, lg, W1, W2, w.k, w.renormalize)
+            om.layer_backward(fwd, dy, x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8")
         dt = time.perf_counter() - t0
         per_tok = dt / n
         if dt > budget_s / 3 or n >= w.T:
@@ -490,7 +510,7 @@ def run_reference(args, world, rank):
     for _ in range(args.steps):
         fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
         if w.backward:
-            om.layer_backward(fwd, x * 0 + 1.0, x, lg, W1, W2, w.k, w.renormalize)
+            om.layer_backward(fwd, x * 0 + 1.0, x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
     dt = (time.perf_counter() - t0) / args.steps
     flops = w.fwd_flops * (3 if w.backward else 1) * n / w.T
     value = flops / dt / 1e12

@@ -11,7 +11,12 @@ Mixtral; first section): a tiny fp32 layer, a Mixtral-shaped layer, a
 Qwen3-235B-shaped layer and two DeepSeek-V3-shaped layers.  The pages train on
 real data; here every tensor is synthetic and seeded.
 
-Recipe (per workload, seed ``s`` = its position in ``WORKLOADS``):
+A sixth entry, the MXFP8 training step, is the DeepSeek-V3-shaped training
+layer again with every GEMM on MXFP8 operands: it reuses that layer's seed, so
+both see the same routing, activations, weights and upstream gradient.
+
+Recipe (per workload, seed ``s`` = its position in ``WORKLOADS``, shared by the
+MXFP8 training step with the bf16 one):
 
 * router logits ``z + b`` with ``z ~ N(0,1)`` of shape [T, E] and a
   per-expert bias ``b`` (zero, Gaussian, or the log of a Zipf pmf over a seeded
@@ -77,6 +82,7 @@ WORKLOADS = [
     Workload("qwen3-235b-bf16", 8192, 4096, 128, 8, 1536, "bf16", "zipf", 1.1, 2),
     Workload("dsv3-mxfp8", 8192, 7168, 256, 8, 2048, "mxfp8", "zipf", 1.3, 3),
     Workload("dsv3-bf16-train", 16384, 7168, 256, 8, 2048, "bf16", "zipf", 1.5, 4, backward=True),
+    Workload("dsv3-mxfp8-train", 16384, 7168, 256, 8, 2048, "mxfp8", "zipf", 1.5, 4, backward=True),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}
