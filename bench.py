@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--T", type=int, default=None, help="override tokens (small profiling cases)")
     ap.add_argument("--f", type=int, default=None, help="override expert hidden dim (profiling)")
     ap.add_argument("--E", type=int, default=None, help="override expert count (profiling)")
+    ap.add_argument("--router-gemm", action="store_true",
+                    help="also time the router GEMM fused with top-k (a seeded W_r) against routing from logits")
+    ap.add_argument("--capacity-factor", type=float, default=None,
+                    help="also time the capacity-based (drop/pad) forward with C = ceil(CF * T*k / E), the contrast case")
     return ap.parse_args()
 
 
@@ -352,7 +356,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f,
                    "M_rows": w.M, "backward": w.backward,
                    "timing": "eager launches" if args.eager else "whole step captured in one CUDA graph, replayed",
-                   "l2": f"inputs larger than L2: {(W1.numel() + W2.numel()) * W1.element_size() / 1e9:.2f} GB of expert weights streamed per step",
+                   "l2": l2_note(W1, W2),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "stages_ms": {k: round(v, 4) for k, v in per.items()},   # eager pass, events between stages
         "permute_gbs": round(perm_b / (per["dispatch"] * 1e-3) / 1e9, 1),
@@ -365,11 +369,100 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches * args.steps,
         "wall_s_timed": round(wall, 3),
     }
+    if args.router_gemm:
+        line["router_gemm"] = router_leg(w, x, lg, layer, pk)
+    if args.capacity_factor is not None:
+        line["capacity_contrast"] = capacity_leg(w, x, lg, layer, W1, W2, args.capacity_factor, ms)
     if not args.no_e2e:
         line["e2e"] = e2e(args, w, layer, x, lg_h, dy, world, flops)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
     return line
+
+
+def l2_note(W1, W2):
+    nbytes = (W1.numel() + W2.numel()) * W1.element_size()
+    if nbytes > L2_BYTES:
+        return f"inputs larger than L2: {nbytes / 1e9:.2f} GB of expert weights streamed per step"
+    return f"inputs smaller than L2 ({nbytes / 1e6:.1f} MB of expert weights, resident between steps; not flushed)"
+
+
+def _time_ms(fn, reps=20, warm=3):
+    """Mean device time of fn over reps calls (CUDA events on the current stream)."""
+    import torch
+    for _ in range(warm):
+        fn()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(s)
+    for _ in range(reps):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def router_leg(w, x, lg, layer, pk):
+    """The router GEMM fused with the top-k selection (moe_route_topk_gemm, seeded
+    W_r [E, d] ~ N(0, 1/d)) against routing from given logits (moe_route_topk):
+    device time per call, eager, 20 calls after 3 warm-ups."""
+    import torch
+    import ragged_grouped_gemm_topk_gb300 as pkg
+    from ragged_grouped_gemm_topk_gb300 import workloads as W
+    if w.E > 256 or w.k > 8:
+        return {"unavailable": "the fused router takes E <= 256 and k <= 8"}
+    xr = x if x.dtype in (torch.bfloat16, torch.float32) else x.bfloat16()
+    Wr = W.make_matrix(w.E, w.d, seed=1000 * w.seed + 9, dtype=xr.dtype, device=x.device, scale=w.d ** -0.5)
+    fused = lambda: pkg.moe_route_topk_gemm(xr, Wr, w.k, w.renormalize, topk_idx=layer.topk_idx,
+                                            topk_w=layer.topk_w, counts=layer.counts, dev_status=layer.dev_status)
+    t_f = _time_ms(fused)
+    t_p = _time_ms(lambda: layer.route(lg))
+    flops = 2.0 * w.T * w.d * w.E
+    peak = pk["bf16_sus"] * (0.5 if xr.dtype == torch.float32 else 1.0)
+    return {"ms": round(t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
+            "frac_of_peak": round(flops / (t_f * 1e-3) / 1e12 / peak, 4),
+            "route_from_logits_ms": round(t_p, 4), "logits_bytes_not_written": w.T * w.E * 4,
+            "timing": "eager, 20 calls; the tile is 128 tokens x 256 expert columns (E padded to 256)"}
+
+
+def capacity_leg(w, x, lg, layer, W1, W2, cf, dropless_ms):
+    """The capacity-based forward (the pages' contrast to dropless routing): each
+    expert keeps its first C = ceil(cf * T*k / E) tokens, is padded to C rows, and
+    the two grouped GEMMs run over all E*C rows; eager, 20 steps after 3 warm-ups."""
+    import torch
+    import ragged_grouped_gemm_topk_gb300 as pkg
+    if w.dtype not in ("bf16", "f32") or w.backward:
+        return {"unavailable": "capacity mode is built for the bf16 / fp32 forward"}
+    C = int(math.ceil(cf * w.M / w.E))
+    rows = w.E * C
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    bufs = {"offsets": torch.empty(w.E + 1, **i32), "dest_row": torch.empty(w.T, w.k, **i32),
+            "src_pair": torch.empty(max(rows, 1), **i32), "xp": torch.empty(max(rows, 1), w.d, dtype=x.dtype, device=dev)}
+    ws = torch.empty(max(int(pkg.binding._lib.load().moe_permute_capacity_workspace_size(w.T, w.k, w.E)), 16),
+                     dtype=torch.uint8, device=dev)
+    h = torch.empty(max(rows, 1), w.f, dtype=x.dtype, device=dev)
+    yp = torch.empty(max(rows, 1), w.d, dtype=x.dtype, device=dev)
+    y = torch.empty(w.T, w.d, dtype=x.dtype, device=dev)
+
+    def step():
+        layer.route(lg)
+        pkg.moe_permute_capacity(x, layer.topk_idx, layer.counts, w.E, C, workspace=ws,
+                                 dev_status=layer.dev_status, **bufs)
+        pkg.moe_grouped_gemm_fwd(bufs["xp"][:rows], W1, bufs["offsets"], epi="swiglu", out=h[:rows],
+                                 dev_status=layer.dev_status)
+        pkg.moe_grouped_gemm_fwd(h[:rows], W2, bufs["offsets"], out=yp[:rows], dev_status=layer.dev_status)
+        pkg.moe_unpermute_combine_capacity(yp[:rows], bufs["dest_row"], layer.topk_w, out=y,
+                                           dev_status=layer.dev_status)
+    t = _time_ms(step)
+    dropped = int((bufs["dest_row"] < 0).sum().item())
+    kept = w.M - dropped
+    return {"capacity_factor": cf, "capacity": C, "computed_rows": rows, "dropless_rows": w.M,
+            "dropped_frac": round(dropped / w.M, 4), "padding_frac": round((rows - kept) / max(rows, 1), 4),
+            "ms_per_step": round(t, 4), "dropless_ms_per_step": round(dropless_ms, 4),
+            "useful_tflops": round(w.fwd_flops * kept / w.M / (t * 1e-3) / 1e12, 1),
+            "timing": "eager, 20 steps (route, capacity dispatch, GEMM1 + SwiGLU, GEMM2, combine)"}
 
 
 def e2e(args, w, layer, x, lg_h, dy, world, flops):

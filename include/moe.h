@@ -104,6 +104,22 @@ moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int renorm
                             int32_t* topk_idx, float* topk_w, int32_t* counts,
                             int32_t* dev_status, cudaStream_t stream);
 
+/* Router GEMM fused with the top-k selection ([1] "Optimisation 2": the fused
+ * router kernel; [1] opening section: the router scores each token against every
+ * expert).  logits = x . W_r^T on the tensor cores, then, in the GEMM epilogue,
+ * the selection and weights of moe_route_topk on those fp32 logits (same rules:
+ * value descending, lower expert id first on ties, -inf masked, NaN flagged).
+ *   x         [T, d] in dtype (MOE_BF16, or MOE_F32 computed as TF32), 16-byte aligned.
+ *   w_router  [E, d] in dtype.
+ *   logits    [T, E] float32 out, or NULL (the logits then never reach memory;
+ *             the router backward with renormalize == 0 needs them).
+ *   topk_idx, topk_w, counts: as moe_route_topk (counts zeroed inside).
+ * Limits: d % 32 == 0, 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 0. */
+moe_status_t moe_route_topk_gemm(const void* x, const void* w_router, moe_dtype_t dtype, int T, int d,
+                                 int E, int k, int renormalize, float* logits, int32_t* topk_idx,
+                                 float* topk_w, int32_t* counts, int32_t* dev_status,
+                                 cudaStream_t stream);
+
 /* ---------------------------------------------------------------- dispatch --
  * Local dispatch: reorder the T*k (token, slot) pairs into expert-contiguous
  * rows ([1] "Optimisation 2": dispatch rearranges tokens locally; Figure 3).
@@ -293,6 +309,38 @@ moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype, int T, int
                                    const int32_t* dest_row, const float* topk_w,
                                    void* y, moe_dtype_t y_dtype, int32_t* dev_status,
                                    cudaStream_t stream);
+
+/* ---------------------------------------------------------------- capacity --
+ * Capacity-based dispatch, the contrast case of [1] (first section: a fixed
+ * per-expert capacity pads experts with fewer tokens and drops the tokens that
+ * overflow the busy ones; dropless routing needs neither).  Not on the dropless
+ * path: it exists to measure what padding and dropping cost.
+ *
+ * moe_permute_capacity: every expert e owns rows [e*C, (e+1)*C) of xp.  Its pairs,
+ * in the dropless order (token ascending), fill its first min(count_e, C) rows; the
+ * rest are zero; its pairs past the first C are dropped.
+ *   x         [T, d] MOE_BF16 or MOE_F32 (rows a multiple of 16 bytes).
+ *   topk_idx, counts: from moe_route_topk.
+ *   offsets   [E+1] int32 out: e*C (uniform groups for the grouped GEMM).
+ *   dest_row  [T, k] int32 out: the pair's row, or -1 when dropped.
+ *   src_pair  [E*C] int32 out: the pair in each row, or -1 for padding.
+ *   xp        [E*C, d] out, same dtype as x.
+ *   workspace moe_permute_capacity_workspace_size(T, k, E) bytes of device scratch.
+ * capacity C >= 0 (C = 0 drops everything).  Errors as moe_permute. */
+size_t moe_permute_capacity_workspace_size(int T, int k, int E);
+moe_status_t moe_permute_capacity(const void* x, moe_dtype_t x_dtype, int T, int d,
+                                  const int32_t* topk_idx, int k, int E, int capacity,
+                                  const int32_t* counts, int32_t* offsets, int32_t* dest_row,
+                                  int32_t* src_pair, void* xp, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
+/* Combine for the capacity layout: as moe_unpermute_combine, with yp [rows, d]
+ * (rows = E*C) and dest_row entries of -1 (dropped pairs) contributing nothing;
+ * any other index outside [0, rows) sets MOE_DEV_BAD_INDEX. */
+moe_status_t moe_unpermute_combine_capacity(const void* yp, moe_dtype_t dtype, int rows, int T, int d,
+                                            int k, const int32_t* dest_row, const float* topk_w,
+                                            void* y, moe_dtype_t y_dtype, int32_t* dev_status,
+                                            cudaStream_t stream);
 
 /* Backward of combine:
  *   dyp[dest_row[t, j]] = w[t, j] * dy[t]          (dyp [T*k, d] in dtype)

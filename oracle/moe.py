@@ -79,6 +79,13 @@ def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
     return idx, w, counts
 
 
+def router_logits(x: np.ndarray, w_router: np.ndarray) -> np.ndarray:
+    """Router scores ([1] opening paragraph: a learnable router scores each token
+    against every expert): logits[t, e] = <x[t], W_r[e]>, float64.  x [T,d],
+    W_r [E,d] -> [T,E]."""
+    return np.asarray(x, dtype=np.float64) @ np.asarray(w_router, dtype=np.float64).T
+
+
 # ----------------------------------------------------------------------------- dispatch
 
 def permute_maps(idx: np.ndarray, E: int):
@@ -192,6 +199,68 @@ def layer_forward(x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False):
     y = combine(Yp, dest_row, w)
     return dict(idx=idx, w=w, counts=counts, offsets=offsets, dest_row=dest_row,
                 src_pair=src_pair, Xp=Xp, GU=GU, H=H, Yp=Yp, y=y)
+
+
+# ----------------------------------------------------------------------------- capacity (contrast)
+
+def permute_capacity(idx: np.ndarray, E: int, C: int):
+    """Capacity-based dispatch, the contrast case of [1] (first section: a fixed
+    per-expert capacity pads experts that get fewer tokens and drops the tokens
+    that overflow).  Tokens are taken in order; each expert keeps its first C and
+    drops the rest.  Expert e owns rows [e*C, (e+1)*C).
+
+    Returns offsets [E+1] (= e*C), dest_row [T,k] (row, or -1 when dropped) and
+    src_pair [E*C] (the pair t*k+j in each row, or -1 for padding)."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    dest = np.full((T, k), -1, dtype=np.int64)
+    src = np.full(E * C, -1, dtype=np.int64)
+    filled = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if filled[e] < C:
+                row = e * C + filled[e]
+                dest[t, j] = row
+                src[row] = t * k + j
+            filled[e] += 1
+    return np.arange(E + 1, dtype=np.int64) * C, dest, src
+
+
+def permute_rows_capacity(x: np.ndarray, src_pair: np.ndarray, k: int) -> np.ndarray:
+    """Rows of the capacity layout: the token of each kept pair, zeros for padding."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros((len(src_pair), x.shape[1]))
+    kept = src_pair >= 0
+    out[kept] = x[src_pair[kept] // k]
+    return out
+
+
+def combine_capacity(Yp: np.ndarray, dest_row: np.ndarray, w) -> np.ndarray:
+    """y[t] = sum over the kept slots j of w[t,j] Yp[dest_row[t,j]]; dropped slots
+    (dest_row -1) add nothing."""
+    Yp = np.asarray(Yp, dtype=np.float64)
+    T, k = dest_row.shape
+    y = np.zeros((T, Yp.shape[1]))
+    for j in range(k):
+        kept = dest_row[:, j] >= 0
+        wj = np.ones(T) if w is None else np.asarray(w, dtype=np.float64)[:, j]
+        y[kept] += wj[kept, None] * Yp[dest_row[kept, j]]
+    return y
+
+
+def layer_forward_capacity(x, logits, W1, W2, k, C, renormalize=True):
+    """The layer with capacity-based dispatch: route, keep each expert's first C
+    tokens (zero-padded to C rows), the same SwiGLU experts over every row, combine
+    the kept slots."""
+    E = W1.shape[0]
+    idx, w, counts = route_topk(logits, k, renormalize)
+    offsets, dest_row, src_pair = permute_capacity(idx, E, C)
+    Xp = permute_rows_capacity(x, src_pair, k)
+    GU, H, Yp = expert_ffn(Xp, W1, W2, offsets)
+    y = combine_capacity(Yp, dest_row, w)
+    return dict(idx=idx, w=w, counts=counts, offsets=offsets, dest_row=dest_row, src_pair=src_pair,
+                Xp=Xp, Yp=Yp, y=y)
 
 
 # ----------------------------------------------------------------------------- backward

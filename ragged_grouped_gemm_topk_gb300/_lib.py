@@ -42,9 +42,13 @@ SIGNATURES = {
     "moe_grouped_gemm_fwd_mxfp8_out": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
     "moe_grouped_gemm_dgrad": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
     "moe_quantize_mxfp8_transposed": (st, [vp, i32, i32, i32, i32, vp, vp, vp]),
+    "moe_route_topk_gemm": (st, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_grouped_gemm_dgrad_mxfp8": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
     "moe_grouped_gemm_wgrad": (st, [OP, OP, vp, i32, i32, i32, i32, vp, i32, vp, vp]),
     "moe_unpermute_combine": (st, [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]),
+    "moe_permute_capacity_workspace_size": (sz, [i32, i32, i32]),
+    "moe_permute_capacity": (st, [vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
+    "moe_unpermute_combine_capacity": (st, [vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]),
     "moe_unpermute_combine_bwd": (st, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_route_topk_bwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
 }

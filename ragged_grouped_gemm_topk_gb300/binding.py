@@ -63,6 +63,25 @@ def moe_route_topk(logits, k, renormalize=True, *, topk_idx=None, topk_w=None, c
     return topk_idx, topk_w, counts
 
 
+def moe_route_topk_gemm(x, w_router, k, renormalize=True, *, logits=None, want_logits=False, topk_idx=None,
+                        topk_w=None, counts=None, dev_status=None):
+    """Router GEMM fused with top-k: x [T,d], w_router [E,d] (bf16 or fp32) ->
+    (topk_idx, topk_w, counts[, logits [T,E] fp32 when asked for])."""
+    T, d = x.shape
+    E, d2 = w_router.shape
+    if d2 != d:
+        raise ValueError("x and w_router disagree on d")
+    dev = x.device
+    topk_idx = topk_idx if topk_idx is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = counts if counts is not None else torch.empty(E, dtype=torch.int32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    _lib.call("moe_route_topk_gemm", _ptr(x), _ptr(w_router), _dt(x), T, d, E, k, int(bool(renormalize)),
+              _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(dev_status), _stream())
+    return (topk_idx, topk_w, counts, logits) if logits is not None else (topk_idx, topk_w, counts)
+
+
 def moe_permute_workspace_size(T, k, E) -> int:
     return int(_lib.load().moe_permute_workspace_size(T, k, E))
 
@@ -228,6 +247,38 @@ def moe_unpermute_combine(yp, dest_row, topk_w, *, out_dtype=None, out=None, dev
     if out is None:
         out = torch.empty(T, d, dtype=out_dtype or yp.dtype, device=yp.device)
     _lib.call("moe_unpermute_combine", _ptr(yp), _dt(yp), T, d, k, _ptr(dest_row), _ptr(topk_w),
+              _ptr(out), _dt(out), _ptr(dev_status), _stream())
+    return out
+
+
+def moe_permute_capacity(x, topk_idx, counts, E, capacity, *, offsets=None, dest_row=None, src_pair=None, xp=None,
+                         workspace=None, dev_status=None):
+    """Capacity-based dispatch (the contrast case): xp [E*C, d] with expert e's
+    first min(count_e, C) tokens in rows [e*C, e*C + ...), zero padding after them,
+    overflowing pairs dropped (dest_row -1).  Returns a dict like moe_permute."""
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    offsets = offsets if offsets is not None else torch.empty(E + 1, **i32)
+    dest_row = dest_row if dest_row is not None else torch.empty(T, k, **i32)
+    src_pair = src_pair if src_pair is not None else torch.empty(E * capacity, **i32)
+    xp = xp if xp is not None else torch.empty(E * capacity, d, dtype=x.dtype, device=dev)
+    nbytes = int(_lib.load().moe_permute_capacity_workspace_size(T, k, E))
+    workspace = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _lib.call("moe_permute_capacity", _ptr(x), _dt(x), T, d, _ptr(topk_idx), k, E, int(capacity), _ptr(counts),
+              _ptr(offsets), _ptr(dest_row), _ptr(src_pair), _ptr(xp), _ptr(workspace),
+              workspace.numel(), _ptr(dev_status), _stream())
+    return {"offsets": offsets, "dest_row": dest_row, "src_pair": src_pair, "xp": xp}
+
+
+def moe_unpermute_combine_capacity(yp, dest_row, topk_w, *, out_dtype=None, out=None, dev_status=None):
+    """Combine of the capacity layout: dropped pairs (dest_row -1) contribute nothing."""
+    T, k = dest_row.shape
+    rows, d = yp.shape
+    if out is None:
+        out = torch.empty(T, d, dtype=out_dtype or yp.dtype, device=yp.device)
+    _lib.call("moe_unpermute_combine_capacity", _ptr(yp), _dt(yp), rows, T, d, k, _ptr(dest_row), _ptr(topk_w),
               _ptr(out), _dt(out), _ptr(dev_status), _stream())
     return out
 

@@ -75,13 +75,12 @@ constexpr int kSliceChunks = 128;
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
-    const uint8_t* __restrict__ yp, int T, int d, int k, const int32_t* __restrict__ dest_row,
-    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int32_t* status) {
+    const uint8_t* __restrict__ yp, int M, int T, int d, int k, const int32_t* __restrict__ dest_row,
+    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int allow_drop, int32_t* status) {
   pdl_begin();
   constexpr int N = Elt<Tin>::kN;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const int M = T * k;
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
   const size_t out_row = static_cast<size_t>(d) * sizeof(Tout);
   const int n16 = static_cast<int>(in_row / 16);
@@ -97,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
       const size_t p = static_cast<size_t>(t) * k + lane;
       src = dest_row[p];
       w = topk_w ? topk_w[p] : 1.f;
-      if (src < 0 || src >= M) {
+      if ((src < 0 || src >= M) && !(src == -1 && allow_drop)) {   // -1: a dropped slot (capacity mode)
         if (slice == 0) flag_error(status, MOE_DEV_BAD_INDEX);
         src = -1;
       }
@@ -144,14 +143,13 @@ constexpr int kFixedSlice = 256;   // 16-byte chunks per work item
 
 template <typename Tin, typename Tout, int K>
 __global__ void __launch_bounds__(kThreads) combine_fixed_kernel(
-    const uint8_t* __restrict__ yp, int T, int d, const int32_t* __restrict__ dest_row,
-    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int32_t* status) {
+    const uint8_t* __restrict__ yp, int M, int T, int d, const int32_t* __restrict__ dest_row,
+    const float* __restrict__ topk_w, uint8_t* __restrict__ y, int allow_drop, int32_t* status) {
   pdl_begin();
   constexpr int N = Elt<Tin>::kN;
   constexpr int U = (16 / K) < 8 ? (16 / K) : 8;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const int M = T * K;
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
   const size_t out_row = static_cast<size_t>(d) * sizeof(Tout);
   const int n16 = static_cast<int>(in_row / 16);
@@ -167,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) combine_fixed_kernel(
       const size_t p = static_cast<size_t>(t) * K + lane;
       src = dest_row[p];
       w = topk_w ? topk_w[p] : 1.f;
-      if (src < 0 || src >= M) {
+      if ((src < 0 || src >= M) && !(src == -1 && allow_drop)) {   // -1: a dropped slot (capacity mode)
         if (slice == 0) flag_error(status, MOE_DEV_BAD_INDEX);
         src = -1;
       }
@@ -267,13 +265,13 @@ int grid_for(long long tasks, int sms) {
 }
 
 template <typename Tin, typename Tout>
-void launch_fixed(int k, int grid, cudaStream_t stream, const uint8_t* a, int T, int d, const int32_t* dest_row,
-                  const float* topk_w, uint8_t* o, int32_t* dev_status) {
+void launch_fixed(int k, int grid, cudaStream_t stream, const uint8_t* a, int M, int T, int d,
+                  const int32_t* dest_row, const float* topk_w, uint8_t* o, int drop, int32_t* dev_status) {
   switch (k) {
-    case 1: launch_pdl(combine_fixed_kernel<Tin, Tout, 1>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
-    case 2: launch_pdl(combine_fixed_kernel<Tin, Tout, 2>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
-    case 4: launch_pdl(combine_fixed_kernel<Tin, Tout, 4>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
-    default: launch_pdl(combine_fixed_kernel<Tin, Tout, 8>, grid, kThreads, 0, stream, a, T, d, dest_row, topk_w, o, dev_status); break;
+    case 1: launch_pdl(combine_fixed_kernel<Tin, Tout, 1>, grid, kThreads, 0, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status); break;
+    case 2: launch_pdl(combine_fixed_kernel<Tin, Tout, 2>, grid, kThreads, 0, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status); break;
+    case 4: launch_pdl(combine_fixed_kernel<Tin, Tout, 4>, grid, kThreads, 0, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status); break;
+    default: launch_pdl(combine_fixed_kernel<Tin, Tout, 8>, grid, kThreads, 0, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status); break;
   }
 }
 
@@ -282,21 +280,22 @@ void launch_fixed(int k, int grid, cudaStream_t stream, const uint8_t* a, int T,
 
 using namespace moe;
 
-extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype, int T, int d,
-                                              int k, const int32_t* dest_row,
-                                              const float* topk_w, void* y, moe_dtype_t y_dtype,
-                                              int32_t* dev_status, cudaStream_t stream) {
-  if (T < 0 || d < 0 || k < 1 || k > 32 || d % 8 ||
+namespace moe {
+namespace {
+moe_status_t combine_impl(const char* fn, const void* yp, moe_dtype_t dtype, int M, int T, int d, int k,
+                          const int32_t* dest_row, const float* topk_w, void* y, moe_dtype_t y_dtype,
+                          int drop, int32_t* dev_status, cudaStream_t stream) {
+  if (T < 0 || d < 0 || M < 0 || k < 1 || k > 32 || d % 8 ||
       (dtype != MOE_BF16 && dtype != MOE_F32) || (y_dtype != MOE_BF16 && y_dtype != MOE_F32)) {
-    set_error("moe_unpermute_combine: need T, d >= 0, d %% 8 == 0, 1 <= k <= 32, BF16/F32");
+    set_error("%s: need T, d, rows >= 0, d %% 8 == 0, 1 <= k <= 32, BF16/F32", fn);
     return MOE_ERR_INVALID_ARG;
   }
   if (static_cast<long long>(T) * k >= (1LL << 31)) {
-    set_error("moe_unpermute_combine: T*k must fit in int32");
+    set_error("%s: T*k must fit in int32", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (T > 0 && d > 0 && (!yp || !y || !dest_row || !aligned16(yp) || !aligned16(y))) {
-    set_error("moe_unpermute_combine: null or misaligned pointer");
+  if (T > 0 && d > 0 && (!y || !dest_row || !aligned16(yp) || !aligned16(y) || (M > 0 && !yp))) {
+    set_error("%s: null or misaligned pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
@@ -307,22 +306,44 @@ extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype,
   uint8_t* o = static_cast<uint8_t*>(y);
   if (k == 1 || k == 2 || k == 4 || k == 8) {
     const int grid = grid_for(static_cast<long long>(T) * ((n16 + kFixedSlice - 1) / kFixedSlice), sms);
-    if (dtype == MOE_BF16 && y_dtype == MOE_BF16) launch_fixed<uint16_t, uint16_t>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
-    else if (dtype == MOE_BF16) launch_fixed<uint16_t, float>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
-    else if (y_dtype == MOE_BF16) launch_fixed<float, uint16_t>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
-    else launch_fixed<float, float>(k, grid, stream, a, T, d, dest_row, topk_w, o, dev_status);
-    return check_launch("moe_unpermute_combine");
+    if (dtype == MOE_BF16 && y_dtype == MOE_BF16) launch_fixed<uint16_t, uint16_t>(k, grid, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status);
+    else if (dtype == MOE_BF16) launch_fixed<uint16_t, float>(k, grid, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status);
+    else if (y_dtype == MOE_BF16) launch_fixed<float, uint16_t>(k, grid, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status);
+    else launch_fixed<float, float>(k, grid, stream, a, M, T, d, dest_row, topk_w, o, drop, dev_status);
+    return check_launch(fn);
   }
   const int grid = grid_for(static_cast<long long>(T) * ((n16 + kSliceChunks - 1) / kSliceChunks), sms);
   if (dtype == MOE_BF16 && y_dtype == MOE_BF16)
-    launch_pdl(combine_kernel<uint16_t, uint16_t>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<uint16_t, uint16_t>, grid, kThreads, 0, stream, a, M, T, d, k, dest_row, topk_w, o, drop, dev_status);
   else if (dtype == MOE_BF16)
-    launch_pdl(combine_kernel<uint16_t, float>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<uint16_t, float>, grid, kThreads, 0, stream, a, M, T, d, k, dest_row, topk_w, o, drop, dev_status);
   else if (y_dtype == MOE_BF16)
-    launch_pdl(combine_kernel<float, uint16_t>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
+    launch_pdl(combine_kernel<float, uint16_t>, grid, kThreads, 0, stream, a, M, T, d, k, dest_row, topk_w, o, drop, dev_status);
   else
-    launch_pdl(combine_kernel<float, float>, grid, kThreads, 0, stream, a, T, d, k, dest_row, topk_w, o, dev_status);
-  return check_launch("moe_unpermute_combine");
+    launch_pdl(combine_kernel<float, float>, grid, kThreads, 0, stream, a, M, T, d, k, dest_row, topk_w, o, drop, dev_status);
+  return check_launch(fn);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype, int T, int d,
+                                              int k, const int32_t* dest_row,
+                                              const float* topk_w, void* y, moe_dtype_t y_dtype,
+                                              int32_t* dev_status, cudaStream_t stream) {
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("moe_unpermute_combine: T*k must fit in int32");
+    return MOE_ERR_INVALID_ARG;
+  }
+  return combine_impl("moe_unpermute_combine", yp, dtype, T > 0 && k > 0 ? T * k : 0, T, d, k, dest_row, topk_w,
+                      y, y_dtype, 0, dev_status, stream);
+}
+
+extern "C" moe_status_t moe_unpermute_combine_capacity(const void* yp, moe_dtype_t dtype, int rows, int T,
+                                                       int d, int k, const int32_t* dest_row,
+                                                       const float* topk_w, void* y, moe_dtype_t y_dtype,
+                                                       int32_t* dev_status, cudaStream_t stream) {
+  return combine_impl("moe_unpermute_combine_capacity", yp, dtype, rows, T, d, k, dest_row, topk_w, y, y_dtype,
+                      1, dev_status, stream);
 }
 
 extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp,

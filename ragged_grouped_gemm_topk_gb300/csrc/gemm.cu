@@ -79,7 +79,8 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 
 enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
-enum { kEpiNone = 0, kEpiSwiglu = 1, kEpiDswiglu = 2 };
+enum { kEpiNone = 0, kEpiSwiglu = 1, kEpiDswiglu = 2, kEpiTopk = 3 };
+constexpr int kTopkMax = 8;                       // router epilogue: experts per token
 
 // Instruction descriptor (kind::f16 / kind::tf32): D = f32 (bit 4), A/B format
 // (bits 7-9 / 10-12: 1 = bf16, 2 = tf32), A/B major (bits 15 / 16: 1 = MN-major),
@@ -178,7 +179,23 @@ struct Params {
   int32_t* status;
   const uint8_t* sfa;      // MXFP8 wgrad: tiled column-wise scales of dC (the MMA's A) ...
   const uint8_t* sfb;      // ... and of A (the MMA's B)
+  int32_t* topk_idx;       // router epilogue: [M, k] selected experts,
+  float* topk_w;           //   [M, k] their weights,
+  int32_t* counts;         //   [N] tokens per expert (zeroed by the host entry)
+  int k_sel;               //   experts per token (<= kTopkMax)
+  int renorm;              //   softmax over the selected logits (1) or over all (0)
 };
+
+// Rows of group e.  Without an offsets array the problem is one dense group of M rows.
+__device__ __forceinline__ void group_range(const Params& p, int e, int& beg, int& end) {
+  if (p.offsets == nullptr) {
+    beg = 0;
+    end = p.M;
+  } else {
+    beg = __ldg(p.offsets + e);
+    end = __ldg(p.offsets + e + 1);
+  }
+}
 
 struct Tile {
   int e;
@@ -241,7 +258,8 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
   }
   Tile t;
   t.e = lo;
-  const int beg = __ldg(p.offsets + lo), end = __ldg(p.offsets + lo + 1);
+  int beg, end;
+  group_range(p, lo, beg, end);
   const int cnt = group_ok(beg, end, M) ? end - beg : 0;
   if (kMode == kWgrad) {
     t.n0 = (local % g.nt) * kBM;
@@ -300,8 +318,10 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
     return;
   }
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    int cnt = offs[e + 1] - offs[e];
-    if (!group_ok(offs[e], offs[e + 1], p.M)) {
+    int beg, end;
+    group_range(p, e, beg, end);
+    int cnt = end - beg;
+    if (!group_ok(beg, end, p.M)) {
       if (blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
       cnt = 0;
     }
@@ -907,6 +927,104 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             store32<OutT>(out + grow * 2 * f + f + col, du);
           }
         }
+      } else if constexpr (kEpi == kEpiTopk) {
+        // Router: this thread's row holds the token's E = p.N logits (fp32, columns
+        // past E are zero and ignored).  One pass keeps the top kTopkMax in
+        // registers, sorted by value descending; a value enters only if strictly
+        // larger, so among equal logits the lower expert id (seen first) stays
+        // ahead.  The same pass keeps a running max and sum of exp for the full
+        // softmax.  NaN logits are flagged and treated as -inf.
+        const bool valid = r < t.rows;
+        const size_t grow = static_cast<size_t>(t.row0 + r);
+        const int E = p.N;
+        float tv[kTopkMax];
+        int ti[kTopkMax];
+#pragma unroll
+        for (int j = 0; j < kTopkMax; ++j) {
+          tv[j] = -INFINITY;
+          ti[j] = -1;
+        }
+        float run_m = -INFINITY, run_s = 0.f;
+        bool nan = false;
+        float* lout = static_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < (E + 31) / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float lg[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) lg[i] = __uint_as_float(v[i]);
+            const int col = c * 32;
+            if (lout != nullptr) {
+              if (col + 32 <= E && E % 4 == 0) {
+                float4* d4 = reinterpret_cast<float4*>(lout + grow * E + col);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) d4[q4] = make_float4(lg[4 * q4], lg[4 * q4 + 1], lg[4 * q4 + 2], lg[4 * q4 + 3]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col + i < E) lout[grow * E + col + i] = lg[i];
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (col + i >= E) break;
+              float x = lg[i];
+              if (isnan(x)) {
+                nan = true;
+                x = -INFINITY;
+              }
+              if (x == -INFINITY) {
+                // masked expert: no softmax mass
+              } else if (x > run_m) {
+                run_s = run_s * expf(run_m - x) + 1.f;
+                run_m = x;
+              } else {
+                run_s += expf(x - run_m);
+              }
+              if (x > tv[kTopkMax - 1] || ti[kTopkMax - 1] < 0) {
+                // insert (x, col + i) keeping the list sorted; strict compares keep
+                // earlier (lower-id) equal values ahead
+#pragma unroll
+                for (int j = kTopkMax - 1; j > 0; --j) {
+                  const bool up = x > tv[j - 1] || ti[j - 1] < 0;
+                  const bool here = x > tv[j] || ti[j] < 0;
+                  tv[j] = up ? tv[j - 1] : (here ? x : tv[j]);
+                  ti[j] = up ? ti[j - 1] : (here ? col + i : ti[j]);
+                }
+                if (x > tv[0] || ti[0] < 0) {
+                  tv[0] = x;
+                  ti[0] = col + i;
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+        released = true;
+        if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_error(p.status, MOE_DEV_NAN_LOGIT);
+        const int ksel = p.k_sel;
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < kTopkMax; ++j)
+          if (j < ksel) den += expf(tv[j] - tv[0]);
+#pragma unroll
+        for (int j = 0; j < kTopkMax; ++j) {
+          if (j < ksel) {
+            if (valid) {
+              const float w = p.renorm ? expf(tv[j] - tv[0]) / den : expf(tv[j] - run_m) / run_s;
+              p.topk_idx[grow * ksel + j] = ti[j];
+              p.topk_w[grow * ksel + j] = w;
+            }
+            // one atomic per distinct expert in the warp
+            const int id = valid ? ti[j] : -1;
+            const uint32_t same = __match_any_sync(0xFFFFFFFFu, id);
+            if (id >= 0 && lane == __ffs(same) - 1) atomicAdd(&p.counts[id], __popc(same));
+          }
+        }
       } else {
         const bool valid = r < t.rows;
         const size_t grow = static_cast<size_t>(t.row0 + r);
@@ -1295,6 +1413,48 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, co
   Params p{offsets, M, K, N, E, dA, nullptr, preact, nullptr, dev_status};
   if (epi == MOE_EPI_DSWIGLU) return launch<2, kFwd, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
   return launch<2, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
+}
+
+extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router, moe_dtype_t dtype, int T,
+                                            int d, int E, int k, int renormalize, float* logits,
+                                            int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                            int32_t* dev_status, cudaStream_t stream) {
+  // logits = x . W_r^T on the tensor cores, top-k selection and softmax weights in
+  // the GEMM epilogue: the logits need not make a round trip through memory.
+  const char* fn = "moe_route_topk_gemm";
+  if (T < 0 || d <= 0 || d % 32 || E < 1 || E > kBN || k < 1 || k > E || k > kTopkMax ||
+      (dtype != MOE_BF16 && dtype != MOE_F32)) {
+    set_error("%s: need T >= 0, d %% 32 == 0, 1 <= E <= %d, 1 <= k <= min(E, %d), BF16 or F32 (T=%d d=%d E=%d k=%d)",
+              fn, kBN, kTopkMax, T, d, E, k);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!counts || (T > 0 && (!x || !w_router || !topk_idx || !topk_w)) || !aligned16(x) || !aligned16(w_router) ||
+      !aligned16(logits)) {
+    set_error("%s: null or misaligned pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * sizeof(int32_t), stream);
+  if (e != cudaSuccess) {
+    set_error("%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  if (T == 0) return MOE_OK;
+  const int eb = elem_bytes(dtype);
+  const uint32_t bk = kBKBytes / eb;
+  CUtensorMap ta, tb;
+  const uint64_t adims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(T)};
+  const uint32_t abox[2] = {bk, kBM};
+  const uint64_t bdims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(E), 1};
+  const uint32_t bbox[3] = {bk, kBN, 1};           // rows past E read as zeros
+  if (!make_map(&ta, map_type(dtype), eb, x, 2, adims, abox) ||
+      !make_map(&tb, map_type(dtype), eb, w_router, 3, bdims, bbox))
+    return MOE_ERR_INVALID_ARG;
+  Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr,
+           topk_idx, topk_w, counts, k, renormalize ? 1 : 0};
+  if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
+  return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,

@@ -31,8 +31,17 @@ class MoELayer:
     layout.  Activations and gradients are kept in bf16 between the GEMMs.
     """
 
-    def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False):
+    def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False,
+                 w_router=None, keep_logits=False):
+        """``w_router`` [E, d] (bf16, or fp32 for the fp32 layer) makes the layer score
+        the tokens itself: ``forward(x)`` then runs the router GEMM fused with the
+        top-k selection instead of taking logits.  With ``keep_logits`` (or when
+        training without renormalisation, whose router backward needs them) the
+        fused router also writes its fp32 logits to ``self.logits``."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
+        self.w_router = w_router
+        keep = w_router is not None and (keep_logits or (training and not renormalize))
+        self.logits = torch.empty(T, E, dtype=torch.float32, device=W1.device) if keep else None
         self.dtype, self.renormalize, self.training = dtype, renormalize, training
         dev = W1.device
         self.device = dev
@@ -95,9 +104,16 @@ class MoELayer:
             self.dW2 = torch.empty_like(W2)
 
     # ------------------------------------------------------------------ forward
-    def route(self, logits):
-        B.moe_route_topk(logits, self.k, self.renormalize, topk_idx=self.topk_idx,
-                         topk_w=self.topk_w, counts=self.counts, dev_status=self.dev_status)
+    def route(self, logits, x=None):
+        if logits is None:
+            if self.w_router is None:
+                raise ValueError("no logits and no router weights")
+            B.moe_route_topk_gemm(x, self.w_router, self.k, self.renormalize, logits=self.logits,
+                                  topk_idx=self.topk_idx, topk_w=self.topk_w, counts=self.counts,
+                                  dev_status=self.dev_status)
+        else:
+            B.moe_route_topk(logits, self.k, self.renormalize, topk_idx=self.topk_idx,
+                             topk_w=self.topk_w, counts=self.counts, dev_status=self.dev_status)
 
     def dispatch(self, x):
         if self.dtype == "mxfp8" and self.training:
@@ -142,9 +158,10 @@ class MoELayer:
                                 dev_status=self.dev_status)
         return y
 
-    def forward(self, x, logits, out=None):
-        """y [T, d] (written to ``out`` when given, else to the layer's own buffer)."""
-        self.route(logits)
+    def forward(self, x, logits=None, out=None):
+        """y [T, d] (written to ``out`` when given, else to the layer's own buffer).
+        Without ``logits`` the layer's router weights score the tokens."""
+        self.route(logits, x)
         self.dispatch(x)
         self.expert_mlp()
         return self.combine(out)
@@ -153,7 +170,8 @@ class MoELayer:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
         scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
         MXFP8 training adds the row- and column-wise quantisation of Xp and of H."""
-        return 2 + 2 + 2 + 1 + (4 if self.dtype == "mxfp8" and self.training else 0)
+        route = 1 if self.w_router is not None else 2     # fused router GEMM (counts zeroed by a memset)
+        return route + 2 + 2 + 1 + (4 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd;
@@ -191,6 +209,8 @@ class MoELayer:
             B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
         dx = self.dx if dx_out is None else dx_out
         B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=dx, dev_status=st)
+        if logits is None:
+            logits = self.logits          # the fused router's own (None is fine when renormalised)
         B.moe_route_topk_bwd(self.dw, self.topk_w, self.topk_idx, self.E, logits=logits,
                              renormalize=self.renormalize, out=self.dlogits, dev_status=st)
         return dx, self.dlogits, self.dW1, self.dW2

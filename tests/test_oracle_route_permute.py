@@ -154,3 +154,57 @@ def test_combine_of_permute_is_identity(k):
     assert (moe.combine(xp, dest, w) == x).all()
     if k == 1:
         assert (moe.combine(xp, dest, None) == x).all()
+
+
+def test_router_logits_bruteforce_and_one_hot():
+    """logits[t, e] = sum_i x[t, i] W_r[e, i]: a triple loop on a tiny case, and a
+    one-hot token reads out one column of W_r (a transposed W_r would read a row)."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((5, 7))
+    Wr = rng.standard_normal((3, 7))
+    got = moe.router_logits(x, Wr)
+    for t in range(5):
+        for e in range(3):
+            assert abs(got[t, e] - sum(x[t, i] * Wr[e, i] for i in range(7))) < 1e-12
+    onehot = np.zeros((1, 7))
+    onehot[0, 4] = 1.0
+    assert np.array_equal(moe.router_logits(onehot, Wr)[0], Wr[:, 4])
+
+
+def test_capacity_keeps_first_tokens_and_drops_the_rest():
+    """Each expert keeps exactly min(count, C) pairs, those of its C lowest token
+    ids (checked against a sort of the routed tokens), at rows e*C.. in token
+    order; the other pairs are dropped; every row is used at most once."""
+    rng = np.random.default_rng(41)
+    T, E, k, C = 60, 6, 2, 7
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[:, 1] += 3.0                                          # an overloaded expert
+    idx, _, counts = moe.route_topk(lg, k)
+    offsets, dest, src = moe.permute_capacity(idx, E, C)
+    assert np.array_equal(offsets, np.arange(E + 1) * C)
+    for e in range(E):
+        toks = sorted(t for t in range(T) for j in range(k) if idx[t, j] == e)
+        keep = toks[:C]
+        rows = [dest[t, j] for t in range(T) for j in range(k) if idx[t, j] == e and dest[t, j] >= 0]
+        assert len(rows) == min(counts[e], C)
+        assert sorted(rows) == list(range(e * C, e * C + len(keep)))
+        assert [src[r] // k for r in range(e * C, e * C + len(keep))] == keep
+        assert (src[e * C + len(keep):(e + 1) * C] == -1).all()
+    assert counts[1] > C and (dest == -1).sum() == sum(max(int(c) - C, 0) for c in counts)
+
+
+def test_capacity_large_enough_is_dropless_and_zero_drops_everything():
+    """C >= the largest count: nothing is dropped and combine(permute(x)) = x for
+    k=1; C = 0: every pair is dropped and the combine is zero."""
+    rng = np.random.default_rng(42)
+    T, E = 50, 5
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    idx, w, counts = moe.route_topk(lg, 1)
+    x = rng.standard_normal((T, 8))
+    C = int(counts.max())
+    _, dest, src = moe.permute_capacity(idx, E, C)
+    assert (dest >= 0).all()
+    np.testing.assert_array_equal(moe.combine_capacity(moe.permute_rows_capacity(x, src, 1), dest, w), x)
+    _, dest0, src0 = moe.permute_capacity(idx, E, 0)
+    assert (dest0 == -1).all() and len(src0) == 0
+    assert (moe.combine_capacity(np.zeros((0, 8)), dest0, w) == 0).all()
