@@ -117,3 +117,37 @@ def test_mxfp8_backward_pins_catch_planted_mistake(monkeypatch, target, attr, fa
     monkeypatch.setattr(target, attr, fake)
     with pytest.raises(AssertionError):
         check()
+
+
+from oracle import nvfp4  # noqa: E402
+import test_oracle_nvfp4 as fp4_pins  # noqa: E402
+
+_real_e2m1 = nvfp4.e2m1_encode
+
+
+def _e2m1_ties_away(y):
+    y = np.asarray(y, dtype=np.float64)
+    mag = np.abs(y)
+    code = np.argmin(np.abs(mag[..., None] - nvfp4.E2M1_POS[::-1]), axis=-1)
+    code = (7 - code).astype(np.uint8)                        # on a tie the larger magnitude wins
+    code = np.where(mag >= 6, 7, code)
+    return (code | np.where(np.signbit(y), 0x8, 0)).astype(np.uint8)
+
+
+def _quantize_swapped_nibbles(a, g=None):
+    c, s, gg = _real_quantize(a, g)
+    return ((c >> 4) | (c << 4)).astype(np.uint8), s, gg
+
+
+_real_quantize = nvfp4.quantize
+
+
+@pytest.mark.parametrize("attr,fake,check", [
+    ("e2m1_encode", _e2m1_ties_away, lambda: fp4_pins.test_e2m1_midpoints_round_to_even_and_saturate()),
+    ("quantize", _quantize_swapped_nibbles, lambda: fp4_pins.test_golden_blocks()),
+    ("TENSOR_NUM", np.float32(448.0), lambda: fp4_pins.test_golden_blocks()),
+], ids=["e2m1-ties-away", "nibbles-swapped", "tensor-scale-448"])
+def test_nvfp4_pins_catch_planted_mistake(monkeypatch, attr, fake, check):
+    monkeypatch.setattr(nvfp4, attr, fake)
+    with pytest.raises(AssertionError):
+        check()
