@@ -50,7 +50,9 @@ typedef enum {
 typedef enum {
   MOE_F32 = 0,  /* float32 storage (GEMMs run on the tensor cores as TF32) */
   MOE_BF16 = 1, /* bfloat16 */
-  MOE_E4M3 = 2  /* MXFP8: FP8 E4M3 codes plus one E8M0 scale byte per 32 elements */
+  MOE_E4M3 = 2, /* MXFP8: FP8 E4M3 codes plus one E8M0 scale byte per 32 elements */
+  MOE_E2M1 = 3  /* NVFP4: E2M1 codes two per byte, one E4M3 scale byte per 16 elements
+                   and one fp32 tensor scale (moe_quantize_nvfp4) */
 } moe_dtype_t;
 
 typedef enum {
@@ -66,12 +68,15 @@ typedef enum {
 #define MOE_DEV_TIMEOUT 4   /* a bounded pipeline wait gave up; outputs are garbage */
 
 /* One GEMM operand.  For MOE_E4M3, `scales` points at the E8M0 bytes, one per 32
- * consecutive elements along the contraction dimension ([rows, K/32] row-major);
- * it is ignored (may be NULL) for the other dtypes. */
+ * consecutive elements along the contraction dimension ([rows, K/32] row-major).
+ * For MOE_E2M1, `ptr` holds the packed codes [rows, K/2], `scales` the E4M3 bytes
+ * [rows, K/16] and `tensor_scale` the fp32 encode scale g of the tensor (as written
+ * by moe_quantize_nvfp4).  Both are ignored (may be NULL) for the other dtypes. */
 typedef struct {
   const void* ptr;
   moe_dtype_t dtype;
   const uint8_t* scales;
+  const float* tensor_scale;
 } moe_operand_t;
 
 int moe_version(void);                    /* (major << 16) | (minor << 8) | patch */
@@ -217,6 +222,21 @@ moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, in
 moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype, int G, int R, int C,
                                            uint8_t* codes, uint8_t* scales, cudaStream_t stream);
 
+/* NVFP4 quantisation ([3] contribution 3 names NVFP4 as the Blackwell FP4 recipe;
+ * the encoding follows NVIDIA's published NVFP4 format): E2M1 elements, one E4M3
+ * scale per 16 consecutive elements of a row, one fp32 scale for the tensor.  All
+ * rounding that decides a code is fp32, in this order: g = 2688 / amax(tensor)
+ * (1 for an all-zero tensor); s = E4M3_rn_sat((amax_block / 6) * g); code =
+ * E2M1_rn_sat(v * (g / s)) (v * 0 when s decodes to 0); decoded v = e2m1 * s / g.
+ *   in      [rows, K] MOE_BF16 or MOE_F32, 16-byte aligned; K % 16 == 0.
+ *   codes   [rows, K/2] uint8 out, two codes per byte (element 2i in the low
+ *           nibble), 8-byte aligned.
+ *   scales  [rows, K/16] uint8 out (E4M3, sign bit clear).
+ *   tensor_scale  float[2] device: [0] receives g; [1] is scratch for the amax.
+ * A weight stack [E, N, K] is one tensor (rows = E*N): one g for all experts. */
+moe_status_t moe_quantize_nvfp4(const void* in, moe_dtype_t in_dtype, int rows, int K, uint8_t* codes,
+                                uint8_t* scales, float* tensor_scale, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- grouped GEMM
  * Ragged grouped GEMM ([1] "Optimisation 1": one kernel launch covers every
  * expert and computes only the valid token rows of each; the per-expert sizes
@@ -232,7 +252,9 @@ moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype,
  *     preact != NULL the pre-activations [M, 2f] (gate | up) are stored too, in
  *     c_dtype, for the backward.
  * dtypes: F32 x F32 (TF32 tensor cores), BF16 x BF16, E4M3 x E4M3 (MXFP8 with
- *   E8M0 scales per 32 along K; both scale pointers required).
+ *   E8M0 scales per 32 along K; both scale pointers required), E2M1 x E2M1
+ *   (NVFP4: E4M3 scales per 16 along K and the two tensor scales; the product is
+ *   multiplied by 1 / (g_A * g_B) before the epilogue; K % 256 == 0).
  * Limits: K % 32 == 0, N % 32 == 0 (SWIGLU: f % 32 == 0), E <= 1024,
  *   16-byte aligned pointers, M < 2^31.
  */

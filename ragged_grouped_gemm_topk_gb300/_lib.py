@@ -12,7 +12,7 @@ import os
 from . import build as _build
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = range(5)
-MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1 = 0, 1, 2, 3
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_DSWIGLU = 0, 1, 2
 MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_INDEX, MOE_DEV_TIMEOUT = 1, 2, 4
 
@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 
 class Operand(C.Structure):
-    _fields_ = [("ptr", C.c_void_p), ("dtype", C.c_int), ("scales", C.c_void_p)]
+    _fields_ = [("ptr", C.c_void_p), ("dtype", C.c_int), ("scales", C.c_void_p), ("tensor_scale", C.c_void_p)]
 
 
 vp, i32, sz, st = C.c_void_p, C.c_int, C.c_size_t, C.c_int
@@ -43,6 +43,7 @@ SIGNATURES = {
     "moe_grouped_gemm_dgrad": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
     "moe_quantize_mxfp8_transposed": (st, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "moe_route_topk_gemm": (st, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
+    "moe_quantize_nvfp4": (st, [vp, i32, i32, i32, vp, vp, vp, vp]),
     "moe_grouped_gemm_dgrad_mxfp8": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
     "moe_grouped_gemm_wgrad": (st, [OP, OP, vp, i32, i32, i32, i32, vp, i32, vp, vp]),
     "moe_unpermute_combine": (st, [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]),

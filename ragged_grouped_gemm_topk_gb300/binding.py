@@ -42,8 +42,12 @@ def _dt(t):
         raise ValueError(f"unsupported dtype {t.dtype}") from None
 
 
-def _operand(t, scales=None):
-    return _lib.Operand(t.data_ptr(), _dt(t), scales.data_ptr() if scales is not None else None)
+def _operand(t, scales=None, tensor_scale=None):
+    """A GEMM operand; uint8 codes are MXFP8 (E4M3), or NVFP4 (packed E2M1) when a
+    tensor scale is given."""
+    dt = _lib.MOE_E2M1 if tensor_scale is not None else _dt(t)
+    return _lib.Operand(t.data_ptr(), dt, scales.data_ptr() if scales is not None else None,
+                        tensor_scale.data_ptr() if tensor_scale is not None else None)
 
 
 def version() -> int:
@@ -151,12 +155,30 @@ def moe_quantize_mxfp8_transposed(inp, *, codes=None, scales=None):
     return codes, scales
 
 
+def moe_quantize_nvfp4(inp, *, codes=None, scales=None, tensor_scale=None):
+    """NVFP4 of inp [rows, K] (bf16/fp32; a weight stack [E, N, K] as one tensor) ->
+    (codes u8 [.., K/2] packed, scales u8 [.., K/16] E4M3, tensor_scale fp32 [2] with
+    the encode scale g in element 0)."""
+    K = inp.shape[-1]
+    lead = inp.shape[:-1]
+    rows = inp.numel() // K if K else 0
+    codes = codes if codes is not None else torch.empty(*lead, K // 2, dtype=torch.uint8, device=inp.device)
+    scales = scales if scales is not None else torch.empty(*lead, K // 16, dtype=torch.uint8, device=inp.device)
+    tensor_scale = tensor_scale if tensor_scale is not None else torch.empty(2, dtype=torch.float32, device=inp.device)
+    _lib.call("moe_quantize_nvfp4", _ptr(inp), _dt(inp), rows, K, _ptr(codes), _ptr(scales), _ptr(tensor_scale),
+              _stream())
+    return codes, scales, tensor_scale
+
+
 def moe_grouped_gemm_fwd(A, B, offsets, *, epi="none", A_scales=None, B_scales=None,
                          out_dtype=torch.bfloat16, out=None, preact=None, want_preact=False,
-                         dev_status=None):
-    """C = ragged A [M,K] . B[e]^T with B [E,N,K]; epi "swiglu" gives [M, N/2]."""
+                         dev_status=None, A_tensor_scale=None, B_tensor_scale=None):
+    """C = ragged A [M,K] . B[e]^T with B [E,N,K]; epi "swiglu" gives [M, N/2].
+    NVFP4 (tensor scales given): A and B are packed codes [M, K/2] and [E, N, K/2]."""
     M, K = A.shape
     E, N, K2 = B.shape
+    if A_tensor_scale is not None:
+        K, K2 = 2 * K, 2 * K2
     if K2 != K:
         raise ValueError("A and B disagree on K")
     n_out = N // 2 if epi == "swiglu" else N
@@ -164,7 +186,7 @@ def moe_grouped_gemm_fwd(A, B, offsets, *, epi="none", A_scales=None, B_scales=N
         out = torch.empty(M, n_out, dtype=out_dtype, device=A.device)
     if want_preact and preact is None:
         preact = torch.empty(M, N, dtype=out.dtype, device=A.device)
-    a, b = _operand(A, A_scales), _operand(B, B_scales)
+    a, b = _operand(A, A_scales, A_tensor_scale), _operand(B, B_scales, B_tensor_scale)
     _lib.call("moe_grouped_gemm_fwd", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E, _EPI[epi],
               _ptr(out), _dt(out), _ptr(preact), _ptr(dev_status), _stream())
     return (out, preact) if want_preact or preact is not None else out

@@ -59,6 +59,30 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Eight floats -> eight E2M1 codes packed in 32 bits (element i in bits 4i..4i+3),
+// round-to-nearest-even with saturation to +-6.  The cvt puts its first source in
+// the high nibble.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Value of a non-negative E4M3 byte (sign bit clear, not NaN) from its bit fields:
+// exponent field 0 -> man * 2^-9, else (8 + man) * 2^(exp - 10).  Exact.
+__device__ __forceinline__ float ue4m3_value(uint32_t code) {
+  const uint32_t exp = (code >> 3) & 0xFu, man = code & 0x7u;
+  if (exp == 0) return static_cast<float>(man) * 0.001953125f;
+  return __uint_as_float(((exp + 120u) << 23) | (man << 20));
+}
+
 // MXFP8 shared-exponent rule (OCP Microscaling Formats v1.0): X = floor(log2 amax)
 // - 8 (8 = E4M3's largest exponent), clamped at -127, stored as the E8M0 byte
 // X + 127; an all-zero block gets byte 127.  Returns the byte and the exact power
@@ -322,6 +346,19 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uin
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// NVFP4 block-scaled MMA: E2M1 operands (K = 64 per instruction), four E4M3 scale
+// bytes per row per instruction (one per 16 elements).
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
       "[%5], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

@@ -68,7 +68,12 @@ constexpr int kEpiOff = 0;
 // staging boxes per epilogue warp (rotating: a box is staged while the previous
 // ones are still being read by their TMA stores) and raw scale-row slots (MXFP8)
 template <int kKind>
-constexpr int epi_bufs() { return kKind == 2 ? 1 : 2; }
+constexpr int epi_bufs() { return kKind == 2 ? 1 : (kKind == 3 ? 0 : 2); }
+// NVFP4 (kind 3): each stage's raw E4M3 scale rows (A 128 x 16 B, B 256 x 16 B) land
+// next to the stage and are re-laid in place into its twelve 512-byte atoms (A: one
+// per 64-element MMA; B: two per MMA, rows 0-127 and 128-255).  No staging boxes:
+// the epilogue stores directly, so the four 48 KB stages still fit.
+constexpr int kNvAtomBytes = 6144;
 template <int kKind>
 constexpr int raw_slots() { return 2; }
 template <int kKind>
@@ -113,7 +118,7 @@ struct Smem {
 // are copied to TMEM scale slots (see Tl for the TMEM layout).
 template <int kKind>
 struct Cfg {
-  static constexpr bool kMx = kKind == 2;
+  static constexpr bool kMx = kKind >= 2;     // block-scaled (2 = MXFP8, 3 = NVFP4)
   static constexpr int kStage = kStageBytes;
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
@@ -135,11 +140,12 @@ constexpr int kMxWgRows = 128;                    // MXFP8 wgrad: contraction ro
 template <int kKind, int kMode>
 constexpr int stages_for() { return kStages; }
 template <int kKind, int kMode>
-constexpr int threads_for() { return (kKind == 2 || kMode == kWgrad) ? 224 : 192; }
+constexpr int threads_for() { return (kKind >= 2 || kMode == kWgrad) ? 224 : 192; }
 template <int kKind, int kMode>
 constexpr size_t extra_smem() {
   return kMode == kWgrad ? wg_atom_off<kKind>() + (kKind == 2 ? kStages * kAtomBytes : 0)
-                        : (kMode == kFwd ? (kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
+                        : (kMode == kFwd ? (kKind == 3 ? kStages * kNvAtomBytes
+                                                       : kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
                                                        : atom_off<kKind>())
                                          : 0);
 }
@@ -169,6 +175,13 @@ __host__ __device__ constexpr uint32_t make_idesc_mx(int m, int n) {
   return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Block-scaled instruction descriptor (kind::mxf4nvf4): E2M1 A and B (format 1),
+// K-major, N >> 3 at bit 17, E4M3 scales (bit 23 clear), M >> 4 at bit 24; with
+// 16-element blocks each MMA (K = 64) reads four scale bytes per row, so no scale ids.
+__host__ __device__ constexpr uint32_t make_idesc_nvf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 struct Params {
   const int32_t* offsets;
   int M, N, K, E;
@@ -179,6 +192,8 @@ struct Params {
   int32_t* status;
   const uint8_t* sfa;      // MXFP8 wgrad: tiled column-wise scales of dC (the MMA's A) ...
   const uint8_t* sfb;      // ... and of A (the MMA's B)
+  const float* ts_a;       // NVFP4: tensor encode scales of A and B (the product is
+  const float* ts_b;       //   multiplied by 1 / (g_A * g_B))
   int32_t* topk_idx;       // router epilogue: [M, k] selected experts,
   float* topk_w;           //   [M, k] their weights,
   int32_t* counts;         //   [N] tokens per expert (zeroed by the host entry)
@@ -354,6 +369,15 @@ __device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p)
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
 
+// NVFP4: scale 32 accumulator words by alpha (a no-op for the other kinds).
+template <int kKind>
+__device__ __forceinline__ void nv_scale(uint32_t (&v)[32], float alpha) {
+  if constexpr (kKind == 3) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+  }
+}
+
 // Store 32 consecutive fp32 values as OutT (16-byte stores).
 template <typename OutT>
 __device__ __forceinline__ void store32(OutT* dst, const float (&v)[32]) {
@@ -407,12 +431,14 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
                                                int n_out) {
   constexpr int kElemBytes = kEpiRowBytes / kBoxElems;
   const size_t row_bytes = static_cast<size_t>(n_out) * kElemBytes;
-  if (rows_valid >= 32) {
+  if constexpr (kBufs == 0) {
+    // no staging boxes (NVFP4): every row is stored directly below
+  } else if (rows_valid >= 32) {
 #pragma unroll
     for (int c = 0; c < kWords / 16; ++c) {
       if (col0 + c * kBoxElems >= n_out) break;
-      uint8_t* buf = stg + (c % kBufs) * kEpiBox;
-      if (lane == 0) bulk_wait_read<kBufs - 1>();   // the box that last used buf has been read
+      uint8_t* buf = stg + (c % (kBufs > 0 ? kBufs : 1)) * kEpiBox;
+      if (lane == 0) bulk_wait_read<(kBufs > 0 ? kBufs - 1 : 0)>();   // the box that last used buf has been read
       __syncwarp();
       const int sw = (lane >> 1) & 3;
 #pragma unroll
@@ -428,7 +454,8 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
         bulk_commit();
       }
     }
-  } else if (lane < rows_valid) {
+  }
+  if ((kBufs == 0 || rows_valid < 32) && lane < rows_valid) {
 #pragma unroll
     for (int c = 0; c < kWords / 16; ++c) {
       const int col = col0 + c * kBoxElems;
@@ -504,7 +531,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
         const Tile t = tile_info(s, g, tile, p);
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (C::kMx && kMode == kFwd && kb % 4 == 0) {
+          if (kKind == 2 && kMode == kFwd && kb % 4 == 0) {
             // raw E8M0 rows, 16 bytes per row = the scales of 4 K-blocks, into slot ss
             if (!mbar_wait(&s.sempty[ss], ss_phase ^ 1u, p.status, &s.abort)) break;
             uint8_t* rsa = tiles + NS * C::kStage + raw_off<kKind>() + ss * kSfSlot;
@@ -526,7 +553,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           uint8_t* sa = tiles + stage * C::kStage;
           uint8_t* sb = sa + kAStage;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, kStageBytes + (C::kMx && kMode == kWgrad ? kAtomBytes : 0));
+          mbar_arrive_expect_tx(bar, kStageBytes + (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
+                                         (kKind == 3 ? kNvAtomBytes : 0));
           if (kMode == kFwd) {
             const int kx = kb * (kBKBytes / eb);
             tma_load_2d(sa, &tmA, bar, kx, t.row0);
@@ -535,6 +563,14 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
               tma_load_3d(sb + kBStage / 2, &tmB, bar, kx, g.n_out + t.col0, t.e);
             } else {
               tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
+            }
+            if constexpr (kKind == 3) {
+              // raw scale rows of this stage: 16 bytes (= 256 elements) per row
+              uint8_t* at = tiles + NS * C::kStage + stage * kNvAtomBytes;
+              const int brow = t.e * p.N;
+              tma_load_2d(at, &tmSA, bar, 16 * kb, t.row0);
+              tma_load_2d(at + 2048, &tmSB, bar, 16 * kb, brow + t.col0);
+              tma_load_2d(at + 4096, &tmSB, bar, 16 * kb, brow + (kEpi == kEpiSwiglu ? g.n_out : kBM) + t.col0);
             }
           } else if (kMode == kDgrad) {
             const int nx = kb * kMnRows;                  // contraction index (N of B)
@@ -565,7 +601,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = C::kMx ? make_idesc_mx(kBM, BN) | (kMode == kWgrad ? (3u << 15) : 0u)
+    constexpr uint32_t idesc = kKind == 3 ? make_idesc_nvf4(kBM, BN)
+                               : C::kMx ? make_idesc_mx(kBM, BN) | (kMode == kWgrad ? (3u << 15) : 0u)
                                       : make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -606,6 +643,35 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
               const uint64_t bd = make_sdesc(sb + kk * 4096, kBStage / 2, 1024, 2);
               const uint32_t id = idesc | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4);
               tc_mma_mxf8(d_tmem, ad, bd, id, slot, slot + TL::kSfB, (kb | kk) != 0 ? 1u : 0u);
+            }
+            tc_commit(&s.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == NS) { stage = 0; phase ^= 1u; }
+          continue;
+        }
+        if (kKind == 3) {
+          // NVFP4: wait for the atoms (the scale warp saw the stage land), then per
+          // MMA kk copy its atoms into a 32-column region (A at +0, B rows 0-127 at
+          // +16, rows 128-255 at +20: the alignments of the MXFP8 slots) and issue the
+          // K=64 MMA.  Two region sets alternate by stage: a copy is issued after the
+          // MMAs that read the set before, by the same thread, and runs after them.
+          if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(tiles + stage * C::kStage);
+            const uint32_t sb = sa + kAStage;
+            const uint32_t at = smem_u32(tiles + NS * C::kStage + stage * kNvAtomBytes);
+            const uint32_t set = tmem + TL::kSfBase + 128u * static_cast<uint32_t>(stage & 1);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t slot = set + 32u * static_cast<uint32_t>(kk);
+              tc_cp_32x128b_warpx4(slot, make_sdesc(at + kk * 512, 0, 128, 0));
+              tc_cp_32x128b_warpx4(slot + 16, make_sdesc(at + 2048 + kk * 1024, 0, 128, 0));
+              tc_cp_32x128b_warpx4(slot + 20, make_sdesc(at + 2048 + kk * 1024 + 512, 0, 128, 0));
+              const uint64_t ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
+              const uint64_t bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
+              tc_mma_nvf4(d_tmem, ad, bd, idesc, slot, slot + 16, (kb | kk) != 0 ? 1u : 0u);
             }
             tc_commit(&s.empty[stage]);
           }
@@ -680,7 +746,43 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       __syncwarp();
       if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
     }
-  } else if (C::kMx && kMode == kFwd && warp == 6) {
+  } else if (kKind == 3 && warp == 6) {
+    // ------------------------------------------------------------------ NVFP4 scale layout
+    // Each stage's raw rows (A 128 x 16 B at +0, B 256 x 16 B at +2048) become, in
+    // place, the atoms of its four MMAs: byte (m % 32) * 16 + (m / 32) * 4 + j of atom
+    // kk is the scale of row m, 16-element block 4 kk + j (word kk of the row).
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+      const Tile t = tile_info(s, g, tile, p);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
+        uint8_t* at = tiles + NS * C::kStage + stage * kNvAtomBytes;
+        uint4 ra[4], rb[2][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ra[i] = *reinterpret_cast<const uint4*>(at + (lane + 32 * i) * 16);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rb[h][i] = *reinterpret_cast<const uint4*>(at + 2048 + h * 2048 + (lane + 32 * i) * 16);
+        __syncwarp();
+        auto word = [](const uint4& v, int w) { return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w)); };
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          *reinterpret_cast<uint4*>(at + kk * 512 + lane * 16) =
+              make_uint4(word(ra[0], kk), word(ra[1], kk), word(ra[2], kk), word(ra[3], kk));
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint4*>(at + 2048 + kk * 1024 + h * 512 + lane * 16) =
+                make_uint4(word(rb[h][0], kk), word(rb[h][1], kk), word(rb[h][2], kk), word(rb[h][3], kk));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.sfready[stage]);
+        if (++stage == NS) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (kKind == 2 && kMode == kFwd && warp == 6) {
     // ------------------------------------------------------------------ MXFP8 scale layout
     // Every 4 K-blocks: take the raw scale rows of the slot (row r: 16 bytes, the
     // scales of 4 K-blocks) into registers and free the slot.  Every K-block: write
@@ -742,6 +844,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     // the global stores of the tile follow from registers (or, for wgrad, from a
     // shared-memory staging buffer by TMA), overlapping the next tile's MMAs.
     const int q = warp & 3;                 // TMEM lane quarter of this warp
+    float alpha = 1.f;                      // NVFP4: undo the two tensor encode scales
+    if constexpr (kKind == 3) alpha = __fdiv_rn(1.f, __fmul_rn(__ldg(p.ts_a), __ldg(p.ts_b)));
     const int r = q * 32 + lane;            // tile row owned by this thread
     OutT* out = static_cast<OutT*>(p.out);
     int acc = 0;
@@ -816,6 +920,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
+            nv_scale<kKind>(v, alpha);
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
@@ -864,6 +969,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             tmem_ld32(tb + c * 32, gv);
             tmem_ld32(tb + 128 + c * 32, uv);
             tmem_ld_wait();
+            nv_scale<kKind>(gv, alpha);
+            nv_scale<kKind>(uv, alpha);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               pk[c * 16 + i] = pack_bf16x2(silu_f(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]),
@@ -881,6 +988,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             tmem_ld32(tb + c * 32, gv);
             tmem_ld32(tb + 128 + c * 32, uv);
             tmem_ld_wait();
+            nv_scale<kKind>(gv, alpha);
+            nv_scale<kKind>(uv, alpha);
             const int col = t.col0 + c * 32;
             if (valid && col < g.n_out) {
               float h[32];
@@ -1035,6 +1144,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
+            nv_scale<kKind>(v, alpha);
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
           }
@@ -1063,6 +1173,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             uint32_t v[32];
             tmem_ld32(tb + c * 32, v);
             tmem_ld_wait();
+            nv_scale<kKind>(v, alpha);
             const int col = t.col0 + c * 32;
             if (valid && col < g.n_out) {
               float f[32];
@@ -1245,7 +1356,36 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
     set_error("%s: MXFP8 needs 16-byte aligned A and B scales and K %% 512 == 0", fn);
     return MOE_ERR_INVALID_ARG;
   }
+  if (A->dtype == MOE_E2M1 && (!A->scales || !B->scales || !A->tensor_scale || !B->tensor_scale || K % 256 ||
+                               !aligned16(A->scales) || !aligned16(B->scales))) {
+    set_error("%s: NVFP4 needs 16-byte aligned A and B scales, both tensor scales and K %% 256 == 0", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (M == 0) return MOE_OK;
+  if (A->dtype == MOE_E2M1) {
+    // codes [rows, K/2] bytes: the kernel walks K in bytes, 128 (= 256 elements) per stage
+    const bool swn = epi == MOE_EPI_SWIGLU;
+    CUtensorMap ta, tb, tsa, tsb;
+    const uint64_t adims[2] = {static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M)};
+    const uint32_t abox[2] = {kBKBytes, kBM};
+    const uint64_t bdims[3] = {static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
+    const uint32_t bbox[3] = {kBKBytes, static_cast<uint32_t>(swn ? kBN / 2 : kBN), 1};
+    const uint64_t sadims[2] = {static_cast<uint64_t>(K / 16), static_cast<uint64_t>(M)};
+    const uint64_t sbdims[2] = {static_cast<uint64_t>(K / 16), static_cast<uint64_t>(N) * static_cast<uint64_t>(E)};
+    const uint32_t sbox[2] = {16, kBM};
+    if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->ptr, 2, adims, abox) ||
+        !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->ptr, 3, bdims, bbox) ||
+        !make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_INVALID_ARG;
+    Params p{offsets, M, N, K / 2, E, C, preact, nullptr, nullptr, dev_status, nullptr, nullptr,
+             A->tensor_scale, B->tensor_scale};
+    const bool f32o = c_dtype == MOE_F32;
+    if (swn) return f32o ? launch<3, kFwd, kEpiSwiglu, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
+                         : launch<3, kFwd, kEpiSwiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+    return f32o ? launch<3, kFwd, kEpiNone, float>(ta, tb, p, stream, sms, fn, &tsa, &tsb)
+                : launch<3, kFwd, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb);
+  }
   const int eb = elem_bytes(A->dtype);
   const uint32_t bk = kBKBytes / eb;
   CUtensorMap ta, tb;
@@ -1451,7 +1591,7 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
   if (!make_map(&ta, map_type(dtype), eb, x, 2, adims, abox) ||
       !make_map(&tb, map_type(dtype), eb, w_router, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
-  Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr,
+  Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr, nullptr, nullptr,
            topk_idx, topk_w, counts, k, renormalize ? 1 : 0};
   if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
   return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);

@@ -1,0 +1,128 @@
+"""NVFP4 on the GPU against the NVFP4 oracle: the quantiser bit-exact (codes,
+scales and the fp32 tensor scale), including the hand-worked blocks."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import ragged_grouped_gemm_topk_gb300 as moe_gpu
+from ragged_grouped_gemm_topk_gb300 import workloads as W
+from oracle import nvfp4 as o4
+from _parity import f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "nvfp4_blocks.txt")
+
+
+def _check_quant(t):
+    codes, scales, ts = moe_gpu.moe_quantize_nvfp4(t)
+    c, s, g = o4.quantize(t.float().cpu().numpy().reshape(-1, t.shape[-1]))
+    assert ts[0].item() == float(g)
+    assert (scales.cpu().numpy().reshape(s.shape) == s).all()
+    assert (codes.cpu().numpy().reshape(c.shape) == c).all()
+    return codes, scales, ts, (c, s, g)
+
+
+def test_quantize_nvfp4_golden_blocks():
+    need_gpu()
+    vals = [l.split()[1:] for l in open(GOLDEN) if l.startswith("values")][0]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float32, device="cuda")[None, :]
+    codes, scales, ts, _ = _check_quant(t)
+    assert ts[0].item() == 448.0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("rows,K", [(1, 16), (37, 64), (300, 512), (64, 7168)])
+def test_quantize_nvfp4_bit_exact(dtype, rows, K):
+    need_gpu()
+    t = W.make_matrix(rows, K, seed=rows + K, dtype=dtype, device="cuda", scale=3.0)
+    if rows > 10:
+        t[3] *= 2.0 ** -14                           # tiny rows: subnormal E4M3 block scales
+        t[4, :16] = 0                                # an all-zero block
+        t[5, 1] = -0.0
+        t[6] *= 2.0 ** 6                             # the tensor's amax comes from here
+    _check_quant(t)
+
+
+def test_quantize_nvfp4_weight_stack_and_zero_tensor():
+    need_gpu()
+    Wt = W.make_matrix(4 * 96, 256, seed=7, dtype=torch.bfloat16, device="cuda").view(4, 96, 256)
+    codes, scales, ts, _ = _check_quant(Wt)
+    assert codes.shape == (4, 96, 128) and scales.shape == (4, 96, 16)
+    z = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
+    codes, scales, ts, _ = _check_quant(z)
+    assert ts[0].item() == 1.0 and int(codes.sum()) == 0 and int(scales.sum()) == 0
+
+
+# ----------------------------------------------------------------------------- NVFP4 grouped GEMM
+
+from oracle import moe as om  # noqa: E402
+from _parity import ragged_offsets, rel_l2  # noqa: E402
+
+COUNTS = {"mixed": [0, 1, 130, 257, 3, 128, 0, 64], "singles": [1] * 37, "one-expert": [700]}
+
+
+def _mats(M, K, N, E, seed):
+    A = W.make_matrix(M, K, seed=seed, dtype=torch.bfloat16, device="cuda")
+    B = W.make_matrix(E * N, K, seed=seed + 1, dtype=torch.bfloat16, device="cuda", scale=K ** -0.5).view(E, N, K)
+    Aq, As, Ag, (ca, sa, ga) = _check_quant(A)
+    Bq, Bs, Bg, (cb, sb, gb) = _check_quant(B)
+    A_deq = o4.dequantize(ca, sa, ga)
+    B_deq = o4.dequantize(cb, sb, gb).reshape(E, N, K)
+    return (Aq, As, Ag, A_deq), (Bq, Bs, Bg, B_deq)
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
+@pytest.mark.parametrize("K,N", [(256, 256), (512, 320), (1024, 64)])
+def test_fwd_nvfp4_plain(counts, K, N):
+    """C = A . B[e]^T on NVFP4 operands against the oracle on the same decoded
+    values (only the fp32 accumulation and the bf16 store round); rows outside
+    every group untouched."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    rows = int(sum(cnt))
+    M = rows + 2
+    (Aq, As, Ag, A_deq), (Bq, Bs, Bg, B_deq) = _mats(M, K, N, E, seed=K + N + 41)
+    off = ragged_offsets(cnt)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, A_scales=As, B_scales=Bs, A_tensor_scale=Ag, B_tensor_scale=Bg, out=C)
+    want = om.grouped_gemm(A_deq, B_deq, off.cpu().numpy())
+    got = f64(C)
+    assert np.isnan(got[rows:]).all()
+    err = rel_l2(got[:rows], want[:rows])
+    assert err < 1e-2, err
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+@pytest.mark.parametrize("K,f", [(256, 128), (512, 96), (768, 288)])
+def test_fwd_nvfp4_swiglu(counts, K, f):
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt))
+    (Aq, As, Ag, A_deq), (Bq, Bs, Bg, B_deq) = _mats(M, K, 2 * f, E, seed=K + f + 43)
+    off = ragged_offsets(cnt)
+    H, GU = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi="swiglu", A_scales=As, B_scales=Bs, A_tensor_scale=Ag,
+                                         B_tensor_scale=Bg, out_dtype=torch.float32, want_preact=True)
+    gu = om.grouped_gemm(A_deq, B_deq, off.cpu().numpy())
+    assert rel_l2(f64(GU), gu) < 1e-3                      # fp32 out: the accumulation rounding only
+    assert rel_l2(f64(H), om.swiglu(gu)) < 1e-3
+    Hb = moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, epi="swiglu", A_scales=As, B_scales=Bs, A_tensor_scale=Ag,
+                                      B_tensor_scale=Bg)
+    assert rel_l2(f64(Hb), om.swiglu(gu)) < 1e-2
+
+
+def test_fwd_nvfp4_requires_k_multiple_of_256_and_scales():
+    need_gpu()
+    (Aq, As, Ag, _), (Bq, Bs, Bg, _) = _mats(64, 512, 64, 2, seed=3)
+    off = ragged_offsets([32, 32])
+    with pytest.raises(moe_gpu.binding.MoeError, match="256"):
+        moe_gpu.moe_grouped_gemm_fwd(Aq[:, :64].contiguous(), Bq[:, :, :64].contiguous(), off,
+                                     A_scales=As[:, :8].contiguous(), B_scales=Bs[:, :, :8].contiguous(),
+                                     A_tensor_scale=Ag, B_tensor_scale=Bg)
+    with pytest.raises(moe_gpu.binding.MoeError):
+        moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, A_scales=As, B_scales=None, A_tensor_scale=Ag, B_tensor_scale=Bg)
