@@ -146,7 +146,9 @@ def stage_bytes(w):
     scales, column-wise codes + scales): x read once, the three outputs written
     once."""
     s = 4 if w.dtype == "f32" else 2
-    if w.dtype == "mxfp8" and w.backward:
+    if w.dtype == "nvfp4":                      # bf16 Xp, then its NVFP4 codes + scales
+        xp_out = w.M * w.d * (2 + 0.5 + 1 / 16)
+    elif w.dtype == "mxfp8" and w.backward:
         xp_out = w.M * w.d * (2 + 2 * (1 + 1 / 32))
     elif w.dtype == "mxfp8":
         xp_out = w.M * w.d * (1 + 1 / 32)
@@ -163,6 +165,8 @@ def gemm1_bytes(w, e_used):
     read once, H (MXFP8: its codes and scales; when training also the
     pre-activation G|U) written once."""
     M, d, f, E = w.M, w.d, w.f, e_used
+    if w.dtype == "nvfp4":                      # W1 and Xp as NVFP4, H written in bf16
+        return E * 2 * f * d * (0.5 + 1 / 16) + M * d * (0.5 + 1 / 16) + M * f * 2
     if w.dtype == "mxfp8" and w.backward:       # H and G|U in bf16 for the backward
         return E * 2 * f * d * (1 + 1 / 32) + M * d * (1 + 1 / 32) + M * f * 2 + M * 2 * f * 2
     if w.dtype == "mxfp8":
@@ -222,7 +226,17 @@ def run_ours(args, world, rank, local):
         mark(1)
         layer.dispatch(x)
         mark(2)
-        if ev is not None and w.dtype != "mxfp8":
+        if ev is not None and w.dtype == "nvfp4":
+            # GEMM1 alone in the GEMM1 stage; H's quantisation goes with GEMM2
+            pkg.moe_grouped_gemm_fwd(layer.xq, layer.W1q, layer.offsets, epi="swiglu", A_scales=layer.xs,
+                                     B_scales=layer.W1s, A_tensor_scale=layer.xg, B_tensor_scale=layer.W1g,
+                                     out=layer.h, dev_status=layer.dev_status)
+            mark(3)
+            pkg.moe_quantize_nvfp4(layer.h, codes=layer.hq, scales=layer.hs, tensor_scale=layer.hg)
+            pkg.moe_grouped_gemm_fwd(layer.hq, layer.W2q, layer.offsets, A_scales=layer.hs, B_scales=layer.W2s,
+                                     A_tensor_scale=layer.hg, B_tensor_scale=layer.W2g, out=layer.yp,
+                                     dev_status=layer.dev_status)
+        elif ev is not None and w.dtype != "mxfp8":
             # time GEMM1 alone inside the MLP stage (the dominant kernel)
             pkg.moe_grouped_gemm_fwd(layer.xp, layer.W1, layer.offsets, epi="swiglu", out=layer.h,
                                      preact=layer.gu, dev_status=layer.dev_status)
@@ -324,7 +338,7 @@ def run_ours(args, world, rank, local):
     pk = peaks()
     g1_flops = 4.0 * w.M * w.d * w.f
     g1_tflops = g1_flops / (per["gemm1"] * 1e-3) / 1e12
-    dtype_peak = pk["bf16_sus"] * (2.0 if w.dtype == "mxfp8" else (0.5 if w.dtype == "f32" else 1.0))
+    dtype_peak = pk["bf16_sus"] * {"mxfp8": 2.0, "nvfp4": 6.0, "f32": 0.5}.get(w.dtype, 1.0)
     # the roofline that binds GEMM1: tensor time at the dtype's peak vs HBM time of
     # its algorithmic bytes at the measured copy bandwidth
     e_used = int((layer.counts > 0).sum().item())     # read after the timed region
@@ -332,6 +346,7 @@ def run_ours(args, world, rank, local):
     g1_s = per["gemm1"] * 1e-3
     hbm_bound = g1_bytes / (pk["hbm"] * 1e9) > g1_flops / (dtype_peak * 1e12)
     peak_src = (f"{pk['source']} bf16 sustained" + (" x2 (fp8 nominal ratio)" if w.dtype == "mxfp8" else "")
+                + (" x6 (fp4 nominal ratio, 13.5 / 2.25 PFLOP/s dense)" if w.dtype == "nvfp4" else "")
                 + (" x0.5 (tf32 nominal ratio)" if w.dtype == "f32" else ""))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": round(g1_bytes / g1_s / 1e9, 1), "peak": pk["hbm"], "unit": "GB/s",
@@ -351,7 +366,7 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"f32": "tf32", "bf16": "bf16", "mxfp8": "mxfp8-e4m3"}[w.dtype],
+        "dtype": {"f32": "tf32", "bf16": "bf16", "mxfp8": "mxfp8-e4m3", "nvfp4": "nvfp4-e2m1"}[w.dtype],
         "data": "synthetic (seeded; no dataset or trained weights)",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f,
                    "M_rows": w.M, "backward": w.backward,
@@ -570,7 +585,8 @@ def cpu_baseline(w, budget_s=12.0):
     while True:
         x, lg, W1, W2 = oracle_sample(w, n)
         t0 = time.perf_counter()
-        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8")
+        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8",
+                               nvfp4_operands=w.dtype == "nvfp4")
         if w.backward:
             dy = x * 0 + 1.0
             om.layer_backward(fwd, dy, x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=w.dtype == "mxfp8")
@@ -594,14 +610,15 @@ def run_reference(args, world, rank):
     w = W.BY_NAME[args.workload]
     if rank != 0:
         return None
-    n = 16 if w.dtype != "mxfp8" else 4
+    n = 16 if w.dtype not in ("mxfp8", "nvfp4") else 4
     x, lg, W1, W2 = oracle_sample(w, n)
     mx = w.dtype == "mxfp8"
+    fp4 = w.dtype == "nvfp4"
     for _ in range(args.warmup):
-        om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
+        om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx, nvfp4_operands=fp4)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
+        fwd = om.layer_forward(x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx, nvfp4_operands=fp4)
         if w.backward:
             om.layer_backward(fwd, x * 0 + 1.0, x, lg, W1, W2, w.k, w.renormalize, mxfp8_operands=mx)
     dt = (time.perf_counter() - t0) / args.steps

@@ -39,7 +39,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import mxfp8
+from . import mxfp8, nvfp4
 
 
 # ----------------------------------------------------------------------------- route
@@ -179,17 +179,31 @@ def mx_roundtrip(a: np.ndarray) -> np.ndarray:
     return mxfp8.dequantize_rowwise(*mxfp8.quantize_rowwise(a2)).reshape(shp)
 
 
-def layer_forward(x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False):
+def nvfp4_roundtrip(a: np.ndarray) -> np.ndarray:
+    """Values an NVFP4 operand carries: the whole array is one tensor (one fp32
+    tensor scale), quantised row-wise along its last axis in blocks of 16."""
+    shp = a.shape
+    a2 = np.asarray(a, dtype=np.float32).reshape(-1, shp[-1])
+    return nvfp4.dequantize(*nvfp4.quantize(a2)).reshape(shp)
+
+
+def layer_forward(x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False, nvfp4_operands=False):
     """Route -> dispatch -> grouped MLP -> combine ([3] "Method overview").
 
     With ``mxfp8_operands`` both GEMMs take MXFP8 operands (row-wise scales
     along the contraction): Xp, W1, H and W2 are each quantised and the GEMMs run
-    on the exactly dequantised values."""
+    on the exactly dequantised values.  ``nvfp4_operands`` does the same with
+    NVFP4 (each of Xp, W1, H, W2 one tensor with its own tensor scale)."""
     E = W1.shape[0]
     idx, w, counts = route_topk(logits, k, renormalize)
     offsets, dest_row, src_pair = permute_maps(idx, E)
     Xp = permute(x, src_pair, k)
-    if mxfp8_operands:
+    if nvfp4_operands:
+        Xq, W1q, W2q = nvfp4_roundtrip(Xp), nvfp4_roundtrip(W1), nvfp4_roundtrip(W2)
+        GU = grouped_gemm(Xq, W1q, offsets)
+        H = swiglu(GU)
+        Yp = grouped_gemm(nvfp4_roundtrip(H), W2q, offsets)
+    elif mxfp8_operands:
         Xq, W1q, W2q = mx_roundtrip(Xp), mx_roundtrip(W1), mx_roundtrip(W2)
         GU = grouped_gemm(Xq, W1q, offsets)
         H = swiglu(GU)

@@ -162,7 +162,7 @@ constexpr size_t smem_for() {
 template <int kKind, int kMode, int kEpi>
 struct Tl {
   static constexpr int BN = kBN;
-  static constexpr int kAcc = kKind == 2 ? 1 : 2;
+  static constexpr int kAcc = kKind >= 2 ? 1 : 2;   // block-scaled: columns 256-511 hold the scales
   static constexpr uint32_t kSfBase = 256u;
   static constexpr uint32_t kSfStride = 32u;
   static constexpr uint32_t kSfB = 16u;

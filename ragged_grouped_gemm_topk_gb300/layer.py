@@ -65,7 +65,18 @@ class MoELayer:
         self.y = torch.empty(T, d, dtype=store, device=dev)
         self.gu = torch.empty(M, 2 * f, dtype=store, device=dev) if training else None
         u8 = dict(dtype=torch.uint8, device=dev)
-        if dtype == "mxfp8":
+        if dtype == "nvfp4":
+            if training:
+                raise NotImplementedError("the NVFP4 layer is forward only")
+            # each of W1, W2, Xp, H is one NVFP4 tensor (one fp32 tensor scale)
+            self.W1q, self.W1s, self.W1g = B.moe_quantize_nvfp4(W1)
+            self.W2q, self.W2s, self.W2g = B.moe_quantize_nvfp4(W2)
+            self.xp = torch.empty(M, d, dtype=store, device=dev)
+            self.xq, self.xs = torch.empty(M, d // 2, **u8), torch.empty(M, d // 16, **u8)
+            self.xg = torch.empty(2, dtype=torch.float32, device=dev)
+            self.hq, self.hs = torch.empty(M, f // 2, **u8), torch.empty(M, f // 16, **u8)
+            self.hg = torch.empty(2, dtype=torch.float32, device=dev)
+        elif dtype == "mxfp8":
             self.xq = torch.empty(M, d, **u8)
             self.xs = torch.empty(M, d // 32, **u8)
             self.hq = torch.empty(M, f, **u8)
@@ -116,7 +127,12 @@ class MoELayer:
                              topk_w=self.topk_w, counts=self.counts, dev_status=self.dev_status)
 
     def dispatch(self, x):
-        if self.dtype == "mxfp8" and self.training:
+        if self.dtype == "nvfp4":
+            B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
+                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
+                          workspace=self.workspace, dev_status=self.dev_status)
+            B.moe_quantize_nvfp4(self.xp, codes=self.xq, scales=self.xs, tensor_scale=self.xg)
+        elif self.dtype == "mxfp8" and self.training:
             # bf16 Xp (kept for the weight gradient), then both MXFP8 forms of it
             B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
                           dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
@@ -133,7 +149,15 @@ class MoELayer:
                           workspace=self.workspace, dev_status=self.dev_status)
 
     def expert_mlp(self):
-        if self.dtype == "mxfp8" and self.training:
+        if self.dtype == "nvfp4":
+            B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
+                                   B_scales=self.W1s, A_tensor_scale=self.xg, B_tensor_scale=self.W1g,
+                                   out=self.h, dev_status=self.dev_status)
+            B.moe_quantize_nvfp4(self.h, codes=self.hq, scales=self.hs, tensor_scale=self.hg)
+            B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
+                                   A_tensor_scale=self.hg, B_tensor_scale=self.W2g, out=self.yp,
+                                   dev_status=self.dev_status)
+        elif self.dtype == "mxfp8" and self.training:
             # GEMM1 keeps H and the pre-activations in bf16 for the backward
             B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
                                    B_scales=self.W1s, out=self.h, preact=self.gu, dev_status=self.dev_status)
@@ -171,7 +195,8 @@ class MoELayer:
         scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
         MXFP8 training adds the row- and column-wise quantisation of Xp and of H."""
         route = 1 if self.w_router is not None else 2     # fused router GEMM (counts zeroed by a memset)
-        return route + 2 + 2 + 1 + (4 if self.dtype == "mxfp8" and self.training else 0)
+        nv = 4 if self.dtype == "nvfp4" else 0            # amax + quantise, of Xp and of H
+        return route + 2 + 2 + 1 + nv + (4 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd;

@@ -13,7 +13,9 @@ real data; here every tensor is synthetic and seeded.
 
 A sixth entry, the MXFP8 training step, is the DeepSeek-V3-shaped training
 layer again with every GEMM on MXFP8 operands: it reuses that layer's seed, so
-both see the same routing, activations, weights and upstream gradient.
+both see the same routing, activations, weights and upstream gradient.  A
+seventh, the NVFP4 layer, is the DeepSeek-V3-shaped MXFP8 layer's forward with
+NVFP4 operands, on that layer's seed and inputs.
 
 Recipe (per workload, seed ``s`` = its position in ``WORKLOADS``, shared by the
 MXFP8 training step with the bf16 one):
@@ -47,7 +49,7 @@ class Workload:
     E: int          # routed experts
     k: int          # experts per token
     f: int          # expert FFN hidden dim (SwiGLU: W1 has 2f rows)
-    dtype: str      # "f32", "bf16" or "mxfp8" (mxfp8: bf16 storage, E4M3+E8M0 GEMM operands)
+    dtype: str      # "f32", "bf16", "mxfp8" or "nvfp4" (bf16 storage, block-scaled GEMM operands)
     bias: str       # "none", "gauss" or "zipf"
     bias_param: float
     seed: int
@@ -83,6 +85,7 @@ WORKLOADS = [
     Workload("dsv3-mxfp8", 8192, 7168, 256, 8, 2048, "mxfp8", "zipf", 1.3, 3),
     Workload("dsv3-bf16-train", 16384, 7168, 256, 8, 2048, "bf16", "zipf", 1.5, 4, backward=True),
     Workload("dsv3-mxfp8-train", 16384, 7168, 256, 8, 2048, "mxfp8", "zipf", 1.5, 4, backward=True),
+    Workload("dsv3-nvfp4", 8192, 7168, 256, 8, 2048, "nvfp4", "zipf", 1.3, 3),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}

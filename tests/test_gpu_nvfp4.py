@@ -62,7 +62,8 @@ def test_quantize_nvfp4_weight_stack_and_zero_tensor():
 from oracle import moe as om  # noqa: E402
 from _parity import ragged_offsets, rel_l2  # noqa: E402
 
-COUNTS = {"mixed": [0, 1, 130, 257, 3, 128, 0, 64], "singles": [1] * 37, "one-expert": [700]}
+COUNTS = {"mixed": [0, 1, 130, 257, 3, 128, 0, 64], "singles": [1] * 37, "one-expert": [700],
+          "many-tiles": [5200, 0, 5100]}      # with 2+ column tiles: more tiles than SMs
 
 
 def _mats(M, K, N, E, seed):
@@ -75,7 +76,7 @@ def _mats(M, K, N, E, seed):
     return (Aq, As, Ag, A_deq), (Bq, Bs, Bg, B_deq)
 
 
-@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
+@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert", "many-tiles"], ids=str)
 @pytest.mark.parametrize("K,N", [(256, 256), (512, 320), (1024, 64)])
 def test_fwd_nvfp4_plain(counts, K, N):
     """C = A . B[e]^T on NVFP4 operands against the oracle on the same decoded
@@ -97,7 +98,7 @@ def test_fwd_nvfp4_plain(counts, K, N):
     assert err < 1e-2, err
 
 
-@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+@pytest.mark.parametrize("counts", ["mixed", "singles", "many-tiles"], ids=str)
 @pytest.mark.parametrize("K,f", [(256, 128), (512, 96), (768, 288)])
 def test_fwd_nvfp4_swiglu(counts, K, f):
     need_gpu()
@@ -126,3 +127,28 @@ def test_fwd_nvfp4_requires_k_multiple_of_256_and_scales():
                                      A_tensor_scale=Ag, B_tensor_scale=Bg)
     with pytest.raises(moe_gpu.binding.MoeError):
         moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, A_scales=As, B_scales=None, A_tensor_scale=Ag, B_tensor_scale=Bg)
+
+
+# ----------------------------------------------------------------------------- NVFP4 layer
+
+from _parity import i64, logits_dev  # noqa: E402
+
+
+def test_nvfp4_layer_scaled():
+    """DeepSeek-V3-shaped NVFP4 layer at reduced size: maps exact; H (the GPU's own
+    bf16 H) quantised bit-exactly as the oracle quantises it; the output against the
+    oracle's NVFP4 chain (which quantises its own float64 H: the two H tensor scales
+    differ in their last bits, so a few codes differ)."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-nvfp4"].scaled(T=400, d=512, f=512, name="fp4-small")
+    x, W1, W2, lg = W.make_x(w, "cuda"), W.make_w1(w, "cuda"), W.make_w2(w, "cuda"), logits_dev(w)
+    layer = moe_gpu.MoELayer(w.T, w.d, w.E, w.k, w.f, W1, W2, dtype="nvfp4", renormalize=w.renormalize)
+    y = layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    ref = om.layer_forward(f64(x), lg.cpu().numpy(), f64(W1), f64(W2), w.k, nvfp4_operands=True)
+    assert (i64(layer.src_pair) == ref["src_pair"]).all()
+    c, s, g = o4.quantize(layer.h.float().cpu().numpy())
+    assert layer.hg[0].item() == float(g)
+    assert (layer.hs.cpu().numpy() == s).all() and (layer.hq.cpu().numpy() == c).all()
+    assert rel_l2(f64(y), ref["y"]) < 5e-2

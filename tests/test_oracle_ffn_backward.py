@@ -258,3 +258,27 @@ def test_mxfp8_backward_close_to_exact():
     for name in ("dx", "dW1", "dW2", "dlogits"):
         err = np.linalg.norm(mx[name] - exact[name]) / np.linalg.norm(exact[name])
         assert 0 < err < 0.2, (name, err)
+
+
+def test_nvfp4_layer_forward_close_to_exact_and_exact_on_representable_operands():
+    """The NVFP4 layer stays within FP4's error of the exact one (E2M1 keeps one
+    mantissa bit), and the round trip of a whole weight stack (one tensor scale
+    across the experts) is the identity on representable values."""
+    from oracle import nvfp4
+    T, d, E, k, f = 48, 64, 4, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=91)
+    exact = moe.layer_forward(x, lg, W1, W2, k)
+    fp4 = moe.layer_forward(x, lg, W1, W2, k, nvfp4_operands=True)
+    err = np.linalg.norm(fp4["y"] - exact["y"]) / np.linalg.norm(exact["y"])
+    assert 0 < err < 0.35, err
+    # representable weights: E2M1 values with a 6 in every 16-element block, so the
+    # tensor scale is 448, every block scale 448 and every element maps to itself
+    rng = np.random.default_rng(92)
+    vals = np.array([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    def rep(shape):
+        a = rng.choice(vals, size=shape) * rng.choice([-1.0, 1.0], size=shape)
+        a[..., ::16] = 6.0
+        return a
+    W1r, W2r = rep((E, 2 * f, d)), rep((E, d, f))
+    assert np.array_equal(moe.nvfp4_roundtrip(W1r), W1r)
+    assert np.array_equal(nvfp4.dequantize(*nvfp4.quantize(W2r.reshape(-1, f))).reshape(W2r.shape), W2r)
