@@ -146,8 +146,8 @@ def stage_bytes(w):
     scales, column-wise codes + scales): x read once, the three outputs written
     once."""
     s = 4 if w.dtype == "f32" else 2
-    if w.dtype == "nvfp4":                      # bf16 Xp, then its NVFP4 codes + scales
-        xp_out = w.M * w.d * (2 + 0.5 + 1 / 16)
+    if w.dtype == "nvfp4":                      # NVFP4 codes + scales (x read twice: amax, scatter)
+        xp_out = w.M * w.d * (0.5 + 1 / 16)
     elif w.dtype == "mxfp8" and w.backward:
         xp_out = w.M * w.d * (2 + 2 * (1 + 1 / 32))
     elif w.dtype == "mxfp8":

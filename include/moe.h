@@ -237,6 +237,18 @@ moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype,
 moe_status_t moe_quantize_nvfp4(const void* in, moe_dtype_t in_dtype, int rows, int K, uint8_t* codes,
                                 uint8_t* scales, float* tensor_scale, cudaStream_t stream);
 
+/* Dispatch with NVFP4 rows: moe_permute's maps, and instead of bf16 rows the NVFP4
+ * codes [T*k, d/2] and scales [T*k, d/16] of the permuted rows, bit-identical to
+ * moe_quantize_nvfp4 of moe_permute's rows (the tensor amax of x is that of the
+ * permuted rows: every token is routed).  x is read twice (its amax, then the
+ * scatter); the bf16 rows are never written.  tensor_scale as moe_quantize_nvfp4.
+ * d % 16 == 0; codes 4-byte aligned; workspace as moe_permute. */
+moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, int T, int d, const int32_t* topk_idx,
+                               int k, int E, const int32_t* counts, int32_t* offsets, int32_t* dest_row,
+                               int32_t* src_pair, uint8_t* xp_codes, uint8_t* xp_scales, float* tensor_scale,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               cudaStream_t stream);
+
 /* ---------------------------------------------------------------- grouped GEMM
  * Ragged grouped GEMM ([1] "Optimisation 1": one kernel launch covers every
  * expert and computes only the valid token rows of each; the per-expert sizes

@@ -170,6 +170,30 @@ def moe_quantize_nvfp4(inp, *, codes=None, scales=None, tensor_scale=None):
     return codes, scales, tensor_scale
 
 
+def moe_permute_nvfp4(x, topk_idx, counts, E, *, offsets=None, dest_row=None, src_pair=None, codes=None,
+                      scales=None, tensor_scale=None, workspace=None, dev_status=None):
+    """Dispatch with NVFP4 rows: a dict with offsets, dest_row, src_pair and the rows'
+    codes [T*k, d/2], scales [T*k, d/16] and tensor_scale (fp32 [2], g in element 0)."""
+    T, k = topk_idx.shape
+    d = x.shape[1]
+    dev = x.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    M = T * k
+    offsets = offsets if offsets is not None else torch.empty(E + 1, **i32)
+    dest_row = dest_row if dest_row is not None else torch.empty(T, k, **i32)
+    src_pair = src_pair if src_pair is not None else torch.empty(M, **i32)
+    codes = codes if codes is not None else torch.empty(M, d // 2, dtype=torch.uint8, device=dev)
+    scales = scales if scales is not None else torch.empty(M, d // 16, dtype=torch.uint8, device=dev)
+    tensor_scale = tensor_scale if tensor_scale is not None else torch.empty(2, dtype=torch.float32, device=dev)
+    nbytes = moe_permute_workspace_size(T, k, E)
+    workspace = workspace if workspace is not None else torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _lib.call("moe_permute_nvfp4", _ptr(x), _dt(x), T, d, _ptr(topk_idx), k, E, _ptr(counts), _ptr(offsets),
+              _ptr(dest_row), _ptr(src_pair), _ptr(codes), _ptr(scales), _ptr(tensor_scale), _ptr(workspace),
+              workspace.numel(), _ptr(dev_status), _stream())
+    return {"offsets": offsets, "dest_row": dest_row, "src_pair": src_pair, "codes": codes, "scales": scales,
+            "tensor_scale": tensor_scale}
+
+
 def moe_grouped_gemm_fwd(A, B, offsets, *, epi="none", A_scales=None, B_scales=None,
                          out_dtype=torch.bfloat16, out=None, preact=None, want_preact=False,
                          dev_status=None, A_tensor_scale=None, B_tensor_scale=None):

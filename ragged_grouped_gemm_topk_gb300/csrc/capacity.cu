@@ -17,7 +17,8 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
                             const int32_t* topk_idx, int k, int E, const int32_t* counts,
                             int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
                             moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
-                            int32_t* dev_status, cudaStream_t stream, int sms);
+                            int32_t* dev_status, cudaStream_t stream, int sms,
+                            const uint32_t* amax_bits, float* tensor_scale);
 size_t permute_hist_bytes(int T, int E);
 
 namespace {
@@ -123,7 +124,7 @@ extern "C" moe_status_t moe_permute_capacity(const void* x, moe_dtype_t x_dtype,
   const int pairs = T * k;
   // dropless maps only (no rows): dest_row receives the dropless rows
   moe_status_t st = permute_launch(nullptr, x_dtype, T, d, topk_idx, k, E, counts, off_drop, dest_row, src_drop,
-                                   nullptr, x_dtype, nullptr, hist, dev_status, stream, sms);
+                                   nullptr, x_dtype, nullptr, hist, dev_status, stream, sms, nullptr, nullptr);
   if (st != MOE_OK) return st;
   if (pairs > 0) {
     const int g = (pairs + kCapThreads - 1) / kCapThreads;

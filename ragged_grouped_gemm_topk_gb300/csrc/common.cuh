@@ -83,6 +83,17 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
   return __uint_as_float(((exp + 120u) << 23) | (man << 20));
 }
 
+// NVFP4 scaling of one 16-element block with block amax `amax` in a tensor whose
+// encode scale is g: the E4M3 scale byte s = E4M3_rn_sat((amax / 6) * g) and the
+// multiplier g / s (0 when s decodes to 0), every step one fp32 rounding.
+__device__ __forceinline__ float nvfp4_tensor_scale(float amax_t) { return amax_t == 0.f ? 1.f : 2688.f / amax_t; }
+__device__ __forceinline__ void nvfp4_block_scale(float amax, float g, uint32_t* scode, float* inv) {
+  const float sf = __fmul_rn(__fdiv_rn(amax, 6.f), g);
+  *scode = f32x2_to_e4m3x2(sf, 0.f) & 0xFFu;
+  const float sval = ue4m3_value(*scode);
+  *inv = sval == 0.f ? 0.f : __fdiv_rn(g, sval);
+}
+
 // MXFP8 shared-exponent rule (OCP Microscaling Formats v1.0): X = floor(log2 amax)
 // - 8 (8 = E4M3's largest exponent), clamped at -127, stored as the E8M0 byte
 // X + 127; an all-zero block gets byte 127.  Returns the byte and the exact power

@@ -132,13 +132,22 @@ __device__ __forceinline__ void mx_chunk(const Vec16& v, uint32_t (&codes)[2], u
 // destinations are resolved so that the two latencies overlap.
 constexpr int kScatterU = 8;
 
-template <typename Tin, bool kQuant>
+// kQuant: 0 = copy rows, 1 = MXFP8 rows, 2 = NVFP4 rows (packed E2M1 codes [.., d/2],
+// E4M3 scales per 16 [.., d/16], tensor scale from the amax of x in *amax_bits, which
+// is the amax of the permuted rows: every token is routed).
+template <typename Tin, int kQuant>
 __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     const uint8_t* __restrict__ x, int T, int d, const int32_t* __restrict__ idx, int k, int E,
     const int32_t* __restrict__ counts, const int32_t* local_rank, const int32_t* __restrict__ block_hist,
     int nblk, int32_t* __restrict__ offsets, int32_t* dest_row, int32_t* __restrict__ src_pair,
-    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_scales, int32_t* status) {
+    uint8_t* __restrict__ xp, uint8_t* __restrict__ xp_scales, const uint32_t* amax_bits, float* tensor_scale,
+    int32_t* status) {
   pdl_begin();
+  float g4 = 1.f;
+  if constexpr (kQuant == 2) {
+    g4 = nvfp4_tensor_scale(__uint_as_float(*amax_bits));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = g4;
+  }
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   // offsets = exclusive scan of the routed counts, in every CTA (E <= 1024)
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     }
   }
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
-  const size_t out_row = kQuant ? static_cast<size_t>(d) : in_row;
+  const size_t out_row = kQuant == 2 ? static_cast<size_t>(d) / 2 : (kQuant ? static_cast<size_t>(d) : in_row);
   const int n16 = static_cast<int>(in_row / 16);
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
     const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
@@ -238,7 +247,38 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
       for (int i = 0; i < kScatterU; ++i) {
         const int c = base + 32 * i + lane;
         const bool active = c < n16;
-        if constexpr (kQuant) {
+        if constexpr (kQuant == 2) {
+          if (base + 32 * i >= n16) break;     // warp-uniform
+          // a 16-element block spans 16 / EPL lanes
+          constexpr int EPL = Mx<Tin>::kEpl;
+          constexpr int LPB = 16 / EPL;
+          float f[EPL];
+          Mx<Tin>::values(v[i], f);
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+          for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+          uint32_t scode;
+          float inv;
+          nvfp4_block_scale(amax, g4, &scode, &inv);
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = e < EPL ? __fmul_rn(f[e < EPL ? e : 0], inv) : 0.f;
+          const uint32_t packed = f32x8_to_e2m1x8(y);   // EPL codes in the low EPL nibbles
+          for (int j = 0; j < k; ++j) {
+            const int dj = __shfl_sync(kFull, dest, j);
+            if (active && dj >= 0) {
+              uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * (EPL / 2);
+              if (EPL == 8)
+                *reinterpret_cast<uint32_t*>(orow) = packed;
+              else
+                *reinterpret_cast<uint16_t*>(orow) = static_cast<uint16_t>(packed);
+              if ((lane % LPB) == 0)
+                xp_scales[static_cast<size_t>(dj) * (d / 16) + (c * EPL) / 16] = static_cast<uint8_t>(scode);
+            }
+          }
+        } else if constexpr (kQuant == 1) {
           if (base + 32 * i >= n16) break;     // warp-uniform: no lane of this chunk row is active
           uint32_t codes[2], sbyte;
           mx_chunk<Tin>(v[i], codes, &sbyte);
@@ -589,11 +629,14 @@ int scatter_grid(int T, int sms) {
 
 // Launches the three permute kernels; shared by the workspace and the
 // fixed-scratch entry points.
+// xp_dtype MOE_E2M1: NVFP4 rows, with the tensor amax already in *amax_bits and the
+// tensor scale written to *tensor_scale.
 moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
                             const int32_t* topk_idx, int k, int E, const int32_t* counts,
                             int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
                             moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
-                            int32_t* dev_status, cudaStream_t stream, int sms) {
+                            int32_t* dev_status, cudaStream_t stream, int sms,
+                            const uint32_t* amax_bits, float* tensor_scale) {
   const int nblk = (T + kTokensPerRankBlock - 1) / kTokensPerRankBlock;
   const size_t rank_smem = static_cast<size_t>(2) * 8 * E * sizeof(uint32_t);  // mask + base, [8][E] each
   if (rank_smem > 48 * 1024) {
@@ -615,23 +658,32 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
   uint8_t* xpb = static_cast<uint8_t*>(xp);
   // dest_row holds each pair's within-block rank until the scatter overwrites that
   // same element with the pair's final row (read and write by the same thread).
-  if (xp_dtype == MOE_E4M3) {
+  if (xp_dtype == MOE_E2M1) {
     if (x_dtype == MOE_BF16)
-      launch_pdl(permute_scatter_kernel<uint16_t, true>, grid, kScatterThreads, 0, stream, 
-          xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales,
-          dev_status);
+      launch_pdl(permute_scatter_kernel<uint16_t, 2>, grid, kScatterThreads, 0, stream, xb, T, d, topk_idx, k, E,
+                 counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales, amax_bits, tensor_scale,
+                 dev_status);
     else
-      launch_pdl(permute_scatter_kernel<float, true>, grid, kScatterThreads, 0, stream, 
+      launch_pdl(permute_scatter_kernel<float, 2>, grid, kScatterThreads, 0, stream, xb, T, d, topk_idx, k, E,
+                 counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales, amax_bits, tensor_scale,
+                 dev_status);
+  } else if (xp_dtype == MOE_E4M3) {
+    if (x_dtype == MOE_BF16)
+      launch_pdl(permute_scatter_kernel<uint16_t, 1>, grid, kScatterThreads, 0, stream, 
           xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales,
-          dev_status);
+          nullptr, nullptr, dev_status);
+    else
+      launch_pdl(permute_scatter_kernel<float, 1>, grid, kScatterThreads, 0, stream, 
+          xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, xp_scales,
+          nullptr, nullptr, dev_status);
   } else if (x_dtype == MOE_BF16) {
-    launch_pdl(permute_scatter_kernel<uint16_t, false>, grid, kScatterThreads, 0, stream, 
+    launch_pdl(permute_scatter_kernel<uint16_t, 0>, grid, kScatterThreads, 0, stream, 
         xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, nullptr,
-        dev_status);
+        nullptr, nullptr, dev_status);
   } else {
-    launch_pdl(permute_scatter_kernel<float, false>, grid, kScatterThreads, 0, stream, 
+    launch_pdl(permute_scatter_kernel<float, 0>, grid, kScatterThreads, 0, stream, 
         xb, T, d, topk_idx, k, E, counts, dest_row, hist, nblk, offsets, dest_row, src_pair, xpb, nullptr,
-        dev_status);
+        nullptr, nullptr, dev_status);
   }
   return check_launch("moe_permute");
 }
@@ -705,7 +757,7 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, i
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp,
                         xp_dtype, xp_scales, static_cast<int32_t*>(workspace), dev_status, stream,
-                        sms);
+                        sms, nullptr, nullptr);
 }
 
 extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows,
@@ -787,4 +839,46 @@ extern "C" moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_
                static_cast<const uint8_t*>(in), G, R, C, codes, scales);
   }
   return check_launch("moe_quantize_mxfp8_transposed");
+}
+
+namespace moe {
+void nvfp4_amax_launch(const void* in, moe_dtype_t dtype, long long elems, uint32_t* amax_bits,
+                       cudaStream_t stream, int sms);
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, int T, int d,
+                                          const int32_t* topk_idx, int k, int E, const int32_t* counts,
+                                          int32_t* offsets, int32_t* dest_row, int32_t* src_pair,
+                                          uint8_t* xp_codes, uint8_t* xp_scales, float* tensor_scale,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                          cudaStream_t stream) {
+  const char* fn = "moe_permute_nvfp4";
+  if (T < 0 || d < 0 || d % 16 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E ||
+      (x_dtype != MOE_BF16 && x_dtype != MOE_F32) || static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("%s: need T, d >= 0, d %% 16 == 0, 1 <= E <= 1024, 1 <= k <= min(E, 32), BF16/F32 x", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!counts || !offsets || !tensor_scale || (T > 0 && (!x || !topk_idx || !dest_row || !src_pair ||
+                                                        (d > 0 && (!xp_codes || !xp_scales)))) ||
+      !aligned16(x) || (reinterpret_cast<uintptr_t>(xp_codes) & 3) || (reinterpret_cast<uintptr_t>(tensor_scale) & 3)) {
+    set_error("%s: null or misaligned pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!workspace || workspace_bytes < permute_hist_bytes(T, E)) {
+    set_error("%s: workspace of %zu bytes needed", fn, permute_hist_bytes(T, E));
+    return MOE_ERR_WORKSPACE;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  uint32_t* amax_bits = reinterpret_cast<uint32_t*>(tensor_scale + 1);
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) {
+    set_error("%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  // the amax of x is the amax of the permuted rows (every token is routed)
+  nvfp4_amax_launch(x, x_dtype, static_cast<long long>(T) * d, amax_bits, stream, sms);
+  return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp_codes,
+                        MOE_E2M1, xp_scales, static_cast<int32_t*>(workspace), dev_status, stream, sms,
+                        amax_bits, tensor_scale);
 }

@@ -52,8 +52,7 @@ __global__ void __launch_bounds__(kQThreads) nvfp4_quantize_kernel(
     const uint8_t* __restrict__ in, long long nblk, const uint32_t* amax_bits, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* g_out) {
   pdl_begin();
-  const float amax_t = __uint_as_float(*amax_bits);
-  const float g = amax_t == 0.f ? 1.f : 2688.f / amax_t;
+  const float g = nvfp4_tensor_scale(__uint_as_float(*amax_bits));
   if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
   for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk;
        b += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -83,11 +82,9 @@ __global__ void __launch_bounds__(kQThreads) nvfp4_quantize_kernel(
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    float sf = __fdiv_rn(amax, 6.f);
-    sf = __fmul_rn(sf, g);
-    const uint32_t scode = f32x2_to_e4m3x2(sf, 0.f) & 0xFFu;
-    const float sval = ue4m3_value(scode);
-    const float inv = sval == 0.f ? 0.f : __fdiv_rn(g, sval);
+    uint32_t scode;
+    float inv;
+    nvfp4_block_scale(amax, g, &scode, &inv);
     float y[2][8];
 #pragma unroll
     for (int i = 0; i < 16; ++i) y[i / 8][i % 8] = __fmul_rn(v[i], inv);
@@ -97,6 +94,21 @@ __global__ void __launch_bounds__(kQThreads) nvfp4_quantize_kernel(
 }
 
 }  // namespace
+
+// The tensor amax into *amax_bits (as float bits; the caller zeroes it first).
+void nvfp4_amax_launch(const void* in, moe_dtype_t dtype, long long elems, uint32_t* amax_bits,
+                       cudaStream_t stream, int sms) {
+  const long long n16 = elems * (dtype == MOE_BF16 ? 2 : 4) / 16;
+  const long long g1 = (n16 + kQThreads - 1) / kQThreads;
+  const int grid = static_cast<int>(g1 < 1 ? 1 : (g1 < sms * 8 ? g1 : sms * 8));
+  if (dtype == MOE_BF16)
+    launch_pdl(nvfp4_amax_kernel<uint16_t>, grid, kQThreads, 0, stream, static_cast<const uint8_t*>(in), n16,
+               amax_bits);
+  else
+    launch_pdl(nvfp4_amax_kernel<float>, grid, kQThreads, 0, stream, static_cast<const uint8_t*>(in), n16,
+               amax_bits);
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -126,17 +138,15 @@ extern "C" moe_status_t moe_quantize_nvfp4(const void* in, moe_dtype_t in_dtype,
   const long long n16 = elems * eb / 16;
   const long long nblk = elems / 16;
   const uint8_t* src = static_cast<const uint8_t*>(in);
-  const long long g1 = (n16 + kQThreads - 1) / kQThreads, g2 = (nblk + kQThreads - 1) / kQThreads;
-  const int grid1 = static_cast<int>(g1 < 1 ? 1 : (g1 < sms * 8 ? g1 : sms * 8));
+  (void)n16;
+  const long long g2 = (nblk + kQThreads - 1) / kQThreads;
   const int grid2 = static_cast<int>(g2 < 1 ? 1 : (g2 < sms * 8 ? g2 : sms * 8));
-  if (in_dtype == MOE_BF16) {
-    launch_pdl(nvfp4_amax_kernel<uint16_t>, grid1, kQThreads, 0, stream, src, n16, amax_bits);
+  nvfp4_amax_launch(in, in_dtype, elems, amax_bits, stream, sms);
+  if (in_dtype == MOE_BF16)
     launch_pdl(nvfp4_quantize_kernel<uint16_t>, grid2, kQThreads, 0, stream, src, nblk,
                static_cast<const uint32_t*>(amax_bits), codes, scales, tensor_scale);
-  } else {
-    launch_pdl(nvfp4_amax_kernel<float>, grid1, kQThreads, 0, stream, src, n16, amax_bits);
+  else
     launch_pdl(nvfp4_quantize_kernel<float>, grid2, kQThreads, 0, stream, src, nblk,
                static_cast<const uint32_t*>(amax_bits), codes, scales, tensor_scale);
-  }
   return check_launch(fn);
 }

@@ -35,7 +35,8 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
                             const int32_t* topk_idx, int k, int E, const int32_t* counts,
                             int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
                             moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
-                            int32_t* dev_status, cudaStream_t stream, int sms);
+                            int32_t* dev_status, cudaStream_t stream, int sms,
+                            const uint32_t* amax_bits, float* tensor_scale);
 size_t permute_hist_bytes(int T, int E);
 
 namespace {
@@ -92,5 +93,5 @@ extern "C" moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, 
   int32_t* scratch = scratch_on_current_device();
   if (!scratch) return MOE_ERR_CUDA;
   return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp,
-                        xp_dtype, xp_scales, scratch, dev_status, stream, sms);
+                        xp_dtype, xp_scales, scratch, dev_status, stream, sms, nullptr, nullptr);
 }

@@ -71,7 +71,7 @@ class MoELayer:
             # each of W1, W2, Xp, H is one NVFP4 tensor (one fp32 tensor scale)
             self.W1q, self.W1s, self.W1g = B.moe_quantize_nvfp4(W1)
             self.W2q, self.W2s, self.W2g = B.moe_quantize_nvfp4(W2)
-            self.xp = torch.empty(M, d, dtype=store, device=dev)
+            self.xp = None                         # the dispatch writes NVFP4 rows only
             self.xq, self.xs = torch.empty(M, d // 2, **u8), torch.empty(M, d // 16, **u8)
             self.xg = torch.empty(2, dtype=torch.float32, device=dev)
             self.hq, self.hs = torch.empty(M, f // 2, **u8), torch.empty(M, f // 16, **u8)
@@ -128,10 +128,9 @@ class MoELayer:
 
     def dispatch(self, x):
         if self.dtype == "nvfp4":
-            B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
-                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
-                          workspace=self.workspace, dev_status=self.dev_status)
-            B.moe_quantize_nvfp4(self.xp, codes=self.xq, scales=self.xs, tensor_scale=self.xg)
+            B.moe_permute_nvfp4(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
+                                dest_row=self.dest_row, src_pair=self.src_pair, codes=self.xq, scales=self.xs,
+                                tensor_scale=self.xg, workspace=self.workspace, dev_status=self.dev_status)
         elif self.dtype == "mxfp8" and self.training:
             # bf16 Xp (kept for the weight gradient), then both MXFP8 forms of it
             B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
@@ -195,7 +194,7 @@ class MoELayer:
         scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
         MXFP8 training adds the row- and column-wise quantisation of Xp and of H."""
         route = 1 if self.w_router is not None else 2     # fused router GEMM (counts zeroed by a memset)
-        nv = 4 if self.dtype == "nvfp4" else 0            # amax + quantise, of Xp and of H
+        nv = 3 if self.dtype == "nvfp4" else 0            # amax of x; amax + quantise of H
         return route + 2 + 2 + 1 + nv + (4 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:

@@ -152,3 +152,21 @@ def test_nvfp4_layer_scaled():
     assert layer.hg[0].item() == float(g)
     assert (layer.hs.cpu().numpy() == s).all() and (layer.hq.cpu().numpy() == c).all()
     assert rel_l2(f64(y), ref["y"]) < 5e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("T,d,E,k", [(300, 256, 8, 2), (1000, 512, 64, 8), (77, 48, 4, 3)])
+def test_permute_nvfp4_equals_permute_then_quantize(dtype, T, d, E, k):
+    """The fused NVFP4 dispatch writes, bit for bit, the NVFP4 of the rows moe_permute
+    writes (and the same maps), which the quantiser tests pin to the oracle."""
+    need_gpu()
+    w = W.BY_NAME["qwen3-235b-bf16"].scaled(T=T, E=E, k=k, d=d, name="fp4-perm")
+    x = W.make_x(w, "cuda").to(dtype)
+    idx, wt, counts = moe_gpu.moe_route_topk(logits_dev(w), k)
+    ref = moe_gpu.moe_permute(x, idx, counts, E)
+    rc, rs, rg = moe_gpu.moe_quantize_nvfp4(ref["xp"])
+    out = moe_gpu.moe_permute_nvfp4(x, idx, counts, E)
+    for key in ("offsets", "dest_row", "src_pair"):
+        assert torch.equal(out[key], ref[key]), key
+    assert out["tensor_scale"][0].item() == rg[0].item()
+    assert torch.equal(out["codes"], rc) and torch.equal(out["scales"], rs)
