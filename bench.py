@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -104,7 +105,9 @@ class Clocks:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.p = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples: MOE_CLOCKS_DIR if set (to keep them), else the temp directory
+        self.path = os.path.join(os.environ.get("MOE_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"clocks_{os.getpid()}.csv")
 
     def start(self):
         try:

@@ -23,7 +23,7 @@ The pages give no formulas.  Every step below is the plainest definition that
 matches them; the readings (softmax scoring with renormalised top-k weights,
 lower expert id wins ties, (expert, token) ordering of the permuted rows,
 SwiGLU experts with gate rows first, routing weight applied in combine) are
-listed in DESIGN.md.
+stated where each function uses them.
 
 Arrays are numpy; floating-point inputs are the exact stored values (bf16 or
 fp32) widened to float64, and all arithmetic is float64.

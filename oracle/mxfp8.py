@@ -16,7 +16,7 @@ NaN), and its FP32 -> MX conversion: shared exponent
 ``X = floor(log2(max_i |V_i|)) - emax_elem`` with ``emax_elem = 8`` for E4M3,
 element codes ``P_i = RNE(V_i / 2^X)`` clamped to the largest normal.
 
-Readings taken where the definition is silent (each listed in the design doc):
+Readings taken where the definition is silent (each also listed with the design's other readings):
 * an all-zero block (amax == 0) gets scale byte 127 (2^0) and zero codes;
 * X is clamped to the E8M0 range [-127, 127];
 * the sign of a zero is kept (-0 encodes as 0x80);

@@ -13,9 +13,8 @@ mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), a block of 16 consecutive
 elements sharing one FP8 E4M3 scale, and a second, fp32 scale for the whole
 tensor so that the block scales use the E4M3 range.
 
-Readings taken where the description leaves the arithmetic open (each listed in
-the design doc), written so that every rounding that decides a code happens in fp32,
-in this order, on both sides:
+Readings taken where the description leaves the arithmetic open, written so that
+every rounding that decides a code happens in fp32, in this order, on both sides:
 * tensor encode scale g = 2688 / amax(tensor) (2688 = 448 * 6, the largest E4M3
   times the largest E2M1), one fp32 division; an all-zero tensor gets g = 1;
 * block scale: s = E4M3(fp32(fp32(amax_block / 6) * g)), round to nearest even,
