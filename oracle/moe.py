@@ -456,6 +456,29 @@ def token_backward(x_t, logits_t, dy_t, W1, W2, k, renormalize=True):
     return dx, dl
 
 
+def expert_backward_mxfp8(X_e, dYp_e, w1, w2):
+    """Forward and backward of one expert on MXFP8 operands, from its own rows X_e
+    [c, d] and upstream dYp_e [c, d]; w1 [2f, d], w2 [d, f].  Every quantisation
+    of the layer's MXFP8 step is local to the expert: row-wise blocks lie in a row,
+    the weights' blocks in the expert's own weights, and the column-wise blocks of
+    the weight gradients restart at the group's first row, which is X_e's first.
+    Returns GU, H, dGU, dXp, dW1, dW2 (the same values ``layer_backward`` with
+    ``mxfp8_operands`` gives for this expert)."""
+    X = np.asarray(X_e, dtype=np.float64)
+    dY = np.asarray(dYp_e, dtype=np.float64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    one = np.array([0, X.shape[0]])
+    GU = mx_roundtrip(X) @ mx_roundtrip(w1).T
+    H = swiglu(GU)
+    dH = mx_roundtrip(dY) @ mx_roundtrip_dim1(w2[None])[0]
+    dGU = dswiglu(dH, GU)
+    dXp = mx_roundtrip(dGU) @ mx_roundtrip_dim1(w1[None])[0]
+    dW2 = mx_roundtrip_colwise(dY, one).T @ mx_roundtrip_colwise(H, one)
+    dW1 = mx_roundtrip_colwise(dGU, one).T @ mx_roundtrip_colwise(X, one)
+    return dict(GU=GU, H=H, dGU=dGU, dXp=dXp, dW1=dW1, dW2=dW2)
+
+
 def expert_wgrad_sampled(X_e, dYp_e, w1, w2, w1_rows, w2_cols):
     """Selected rows of dW1[e] and columns of dW2[e] for one expert, from its own
     rows X_e [c, d] and upstream dYp_e [c, d]; w1 [2f, d], w2 [d, f].

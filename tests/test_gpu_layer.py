@@ -310,3 +310,38 @@ def test_train_full_size_sampled():
     e_t = torch.from_numpy(empty).cuda()
     assert int(torch.count_nonzero(layer.dW1[e_t]).item()) == 0
     assert int(torch.count_nonzero(layer.dW2[e_t]).item()) == 0
+
+
+def test_mxfp8_train_full_size_sampled():
+    """The DeepSeek-V3-shaped MXFP8 training step at full size: maps in full, and for
+    the median, the smallest non-empty and an upper-quartile expert the whole MXFP8
+    chain of that expert (every quantisation in it is local to the expert) against
+    dGU, dXp, dW1 and dW2; experts without rows get exact zero gradients."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-mxfp8-train"]
+    layer, x, W1, W2, lg = _build(w, training=True)
+    dy = W.make_dy(w, "cuda")
+    layer.forward(x, lg)
+    layer.backward(dy, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    lg_h = lg.cpu().numpy()
+    idx, wt, counts = om.route_topk(lg_h, w.k)
+    offsets, dest, src = om.permute_maps(idx, w.E)
+    assert (i64(layer.offsets) == offsets).all() and (i64(layer.src_pair) == src).all()
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    for e in (int(order[len(order) // 2]), int(order[0]), int(order[(3 * len(order)) // 4])):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        pairs = src[lo:hi]
+        tok = torch.from_numpy(pairs // w.k).cuda()
+        X_e = f64(x[tok])
+        dYp_e = wt[pairs // w.k, pairs % w.k][:, None] * f64(dy[tok])
+        ref = om.expert_backward_mxfp8(X_e, dYp_e, f64(W1[e]), f64(W2[e]))
+        for name, got in (("dGU", layer.dgu[lo:hi]), ("dXp", layer.dxp[lo:hi]), ("dW1", layer.dW1[e]),
+                          ("dW2", layer.dW2[e])):
+            err = rel_l2(f64(got), ref[name])
+            assert err < TOL_MXFP8, (e, hi - lo, name, err)
+    e_t = torch.from_numpy(np.nonzero(counts == 0)[0]).cuda()
+    assert int(torch.count_nonzero(layer.dW1[e_t]).item()) == 0
+    assert int(torch.count_nonzero(layer.dW2[e_t]).item()) == 0

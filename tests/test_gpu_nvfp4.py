@@ -170,3 +170,56 @@ def test_permute_nvfp4_equals_permute_then_quantize(dtype, T, d, E, k):
         assert torch.equal(out[key], ref[key]), key
     assert out["tensor_scale"][0].item() == rg[0].item()
     assert torch.equal(out["codes"], rc) and torch.equal(out["scales"], rs)
+
+
+def test_nvfp4_layer_full_size_by_stage():
+    """The DeepSeek-V3-shaped NVFP4 layer at full size, stage by stage on samples: the
+    tensor scale of Xp (from the amax of x) and the codes of sampled Xp rows; W1 and W2
+    codes of sampled experts (their tensor scale from the amax of the whole stack);
+    sampled rows of H and Yp against the oracle on the decoded operands; and H
+    re-quantised by the oracle from the GPU's bf16 H (its tensor scale from all of H)."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-nvfp4"]
+    x, W1, W2, lg = W.make_x(w, "cuda"), W.make_w1(w, "cuda"), W.make_w2(w, "cuda"), logits_dev(w)
+    layer = moe_gpu.MoELayer(w.T, w.d, w.E, w.k, w.f, W1, W2, dtype="nvfp4", renormalize=w.renormalize)
+    layer.forward(x, lg)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    rng = np.random.default_rng(17)
+    idx, wt, counts = om.route_topk(lg.cpu().numpy(), w.k)
+    offsets, dest, src = om.permute_maps(idx, w.E)
+    assert (i64(layer.src_pair) == src).all()
+    gx = o4.tensor_scale(x.float().cpu().numpy())
+    assert layer.xg[0].item() == float(gx)
+    rows = np.sort(rng.choice(w.M, size=64, replace=False))
+    c, s, _ = o4.quantize(x[torch.from_numpy(src[rows] // w.k).cuda()].float().cpu().numpy(), gx)
+    r_t = torch.from_numpy(rows).cuda()
+    assert (layer.xq[r_t].cpu().numpy() == c).all() and (layer.xs[r_t].cpu().numpy() == s).all()
+    # the weight stacks' tensor scales from their amax (a torch reduction of the inputs)
+    g1 = np.float32(2688.0) / np.float32(W1.abs().max().float().item())
+    g2 = np.float32(2688.0) / np.float32(W2.abs().max().float().item())
+    assert layer.W1g[0].item() == float(g1) and layer.W2g[0].item() == float(g2)
+    h_all = layer.h.float().cpu().numpy()
+    gh = o4.tensor_scale(h_all)
+    assert layer.hg[0].item() == float(gh)
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    got_h, want_h, got_y, want_y = [], [], [], []
+    for e in (int(order[-1]), int(order[len(order) // 2]), int(order[0])):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        c1, s1, _ = o4.quantize(W1[e].float().cpu().numpy(), g1)
+        assert (layer.W1q[e].cpu().numpy() == c1).all() and (layer.W1s[e].cpu().numpy() == s1).all()
+        c2, s2, _ = o4.quantize(W2[e].float().cpu().numpy(), g2)
+        assert (layer.W2q[e].cpu().numpy() == c2).all() and (layer.W2s[e].cpu().numpy() == s2).all()
+        rr = np.sort(rng.choice(np.arange(lo, hi), size=min(8, hi - lo), replace=False))
+        rr_t = torch.from_numpy(rr).cuda()
+        xa = o4.dequantize(layer.xq[rr_t].cpu().numpy(), layer.xs[rr_t].cpu().numpy(), gx)
+        gu = xa @ o4.dequantize(c1, s1, g1).T
+        got_h.append(h_all[rr])
+        want_h.append(om.swiglu(gu))
+        hc, hs, _ = o4.quantize(h_all[rr], gh)                      # the oracle's own quantisation of H
+        assert (layer.hq[rr_t].cpu().numpy() == hc).all() and (layer.hs[rr_t].cpu().numpy() == hs).all()
+        got_y.append(f64(layer.yp[rr_t]))
+        want_y.append(o4.dequantize(hc, hs, gh) @ o4.dequantize(c2, s2, g2).T)
+    assert rel_l2(np.concatenate(got_h), np.concatenate(want_h)) < 1e-2
+    assert rel_l2(np.concatenate(got_y), np.concatenate(want_y)) < 1e-2

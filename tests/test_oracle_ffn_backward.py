@@ -282,3 +282,24 @@ def test_nvfp4_layer_forward_close_to_exact_and_exact_on_representable_operands(
     W1r, W2r = rep((E, 2 * f, d)), rep((E, d, f))
     assert np.array_equal(moe.nvfp4_roundtrip(W1r), W1r)
     assert np.array_equal(nvfp4.dequantize(*nvfp4.quantize(W2r.reshape(-1, f))).reshape(W2r.shape), W2r)
+
+
+def test_expert_backward_mxfp8_matches_layer_backward():
+    """The per-expert MXFP8 backward (used to check full-size layers expert by expert)
+    equals the whole-layer MXFP8 backward restricted to each expert."""
+    T, d, E, k, f = 60, 64, 4, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=101)
+    dy = np.random.default_rng(102).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=True)
+    bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k, mxfp8_operands=True)
+    off = fwd["offsets"]
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        got = moe.expert_backward_mxfp8(fwd["Xp"][lo:hi], bwd["dYp"][lo:hi], W1[e], W2[e])
+        np.testing.assert_allclose(got["GU"], fwd["GU"][lo:hi], rtol=1e-12, atol=1e-13)
+        for name in ("dGU", "dXp"):
+            np.testing.assert_allclose(got[name], bwd[name][lo:hi], rtol=1e-12, atol=1e-13, err_msg=name)
+        np.testing.assert_allclose(got["dW1"], bwd["dW1"][e], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(got["dW2"], bwd["dW2"][e], rtol=1e-12, atol=1e-13)
