@@ -441,7 +441,7 @@ def router_leg(w, x, lg, layer, pk):
     return {"ms": round(t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
             "frac_of_peak": round(flops / (t_f * 1e-3) / 1e12 / peak, 4),
             "route_from_logits_ms": round(t_p, 4), "logits_bytes_not_written": w.T * w.E * 4,
-            "timing": "eager, 20 calls; the tile is 128 tokens x 256 expert columns (E padded to 256)"}
+            "timing": "eager, 20 calls; the tile is 128 tokens x E expert columns (E rounded up to 16)"}
 
 
 def capacity_leg(w, x, lg, layer, W1, W2, cf, dropless_ms):

@@ -199,6 +199,7 @@ struct Params {
   int32_t* counts;         //   [N] tokens per expert (zeroed by the host entry)
   int k_sel;               //   experts per token (<= kTopkMax)
   int renorm;              //   softmax over the selected logits (1) or over all (0)
+  int n_mma;               //   MMA width: E rounded up to 16 (the B tile holds that many rows)
 };
 
 // Rows of group e.  Without an offsets array the problem is one dense group of M rows.
@@ -553,7 +554,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           uint8_t* sa = tiles + stage * C::kStage;
           uint8_t* sb = sa + kAStage;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, kStageBytes + (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
+          mbar_arrive_expect_tx(bar, (kEpi == kEpiTopk ? kAStage + p.n_mma * kBKBytes : kStageBytes) +
+                                         (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
                                          (kKind == 3 ? kNvAtomBytes : 0));
           if (kMode == kFwd) {
             const int kx = kb * (kBKBytes / eb);
@@ -601,9 +603,11 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = kKind == 3 ? make_idesc_nvf4(kBM, BN)
-                               : C::kMx ? make_idesc_mx(kBM, BN) | (kMode == kWgrad ? (3u << 15) : 0u)
-                                      : make_idesc<kKind>(kBM, kBN, kMode == kWgrad, kMode != kFwd);
+    // the router's MMA is only as wide as its (16-rounded) expert count
+    const uint32_t idesc = kKind == 3 ? make_idesc_nvf4(kBM, BN)
+                           : C::kMx ? make_idesc_mx(kBM, BN) | (kMode == kWgrad ? (3u << 15) : 0u)
+                                    : make_idesc<kKind>(kBM, kEpi == kEpiTopk ? p.n_mma : kBN, kMode == kWgrad,
+                                                        kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
@@ -1587,12 +1591,13 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
   const uint64_t adims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(T)};
   const uint32_t abox[2] = {bk, kBM};
   const uint64_t bdims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(E), 1};
-  const uint32_t bbox[3] = {bk, kBN, 1};           // rows past E read as zeros
+  const int n_mma = ((E + 15) / 16) * 16;          // MMA width: E rounded up to 16
+  const uint32_t bbox[3] = {bk, static_cast<uint32_t>(n_mma), 1};   // rows past E read as zeros
   if (!make_map(&ta, map_type(dtype), eb, x, 2, adims, abox) ||
       !make_map(&tb, map_type(dtype), eb, w_router, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
   Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr, nullptr, nullptr,
-           topk_idx, topk_w, counts, k, renormalize ? 1 : 0};
+           topk_idx, topk_w, counts, k, renormalize ? 1 : 0, n_mma};
   if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
   return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
 }
