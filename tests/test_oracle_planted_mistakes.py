@@ -151,3 +151,29 @@ def test_nvfp4_pins_catch_planted_mistake(monkeypatch, attr, fake, check):
     monkeypatch.setattr(nvfp4, attr, fake)
     with pytest.raises(AssertionError):
         check()
+
+
+_real_capacity = moe.permute_capacity
+
+
+def _capacity_keeps_last(idx, E, C):
+    """Keeps each expert's last C tokens instead of its first C."""
+    T, k = np.asarray(idx).shape
+    rev = np.asarray(idx)[::-1]
+    off, dest, src = _real_capacity(rev, E, C)
+    dest = dest[::-1].copy()
+    src = np.where(src >= 0, (T - 1 - src // k) * k + src % k, -1)
+    return off, dest, src
+
+
+@pytest.mark.parametrize("attr,fake,check", [
+    # features paired in reverse order (x[t, d-1-i] with W_r[e, i])
+    ("router_logits", lambda x, w: np.asarray(x, dtype=np.float64)[:, ::-1] @ np.asarray(w, dtype=np.float64).T,
+     lambda: route_pins.test_router_logits_bruteforce_and_one_hot()),
+    ("permute_capacity", _capacity_keeps_last,
+     lambda: route_pins.test_capacity_keeps_first_tokens_and_drops_the_rest()),
+], ids=["router-reversed-features", "capacity-keeps-last"])
+def test_router_and_capacity_pins_catch_planted_mistake(monkeypatch, attr, fake, check):
+    monkeypatch.setattr(moe, attr, fake)
+    with pytest.raises(AssertionError):
+        check()
