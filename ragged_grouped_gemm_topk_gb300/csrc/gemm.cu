@@ -1058,6 +1058,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           ti[j] = -1;
         }
         float run_m = -INFINITY, run_s = 0.f;
+        const bool full_softmax = p.renorm == 0;
         bool nan = false;
         float* lout = static_cast<float*>(p.out);
 #pragma unroll 1
@@ -1089,13 +1090,15 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
                 nan = true;
                 x = -INFINITY;
               }
-              if (x == -INFINITY) {
-                // masked expert: no softmax mass
-              } else if (x > run_m) {
-                run_s = run_s * expf(run_m - x) + 1.f;
-                run_m = x;
-              } else {
-                run_s += expf(x - run_m);
+              if (full_softmax) {             // only the full-softmax weights need the sum
+                if (x == -INFINITY) {
+                  // masked expert: no softmax mass
+                } else if (x > run_m) {
+                  run_s = run_s * expf(run_m - x) + 1.f;
+                  run_m = x;
+                } else {
+                  run_s += expf(x - run_m);
+                }
               }
               if (x > tv[kTopkMax - 1] || ti[kTopkMax - 1] < 0) {
                 // insert (x, col + i) keeping the list sorted; strict compares keep
