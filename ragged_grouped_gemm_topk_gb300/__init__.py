@@ -1,8 +1,11 @@
 """GB300-native (sm_103a) hot path of dropless Mixture-of-Experts training.
 
 Route -> dispatch -> group-aware MXFP8 quantisation -> ragged grouped GEMM with
-fused SwiGLU -> combine, and its backward, as hand-written CUDA kernels behind
-the C ABI of include/moe.h (libmoe.so).  This package is the thin Python side:
+fused SwiGLU -> combine, and its backward (bf16, or every GEMM on MXFP8 operands),
+as hand-written CUDA kernels behind the C ABI of include/moe.h (libmoe.so); also
+an NVFP4 forward, the router GEMM fused with the top-k selection, and a
+capacity-based (drop/pad) dispatch as the contrast to dropless routing.  This
+package is the thin Python side:
 ``build`` compiles the library, ``binding`` exposes each C entry point under
 the same name, ``layer`` chains them into a layer, ``workloads`` draws seeded
 synthetic inputs.
