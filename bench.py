@@ -363,6 +363,7 @@ def run_ours(args, world, rank, local):
                 "hbm_gbs": round(g1_bytes / g1_s / 1e9, 1), "bytes_per_launch": round(g1_bytes),
                 "experts_with_tokens": e_used}
     perm_b, comb_b = stage_bytes(w)
+    g_disp, g_comb = graph_stage_ms(w, layer, x)
     launches = layer.launches_per_forward() + (layer.launches_per_backward() if w.backward else 0)
     traffic = gemm1_traffic(w.name)
     line = {
@@ -377,12 +378,20 @@ def run_ours(args, world, rank, local):
                    "l2": l2_note(W1, W2),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "stages_ms": {k: round(v, 4) for k, v in per.items()},   # eager pass, events between stages
-        "permute_gbs": round(perm_b / (per["dispatch"] * 1e-3) / 1e9, 1),
-        "combine_gbs": round(comb_b / (per["combine"] * 1e-3) / 1e9, 1),
+        "permute_gbs": round(perm_b / (g_disp * 1e-3) / 1e9, 1),
+        "combine_gbs": round(comb_b / (g_comb * 1e-3) / 1e9, 1),
+        "bandwidth_stages": {
+            "timing": "each stage replayed 20x in one CUDA graph (programmatic dependent launch between "
+                      "replays, as inside the step's graph) over rotating input/output buffer sets larger "
+                      "than L2 in total; eager = the stage between events in the eager pass",
+            "dispatch_ms": round(g_disp, 4), "combine_ms": round(g_comb, 4),
+            "dispatch_ms_eager": round(per["dispatch"], 4), "combine_ms_eager": round(per["combine"], 4),
+            "hbm_frac_permute_eager": round(perm_b / (per["dispatch"] * 1e-3) / 1e9 / pk["hbm"], 4),
+            "hbm_frac_combine_eager": round(comb_b / (per["combine"] * 1e-3) / 1e9 / pk["hbm"], 4)},
         "roofline": {"kernel": "grouped GEMM1 (gate+up, fused SwiGLU)", **roof,
                      "traffic": traffic,
-                     "hbm_frac_permute": round(perm_b / (per["dispatch"] * 1e-3) / 1e9 / pk["hbm"], 4),
-                     "hbm_frac_combine": round(comb_b / (per["combine"] * 1e-3) / 1e9 / pk["hbm"], 4)},
+                     "hbm_frac_permute": round(perm_b / (g_disp * 1e-3) / 1e9 / pk["hbm"], 4),
+                     "hbm_frac_combine": round(comb_b / (g_comb * 1e-3) / 1e9 / pk["hbm"], 4)},
         "clocks": clk,
         "gpu_launches": launches * args.steps,
         "wall_s_timed": round(wall, 3),
@@ -396,6 +405,81 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=12.0)
     return line
+
+
+def graph_stage_ms(w, layer, x, reps=20):
+    """Device time of the dispatch and the combine stage as the step's graph runs them:
+    each stage captured `reps` times in one CUDA graph (consecutive launches chained by
+    programmatic dependent launch) over rotating sets of its input and output buffers,
+    so that the sets together exceed L2 and every replay reads cold data."""
+    import torch
+    import ragged_grouped_gemm_topk_gb300 as pkg
+    dev = x.device
+    M, d = w.M, w.d
+    es = x.element_size()
+    set_bytes = w.T * d * es + M * d * es
+    nbuf = max(2, int(math.ceil(3 * L2_BYTES / set_bytes)))
+    nbuf = min(nbuf, reps)
+    xs = [x] + [x.clone() for _ in range(nbuf - 1)]
+    i32 = dict(dtype=torch.int32, device=dev)
+    maps = [dict(offsets=torch.empty(w.E + 1, **i32), dest_row=torch.empty(w.T, w.k, **i32),
+                 src_pair=torch.empty(M, **i32)) for _ in range(nbuf)]
+    u8 = dict(dtype=torch.uint8, device=dev)
+    if w.dtype == "nvfp4":
+        outs = [dict(codes=torch.empty(M, d // 2, **u8), scales=torch.empty(M, d // 16, **u8),
+                     tensor_scale=torch.empty(2, dtype=torch.float32, device=dev)) for _ in range(nbuf)]
+        def disp(i):
+            pkg.moe_permute_nvfp4(xs[i], layer.topk_idx, layer.counts, w.E, workspace=layer.workspace,
+                                  dev_status=layer.dev_status, **maps[i], **outs[i])
+    elif w.dtype == "mxfp8" and not w.backward:
+        outs = [dict(xp=torch.empty(M, d, **u8), xp_scales=torch.empty(M, d // 32, **u8)) for _ in range(nbuf)]
+        def disp(i):
+            pkg.moe_permute(xs[i], layer.topk_idx, layer.counts, w.E, xp_dtype="mxfp8", workspace=layer.workspace,
+                            dev_status=layer.dev_status, **maps[i], **outs[i])
+    else:
+        outs = [dict(xp=torch.empty(M, d, dtype=x.dtype, device=dev)) for _ in range(nbuf)]
+        if w.dtype == "mxfp8":       # training: bf16 rows, then both MXFP8 forms of them
+            q = [dict(rc=torch.empty(M, d, **u8), rs=torch.empty(M, d // 32, **u8), cc=torch.empty(M, d, **u8),
+                      cs=torch.empty(((M + 127) // 128 + w.E) * (d // 128), 512, **u8)) for _ in range(nbuf)]
+        def disp(i):
+            pkg.moe_permute(xs[i], layer.topk_idx, layer.counts, w.E, workspace=layer.workspace,
+                            dev_status=layer.dev_status, **maps[i], **outs[i])
+            if w.dtype == "mxfp8":
+                pkg.moe_quantize_mxfp8_grouped(outs[i]["xp"], codes=q[i]["rc"], scales=q[i]["rs"])
+                pkg.moe_quantize_mxfp8_grouped(outs[i]["xp"], maps[i]["offsets"], w.E, codes=q[i]["cc"],
+                                               scales=q[i]["cs"], axis=2)
+    yps = [layer.yp] + [layer.yp.clone() for _ in range(nbuf - 1)]
+    ys = [torch.empty(w.T, d, dtype=layer.yp.dtype, device=dev) for _ in range(nbuf)]
+    def comb(i):
+        pkg.moe_unpermute_combine(yps[i], layer.dest_row, layer.topk_w, out=ys[i], dev_status=layer.dev_status)
+
+    def timed(fn):
+        for i in range(nbuf):                    # warm: every buffer set once, outside capture
+            fn(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn(0)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for r in range(reps):
+                fn(r % nbuf)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    t_d, t_c = timed(disp), timed(comb)
+    if int(layer.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.dev_status.item())} after the stage graphs")
+    return t_d, t_c
 
 
 def l2_note(W1, W2):
