@@ -45,6 +45,14 @@ def test_binding_declares_every_symbol():
     assert sorted(_lib.SIGNATURES) == _declared()
 
 
+def test_python_binding_has_every_entry_point_by_name():
+    """One Python function per C entry point, same name (the error-string accessor
+    is internal: failures surface as MoeError carrying its text)."""
+    from ragged_grouped_gemm_topk_gb300 import binding
+    missing = [n for n in _declared() if n != "moe_last_error_string" and not callable(getattr(binding, n, None))]
+    assert not missing, missing
+
+
 def test_host_only_calls(lib):
     lib.moe_version.restype = ctypes.c_int
     assert lib.moe_version() >= 0x100

@@ -61,6 +61,13 @@ def test_noalloc_matches_workspace_entry_point_twice(quant):
         assert torch.equal(got["xp"].view(torch.uint8), want["xp"].view(torch.uint8))
         if quant:
             assert torch.equal(got["xp_scales"], want["xp_scales"])
+        # the same entry point through the Python binding
+        st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        got2 = B.moe_permute_noalloc(x, idx, counts, w.E, xp_dtype="mxfp8" if quant else None, dev_status=st2)
+        torch.cuda.synchronize()
+        assert int(st2.item()) == 0
+        for key in ("offsets", "dest_row", "src_pair", "xp") + (("xp_scales",) if quant else ()):
+            assert torch.equal(got2[key].view(torch.uint8), want[key].view(torch.uint8)), key
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
