@@ -145,14 +145,13 @@ class Clocks:
 
 def stage_bytes(w):
     """Algorithmic bytes of the bandwidth stages (each moved once).  The MXFP8
-    training dispatch writes Xp in bf16 and in both MXFP8 forms (row-wise codes +
-    scales, column-wise codes + scales): x read once, the three outputs written
-    once."""
+    training dispatch writes both MXFP8 forms of Xp (row-wise codes + scales,
+    column-wise codes + scales): x read once, the two outputs written once."""
     s = 4 if w.dtype == "f32" else 2
     if w.dtype == "nvfp4":                      # NVFP4 codes + scales (x read twice: amax, scatter)
         xp_out = w.M * w.d * (0.5 + 1 / 16)
     elif w.dtype == "mxfp8" and w.backward:
-        xp_out = w.M * w.d * (2 + 2 * (1 + 1 / 32))
+        xp_out = w.M * w.d * 2 * (1 + 1 / 32)
     elif w.dtype == "mxfp8":
         xp_out = w.M * w.d * (1 + 1 / 32)
     else:
@@ -431,23 +430,22 @@ def graph_stage_ms(w, layer, x, reps=20):
         def disp(i):
             pkg.moe_permute_nvfp4(xs[i], layer.topk_idx, layer.counts, w.E, workspace=layer.workspace,
                                   dev_status=layer.dev_status, **maps[i], **outs[i])
-    elif w.dtype == "mxfp8" and not w.backward:
+    elif w.dtype == "mxfp8":
         outs = [dict(xp=torch.empty(M, d, **u8), xp_scales=torch.empty(M, d // 32, **u8)) for _ in range(nbuf)]
+        if w.backward:               # training: and the column-wise form, gathered from x
+            q = [dict(codes=torch.empty(M, d, **u8),
+                      scales=torch.empty(((M + 127) // 128 + w.E) * (d // 128), 512, **u8)) for _ in range(nbuf)]
         def disp(i):
             pkg.moe_permute(xs[i], layer.topk_idx, layer.counts, w.E, xp_dtype="mxfp8", workspace=layer.workspace,
                             dev_status=layer.dev_status, **maps[i], **outs[i])
+            if w.backward:
+                pkg.moe_quantize_mxfp8_gathered(xs[i], maps[i]["src_pair"], maps[i]["offsets"], w.E, w.k, axis=2,
+                                                dev_status=layer.dev_status, **q[i])
     else:
         outs = [dict(xp=torch.empty(M, d, dtype=x.dtype, device=dev)) for _ in range(nbuf)]
-        if w.dtype == "mxfp8":       # training: bf16 rows, then both MXFP8 forms of them
-            q = [dict(rc=torch.empty(M, d, **u8), rs=torch.empty(M, d // 32, **u8), cc=torch.empty(M, d, **u8),
-                      cs=torch.empty(((M + 127) // 128 + w.E) * (d // 128), 512, **u8)) for _ in range(nbuf)]
         def disp(i):
             pkg.moe_permute(xs[i], layer.topk_idx, layer.counts, w.E, workspace=layer.workspace,
                             dev_status=layer.dev_status, **maps[i], **outs[i])
-            if w.dtype == "mxfp8":
-                pkg.moe_quantize_mxfp8_grouped(outs[i]["xp"], codes=q[i]["rc"], scales=q[i]["rs"])
-                pkg.moe_quantize_mxfp8_grouped(outs[i]["xp"], maps[i]["offsets"], w.E, codes=q[i]["cc"],
-                                               scales=q[i]["cs"], axis=2)
     yps = [layer.yp] + [layer.yp.clone() for _ in range(nbuf - 1)]
     ys = [torch.empty(w.T, d, dtype=layer.yp.dtype, device=dev) for _ in range(nbuf)]
     def comb(i):

@@ -213,6 +213,24 @@ moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, in
                                         uint8_t* codes, uint8_t* scales,
                                         cudaStream_t stream);
 
+/* Column-wise, group-aware MXFP8 of the dispatched rows without materialising them
+ * (MXFP8 training: the weight gradient of GEMM1 reads Xp column-wise, and nothing
+ * else needs Xp in bf16 once the dispatch writes its row-wise MXFP8 form).  The
+ * rows are Xp[r] = x[src_pair[r] / k], r < T*k, as moe_permute would write them;
+ * the result equals moe_quantize_mxfp8_grouped (axis 1 or 2) of that Xp, bit for
+ * bit ([1] "What dropless MoE needs": grouped quantisation of the expert inputs).
+ *   x         [T, K] MOE_BF16 or MOE_F32 token rows, 16-byte aligned; K % 32 == 0
+ *             (axis 2: K % 128 == 0).
+ *   k         top-k (1..32); src_pair [T*k] and offsets [E+1] from moe_permute.
+ *   axis      1 or 2, codes [T*k, K] and scales as for moe_quantize_mxfp8_grouped.
+ *   dev_status  optional: a src_pair entry outside [0, T*k) sets MOE_DEV_BAD_INDEX
+ *             and its row is quantised as zeros.
+ * MOE_ERR_UNSUPPORTED for any other axis; T == 0 or K == 0 is a no-op. */
+moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x_dtype, int T, int K, int k,
+                                         const int32_t* src_pair, const int32_t* offsets, int E,
+                                         int axis, uint8_t* codes, uint8_t* scales,
+                                         int32_t* dev_status, cudaStream_t stream);
+
 /* Transposed row-wise MXFP8 of a batch of matrices, for weights that a gradient
  * contracts along their first dim (the data gradient contracts B [E, N, K] over N):
  *   in     [G, R, C] MOE_BF16 or MOE_F32, 16-byte aligned; R % 32 == 0, C % 8 == 0.

@@ -15,7 +15,8 @@ from .binding import (moe_check_wait_timeout, moe_grouped_gemm_dgrad, moe_groupe
                       moe_grouped_gemm_fwd, moe_grouped_gemm_fwd_mxfp8_out, moe_grouped_gemm_wgrad,
                       moe_permute, moe_permute_capacity, moe_permute_capacity_workspace_size,
                       moe_permute_noalloc, moe_permute_nvfp4, moe_permute_workspace_size,
-                      moe_quantize_mxfp8_grouped, moe_quantize_mxfp8_transposed, moe_quantize_nvfp4,
-                      moe_route_topk, moe_route_topk_bwd, moe_route_topk_gemm, moe_unpermute_combine,
-                      moe_unpermute_combine_bwd, moe_unpermute_combine_capacity, moe_version, version)
+                      moe_quantize_mxfp8_gathered, moe_quantize_mxfp8_grouped, moe_quantize_mxfp8_transposed,
+                      moe_quantize_nvfp4, moe_route_topk, moe_route_topk_bwd, moe_route_topk_gemm,
+                      moe_unpermute_combine, moe_unpermute_combine_bwd, moe_unpermute_combine_capacity,
+                      moe_version, version)
 from .layer import MoELayer  # noqa: F401

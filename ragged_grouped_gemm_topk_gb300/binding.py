@@ -225,6 +225,27 @@ def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=Non
     return codes, scales
 
 
+def moe_quantize_mxfp8_gathered(x, src_pair, offsets, E, k, *, codes=None, scales=None, axis=2, dev_status=None):
+    """Column-wise group-aware MXFP8 of the dispatched rows Xp[r] = x[src_pair[r] // k]
+    (x [T, K] bf16/fp32; src_pair and offsets from moe_permute) without writing Xp:
+    the codes [T*k, K] and scales of moe_quantize_mxfp8_grouped(Xp, offsets, E, axis)."""
+    T, K = x.shape
+    rows = T * k
+    if axis not in (1, 2):
+        raise ValueError("axis must be 1 or 2")
+    shape = _colwise_scale_shape(rows, K, E, axis)
+    _need(src_pair, "src_pair", _I32, rows)
+    _need(offsets, "offsets", _I32, E + 1)
+    _need(codes, "codes", _U8, rows * K)
+    _need(scales, "scales", _U8, shape[0] * shape[1])
+    _need(dev_status, "dev_status", _I32, 1)
+    codes = codes if codes is not None else torch.empty(rows, K, dtype=_U8, device=x.device)
+    scales = scales if scales is not None else torch.empty(*shape, dtype=_U8, device=x.device)
+    _lib.call("moe_quantize_mxfp8_gathered", _ptr(x), _dt(x), T, K, k, _ptr(src_pair), _ptr(offsets), E, axis,
+              _ptr(codes), _ptr(scales), _ptr(dev_status), _stream())
+    return codes, scales
+
+
 def moe_quantize_mxfp8_transposed(inp, *, codes=None, scales=None):
     """Row-wise MXFP8 of each inp[g]^T for inp [G,R,C] (bf16/fp32) -> (codes u8
     [G,C,R], scales u8 [G*C, R/32])."""

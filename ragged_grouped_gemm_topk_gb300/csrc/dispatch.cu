@@ -368,12 +368,19 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
 // one 512-byte tile at ((Q * K / 128) + c) * 512, where column m of the 128 and block
 // j of the quad sit at byte (m % 32) * 16 + (m / 32) * 4 + j.  Bytes of blocks past a
 // group's last one are not written.
+//
+// gather (optional): the rows to quantise are the dispatched rows Xp[r] =
+// in[gather[r] / gk] (gather = the dispatch's src_pair, gk = top-k), read straight
+// from the token rows instead of from a materialised Xp.  Each warp loads its
+// block's 32 pair indices with one coalesced load into shared memory; a pair index
+// outside [0, gpairs) flags MOE_DEV_BAD_INDEX and its row reads as zeros.
 constexpr int kColThreads = 128;
 
 template <typename Tin, bool kTiled>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const uint8_t* __restrict__ in, int rows, int K, const int32_t* __restrict__ offsets, int E,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const int32_t* __restrict__ gather, int gk,
+    int gpairs, int32_t* status) {
   pdl_begin();
   constexpr int EB = sizeof(Tin);
   constexpr int CPT = 4;                       // columns per thread
@@ -381,6 +388,7 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
   constexpr int kStrip = kColThreads * CPT;
   __shared__ int bpre[1025];                   // block-row prefix per group
   __shared__ int part[kColThreads];
+  __shared__ int grow[kColThreads / 32][32];   // gathered source rows of the task's block, per warp
   // blocks per group (invalid groups count as empty), then an exclusive scan
   constexpr int G = 1024 / kColThreads;        // groups per thread (E <= 1024)
   int cnt[G], sum = 0;
@@ -436,18 +444,32 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     }
     const int r0 = offsets[lo_e] + (br - bpre[lo_e]) * 32;
     const int n = min(32, offsets[lo_e + 1] - r0);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (gather) {                                // every lane, before any lane leaves the task
+      __syncwarp();                              // the previous task's reads of grow are done
+      int srow = -1;
+      if (lane < n) {
+        const int p = gather[r0 + lane];
+        if (p >= 0 && p < gpairs) srow = p / gk;
+        else flag_error(status, MOE_DEV_BAD_INDEX);
+      }
+      grow[wid][lane] = srow;
+      __syncwarp();
+    }
     const int col = strip * kStrip + CPT * threadIdx.x;   // K % 32 == 0: a chunk is all in or all out
     if (col >= K) continue;
     uint32_t raw[32][NW];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint8_t* src = in + static_cast<size_t>(r0 + i) * in_row + static_cast<size_t>(col) * EB;
+      const int srow = gather ? grow[wid][i] : r0 + i;
+      const bool ok = i < n && srow >= 0;
+      const uint8_t* src = in + static_cast<size_t>(ok ? srow : 0) * in_row + static_cast<size_t>(col) * EB;
       if constexpr (NW == 2) {
-        const uint2 u = i < n ? *reinterpret_cast<const uint2*>(src) : make_uint2(0u, 0u);
+        const uint2 u = ok ? *reinterpret_cast<const uint2*>(src) : make_uint2(0u, 0u);
         raw[i][0] = u.x;
         raw[i][1] = u.y;
       } else {
-        const uint4 u = i < n ? *reinterpret_cast<const uint4*>(src) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 u = ok ? *reinterpret_cast<const uint4*>(src) : make_uint4(0u, 0u, 0u, 0u);
         raw[i][0] = u.x;
         raw[i][1] = u.y;
         raw[i][2] = u.z;
@@ -760,6 +782,63 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, i
                         sms, nullptr, nullptr);
 }
 
+namespace {
+void colwise_launch(const void* in, moe_dtype_t in_dtype, int rows, int K, const int32_t* offsets, int E, int axis,
+                    uint8_t* codes, uint8_t* scales, const int32_t* gather, int gk, int gpairs, int32_t* status,
+                    cudaStream_t stream, int sms) {
+  const int strip = kColThreads * 4;
+  const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
+  const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
+  const uint8_t* src = static_cast<const uint8_t*>(in);
+  if (in_dtype == MOE_BF16) {
+    if (axis == 2)
+      launch_pdl(quantize_colwise_kernel<uint16_t, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
+                 codes, scales, gather, gk, gpairs, status);
+    else
+      launch_pdl(quantize_colwise_kernel<uint16_t, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
+                 codes, scales, gather, gk, gpairs, status);
+  } else {
+    if (axis == 2)
+      launch_pdl(quantize_colwise_kernel<float, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
+                 codes, scales, gather, gk, gpairs, status);
+    else
+      launch_pdl(quantize_colwise_kernel<float, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
+                 codes, scales, gather, gk, gpairs, status);
+  }
+}
+}  // namespace
+
+extern "C" moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x_dtype, int T, int K, int k,
+                                                    const int32_t* src_pair, const int32_t* offsets, int E,
+                                                    int axis, uint8_t* codes, uint8_t* scales,
+                                                    int32_t* dev_status, cudaStream_t stream) {
+  const char* fn = "moe_quantize_mxfp8_gathered";
+  if (axis != 1 && axis != 2) {
+    set_error("%s: axis 1 (column-wise) or 2 (column-wise, tiled scales)", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 0 || K < 0 || K % 32 || k < 1 || k > 32 || !offsets || E < 1 || E > 1024 ||
+      (axis == 2 && K % 128) || (x_dtype != MOE_BF16 && x_dtype != MOE_F32)) {
+    set_error("%s: need T, K >= 0, K %% 32 == 0 (axis 2: %% 128), 1 <= k <= 32, offsets, 1 <= E <= 1024, "
+              "BF16/F32 rows", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("%s: T*k must fit in int32", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int rows = T * k;
+  if (rows > 0 && K > 0 && (!x || !src_pair || !codes || !scales || !aligned16(x) || !aligned16(codes))) {
+    set_error("%s: null or misaligned pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0 || K == 0) return MOE_OK;
+  colwise_launch(x, x_dtype, rows, K, offsets, E, axis, codes, scales, src_pair, k, rows, dev_status, stream, sms);
+  return check_launch(fn);
+}
+
 extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, int rows,
                                                    int K, const int32_t* offsets, int E, int axis,
                                                    uint8_t* codes, uint8_t* scales,
@@ -788,17 +867,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (rows == 0 || K == 0) return MOE_OK;
   if (axis >= 1) {
-    const int strip = kColThreads * 4;
-    const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
-    const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
-    const uint8_t* src = static_cast<const uint8_t*>(in);
-    if (in_dtype == MOE_BF16) {
-      if (axis == 2) launch_pdl(quantize_colwise_kernel<uint16_t, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
-      else launch_pdl(quantize_colwise_kernel<uint16_t, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
-    } else {
-      if (axis == 2) launch_pdl(quantize_colwise_kernel<float, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
-      else launch_pdl(quantize_colwise_kernel<float, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E, codes, scales);
-    }
+    colwise_launch(in, in_dtype, rows, K, offsets, E, axis, codes, scales, nullptr, 1, 0, nullptr, stream, sms);
     return check_launch("moe_quantize_mxfp8_grouped");
   }
   const int grid = scatter_grid(rows, sms);

@@ -28,7 +28,9 @@ class MoELayer:
     (the weights along d for GEMM1, along f for GEMM2, and along their output dim
     for the data gradients); the weight gradients read Xp, H, dYp and dGU
     column-wise, group-aware, with scales in the weight-gradient GEMM's tiled
-    layout.  Activations and gradients are kept in bf16 between the GEMMs.
+    layout.  H, G|U, dYp and dGU are kept in bf16 between the GEMMs; Xp exists only
+    in its two MXFP8 forms (the dispatch writes the row-wise one, and the
+    column-wise one is quantised from the token rows through the dispatch map).
     """
 
     def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False,
@@ -85,7 +87,7 @@ class MoELayer:
             self.W2q, self.W2s = B.moe_quantize_mxfp8_grouped(W2.reshape(E * d, f))
             self.W1q, self.W1s = self.W1q.view(E, 2 * f, d), self.W1s.view(E, 2 * f, d // 32)
             self.W2q, self.W2s = self.W2q.view(E, d, f), self.W2s.view(E, d, f // 32)
-            self.xp = torch.empty(M, d, dtype=store, device=dev) if training else None
+            self.xp = None        # training too: both MXFP8 forms of Xp come from x directly
         else:
             self.xp = torch.empty(M, d, dtype=store, device=dev)
         if dtype == "mxfp8" and training:
@@ -132,12 +134,13 @@ class MoELayer:
                                 dest_row=self.dest_row, src_pair=self.src_pair, codes=self.xq, scales=self.xs,
                                 tensor_scale=self.xg, workspace=self.workspace, dev_status=self.dev_status)
         elif self.dtype == "mxfp8" and self.training:
-            # bf16 Xp (kept for the weight gradient), then both MXFP8 forms of it
-            B.moe_permute(x, self.topk_idx, self.counts, self.E, offsets=self.offsets,
-                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
-                          workspace=self.workspace, dev_status=self.dev_status)
-            B.moe_quantize_mxfp8_grouped(self.xp, codes=self.xq, scales=self.xs)
-            B.moe_quantize_mxfp8_grouped(self.xp, self.offsets, self.E, codes=self.xcq, scales=self.xcs, axis=2)
+            # row-wise MXFP8 rows from the dispatch, then the column-wise form for the
+            # weight gradient gathered from the token rows (no bf16 Xp)
+            B.moe_permute(x, self.topk_idx, self.counts, self.E, xp_dtype="mxfp8", offsets=self.offsets,
+                          dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xq,
+                          xp_scales=self.xs, workspace=self.workspace, dev_status=self.dev_status)
+            B.moe_quantize_mxfp8_gathered(x, self.src_pair, self.offsets, self.E, self.k, codes=self.xcq,
+                                          scales=self.xcs, axis=2, dev_status=self.dev_status)
         elif self.dtype == "mxfp8":
             B.moe_permute(x, self.topk_idx, self.counts, self.E, xp_dtype="mxfp8", offsets=self.offsets,
                           dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xq,
@@ -192,10 +195,11 @@ class MoELayer:
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
         scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
-        MXFP8 training adds the row- and column-wise quantisation of Xp and of H."""
+        MXFP8 training adds the gathered column-wise quantisation of Xp and the row-
+        and column-wise quantisation of H."""
         route = 1 if self.w_router is not None else 2     # fused router GEMM (counts zeroed by a memset)
         nv = 3 if self.dtype == "nvfp4" else 0            # amax of x; amax + quantise of H
-        return route + 2 + 2 + 1 + nv + (4 if self.dtype == "mxfp8" and self.training else 0)
+        return route + 2 + 2 + 1 + nv + (3 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd;

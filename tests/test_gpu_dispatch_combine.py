@@ -239,6 +239,75 @@ def test_quantize_colwise_needs_offsets():
         moe_gpu.moe_quantize_mxfp8_grouped(a, None, 0, axis=1)
 
 
+GATHER_CASES = [SMALL[1].scaled(d=128, name="ragged-T257"), SMALL[2].scaled(d=128, name="zipf-E128"),
+                SMALL[3].scaled(d=256, name="zipf-E256-empty"), SMALL[6].scaled(d=128, name="E1000-k32"),
+                W.WORKLOADS[3].scaled(T=512, name="dsv3-T512")]
+
+
+@pytest.mark.parametrize("w", GATHER_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("axis", [1, 2])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_quantize_gathered_colwise_bit_exact(w, axis, dtype):
+    """Column-wise MXFP8 of the dispatched rows read through src_pair equals the
+    oracle's column-wise quantisation of its own permuted rows, codes and every
+    scale byte; the status word stays clear."""
+    need_gpu()
+    x = W.make_x(w, "cuda").to(dtype)
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales = moe_gpu.moe_quantize_mxfp8_gathered(x, out["src_pair"], out["offsets"], w.E, w.k, axis=axis,
+                                                        dev_status=st)
+    c, sc = omx.quantize_colwise_grouped(f64(x)[o_src // w.k], o_off)
+    assert (codes.cpu().numpy() == c).all()
+    if axis == 1:
+        assert (scales[:sc.shape[0]].cpu().numpy() == sc).all()
+    else:
+        idx = tiled_scale_index(o_off, w.d)
+        assert (scales.cpu().numpy().reshape(-1)[idx] == sc).all()
+    assert int(st.item()) == 0
+
+
+def test_quantize_gathered_colwise_full_dsv3_sampled():
+    """Full DeepSeek-V3 training size (T=16384, k=8, d=7168): the codes and tiled
+    scales of sampled column strips of every group's first and last block."""
+    need_gpu()
+    w = W.BY_NAME["dsv3-mxfp8-train"]
+    x = W.make_x(w, "cuda").to(torch.bfloat16)
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x)
+    codes, scales = moe_gpu.moe_quantize_mxfp8_gathered(x, out["src_pair"], out["offsets"], w.E, w.k, axis=2)
+    cols = np.array([0, 1, 127, 128, 3583, 5000, 7167])
+    rng = np.random.default_rng(7)
+    groups = [e for e in range(w.E) if o_off[e + 1] > o_off[e]]
+    for e in rng.choice(groups, size=12, replace=False):
+        lo, hi = int(o_off[e]), int(o_off[e + 1])
+        for r0 in sorted({lo, lo + ((hi - lo - 1) // 32) * 32}):
+            r1 = min(r0 + 32, hi)
+            blk = f64(x[torch.from_numpy(o_src[r0:r1] // w.k).cuda()][:, torch.from_numpy(cols).cuda()])
+            c, sc = omx.quantize_colwise_grouped(blk, np.array([0, r1 - r0]))
+            assert (codes[r0:r1][:, torch.from_numpy(cols).cuda()].cpu().numpy() == c).all()
+            b = (r0 - lo) // 32
+            quad = lo // 128 + e + b // 4
+            flat = scales.view(-1)
+            pos = (quad * (w.d // 128) + cols // 128) * 512 + (cols % 32) * 16 + ((cols % 128) // 32) * 4 + b % 4
+            assert (flat[torch.from_numpy(pos).cuda()].cpu().numpy() == sc[0]).all()
+
+
+def test_quantize_gathered_flags_bad_pair_index():
+    """A src_pair entry outside [0, T*k) sets MOE_DEV_BAD_INDEX and its row reads as
+    zeros (the kernel checks the index before the load)."""
+    need_gpu()
+    w = SMALL[1].scaled(d=64, name="ragged-T257")
+    x = W.make_x(w, "cuda").to(torch.bfloat16)
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x)
+    src = out["src_pair"].clone()
+    src[5] = w.T * w.k + 3
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, _ = moe_gpu.moe_quantize_mxfp8_gathered(x, src, out["offsets"], w.E, w.k, axis=1, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & moe_gpu.binding.MOE_DEV_BAD_INDEX
+    assert (codes[5] == 0).all()
+
+
 def _combine_bound(yp64, dest, w):
     """|fp32 sum of k products rounded once to bf16 - exact| <= 2^-8 * sum_j |w_j yp_j|."""
     T, k = dest.shape
