@@ -222,12 +222,17 @@ moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t in_dtype, in
  *   x         [T, K] MOE_BF16 or MOE_F32 token rows, 16-byte aligned; K % 32 == 0
  *             (axis 2: K % 128 == 0).
  *   k         top-k (1..32); src_pair [T*k] and offsets [E+1] from moe_permute.
+ *   row_w     optional [T*k] fp32 per-pair weights (the routing weights): the rows
+ *             are then w[src_pair[r]] * x[src_pair[r] / k], the product taken in
+ *             fp32 and rounded to x's dtype -- the dYp of moe_unpermute_combine_bwd,
+ *             whose column-wise MXFP8 this gives without dYp being stored.
  *   axis      1 or 2, codes [T*k, K] and scales as for moe_quantize_mxfp8_grouped.
  *   dev_status  optional: a src_pair entry outside [0, T*k) sets MOE_DEV_BAD_INDEX
  *             and its row is quantised as zeros.
  * MOE_ERR_UNSUPPORTED for any other axis; T == 0 or K == 0 is a no-op. */
 moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x_dtype, int T, int K, int k,
-                                         const int32_t* src_pair, const int32_t* offsets, int E,
+                                         const int32_t* src_pair, const float* row_w,
+                                         const int32_t* offsets, int E,
                                          int axis, uint8_t* codes, uint8_t* scales,
                                          int32_t* dev_status, cudaStream_t stream);
 
@@ -403,6 +408,18 @@ moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp, moe_dtype
                                        int T, int d, int k, const int32_t* dest_row,
                                        const float* topk_w, void* dyp, float* dw,
                                        int32_t* dev_status, cudaStream_t stream);
+
+/* Backward of combine for the MXFP8 training step: as moe_unpermute_combine_bwd on
+ * BF16 dy and yp (d % 32 == 0), with dYp written as its row-wise MXFP8 instead of in
+ * BF16 -- codes [T*k, d] uint8 (16-byte aligned) and E8M0 scales [T*k, d/32] --
+ * equal, bit for bit, to moe_quantize_mxfp8_grouped (axis 0) of the BF16 dYp that
+ * moe_unpermute_combine_bwd would write ([1] "What dropless MoE needs": MXFP8
+ * expert matmuls, quantisation fused with the producing kernel as future work).
+ * dw as moe_unpermute_combine_bwd. */
+moe_status_t moe_unpermute_combine_bwd_mxfp8(const void* dy, const void* yp, moe_dtype_t dtype, int T, int d,
+                                             int k, const int32_t* dest_row, const float* topk_w,
+                                             uint8_t* dyp_codes, uint8_t* dyp_scales, float* dw,
+                                             int32_t* dev_status, cudaStream_t stream);
 
 /* Backward of the routing weights with respect to the logits.
  *   renormalize != 0: dlogits[t, idx_j] = w_j (dw_j - sum_i w_i dw_i), 0 for

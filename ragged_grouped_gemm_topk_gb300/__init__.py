@@ -17,6 +17,7 @@ from .binding import (moe_check_wait_timeout, moe_grouped_gemm_dgrad, moe_groupe
                       moe_permute_noalloc, moe_permute_nvfp4, moe_permute_workspace_size,
                       moe_quantize_mxfp8_gathered, moe_quantize_mxfp8_grouped, moe_quantize_mxfp8_transposed,
                       moe_quantize_nvfp4, moe_route_topk, moe_route_topk_bwd, moe_route_topk_gemm,
-                      moe_unpermute_combine, moe_unpermute_combine_bwd, moe_unpermute_combine_capacity,
+                      moe_unpermute_combine, moe_unpermute_combine_bwd, moe_unpermute_combine_bwd_mxfp8,
+                      moe_unpermute_combine_capacity,
                       moe_version, version)
 from .layer import MoELayer  # noqa: F401

@@ -42,7 +42,7 @@ SIGNATURES = {
     "moe_grouped_gemm_fwd_mxfp8_out": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
     "moe_grouped_gemm_dgrad": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp]),
     "moe_quantize_mxfp8_transposed": (st, [vp, i32, i32, i32, i32, vp, vp, vp]),
-    "moe_quantize_mxfp8_gathered": (st, [vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
+    "moe_quantize_mxfp8_gathered": (st, [vp, i32, i32, i32, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp]),
     "moe_route_topk_gemm": (st, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
     "moe_quantize_nvfp4": (st, [vp, i32, i32, i32, vp, vp, vp, vp]),
     "moe_permute_nvfp4": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
@@ -53,6 +53,7 @@ SIGNATURES = {
     "moe_permute_capacity": (st, [vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
     "moe_unpermute_combine_capacity": (st, [vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]),
     "moe_unpermute_combine_bwd": (st, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
+    "moe_unpermute_combine_bwd_mxfp8": (st, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
     "moe_route_topk_bwd": (st, [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),
 }
 

@@ -225,23 +225,28 @@ def moe_quantize_mxfp8_grouped(inp, offsets=None, E=0, *, codes=None, scales=Non
     return codes, scales
 
 
-def moe_quantize_mxfp8_gathered(x, src_pair, offsets, E, k, *, codes=None, scales=None, axis=2, dev_status=None):
+def moe_quantize_mxfp8_gathered(x, src_pair, offsets, E, k, *, row_w=None, codes=None, scales=None, axis=2,
+                                dev_status=None):
     """Column-wise group-aware MXFP8 of the dispatched rows Xp[r] = x[src_pair[r] // k]
     (x [T, K] bf16/fp32; src_pair and offsets from moe_permute) without writing Xp:
-    the codes [T*k, K] and scales of moe_quantize_mxfp8_grouped(Xp, offsets, E, axis)."""
+    the codes [T*k, K] and scales of moe_quantize_mxfp8_grouped(Xp, offsets, E, axis).
+    With row_w ([T, k] fp32 routing weights) the rows are w * x rounded to x's dtype:
+    the dYp of the combine backward (x = dy)."""
     T, K = x.shape
     rows = T * k
     if axis not in (1, 2):
         raise ValueError("axis must be 1 or 2")
     shape = _colwise_scale_shape(rows, K, E, axis)
     _need(src_pair, "src_pair", _I32, rows)
+    _need(row_w, "row_w", _F32, rows)
     _need(offsets, "offsets", _I32, E + 1)
     _need(codes, "codes", _U8, rows * K)
     _need(scales, "scales", _U8, shape[0] * shape[1])
     _need(dev_status, "dev_status", _I32, 1)
     codes = codes if codes is not None else torch.empty(rows, K, dtype=_U8, device=x.device)
     scales = scales if scales is not None else torch.empty(*shape, dtype=_U8, device=x.device)
-    _lib.call("moe_quantize_mxfp8_gathered", _ptr(x), _dt(x), T, K, k, _ptr(src_pair), _ptr(offsets), E, axis,
+    _lib.call("moe_quantize_mxfp8_gathered", _ptr(x), _dt(x), T, K, k, _ptr(src_pair), _ptr(row_w), _ptr(offsets),
+              E, axis,
               _ptr(codes), _ptr(scales), _ptr(dev_status), _stream())
     return codes, scales
 
@@ -512,6 +517,28 @@ def moe_unpermute_combine_bwd(dy, yp, dest_row, topk_w, *, dyp=None, dw=None, de
     _lib.call("moe_unpermute_combine_bwd", _ptr(dy), _ptr(yp), _dt(dy), T, d, k, _ptr(dest_row),
               _ptr(topk_w), _ptr(dyp), _ptr(dw), _ptr(dev_status), _stream())
     return dyp, dw
+
+
+def moe_unpermute_combine_bwd_mxfp8(dy, yp, dest_row, topk_w, *, codes=None, scales=None, dw=None,
+                                    dev_status=None):
+    """Backward of the combine with dYp written as its row-wise MXFP8 (bf16 dy and
+    yp): (codes u8 [T*k, d], scales u8 [T*k, d/32], dw [T,k] fp32)."""
+    T, k = dest_row.shape
+    d = dy.shape[1]
+    M = T * k
+    _need(yp, "yp", dy.dtype, M * d)
+    _need(dest_row, "dest_row", _I32)
+    _need(topk_w, "topk_w", _F32, M)
+    _need(codes, "codes", _U8, M * d)
+    _need(scales, "scales", _U8, M * (d // 32))
+    _need(dw, "dw", _F32, M)
+    _need(dev_status, "dev_status", _I32, 1)
+    codes = codes if codes is not None else torch.empty(M, d, dtype=_U8, device=dy.device)
+    scales = scales if scales is not None else torch.empty(M, d // 32, dtype=_U8, device=dy.device)
+    dw = dw if dw is not None else torch.empty(T, k, dtype=_F32, device=dy.device)
+    _lib.call("moe_unpermute_combine_bwd_mxfp8", _ptr(dy), _ptr(yp), _dt(dy), T, d, k, _ptr(dest_row),
+              _ptr(topk_w), _ptr(codes), _ptr(scales), _ptr(dw), _ptr(dev_status), _stream())
+    return codes, scales, dw
 
 
 def moe_route_topk_bwd(dw, topk_w, topk_idx, E, *, logits=None, renormalize=True, out=None,

@@ -257,6 +257,72 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_kernel(
   }
 }
 
+// As combine_bwd_kernel (bf16), with dYp leaving as its row-wise MXFP8 (codes
+// [T*k, d], E8M0 scales [T*k, d/32]) instead of in bf16: each row value is first
+// rounded to bf16, exactly as the bf16 kernel stores it, then quantised, so the
+// codes and scales equal the row-wise quantiser's on the bf16 dYp.  A lane's
+// 16-byte chunk holds 8 elements, four adjacent lanes one 32-element block (d % 32
+// == 0); the warp walks the row in 32-chunk steps so every lane joins the block
+// shuffles.
+__global__ void __launch_bounds__(kThreads) combine_bwd_mx_kernel(
+    const uint8_t* __restrict__ dy, const uint8_t* __restrict__ yp, int T, int d, int k,
+    const int32_t* __restrict__ dest_row, const float* __restrict__ topk_w, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ dw, int32_t* status) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const int M = T * k;
+  const size_t row = static_cast<size_t>(d) * 2;
+  const int n16 = d / 8;
+  const long long pairs = static_cast<long long>(T) * k;
+  for (long long p = static_cast<long long>(blockIdx.x) * wpb + (threadIdx.x >> 5); p < pairs;
+       p += static_cast<long long>(gridDim.x) * wpb) {
+    const int t = static_cast<int>(p / k);
+    const int sj = dest_row[p];
+    const float wj = topk_w[p];
+    float part = 0.f;
+    if (sj >= 0 && sj < M) {                    // warp-uniform
+      const Vec16* dyr = reinterpret_cast<const Vec16*>(dy + static_cast<size_t>(t) * row);
+      const Vec16* ypr = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * row);
+      for (int base = 0; base < n16; base += 32) {
+        const int c = base + lane;
+        const bool on = c < n16;                // a block's four lanes agree (n16 % 4 == 0)
+        float a[8], b[8], o[8];
+        const Vec16 zero = {{0u, 0u, 0u, 0u}};
+        Elt<uint16_t>::unpack(on ? dyr[c] : zero, a);
+        Elt<uint16_t>::unpack(on ? ypr[c] : zero, b);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          part = fmaf(a[i], b[i], part);
+          o[i] = bf16_to_f32(f32_to_bf16(wj * a[i]));
+          amax = fmaxf(amax, fabsf(o[i]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+        uint32_t sbyte;
+        float inv;
+        mx_scale(amax, &sbyte, &inv);
+        uint32_t q[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          q[h] = static_cast<uint32_t>(f32x2_to_e4m3x2(o[4 * h] * inv, o[4 * h + 1] * inv)) |
+                 (static_cast<uint32_t>(f32x2_to_e4m3x2(o[4 * h + 2] * inv, o[4 * h + 3] * inv)) << 16);
+        if (on) {
+          *reinterpret_cast<uint2*>(codes + static_cast<size_t>(sj) * d + static_cast<size_t>(c) * 8) =
+              make_uint2(q[0], q[1]);
+          if ((lane & 3) == 0) scales[static_cast<size_t>(sj) * (d / 32) + c / 4] = static_cast<uint8_t>(sbyte);
+        }
+      }
+    } else if (lane == 0) {
+      flag_error(status, MOE_DEV_BAD_INDEX);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    if (lane == 0) dw[p] = part;
+  }
+}
+
 int grid_for(long long tasks, int sms) {
   const int wpb = kThreads / 32;
   const long long g = (tasks + wpb - 1) / wpb;
@@ -376,4 +442,32 @@ extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp
   else
     launch_pdl(combine_bwd_kernel<float>, grid, kThreads, 0, stream, a, b, T, d, k, dest_row, topk_w, o, dw, dev_status);
   return check_launch("moe_unpermute_combine_bwd");
+}
+
+extern "C" moe_status_t moe_unpermute_combine_bwd_mxfp8(const void* dy, const void* yp, moe_dtype_t dtype, int T,
+                                                        int d, int k, const int32_t* dest_row,
+                                                        const float* topk_w, uint8_t* dyp_codes,
+                                                        uint8_t* dyp_scales, float* dw, int32_t* dev_status,
+                                                        cudaStream_t stream) {
+  const char* fn = "moe_unpermute_combine_bwd_mxfp8";
+  if (T < 0 || d < 0 || k < 1 || k > 32 || d % 32 || dtype != MOE_BF16) {
+    set_error("%s: need T, d >= 0, d %% 32 == 0, 1 <= k <= 32, BF16 dy and yp", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (static_cast<long long>(T) * k >= (1LL << 31)) {
+    set_error("%s: T*k must fit in int32", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (T > 0 && (!dy || !yp || !dest_row || !topk_w || !dyp_codes || !dyp_scales || !dw || !aligned16(dy) ||
+                !aligned16(yp) || !aligned16(dyp_codes))) {
+    set_error("%s: null or misaligned pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const int grid = grid_for(static_cast<long long>(T) * k, sms);
+  launch_pdl(combine_bwd_mx_kernel, grid, kThreads, 0, stream, static_cast<const uint8_t*>(dy),
+             static_cast<const uint8_t*>(yp), T, d, k, dest_row, topk_w, dyp_codes, dyp_scales, dw, dev_status);
+  return check_launch(fn);
 }

@@ -373,14 +373,17 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
 // in[gather[r] / gk] (gather = the dispatch's src_pair, gk = top-k), read straight
 // from the token rows instead of from a materialised Xp.  Each warp loads its
 // block's 32 pair indices with one coalesced load into shared memory; a pair index
-// outside [0, gpairs) flags MOE_DEV_BAD_INDEX and its row reads as zeros.
+// outside [0, gpairs) flags MOE_DEV_BAD_INDEX and its row reads as zeros.  With
+// gweight (per-pair weights, the routing weights) the rows are gweight[p] *
+// in[p / gk], the product taken in fp32 and rounded to Tin: the rows the combine
+// backward writes as dYp, quantised without being stored.
 constexpr int kColThreads = 128;
 
 template <typename Tin, bool kTiled>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const uint8_t* __restrict__ in, int rows, int K, const int32_t* __restrict__ offsets, int E,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const int32_t* __restrict__ gather, int gk,
-    int gpairs, int32_t* status) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const int32_t* __restrict__ gather,
+    const float* __restrict__ gweight, int gk, int gpairs, int32_t* status) {
   pdl_begin();
   constexpr int EB = sizeof(Tin);
   constexpr int CPT = 4;                       // columns per thread
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
   __shared__ int bpre[1025];                   // block-row prefix per group
   __shared__ int part[kColThreads];
   __shared__ int grow[kColThreads / 32][32];   // gathered source rows of the task's block, per warp
+  __shared__ float gwt[kColThreads / 32][32];  // and their weights
   // blocks per group (invalid groups count as empty), then an exclusive scan
   constexpr int G = 1024 / kColThreads;        // groups per thread (E <= 1024)
   int cnt[G], sum = 0;
@@ -448,12 +452,18 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     if (gather) {                                // every lane, before any lane leaves the task
       __syncwarp();                              // the previous task's reads of grow are done
       int srow = -1;
+      float wr = 1.f;
       if (lane < n) {
         const int p = gather[r0 + lane];
-        if (p >= 0 && p < gpairs) srow = p / gk;
-        else flag_error(status, MOE_DEV_BAD_INDEX);
+        if (p >= 0 && p < gpairs) {
+          srow = p / gk;
+          if (gweight) wr = gweight[p];
+        } else {
+          flag_error(status, MOE_DEV_BAD_INDEX);
+        }
       }
       grow[wid][lane] = srow;
+      gwt[wid][lane] = wr;
       __syncwarp();
     }
     const int col = strip * kStrip + CPT * threadIdx.x;   // K % 32 == 0: a chunk is all in or all out
@@ -474,6 +484,20 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
         raw[i][1] = u.y;
         raw[i][2] = u.z;
         raw[i][3] = u.w;
+      }
+    }
+    if (gweight) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float wr = gwt[wid][i];
+#pragma unroll
+        for (int j = 0; j < NW; ++j) {
+          if constexpr (NW == 2)
+            raw[i][j] = pack_bf16x2(wr * bf16_to_f32(static_cast<uint16_t>(raw[i][j] & 0xFFFFu)),
+                                    wr * bf16_to_f32(static_cast<uint16_t>(raw[i][j] >> 16)));
+          else
+            raw[i][j] = __float_as_uint(wr * __uint_as_float(raw[i][j]));
+        }
       }
     }
     auto decode = [](const uint32_t (&w)[NW], float (&f)[CPT]) {
@@ -784,8 +808,8 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, i
 
 namespace {
 void colwise_launch(const void* in, moe_dtype_t in_dtype, int rows, int K, const int32_t* offsets, int E, int axis,
-                    uint8_t* codes, uint8_t* scales, const int32_t* gather, int gk, int gpairs, int32_t* status,
-                    cudaStream_t stream, int sms) {
+                    uint8_t* codes, uint8_t* scales, const int32_t* gather, const float* gweight, int gk,
+                    int gpairs, int32_t* status, cudaStream_t stream, int sms) {
   const int strip = kColThreads * 4;
   const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
   const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
@@ -793,23 +817,24 @@ void colwise_launch(const void* in, moe_dtype_t in_dtype, int rows, int K, const
   if (in_dtype == MOE_BF16) {
     if (axis == 2)
       launch_pdl(quantize_colwise_kernel<uint16_t, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gk, gpairs, status);
+                 codes, scales, gather, gweight, gk, gpairs, status);
     else
       launch_pdl(quantize_colwise_kernel<uint16_t, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gk, gpairs, status);
+                 codes, scales, gather, gweight, gk, gpairs, status);
   } else {
     if (axis == 2)
       launch_pdl(quantize_colwise_kernel<float, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gk, gpairs, status);
+                 codes, scales, gather, gweight, gk, gpairs, status);
     else
       launch_pdl(quantize_colwise_kernel<float, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gk, gpairs, status);
+                 codes, scales, gather, gweight, gk, gpairs, status);
   }
 }
 }  // namespace
 
 extern "C" moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x_dtype, int T, int K, int k,
-                                                    const int32_t* src_pair, const int32_t* offsets, int E,
+                                                    const int32_t* src_pair, const float* row_w,
+                                                    const int32_t* offsets, int E,
                                                     int axis, uint8_t* codes, uint8_t* scales,
                                                     int32_t* dev_status, cudaStream_t stream) {
   const char* fn = "moe_quantize_mxfp8_gathered";
@@ -835,7 +860,8 @@ extern "C" moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x
   int sms = 0;
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (rows == 0 || K == 0) return MOE_OK;
-  colwise_launch(x, x_dtype, rows, K, offsets, E, axis, codes, scales, src_pair, k, rows, dev_status, stream, sms);
+  colwise_launch(x, x_dtype, rows, K, offsets, E, axis, codes, scales, src_pair, row_w, k, rows, dev_status, stream,
+                 sms);
   return check_launch(fn);
 }
 
@@ -867,7 +893,8 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
   if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
   if (rows == 0 || K == 0) return MOE_OK;
   if (axis >= 1) {
-    colwise_launch(in, in_dtype, rows, K, offsets, E, axis, codes, scales, nullptr, 1, 0, nullptr, stream, sms);
+    colwise_launch(in, in_dtype, rows, K, offsets, E, axis, codes, scales, nullptr, nullptr, 1, 0, nullptr, stream,
+                   sms);
     return check_launch("moe_quantize_mxfp8_grouped");
   }
   const int grid = scatter_grid(rows, sms);

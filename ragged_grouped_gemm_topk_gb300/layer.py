@@ -107,7 +107,8 @@ class MoELayer:
             self.dyq, self.dys = torch.empty(M, d, **u8), torch.empty(M, d // 32, **u8)
             self.dgq, self.dgs = torch.empty(M, 2 * f, **u8), torch.empty(M, 2 * f // 32, **u8)
         if training:
-            self.dyp = torch.empty(M, d, dtype=store, device=dev)
+            # MXFP8: dYp exists only as its two MXFP8 forms (from dy and the routing weights)
+            self.dyp = torch.empty(M, d, dtype=store, device=dev) if dtype != "mxfp8" else None
             self.dw = torch.empty(T, k, dtype=torch.float32, device=dev)
             self.dgu = torch.empty(M, 2 * f, dtype=store, device=dev)
             self.dxp = torch.empty(M, d, dtype=store, device=dev)
@@ -203,8 +204,10 @@ class MoELayer:
 
     def launches_per_backward(self) -> int:
         """combine bwd, dgrad+dSwiGLU, wgrad, dgrad, wgrad, dispatch bwd, router bwd;
-        MXFP8 adds the row- and column-wise quantisation of dYp and of dGU."""
-        return 7 + (4 if self.dtype == "mxfp8" else 0)
+        MXFP8 adds the gathered column-wise quantisation of dYp (its row-wise form
+        comes from the combine backward) and the row- and column-wise quantisation
+        of dGU."""
+        return 7 + (3 if self.dtype == "mxfp8" else 0)
 
     # ------------------------------------------------------------------ backward
     def backward(self, dy, logits=None, dx_out=None):
@@ -213,12 +216,14 @@ class MoELayer:
         if not self.training:
             raise RuntimeError("construct the layer with training=True")
         st = self.dev_status
-        B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
-                                    dev_status=st)
         if self.dtype == "mxfp8":
             off, E = self.offsets, self.E
-            B.moe_quantize_mxfp8_grouped(self.dyp, codes=self.dyq, scales=self.dys)
-            B.moe_quantize_mxfp8_grouped(self.dyp, off, E, codes=self.dycq, scales=self.dycs, axis=2)
+            # dYp = w * dy in its two MXFP8 forms: row-wise from the combine backward,
+            # column-wise gathered from dy through the dispatch map
+            B.moe_unpermute_combine_bwd_mxfp8(dy, self.yp, self.dest_row, self.topk_w, codes=self.dyq,
+                                              scales=self.dys, dw=self.dw, dev_status=st)
+            B.moe_quantize_mxfp8_gathered(dy, self.src_pair, off, E, self.k, row_w=self.topk_w, codes=self.dycq,
+                                          scales=self.dycs, axis=2, dev_status=st)
             B.moe_grouped_gemm_dgrad_mxfp8(self.dyq, self.W2t, off, dC_scales=self.dys, BT_scales=self.W2ts,
                                            epi="dswiglu", preact=self.gu, out=self.dgu, dev_status=st)
             B.moe_grouped_gemm_wgrad(self.hcq, self.dycq, off, E, A_scales=self.hcs, dC_scales=self.dycs,
@@ -230,6 +235,8 @@ class MoELayer:
             B.moe_grouped_gemm_wgrad(self.xcq, self.dgcq, off, E, A_scales=self.xcs, dC_scales=self.dgcs,
                                      out=self.dW1, dev_status=st)
         else:
+            B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
+                                        dev_status=st)
             B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
                                      out=self.dgu, dev_status=st)
             B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)

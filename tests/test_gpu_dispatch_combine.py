@@ -391,6 +391,84 @@ def test_combine_bwd(w):
     assert rel_l2(f64(dw), want_dw) < 1e-5
 
 
+def _dyp_case(w, seed):
+    """Seeded inputs of the MXFP8 combine backward: the oracle's own maps (from its
+    routing of the workload's logits), seeded routing weights, dy and yp; and the
+    dYp the bf16 combine backward stores, w * dy in fp32 rounded to bf16 (the
+    precision in which the kernel takes the value its codes come from)."""
+    o_idx = om.route_topk(W.make_logits(w), w.k)[0]
+    o_off, o_dest, o_src = om.permute_maps(o_idx, w.E)
+    rng = np.random.default_rng(seed)
+    w32 = rng.uniform(0.05, 1.0, size=(w.T, w.k)).astype(np.float32)
+    dy = W.make_matrix(w.T, w.d, seed=seed + 1, dtype=torch.bfloat16, device="cuda")
+    yp = W.make_matrix(w.M, w.d, seed=seed + 2, dtype=torch.bfloat16, device="cuda")
+    prod = (torch.from_numpy(w32)[:, :, None] * dy.cpu().float()[:, None, :]).to(torch.bfloat16)
+    dyp = torch.empty(w.M, w.d, dtype=torch.bfloat16)
+    dyp[torch.from_numpy(o_dest.reshape(-1))] = prod.reshape(-1, w.d)
+    dev = {"dest_row": torch.from_numpy(o_dest.astype(np.int32)).cuda(),
+           "src_pair": torch.from_numpy(o_src.astype(np.int32)).cuda(),
+           "offsets": torch.from_numpy(o_off.astype(np.int32)).cuda(),
+           "topk_w": torch.from_numpy(w32).cuda()}
+    return dy, yp, w32, (o_off, o_dest, o_src), f64(dyp), dev
+
+
+MX_BWD_CASES = [SMALL[1].scaled(d=64, name="ragged-T257"), SMALL[3].scaled(d=256, name="zipf-E256-empty"),
+                W.BY_NAME["dsv3-bf16-train"].scaled(T=1024, name="dsv3-T1024")]
+
+
+@pytest.mark.parametrize("w", MX_BWD_CASES, ids=lambda w: w.name)
+def test_combine_bwd_mxfp8_bit_exact(w):
+    """Row-wise MXFP8 of dYp from the combine backward equals the oracle's row-wise
+    quantisation of the bf16 dYp, codes and scales bit for bit; dw as the bf16 path."""
+    need_gpu()
+    dy, yp, w32, (o_off, o_dest, o_src), dyp64, dev = _dyp_case(w, seed=31)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, dw = moe_gpu.moe_unpermute_combine_bwd_mxfp8(dy, yp, dev["dest_row"], dev["topk_w"],
+                                                                dev_status=st)
+    c, sc = omx.quantize_rowwise(dyp64)
+    assert (codes.cpu().numpy() == c).all()
+    assert (scales.cpu().numpy() == sc).all()
+    want_dw = om.combine_bwd(f64(dy), f64(yp), o_dest, w32.astype(np.float64))[1]
+    assert rel_l2(f64(dw), want_dw) < 1e-5
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("w", MX_BWD_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("axis", [1, 2])
+def test_quantize_gathered_weighted_is_colwise_of_dyp(w, axis):
+    """Column-wise MXFP8 gathered from dy with the routing weights equals the
+    oracle's column-wise quantisation of the bf16 dYp, codes and scales."""
+    need_gpu()
+    if axis == 2 and w.d % 128:
+        pytest.skip("tiled scales need d % 128 == 0")
+    dy, yp, w32, (o_off, o_dest, o_src), dyp64, dev = _dyp_case(w, seed=41)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales = moe_gpu.moe_quantize_mxfp8_gathered(dy, dev["src_pair"], dev["offsets"], w.E, w.k,
+                                                        row_w=dev["topk_w"], axis=axis, dev_status=st)
+    c, sc = omx.quantize_colwise_grouped(dyp64, o_off)
+    assert (codes.cpu().numpy() == c).all()
+    if axis == 1:
+        assert (scales[:sc.shape[0]].cpu().numpy() == sc).all()
+    else:
+        idx = tiled_scale_index(o_off, w.d)
+        assert (scales.cpu().numpy().reshape(-1)[idx] == sc).all()
+    assert int(st.item()) == 0
+
+
+def test_combine_bwd_mxfp8_rejects_bad_args():
+    need_gpu()
+    w = SMALL[1].scaled(d=40, name="d40")
+    dy, yp = torch.zeros(w.T, 40, dtype=torch.bfloat16, device="cuda"), torch.zeros(w.M, 40, dtype=torch.bfloat16,
+                                                                                     device="cuda")
+    dest = torch.zeros(w.T, w.k, dtype=torch.int32, device="cuda")
+    wt = torch.ones(w.T, w.k, dtype=torch.float32, device="cuda")
+    with pytest.raises(moe_gpu.binding.MoeError, match="32"):                 # d % 32
+        moe_gpu.moe_unpermute_combine_bwd_mxfp8(dy, yp, dest, wt)
+    with pytest.raises(moe_gpu.binding.MoeError):                             # fp32 input
+        moe_gpu.moe_unpermute_combine_bwd_mxfp8(torch.zeros(w.T, 64, device="cuda"),
+                                                torch.zeros(w.M, 64, device="cuda"), dest, wt)
+
+
 @pytest.mark.parametrize("renormalize", [True, False])
 def test_route_bwd(renormalize):
     need_gpu()
