@@ -284,13 +284,12 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_mx_kernel(
     if (sj >= 0 && sj < M) {                    // warp-uniform
       const Vec16* dyr = reinterpret_cast<const Vec16*>(dy + static_cast<size_t>(t) * row);
       const Vec16* ypr = reinterpret_cast<const Vec16*>(yp + static_cast<size_t>(sj) * row);
-      for (int base = 0; base < n16; base += 32) {
-        const int c = base + lane;
-        const bool on = c < n16;                // a block's four lanes agree (n16 % 4 == 0)
+      const Vec16 zero = {{0u, 0u, 0u, 0u}};
+      // one chunk: accumulate dw, round w*dy to bf16, quantise its 32-element block
+      auto chunk = [&](const Vec16& va, const Vec16& vb, int c, bool on) {
         float a[8], b[8], o[8];
-        const Vec16 zero = {{0u, 0u, 0u, 0u}};
-        Elt<uint16_t>::unpack(on ? dyr[c] : zero, a);
-        Elt<uint16_t>::unpack(on ? ypr[c] : zero, b);
+        Elt<uint16_t>::unpack(va, a);
+        Elt<uint16_t>::unpack(vb, b);
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -313,6 +312,16 @@ __global__ void __launch_bounds__(kThreads) combine_bwd_mx_kernel(
               make_uint2(q[0], q[1]);
           if ((lane & 3) == 0) scales[static_cast<size_t>(sj) * (d / 32) + c / 4] = static_cast<uint8_t>(sbyte);
         }
+      };
+      // two 32-chunk steps per pass, all four loads issued first; chunks are taken in
+      // the order lane, lane + 32, lane + 64, ... (the bf16 kernel's dw order)
+      for (int base = 0; base < n16; base += 64) {
+        const int c0 = base + lane, c1 = base + 32 + lane;
+        const bool on0 = c0 < n16, on1 = c1 < n16;   // a block's four lanes agree (n16 % 4 == 0)
+        const Vec16 a0 = on0 ? dyr[c0] : zero, b0 = on0 ? ypr[c0] : zero;
+        const Vec16 a1 = on1 ? dyr[c1] : zero, b1 = on1 ? ypr[c1] : zero;
+        chunk(a0, b0, c0, on0);
+        if (base + 32 < n16) chunk(a1, b1, c1, on1);  // warp-uniform
       }
     } else if (lane == 0) {
       flag_error(status, MOE_DEV_BAD_INDEX);

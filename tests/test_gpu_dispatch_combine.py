@@ -413,6 +413,7 @@ def _dyp_case(w, seed):
 
 
 MX_BWD_CASES = [SMALL[1].scaled(d=64, name="ragged-T257"), SMALL[3].scaled(d=256, name="zipf-E256-empty"),
+                SMALL[2].scaled(d=384, name="zipf-E128-d384"),          # a partly filled second 32-chunk step
                 W.BY_NAME["dsv3-bf16-train"].scaled(T=1024, name="dsv3-T1024")]
 
 
