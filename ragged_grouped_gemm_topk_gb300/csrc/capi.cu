@@ -3,6 +3,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace moe {
@@ -10,9 +12,11 @@ namespace moe {
 namespace {
 thread_local char g_err[512] = "";
 
+// Per-device capability cache, safe to fill from several host threads: the SM
+// count is stored before the verdict, which is published with release order.
 struct DevInfo {
-  int checked = 0;  // 0 unknown, 1 ok, -1 not sm_103
-  int sms = 0;
+  std::atomic<int> checked{0};  // 0 unknown, 1 ok, -1 not sm_103
+  std::atomic<int> sms{0};
 };
 DevInfo g_dev[64];
 }  // namespace
@@ -42,18 +46,20 @@ bool device_is_sm103(int* sm_count) {
     return false;
   }
   DevInfo& di = g_dev[dev];
-  if (di.checked == 0) {
+  int verdict = di.checked.load(std::memory_order_acquire);
+  if (verdict == 0) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    di.sms = sms;
-    di.checked = (major == 10 && minor == 3) ? 1 : -1;
-    if (di.checked < 0)
+    verdict = (major == 10 && minor == 3 && sms > 0) ? 1 : -1;
+    di.sms.store(sms, std::memory_order_relaxed);
+    di.checked.store(verdict, std::memory_order_release);
+    if (verdict < 0)
       set_error("device %d is sm_%d%d; libmoe is built for sm_103a only", dev, major, minor);
   }
-  if (sm_count) *sm_count = di.sms;
-  if (di.checked < 0) {
+  if (sm_count) *sm_count = di.sms.load(std::memory_order_relaxed);
+  if (verdict < 0) {
     set_error("device %d is not sm_103; libmoe is built for sm_103a only", dev);
     return false;
   }

@@ -81,6 +81,23 @@ def test_bad_arguments_rejected_before_any_launch():
     assert st == _lib.MOE_ERR_INVALID_ARG                                      # tiled column-wise without groups
     st = L.moe_quantize_mxfp8_grouped(None, _lib.MOE_BF16, 4, 64, None, 0, 3, None, None, None)
     assert st == _lib.MOE_ERR_UNSUPPORTED                                      # no such axis
+    # gathered column-wise quantiser: row-wise axis, width, groups
+    st = L.moe_quantize_mxfp8_gathered(None, _lib.MOE_BF16, 4, 64, 2, None, None, None, 2, 0, None, None, None,
+                                       None)
+    assert st == _lib.MOE_ERR_UNSUPPORTED                                      # axis 0 is not column-wise
+    st = L.moe_quantize_mxfp8_gathered(None, _lib.MOE_BF16, 4, 48, 2, None, None, None, 2, 1, None, None, None,
+                                       None)
+    assert st == _lib.MOE_ERR_INVALID_ARG and b"K" in L.moe_last_error_string()   # K % 32
+    st = L.moe_quantize_mxfp8_gathered(None, _lib.MOE_BF16, 4, 64, 2, None, None, None, 2, 2, None, None, None,
+                                       None)
+    assert st == _lib.MOE_ERR_INVALID_ARG                                      # K % 128 for tiled scales
+    # combine backward with MXFP8 dYp: bf16 only, d % 32
+    st = L.moe_unpermute_combine_bwd_mxfp8(None, None, _lib.MOE_BF16, 4, 40, 2, None, None, None, None, None,
+                                           None, None)
+    assert st == _lib.MOE_ERR_INVALID_ARG
+    st = L.moe_unpermute_combine_bwd_mxfp8(None, None, _lib.MOE_F32, 4, 64, 2, None, None, None, None, None,
+                                           None, None)
+    assert st == _lib.MOE_ERR_INVALID_ARG
 
 
 def test_no_cpu_fallback_in_product_package():
