@@ -28,9 +28,11 @@ class MoELayer:
     (the weights along d for GEMM1, along f for GEMM2, and along their output dim
     for the data gradients); the weight gradients read Xp, H, dYp and dGU
     column-wise, group-aware, with scales in the weight-gradient GEMM's tiled
-    layout.  H, G|U, dYp and dGU are kept in bf16 between the GEMMs; Xp exists only
-    in its two MXFP8 forms (the dispatch writes the row-wise one, and the
-    column-wise one is quantised from the token rows through the dispatch map).
+    layout.  H, G|U and dGU are kept in bf16 between the GEMMs; Xp and dYp exist
+    only in their two MXFP8 forms (Xp: the dispatch writes the row-wise one and the
+    column-wise one is quantised from the token rows through the dispatch map; dYp
+    = w * dy: the combine backward writes the row-wise one and the column-wise one
+    is quantised from dy with the routing weights).
     """
 
     def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False,
