@@ -13,7 +13,7 @@ namespace {
 thread_local char g_err[512] = "";
 
 // Per-device capability cache, safe to fill from several host threads: the SM
-// count is stored before the verdict, which is published with release order.
+// count is stored before the capable, which is published with release order.
 struct DevInfo {
   std::atomic<int> checked{0};  // 0 unknown, 1 ok, -1 not sm_103
   std::atomic<int> sms{0};
@@ -46,20 +46,20 @@ bool device_is_sm103(int* sm_count) {
     return false;
   }
   DevInfo& di = g_dev[dev];
-  int verdict = di.checked.load(std::memory_order_acquire);
-  if (verdict == 0) {
+  int capable = di.checked.load(std::memory_order_acquire);
+  if (capable == 0) {
     int major = 0, minor = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    verdict = (major == 10 && minor == 3 && sms > 0) ? 1 : -1;
+    capable = (major == 10 && minor == 3 && sms > 0) ? 1 : -1;
     di.sms.store(sms, std::memory_order_relaxed);
-    di.checked.store(verdict, std::memory_order_release);
-    if (verdict < 0)
+    di.checked.store(capable, std::memory_order_release);
+    if (capable < 0)
       set_error("device %d is sm_%d%d; libmoe is built for sm_103a only", dev, major, minor);
   }
   if (sm_count) *sm_count = di.sms.load(std::memory_order_relaxed);
-  if (verdict < 0) {
+  if (capable < 0) {
     set_error("device %d is not sm_103; libmoe is built for sm_103a only", dev);
     return false;
   }
