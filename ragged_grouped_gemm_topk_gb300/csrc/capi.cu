@@ -13,7 +13,7 @@ namespace {
 thread_local char g_err[512] = "";
 
 // Per-device capability cache, safe to fill from several host threads: the SM
-// count is stored before the capable, which is published with release order.
+// count is stored before the capability flag, which is published with release order.
 struct DevInfo {
   std::atomic<int> checked{0};  // 0 unknown, 1 ok, -1 not sm_103
   std::atomic<int> sms{0};
