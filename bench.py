@@ -161,6 +161,24 @@ def stage_bytes(w):
     return permute, combine
 
 
+def routing_summary(counts):
+    """The per-expert row histogram of one step's routing: largest count, experts
+    without rows, median of the others, experts with 1..127 rows, the share of the
+    rows taken by the 8 busiest experts, and the padding share of 128-row tiles
+    (rows computed past a group's end / rows computed)."""
+    import numpy as np
+    c = np.asarray(counts, dtype=np.int64)
+    total = int(c.sum())
+    nonempty = c[c > 0]
+    tiled = int((-(-c // 128) * 128).sum())
+    return {"max_count": int(c.max()) if c.size else 0,
+            "empty_experts": int((c == 0).sum()),
+            "median_nonempty": float(np.median(nonempty)) if nonempty.size else 0.0,
+            "experts_below_128_rows": int(((c > 0) & (c < 128)).sum()),
+            "top8_share": round(float(np.sort(c)[::-1][:8].sum()) / total, 4) if total else 0.0,
+            "tile128_padding": round((tiled - total) / tiled, 4) if tiled else 0.0}
+
+
 def gemm1_bytes(w, e_used):
     """Algorithmic HBM bytes of one GEMM1 launch: the W1 of every expert that
     received tokens (and its E8M0 scales for MXFP8) and the permuted activations
@@ -343,7 +361,8 @@ def run_ours(args, world, rank, local):
     dtype_peak = pk["bf16_sus"] * {"mxfp8": 2.0, "nvfp4": 6.0, "f32": 0.5}.get(w.dtype, 1.0)
     # the roofline that binds GEMM1: tensor time at the dtype's peak vs HBM time of
     # its algorithmic bytes at the measured copy bandwidth
-    e_used = int((layer.counts > 0).sum().item())     # read after the timed region
+    counts_h = layer.counts.cpu().numpy()             # read after the timed region
+    e_used = int((counts_h > 0).sum())
     g1_bytes = gemm1_bytes(w, e_used)
     g1_s = per["gemm1"] * 1e-3
     hbm_bound = g1_bytes / (pk["hbm"] * 1e9) > g1_flops / (dtype_peak * 1e12)
@@ -377,6 +396,8 @@ def run_ours(args, world, rank, local):
                    "l2": l2_note(W1, W2),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "stages_ms": {k: round(v, 4) for k, v in per.items()},   # eager pass, events between stages
+        "routing": routing_summary(counts_h),
+        "route_gbs": round((w.T * w.E * 4 + w.T * w.k * 8) / (max(per["route"], 1e-6) * 1e-3) / 1e9, 1),
         "permute_gbs": round(perm_b / (g_disp * 1e-3) / 1e9, 1),
         "combine_gbs": round(comb_b / (g_comb * 1e-3) / 1e9, 1),
         "bandwidth_stages": {

@@ -73,3 +73,16 @@ def test_max_over_ranks_gloo():
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
     assert got == [(0, 3.0), (1, 3.0)]
+
+
+def test_routing_summary_hand_worked():
+    """The routing histogram the bench line reports, on a hand-worked count vector."""
+    sys.path.insert(0, ROOT)
+    import bench
+    counts = [0, 1, 127, 128, 129, 300, 0, 5, 1000, 2, 50, 60]
+    r = bench.routing_summary(counts)
+    # 1802 rows; nonempty sorted 1 2 5 50 60 127 128 129 300 1000; busiest eight hold 1799;
+    # 128-row tiles: 2560 rows computed
+    assert r == {"max_count": 1000, "empty_experts": 2, "median_nonempty": 93.5, "experts_below_128_rows": 6,
+                 "top8_share": 0.9983, "tile128_padding": 0.2961}
+    assert bench.routing_summary([0, 0])["tile128_padding"] == 0.0
