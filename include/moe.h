@@ -168,8 +168,9 @@ moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, int d,
  * and frees nothing.
  * All calls share the one array: calls whose kernels can overlap on the GPU
  * (other streams, other host threads) race and give wrong results -- serialise
- * them.  The first call on a device looks up the array's device address; make
- * that first call before any stream capture. */
+ * them.  The first call in a CUDA context (normally once per device; again
+ * after that device's primary context was reset) looks up the array's device
+ * address; make that first call before any stream capture. */
 moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, int T, int d,
                                  const int32_t* topk_idx, int k, int E, const int32_t* counts,
                                  int32_t* offsets, int32_t* dest_row, int32_t* src_pair,

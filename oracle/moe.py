@@ -69,12 +69,17 @@ def route_topk(logits: np.ndarray, k: int, renormalize: bool = True):
     order = np.lexsort((expert_ids, -l64), axis=-1)          # primary: -logit, then id
     idx = order[:, :k].astype(np.int32)
     sel = np.take_along_axis(l64, idx.astype(np.int64), axis=1)
+    # -inf marks a masked expert (no softmax mass).  A token whose experts are all
+    # masked has no mass anywhere: its k slots (the lowest expert ids, by the
+    # tie-break) get weight 0, so it contributes nothing to the combine.
+    masked = np.isneginf(sel[:, :1])
+    top = np.where(masked, 0.0, sel[:, :1])
     if renormalize:
-        ex = np.exp(sel - sel[:, :1])
-        w = ex / ex.sum(axis=1, keepdims=True)
+        ex = np.where(masked, 0.0, np.exp(sel - top))
+        w = ex / np.where(masked, 1.0, ex.sum(axis=1, keepdims=True))
     else:
-        m = l64.max(axis=1, keepdims=True)
-        w = np.exp(sel - m) / np.exp(l64 - m).sum(axis=1, keepdims=True)
+        ex_all = np.where(masked, 0.0, np.exp(l64 - top))
+        w = np.where(masked, 0.0, np.exp(sel - top)) / np.where(masked, 1.0, ex_all.sum(axis=1, keepdims=True))
     counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
     return idx, w, counts
 
@@ -350,8 +355,10 @@ def route_bwd(dw, w, idx, logits, renormalize=True):
         dl[rows, idx] = w * (dw - inner)
     else:
         l64 = np.asarray(logits, dtype=np.float64)
-        p = np.exp(l64 - l64.max(axis=1, keepdims=True))
-        p /= p.sum(axis=1, keepdims=True)
+        m = l64.max(axis=1, keepdims=True)
+        masked = np.isneginf(m)                    # every expert masked: no probability mass
+        p = np.where(masked, 0.0, np.exp(l64 - np.where(masked, 0.0, m)))
+        p /= np.where(masked, 1.0, p.sum(axis=1, keepdims=True))
         g = np.zeros((T, E))
         g[rows, idx] = dw
         dl = p * (g - inner)

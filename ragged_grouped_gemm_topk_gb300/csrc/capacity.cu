@@ -116,7 +116,7 @@ extern "C" moe_status_t moe_permute_capacity(const void* x, moe_dtype_t x_dtype,
     return MOE_ERR_WORKSPACE;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   // workspace: rank histogram | dropless offsets [E+1] | dropless src_pair [T*k]
   int32_t* hist = static_cast<int32_t*>(workspace);
   int32_t* off_drop = hist + permute_hist_bytes(T, E) / sizeof(int32_t);

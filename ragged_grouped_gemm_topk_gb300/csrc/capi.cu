@@ -18,7 +18,8 @@ struct DevInfo {
   std::atomic<int> checked{0};  // 0 unknown, 1 ok, -1 not sm_103
   std::atomic<int> sms{0};
 };
-DevInfo g_dev[64];
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
 }  // namespace
 
 void set_error(const char* fmt, ...) {
@@ -39,31 +40,36 @@ moe_status_t check_launch(const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool device_is_sm103(int* sm_count) {
+moe_status_t device_check(int* sm_count) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    set_error("no current CUDA device");
-    return false;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    set_error("no usable current CUDA device: %s", ge != cudaSuccess ? cudaGetErrorString(ge) : "ordinal out of range");
+    return ge != cudaSuccess ? MOE_ERR_CUDA : MOE_ERR_UNSUPPORTED;
   }
   DevInfo& di = g_dev[dev];
   int capable = di.checked.load(std::memory_order_acquire);
   if (capable == 0) {
+    // a failed query (for example a sticky error of an earlier call) is reported
+    // as a CUDA error and not cached: the next call asks again
     int major = 0, minor = 0, sms = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      set_error("device %d: attribute query failed: %s", dev, cudaGetErrorString(e));
+      return MOE_ERR_CUDA;
+    }
     capable = (major == 10 && minor == 3 && sms > 0) ? 1 : -1;
     di.sms.store(sms, std::memory_order_relaxed);
     di.checked.store(capable, std::memory_order_release);
-    if (capable < 0)
-      set_error("device %d is sm_%d%d; libmoe is built for sm_103a only", dev, major, minor);
   }
   if (sm_count) *sm_count = di.sms.load(std::memory_order_relaxed);
   if (capable < 0) {
     set_error("device %d is not sm_103; libmoe is built for sm_103a only", dev);
-    return false;
+    return MOE_ERR_UNSUPPORTED;
   }
-  return true;
+  return MOE_OK;
 }
 
 }  // namespace moe
@@ -100,7 +106,7 @@ extern "C" moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   launch_pdl(wait_timeout_kernel, 1, 32, 0, stream, dev_status, static_cast<uint64_t>(limit_us) * 1000ull);
   return check_launch("moe_check_wait_timeout");
 }

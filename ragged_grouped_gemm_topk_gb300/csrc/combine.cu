@@ -374,7 +374,7 @@ moe_status_t combine_impl(const char* fn, const void* yp, moe_dtype_t dtype, int
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (T == 0 || d == 0) return MOE_OK;
   const long long n16 = static_cast<long long>(d) * (dtype == MOE_BF16 ? 2 : 4) / 16;
   const uint8_t* a = static_cast<const uint8_t*>(yp);
@@ -440,7 +440,7 @@ extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (T == 0) return MOE_OK;
   const int grid = grid_for(static_cast<long long>(T) * k, sms);
   const uint8_t* a = static_cast<const uint8_t*>(dy);
@@ -473,7 +473,7 @@ extern "C" moe_status_t moe_unpermute_combine_bwd_mxfp8(const void* dy, const vo
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (T == 0) return MOE_OK;
   const int grid = grid_for(static_cast<long long>(T) * k, sms);
   launch_pdl(combine_bwd_mx_kernel, grid, kThreads, 0, stream, static_cast<const uint8_t*>(dy),

@@ -16,7 +16,9 @@ namespace moe {
 
 void set_error(const char* fmt, ...);
 moe_status_t check_launch(const char* what);
-bool device_is_sm103(int* sm_count);
+// MOE_OK on an sm_103 device (and its SM count), MOE_ERR_UNSUPPORTED on another
+// architecture, MOE_ERR_CUDA when the runtime cannot be queried.
+moe_status_t device_check(int* sm_count);
 bool aligned16(const void* p);
 
 // ----------------------------------------------------------------------------- device basics

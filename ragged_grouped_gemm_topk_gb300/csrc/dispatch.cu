@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
       if (e <= E) s_off[e] = run;
       run += c[u];
     }
+    // the loop reaches index G * kScatterThreads - 1 at most: at E = 1024 the end
+    // of the scan (every routed pair) is written by the last thread
+    if (E == G * kScatterThreads && threadIdx.x == kScatterThreads - 1) s_off[E] = run;
     __syncthreads();
   }
   if (blockIdx.x == 0) {
@@ -800,7 +803,7 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, i
     return MOE_ERR_WORKSPACE;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp,
                         xp_dtype, xp_scales, static_cast<int32_t*>(workspace), dev_status, stream,
                         sms, nullptr, nullptr);
@@ -858,7 +861,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (rows == 0 || K == 0) return MOE_OK;
   colwise_launch(x, x_dtype, rows, K, offsets, E, axis, codes, scales, src_pair, row_w, k, rows, dev_status, stream,
                  sms);
@@ -890,7 +893,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (rows == 0 || K == 0) return MOE_OK;
   if (axis >= 1) {
     colwise_launch(in, in_dtype, rows, K, offsets, E, axis, codes, scales, nullptr, nullptr, 1, 0, nullptr, stream,
@@ -919,7 +922,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (G == 0 || R == 0 || C == 0) return MOE_OK;
   if (in_dtype == MOE_BF16) {
     const long long items = static_cast<long long>(G) * ((R / 32 + kTrRb - 1) / kTrRb) *
@@ -965,7 +968,7 @@ extern "C" moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, in
     return MOE_ERR_WORKSPACE;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   uint32_t* amax_bits = reinterpret_cast<uint32_t*>(tensor_scale + 1);
   cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) {

@@ -1131,7 +1131,9 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         for (int j = 0; j < kTopkMax; ++j) {
           if (j < ksel) {
             if (valid) {
-              const float w = p.renorm ? expf(tv[j] - tv[0]) / den : expf(tv[j] - run_m) / run_s;
+              // every expert masked (-inf): no softmax mass, weight 0
+              const float w = tv[0] == -INFINITY ? 0.f
+                              : p.renorm ? expf(tv[j] - tv[0]) / den : expf(tv[j] - run_m) / run_s;
               p.topk_idx[grow * ksel + j] = ti[j];
               p.topk_w[grow * ksel + j] = w;
             }
@@ -1334,7 +1336,7 @@ moe_status_t common_checks(const char* fn, const moe_operand_t* A, const moe_ope
     set_error("%s: null or misaligned pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (!device_is_sm103(sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(sms); dst != MOE_OK) return dst;
   return MOE_OK;
 }
 
@@ -1581,7 +1583,7 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * sizeof(int32_t), stream);
   if (e != cudaSuccess) {
     set_error("%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));

@@ -126,7 +126,7 @@ extern "C" moe_status_t moe_quantize_nvfp4(const void* in, moe_dtype_t in_dtype,
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   uint32_t* amax_bits = reinterpret_cast<uint32_t*>(tensor_scale + 1);
   cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) {

@@ -18,10 +18,12 @@
 // different host threads) race on it and give wrong results.
 //
 // In host code the array's name is only a host-side stand-in, so its device
-// address is looked up with cudaGetSymbolAddress, once per device, with that
-// device current, on the first call made on that device.  Make that first call
-// before any stream capture.
+// address is looked up with cudaGetSymbolAddress, with the device current, on the
+// first call made in each CUDA context (normally once per device; again after the
+// device's primary context was reset).  Make that first call before any stream
+// capture.
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -45,27 +47,59 @@ constexpr size_t kNoAllocScratchInts = 262144;   // 1 MiB
 
 __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
+// Looked-up addresses, keyed by the CUDA context they belong to.  The key is the
+// driver's context id, which no later context reuses: after cudaDeviceReset (or
+// any other teardown of the primary context) the new context gets a new id, so
+// an address that belonged to the old one is never handed out again.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int32_t* ptr;
+};
 std::mutex g_mu;
-int32_t* g_scratch_ptr[64] = {};
+std::vector<ScratchEntry> g_scratch;
 
-// Device address of the scratch array on the current device (looked up once).
-int32_t* scratch_on_current_device() {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(ptr);
+}
+
+// Device address of the scratch array in the current context (looked up once per
+// context).
+int32_t* scratch_in_current_context() {
+  // make the runtime bind the current device's primary context if nothing has yet
+  // (cudaSetDevice initialises it; it allocates nothing)
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    set_error("moe_permute_noalloc: no current CUDA device");
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+    set_error("moe_permute_noalloc: no usable CUDA device");
+    return nullptr;
+  }
+  static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) {
+    set_error("moe_permute_noalloc: cannot identify the current CUDA context");
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_permute_scratch);
-    if (e != cudaSuccess || !ptr) {
-      set_error("moe_permute_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+  for (const ScratchEntry& e : g_scratch)
+    if (e.ctx_id == id) return e.ptr;
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_permute_scratch);
+  if (e != cudaSuccess || !ptr) {
+    set_error("moe_permute_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  g_scratch.push_back({id, static_cast<int32_t*>(ptr)});
+  return static_cast<int32_t*>(ptr);
 }
 
 }  // namespace
@@ -89,8 +123,8 @@ extern "C" moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, 
     return MOE_ERR_WORKSPACE;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
-  int32_t* scratch = scratch_on_current_device();
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
+  int32_t* scratch = scratch_in_current_context();
   if (!scratch) return MOE_ERR_CUDA;
   return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp,
                         xp_dtype, xp_scales, scratch, dev_status, stream, sms, nullptr, nullptr);

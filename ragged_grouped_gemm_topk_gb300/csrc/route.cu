@@ -92,8 +92,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
       if (j == 0) top0 = bv;
     }
 
+    // a token whose experts are all masked (-inf) has no softmax mass: weight 0
     float w;
-    if (renormalize) {
+    if (top0 == -INFINITY) {
+      w = 0.f;
+    } else if (renormalize) {
       const float ex = lane < k ? expf(sel_v - top0) : 0.f;
       float s = ex;
 #pragma unroll
@@ -153,12 +156,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_bwd_kernel(
       for (int e = lane; e < E; e += 32) m = fmaxf(m, row[e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-      float s = 0.f;
-      for (int e = lane; e < E; e += 32) s += expf(row[e] - m);
+      if (m == -INFINITY) {
+        // every expert masked: no probability mass, no gradient
+        for (int e = lane; e < E; e += 32) out[e] = 0.f;
+      } else {
+        float s = 0.f;
+        for (int e = lane; e < E; e += 32) s += expf(row[e] - m);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-      const float scale = -inner / s;
-      for (int e = lane; e < E; e += 32) out[e] = expf(row[e] - m) * scale;
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+        const float scale = -inner / s;
+        for (int e = lane; e < E; e += 32) out[e] = expf(row[e] - m) * scale;
+      }
     }
     __syncwarp();
     if (lane < k && ej >= 0) out[ej] = wj * (dwj - inner);
@@ -194,7 +202,7 @@ extern "C" moe_status_t moe_route_topk(const float* logits, int T, int E, int k,
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   launch_pdl(zero_i32_kernel, (E + 255) / 256, 256, 0, stream, counts, E);
   if (T > 0) {
     const int V = (E + 31) / 32;
@@ -221,7 +229,7 @@ extern "C" moe_status_t moe_route_topk_bwd(const float* dw, const float* topk_w,
     return MOE_ERR_INVALID_ARG;
   }
   int sms = 0;
-  if (!device_is_sm103(&sms)) return MOE_ERR_UNSUPPORTED;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
   if (T == 0) return MOE_OK;
   const int wpb = kRouteThreads / 32;
   int grid = (T + wpb - 1) / wpb;

@@ -29,6 +29,7 @@ SMALL = [
     W.WORKLOADS[0].scaled(T=64, E=1, k=1, d=32, name="E1"),
     W.WORKLOADS[0].scaled(T=50, E=6, k=6, d=32, name="k=E"),
     W.WORKLOADS[0].scaled(T=77, E=1000, k=32, d=32, name="E1000-k32"),
+    W.WORKLOADS[0].scaled(T=300, E=1024, k=8, d=32, name="E1024-k8"),
 ]
 
 
@@ -486,3 +487,26 @@ def test_route_bwd(renormalize):
         sel = np.zeros_like(want, dtype=bool)
         np.put_along_axis(sel, o_idx.astype(np.int64), True, axis=1)
         assert (got[~sel] == 0).all()
+
+
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_route_fully_masked_token(renormalize):
+    """A token with every expert masked (-inf) gets the lowest expert ids with
+    weight 0 and a zero router gradient, like the oracle; the other tokens of the
+    batch are routed as usual."""
+    need_gpu()
+    w = W.WORKLOADS[2].scaled(T=96, E=40, k=4, name="masked")
+    lg = logits_dev(w)
+    lg[5] = -float("inf")
+    lg[70, 3:] = -float("inf")            # only three experts left for k = 4
+    idx, wt, counts = moe_gpu.moe_route_topk(lg, w.k, renormalize)
+    o_idx, o_w, o_counts = om.route_topk(lg.cpu().numpy(), w.k, renormalize)
+    assert (i64(idx) == o_idx).all() and (i64(counts) == o_counts).all()
+    got = f64(wt)
+    assert not np.isnan(got).any() and (got[5] == 0).all() and got[70, 3] == 0
+    assert np.abs(got - o_w).max() <= TOL_W
+    dw = W.make_matrix(w.T, w.k, seed=4, dtype=torch.float32, device="cuda")
+    dl = f64(moe_gpu.moe_route_topk_bwd(dw, wt, idx, w.E, logits=lg, renormalize=renormalize))
+    want = om.route_bwd(f64(dw), o_w, o_idx, lg.cpu().numpy(), renormalize)
+    assert not np.isnan(dl).any() and (dl[5] == 0).all()
+    assert np.abs(dl - want).max() < 1e-5

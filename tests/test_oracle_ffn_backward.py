@@ -303,3 +303,85 @@ def test_expert_backward_mxfp8_matches_layer_backward():
             np.testing.assert_allclose(got[name], bwd[name][lo:hi], rtol=1e-12, atol=1e-13, err_msg=name)
         np.testing.assert_allclose(got["dW1"], bwd["dW1"][e], rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(got["dW2"], bwd["dW2"][e], rtol=1e-12, atol=1e-13)
+
+
+def _mx_blockwise_row(v):
+    """MXFP8 values of one row along its length, each 32-element block quantised on
+    its own (a [1, 32] call of the row-wise quantiser, pinned separately)."""
+    from oracle import mxfp8
+    v = np.asarray(v, dtype=np.float64)
+    out = np.empty_like(v)
+    for b in range(0, v.size, 32):
+        blk = v[None, b:b + 32]
+        out[b:b + 32] = mxfp8.dequantize_rowwise(*mxfp8.quantize_rowwise(blk))[0]
+    return out
+
+
+def _fp32_tensor_scale(a):
+    """NVFP4 tensor encode scale of a whole tensor, from its definition:
+    fp32(2688 / fp32(amax)), 1 for an all-zero tensor."""
+    amax = np.float32(np.abs(np.asarray(a, dtype=np.float32)).max())
+    return np.float32(1.0) if amax == 0 else np.float32(np.float32(2688.0) / amax)
+
+
+def _nv_blockwise_row(v, g):
+    """NVFP4 values of one row, each 16-element block quantised on its own with the
+    given tensor scale g (a [1, 16] call of the pinned NVFP4 quantiser)."""
+    from oracle import nvfp4
+    v = np.asarray(v, dtype=np.float32)
+    out = np.empty(v.size)
+    for b in range(0, v.size, 16):
+        c, s, gg = nvfp4.quantize(v[None, b:b + 16], g=g)
+        out[b:b + 16] = nvfp4.dequantize(c, s, gg)[0]
+    return out
+
+
+def _silu_mul_torch(g, u):
+    return (F.silu(torch.from_numpy(np.asarray(g, dtype=np.float64))) *
+            torch.from_numpy(np.asarray(u, dtype=np.float64))).numpy()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_blockscaled_forward_elements_from_blockwise_quantisation(fmt):
+    """Each block-scaled forward GEMM element by element, with its operands built
+    here one block at a time: GU[r, n] = <q(Xp[r]), q(W1[e][n])>, H = silu(G) U
+    (torch), Yp[r, c] = <q(H[r]), q(W2[e][c])>, y = sum_j w_j Yp[dest_row[t, j]].
+    MXFP8 blocks are 32 elements with their own E8M0 scale; NVFP4 blocks are 16
+    elements with an E4M3 scale under one fp32 tensor scale per tensor: one for
+    Xp, one for the whole W1 stack (every expert), one for H, one for the whole W2
+    stack."""
+    T, d, E, k, f = 40, 64, 3, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=111)
+    if fmt == "nvfp4":
+        x, W1, W2 = (np.asarray(a, dtype=np.float32).astype(np.float64) for a in (x, W1, W2))
+    fwd = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=fmt == "mxfp8", nvfp4_operands=fmt == "nvfp4")
+    off, src = fwd["offsets"], fwd["src_pair"]
+    Xp = x[src // k]
+    if fmt == "mxfp8":
+        qx = qw1 = qh = qw2 = _mx_blockwise_row
+    else:
+        g_x, g_w1, g_w2 = _fp32_tensor_scale(Xp), _fp32_tensor_scale(W1), _fp32_tensor_scale(W2)
+        qx = lambda v: _nv_blockwise_row(v, g_x)      # noqa: E731
+        qw1 = lambda v: _nv_blockwise_row(v, g_w1)    # noqa: E731
+        qw2 = lambda v: _nv_blockwise_row(v, g_w2)    # noqa: E731
+    # GU and H of every row, from the blockwise operands
+    GU = np.zeros((T * k, 2 * f))
+    for e in range(E):
+        for r in range(int(off[e]), int(off[e + 1])):
+            xr = qx(Xp[r])
+            GU[r] = [xr @ qw1(W1[e][n]) for n in range(2 * f)]
+    np.testing.assert_allclose(fwd["GU"], GU, rtol=1e-12, atol=1e-13)
+    H = _silu_mul_torch(GU[:, :f], GU[:, f:])
+    np.testing.assert_allclose(fwd["H"], H, rtol=1e-12, atol=1e-13)
+    if fmt == "nvfp4":
+        g_h = _fp32_tensor_scale(H)
+        qh = lambda v: _nv_blockwise_row(v, g_h)      # noqa: E731
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        for r in sorted({lo, (lo + hi) // 2, hi - 1} & set(range(lo, hi))):
+            hr = qh(H[r])
+            for c in (0, 7, d - 1):
+                np.testing.assert_allclose(fwd["Yp"][r, c], hr @ qw2(W2[e][c]), rtol=1e-12, atol=1e-13)
+    for t in (0, T // 2, T - 1):
+        want = sum(fwd["w"][t, j] * fwd["Yp"][fwd["dest_row"][t, j]] for j in range(k))
+        np.testing.assert_allclose(fwd["y"][t], want, rtol=1e-13, atol=1e-14)

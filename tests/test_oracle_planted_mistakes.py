@@ -177,3 +177,45 @@ def test_router_and_capacity_pins_catch_planted_mistake(monkeypatch, attr, fake,
     monkeypatch.setattr(moe, attr, fake)
     with pytest.raises(AssertionError):
         check()
+
+
+_real_layer_forward = moe.layer_forward
+
+
+def _layer_forward_variant(h_quantised=True, w1_scale_per_expert=False):
+    """The oracle's block-scaled forward with one step changed: H fed to GEMM2
+    unquantised, or W1 given one NVFP4 tensor scale per expert instead of one for
+    the stack."""
+    def fwd(x, logits, W1, W2, k, renormalize=True, mxfp8_operands=False, nvfp4_operands=False):
+        out = _real_layer_forward(x, logits, W1, W2, k, renormalize)
+        rt = moe.nvfp4_roundtrip if nvfp4_operands else moe.mx_roundtrip
+        off = out["offsets"]
+        if w1_scale_per_expert:
+            W1q = np.stack([rt(W1[e]) for e in range(W1.shape[0])])
+        else:
+            W1q = rt(W1)
+        GU = moe.grouped_gemm(rt(out["Xp"]), W1q, off)
+        H = moe.swiglu(GU)
+        Yp = moe.grouped_gemm(rt(H) if h_quantised else H, rt(W2), off)
+        out.update(GU=GU, H=H, Yp=Yp, y=moe.combine(Yp, out["dest_row"], out["w"]))
+        return out
+    return fwd
+
+
+@pytest.mark.parametrize("fake,fmt", [
+    (_layer_forward_variant(h_quantised=False), "nvfp4"),
+    (_layer_forward_variant(w1_scale_per_expert=True), "nvfp4"),
+    (_layer_forward_variant(h_quantised=False), "mxfp8"),
+], ids=["nvfp4-h-unquantised", "nvfp4-w1-scale-per-expert", "mxfp8-h-unquantised"])
+def test_blockscaled_forward_pins_catch_planted_mistake(monkeypatch, fake, fmt):
+    monkeypatch.setattr(moe, "layer_forward", fake)
+    with pytest.raises(AssertionError):
+        ffn_pins.test_blockscaled_forward_elements_from_blockwise_quantisation(fmt)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_blockscaled_forward_variant_without_mistake_passes(monkeypatch, fmt):
+    """The rebuilt forward with no step changed passes the same pin, so the
+    failures above come from the planted step alone."""
+    monkeypatch.setattr(moe, "layer_forward", _layer_forward_variant())
+    ffn_pins.test_blockscaled_forward_elements_from_blockwise_quantisation(fmt)

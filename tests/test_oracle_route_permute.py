@@ -90,6 +90,24 @@ def test_route_masked_experts():
     assert w[0, 2] == 0.0
 
 
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_route_fully_masked_token_has_zero_weights(renormalize):
+    """A token whose experts are all masked has no softmax mass: its slots hold the
+    lowest expert ids (every logit ties) with weight exactly 0, and its router
+    gradient is 0; the other tokens are unaffected (same as routed alone)."""
+    lg = np.array([[-np.inf] * 5, [0.5, -np.inf, 2.0, 1.0, -1.0]], dtype=np.float32)
+    idx, w, counts = moe.route_topk(lg, 3, renormalize)
+    assert idx[0].tolist() == [0, 1, 2]
+    assert (w[0] == 0.0).all() and not np.isnan(w).any()
+    idx1, w1, _ = moe.route_topk(lg[1:], 3, renormalize)
+    assert (idx[1] == idx1[0]).all() and (w[1] == w1[0]).all()
+    assert counts.tolist() == [2, 1, 2, 1, 0]
+    dl = moe.route_bwd(np.ones((2, 3)), w, idx, lg, renormalize)
+    assert (dl[0] == 0.0).all() and not np.isnan(dl).any()
+    dl1 = moe.route_bwd(np.ones((1, 3)), w1, idx1, lg[1:], renormalize)
+    np.testing.assert_array_equal(dl[1], dl1[0])
+
+
 def _counting_permutation(idx, E):
     """Sequential construction: visit tokens in order and hand each (token, slot)
     the next free row of its expert's group."""

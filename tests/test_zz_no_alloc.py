@@ -47,7 +47,11 @@ def _noalloc(x, idx, counts, E, quant):
 def test_noalloc_matches_workspace_entry_point_twice(quant):
     need_gpu()
     cases = [W.BY_NAME["dsv3-bf16-train"].scaled(T=3000, d=256, name="big"),
-             W.BY_NAME["qwen3-235b-bf16"].scaled(T=333, E=64, k=4, d=128, name="small")]
+             W.BY_NAME["qwen3-235b-bf16"].scaled(T=333, E=64, k=4, d=128, name="small"),
+             # the largest expert count, and a problem that fills the scratch exactly
+             # (ceil(65536 / 256) * 1024 = 262144 entries, the last one included)
+             W.BY_NAME["tiny-fp32"].scaled(T=300, E=1024, k=8, d=32, name="E1024"),
+             W.BY_NAME["tiny-fp32"].scaled(T=65536, E=1024, k=1, d=32, name="at-bound")]
     for w in cases:
         x = W.make_x(w, "cuda")
         lg = torch.from_numpy(W.make_logits(w)).cuda()
