@@ -519,3 +519,50 @@ def expert_wgrad_sampled(X_e, dYp_e, w1, w2, w1_rows, w2_cols):
         h = silu(g) * u
         dw2[:, i] = dY.T @ h
     return dw1, dw2
+
+
+def tokens_forward(x_rows, logits_rows, W1, W2, k, renormalize=True, mxfp8_operands=False):
+    """``token_forward`` for several tokens at once, visiting each expert once: for
+    expert e (ascending id), every (token, slot) routed to it adds w * FFN_e(x[t]).
+    The same per-token sums as ``token_forward``; W1/W2 may be callables
+    e -> expert weights, each called once per expert the tokens use (so a large
+    layer's weights can be fetched one expert at a time)."""
+    lg = np.asarray(logits_rows, dtype=np.float32)
+    idx, w, _ = route_topk(lg, k, renormalize)
+    get1 = W1 if callable(W1) else (lambda e: W1[e])
+    get2 = W2 if callable(W2) else (lambda e: W2[e])
+    X = np.asarray(x_rows, dtype=np.float64)
+    if mxfp8_operands:
+        X = mx_roundtrip(X)
+    y = np.zeros_like(X)
+    for e in np.unique(idx):
+        w1, w2 = np.asarray(get1(int(e)), np.float64), np.asarray(get2(int(e)), np.float64)
+        if mxfp8_operands:
+            w1, w2 = mx_roundtrip(w1), mx_roundtrip(w2)
+        t, j = np.nonzero(idx == e)
+        h = swiglu(X[t] @ w1.T)
+        if mxfp8_operands:
+            h = mx_roundtrip(h)
+        y[t] += w[t, j][:, None] * (h @ w2.T)
+    return y
+
+
+def tokens_backward(x_rows, logits_rows, dy_rows, W1, W2, k, renormalize=True):
+    """``token_backward`` for several tokens at once, visiting each expert once:
+    returns (dx [n, d], dlogits [n, E]).  W1/W2 may be callables e -> weights."""
+    lg = np.asarray(logits_rows, dtype=np.float32)
+    idx, w, _ = route_topk(lg, k, renormalize)
+    get1 = W1 if callable(W1) else (lambda e: W1[e])
+    get2 = W2 if callable(W2) else (lambda e: W2[e])
+    X = np.asarray(x_rows, dtype=np.float64)
+    dY = np.asarray(dy_rows, dtype=np.float64)
+    dx = np.zeros_like(X)
+    dw = np.zeros(idx.shape)
+    for e in np.unique(idx):
+        w1, w2 = np.asarray(get1(int(e)), np.float64), np.asarray(get2(int(e)), np.float64)
+        t, j = np.nonzero(idx == e)
+        GU = X[t] @ w1.T
+        dw[t, j] = np.einsum("nd,nd->n", dY[t], swiglu(GU) @ w2.T)
+        dH = (w[t, j][:, None] * dY[t]) @ w2
+        np.add.at(dx, t, dswiglu(dH, GU) @ w1)
+    return dx, route_bwd(dw, w, idx, lg, renormalize)

@@ -153,11 +153,15 @@ class MoELayer:
                           dest_row=self.dest_row, src_pair=self.src_pair, xp=self.xp,
                           workspace=self.workspace, dev_status=self.dev_status)
 
-    def expert_mlp(self):
+    def expert_mlp(self, mark=None):
+        """GEMM1 (+ SwiGLU), then GEMM2.  ``mark(name)``, when given, is called right
+        after the kernels of GEMM1 are enqueued (timing hooks; nothing else)."""
+        mark = mark or (lambda name: None)
         if self.dtype == "nvfp4":
             B.moe_grouped_gemm_fwd(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
                                    B_scales=self.W1s, A_tensor_scale=self.xg, B_tensor_scale=self.W1g,
                                    out=self.h, dev_status=self.dev_status)
+            mark("gemm1")
             B.moe_quantize_nvfp4(self.h, codes=self.hq, scales=self.hs, tensor_scale=self.hg)
             B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
                                    A_tensor_scale=self.hg, B_tensor_scale=self.W2g, out=self.yp,
@@ -168,17 +172,20 @@ class MoELayer:
                                    B_scales=self.W1s, out=self.h, preact=self.gu, dev_status=self.dev_status)
             B.moe_quantize_mxfp8_grouped(self.h, codes=self.hq, scales=self.hs)
             B.moe_quantize_mxfp8_grouped(self.h, self.offsets, self.E, codes=self.hcq, scales=self.hcs, axis=2)
+            mark("gemm1")
             B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
                                    out=self.yp, dev_status=self.dev_status)
         elif self.dtype == "mxfp8":
             B.moe_grouped_gemm_fwd_mxfp8_out(self.xq, self.W1q, self.offsets, epi="swiglu", A_scales=self.xs,
                                              B_scales=self.W1s, codes=self.hq, scales=self.hs,
                                              dev_status=self.dev_status)
+            mark("gemm1")
             B.moe_grouped_gemm_fwd(self.hq, self.W2q, self.offsets, A_scales=self.hs, B_scales=self.W2s,
                                    out=self.yp, dev_status=self.dev_status)
         else:
             B.moe_grouped_gemm_fwd(self.xp, self.W1, self.offsets, epi="swiglu", out=self.h,
                                    preact=self.gu, dev_status=self.dev_status)
+            mark("gemm1")
             B.moe_grouped_gemm_fwd(self.h, self.W2, self.offsets, out=self.yp, dev_status=self.dev_status)
 
     def combine(self, out=None):
@@ -212,11 +219,14 @@ class MoELayer:
         return 7 + (3 if self.dtype == "mxfp8" else 0)
 
     # ------------------------------------------------------------------ backward
-    def backward(self, dy, logits=None, dx_out=None):
+    def backward(self, dy, logits=None, dx_out=None, mark=None):
         """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward);
-        dx goes to ``dx_out`` when given."""
+        dx goes to ``dx_out`` when given.  ``mark(name)``, when given, is called after
+        each step's kernels are enqueued (combine_bwd, dgrad2, wgrad2, [quant_dgu],
+        dgrad1, wgrad1, dispatch_bwd, route_bwd): timing hooks, nothing else."""
         if not self.training:
             raise RuntimeError("construct the layer with training=True")
+        mark = mark or (lambda name: None)
         st = self.dev_status
         if self.dtype == "mxfp8":
             off, E = self.offsets, self.E
@@ -226,28 +236,41 @@ class MoELayer:
                                               scales=self.dys, dw=self.dw, dev_status=st)
             B.moe_quantize_mxfp8_gathered(dy, self.src_pair, off, E, self.k, row_w=self.topk_w, codes=self.dycq,
                                           scales=self.dycs, axis=2, dev_status=st)
+            mark("combine_bwd")
             B.moe_grouped_gemm_dgrad_mxfp8(self.dyq, self.W2t, off, dC_scales=self.dys, BT_scales=self.W2ts,
                                            epi="dswiglu", preact=self.gu, out=self.dgu, dev_status=st)
+            mark("dgrad2")
             B.moe_grouped_gemm_wgrad(self.hcq, self.dycq, off, E, A_scales=self.hcs, dC_scales=self.dycs,
                                      out=self.dW2, dev_status=st)
+            mark("wgrad2")
             B.moe_quantize_mxfp8_grouped(self.dgu, codes=self.dgq, scales=self.dgs)
             B.moe_quantize_mxfp8_grouped(self.dgu, off, E, codes=self.dgcq, scales=self.dgcs, axis=2)
+            mark("quant_dgu")
             B.moe_grouped_gemm_dgrad_mxfp8(self.dgq, self.W1t, off, dC_scales=self.dgs, BT_scales=self.W1ts,
                                            out=self.dxp, dev_status=st)
+            mark("dgrad1")
             B.moe_grouped_gemm_wgrad(self.xcq, self.dgcq, off, E, A_scales=self.xcs, dC_scales=self.dgcs,
                                      out=self.dW1, dev_status=st)
+            mark("wgrad1")
         else:
             B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
                                         dev_status=st)
+            mark("combine_bwd")
             B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
                                      out=self.dgu, dev_status=st)
+            mark("dgrad2")
             B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
+            mark("wgrad2")
             B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
+            mark("dgrad1")
             B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
+            mark("wgrad1")
         dx = self.dx if dx_out is None else dx_out
         B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=dx, dev_status=st)
+        mark("dispatch_bwd")
         if logits is None:
             logits = self.logits          # the fused router's own (None is fine when renormalised)
         B.moe_route_topk_bwd(self.dw, self.topk_w, self.topk_idx, self.E, logits=logits,
                              renormalize=self.renormalize, out=self.dlogits, dev_status=st)
+        mark("route_bwd")
         return dx, self.dlogits, self.dW1, self.dW2

@@ -86,3 +86,28 @@ def test_routing_summary_hand_worked():
     assert r == {"max_count": 1000, "empty_experts": 2, "median_nonempty": 93.5, "experts_below_128_rows": 6,
                  "top8_share": 0.9983, "tile128_padding": 0.2961}
     assert bench.routing_summary([0, 0])["tile128_padding"] == 0.0
+
+
+def test_gpus_flag_spawns_ranks_without_torchrun():
+    """--gpus 2 in a plain launch starts the two ranks itself (gloo on the CPU):
+    rank 0 prints the one line with n_gpus 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "0", "--workload", "tiny-fp32"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+
+
+def test_gpus_flag_mismatch_fails_loudly():
+    """Under a launcher whose WORLD_SIZE differs from --gpus the bench stops with an
+    error instead of timing the wrong number of replicas."""
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "3", "--steps", "1",
+                        "--warmup", "0", "--workload", "tiny-fp32"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=120, env=env)
+    assert r.returncode != 0
+    assert "does not match WORLD_SIZE" in r.stderr
+    assert not _json_lines(r.stdout)

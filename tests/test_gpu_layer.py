@@ -65,7 +65,7 @@ def _h_values(layer):
     return omx.dequantize_rowwise(layer.hq.cpu().numpy(), layer.hs.cpu().numpy())
 
 
-def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=6, rows_per_expert=12, seed=0):
+def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=16, rows_per_expert=12, seed=0):
     """Full integer parity + sampled float parity for a large workload."""
     rng = np.random.default_rng(seed)
     lg_h = lg.cpu().numpy()
@@ -105,11 +105,13 @@ def check_large_forward(w, layer, x, W1, W2, lg, n_tokens=6, rows_per_expert=12,
     assert rel_l2(np.concatenate(h_got), np.concatenate(h_want)) < tol
     assert rel_l2(np.concatenate(y_got), np.concatenate(y_want)) < tol
 
-    # sampled tokens end to end
+    # sampled tokens end to end (each routed expert's weights fetched once)
+    cache.clear()
     toks = np.sort(rng.choice(w.T, size=n_tokens, replace=False))
-    got = f64(layer.y[torch.from_numpy(toks).cuda()])
-    want = np.stack([om.token_forward(f64(x[t]), lg_h[t], lambda e: get(e, 1), lambda e: get(e, 2),
-                                      w.k, w.renormalize, mxfp8_operands=mx) for t in toks])
+    tt = torch.from_numpy(toks).cuda()
+    got = f64(layer.y[tt])
+    want = om.tokens_forward(f64(x[tt]), lg_h[toks], lambda e: f64(W1[e]), lambda e: f64(W2[e]),
+                             w.k, w.renormalize, mxfp8_operands=mx)
     assert rel_l2(got, want) < tol
 
 
@@ -162,6 +164,67 @@ def test_graph_replay_with_new_logits():
         assert (i64(layer.counts) == ref["counts"]).all()
         assert (i64(layer.src_pair) == ref["src_pair"]).all()
         assert rel_l2(f64(layer.y), ref["y"]) < TOL_BF16
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_graph_replay_training_step(dtype):
+    """The training step (forward + backward) captured once in one CUDA graph, as
+    the benchmark times it, and replayed three times with new x, logits and dy
+    written into the captured buffers: the routing (and the per-expert counts,
+    some experts empty) changes on the device only, and after every replay each
+    output matches the float64 oracle: maps bit-exact, y, dx, dlogits, dW1, dW2
+    within the stated bound, experts without rows exactly zero."""
+    import dataclasses
+    need_gpu()
+    base = W.BY_NAME["dsv3-mxfp8-train" if dtype == "mxfp8" else "dsv3-bf16-train"]
+    w = base.scaled(T=512, E=64, d=512, f=512, name=f"graph-train-{dtype}")
+    layer, x, W1, W2, lg = _build(w, training=True)
+    x_buf, lg_buf, dy_buf = x.clone(), lg.clone(), W.make_dy(w, "cuda")
+    tol = TOL_MXFP8 if dtype == "mxfp8" else TOL_BF16
+
+    def step():
+        layer.forward(x_buf, lg_buf)
+        layer.backward(dy_buf, lg_buf)
+
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()                                # warm-up outside capture
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    seen = set()
+    for rep in range(3):
+        wr = dataclasses.replace(w, seed=w.seed + 17 * (rep + 1))
+        x_buf.copy_(W.make_x(wr, "cuda"))
+        lg_buf.copy_(logits_dev(wr))
+        dy_buf.copy_(W.make_dy(wr, "cuda"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(layer.dev_status.item()) == 0
+        lg_h = lg_buf.cpu().numpy()
+        mx = dtype == "mxfp8"
+        ref = om.layer_forward(f64(x_buf), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=mx)
+        bwd = om.layer_backward(ref, f64(dy_buf), f64(x_buf), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=mx)
+        assert (i64(layer.counts) == ref["counts"]).all()
+        assert (i64(layer.offsets) == ref["offsets"]).all()
+        assert (i64(layer.dest_row) == ref["dest_row"]).all()
+        assert (i64(layer.src_pair) == ref["src_pair"]).all()
+        seen.add(tuple(ref["counts"].tolist()))
+        for name, got, want in (("y", layer.y, ref["y"]), ("dx", layer.dx, bwd["dx"]),
+                                ("dlogits", layer.dlogits, bwd["dlogits"]), ("dW1", layer.dW1, bwd["dW1"]),
+                                ("dW2", layer.dW2, bwd["dW2"])):
+            err = rel_l2(f64(got), want)
+            assert err < tol, (rep, name, err)
+        empty = np.nonzero(ref["counts"] == 0)[0]
+        assert len(empty) > 0
+        e_t = torch.from_numpy(empty).cuda()
+        assert int(torch.count_nonzero(layer.dW1[e_t]).item()) == 0
+        assert int(torch.count_nonzero(layer.dW2[e_t]).item()) == 0
+    assert len(seen) == 3                     # the counts changed between replays
 
 
 @pytest.mark.parametrize("w", [W.BY_NAME["dsv3-bf16-train"].scaled(T=256, d=256, f=128, name="dsv3-train-small"),
@@ -250,7 +313,7 @@ def test_mxfp8_layer_full_size_sampled():
     layer.forward(x, lg)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
-    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=4, rows_per_expert=8)
+    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=16, rows_per_expert=8)
 
 
 def test_train_full_size_sampled():
@@ -266,7 +329,7 @@ def test_train_full_size_sampled():
     layer.backward(dy, lg)
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
-    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=2, rows_per_expert=8)
+    check_large_forward(w, layer, x, W1, W2, lg, n_tokens=16, rows_per_expert=8)
 
     rng = np.random.default_rng(5)
     lg_h = lg.cpu().numpy()
@@ -279,17 +342,12 @@ def test_train_full_size_sampled():
             cache[(e, which)] = f64((W1 if which == 1 else W2)[e])
         return cache[(e, which)]
 
-    toks = np.sort(rng.choice(w.T, size=2, replace=False))
-    got_dx, want_dx, got_dl, want_dl = [], [], [], []
-    for t in toks:
-        dx_t, dl_t = om.token_backward(f64(x[t]), lg_h[t], f64(dy[t]), lambda e: get(e, 1),
-                                       lambda e: get(e, 2), w.k)
-        got_dx.append(f64(layer.dx[t]))
-        want_dx.append(dx_t)
-        got_dl.append(f64(layer.dlogits[t]))
-        want_dl.append(dl_t)
-    assert rel_l2(np.stack(got_dx), np.stack(want_dx)) < TOL_BF16
-    assert rel_l2(np.stack(got_dl), np.stack(want_dl)) < TOL_BF16
+    toks = np.sort(rng.choice(w.T, size=16, replace=False))
+    tt = torch.from_numpy(toks).cuda()
+    want_dx, want_dl = om.tokens_backward(f64(x[tt]), lg_h[toks], f64(dy[tt]), lambda e: f64(W1[e]),
+                                          lambda e: f64(W2[e]), w.k)
+    assert rel_l2(f64(layer.dx[tt]), want_dx) < TOL_BF16
+    assert rel_l2(f64(layer.dlogits[tt]), want_dl) < TOL_BF16
 
     nz = np.nonzero(counts)[0]
     order = nz[np.argsort(counts[nz], kind="stable")]

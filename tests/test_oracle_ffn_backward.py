@@ -385,3 +385,26 @@ def test_blockscaled_forward_elements_from_blockwise_quantisation(fmt):
     for t in (0, T // 2, T - 1):
         want = sum(fwd["w"][t, j] * fwd["Yp"][fwd["dest_row"][t, j]] for j in range(k))
         np.testing.assert_allclose(fwd["y"][t], want, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+def test_tokens_forward_and_backward_match_layer(mx):
+    """The expert-major forms (each expert's weights fetched once) give the layer's
+    rows: forward with and without MXFP8 operands, backward (dx, dlogits)."""
+    T, d, E, k, f = 30, 64, 5, 2, 32
+    lg, x, W1, W2 = _problem(T, d, E, k, f, seed=121, empty=(1,))
+    dy = np.random.default_rng(122).standard_normal((T, d))
+    fwd = moe.layer_forward(x, lg, W1, W2, k, mxfp8_operands=mx)
+    toks = np.array([0, 3, 17, 29])
+    fetched = []
+    def get1(e):
+        fetched.append(e)
+        return W1[e]
+    y = moe.tokens_forward(x[toks], lg[toks], get1, lambda e: W2[e], k, mxfp8_operands=mx)
+    np.testing.assert_allclose(y, fwd["y"][toks], rtol=1e-12, atol=1e-13)
+    assert len(fetched) == len(set(fetched))
+    if not mx:
+        bwd = moe.layer_backward(fwd, dy, x, lg, W1, W2, k)
+        dx, dl = moe.tokens_backward(x[toks], lg[toks], dy[toks], W1, W2, k)
+        np.testing.assert_allclose(dx, bwd["dx"][toks], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(dl, bwd["dlogits"][toks], rtol=1e-11, atol=1e-13)
