@@ -21,10 +21,14 @@
 // Tiles are enumerated on the device from `offsets`, so the host never learns the
 // per-expert sizes:
 //   forward / dgrad  expert e owns ceil(count_e / 128) row tiles x the column
-//                    tiles; row tiles vary fastest so neighbouring CTAs share a
-//                    weight slice in L2.  Rows of the last row tile past the
+//                    tiles, taken in blocks of row tiles that fit L2 (all column
+//                    tiles of a block, row tiles fastest), so neighbouring CTAs
+//                    share a weight slice and each activation row is read from
+//                    DRAM about once.  Rows of the last row tile past the
 //                    group's end are computed but never stored.
-//   wgrad            every expert owns ceil(N/128) x ceil(K/256) tiles of dB[e];
+//   wgrad            every expert owns ceil(N/128) x ceil(K/256) tiles of dB[e]
+//                    (experts largest first, so the equal tiles of a big expert
+//                    run in step on every SM and share its rows in L2);
 //                    the contraction runs over the group's own rows in 64-row
 //                    blocks; rows of the last block past the group's end are
 //                    zeroed in shared memory (and whole 16-row MMA steps beyond it
@@ -57,11 +61,11 @@ constexpr int kSfAStage = 2048;                   // MXFP8: raw A scale rows, 12
 constexpr int kSfBStage = 4096;                   // MXFP8: raw B scale rows, 256 x 16 bytes
 constexpr int kSfSlot = kSfAStage + kSfBStage;    // one raw scale slot (4 K-blocks' worth)
 constexpr int kAtomBytes = 1536;                  // MXFP8 per-stage atoms: A 512 B, B 2 x 512 B
-// Forward kernels' extra shared memory (after the operand stages): one epilogue
-// staging box per epilogue warp (32 rows x 64 bytes: 32 bf16 or 64 E4M3 columns;
-// 1 KB aligned for the 64-byte swizzle), then for MXFP8 the scale atoms of every
-// stage and the two raw scale-row slots.  64-byte boxes measured faster than
-// 128-byte ones for bf16 too (and MXFP8 has room for no more).
+// Forward kernels' extra shared memory (after the operand stages): epilogue staging
+// boxes (two per epilogue warp, one for MXFP8; 32 rows x 64 bytes: 32 bf16 or 64
+// E4M3 columns; 1 KB aligned for the 64-byte swizzle), then for MXFP8 the scale
+// atoms of every stage and the two raw scale-row slots.  64-byte boxes measured
+// faster than 128-byte ones for bf16 too (and MXFP8 has room for no more).
 constexpr int kEpiRowBytes = 64;
 constexpr int kEpiBox = 32 * kEpiRowBytes;
 constexpr int kEpiOff = 0;
@@ -224,6 +228,15 @@ struct Tile {
 
 __device__ __forceinline__ bool group_ok(int beg, int end, int M) { return beg >= 0 && end >= beg && end <= M; }
 
+// Forward / dgrad raster: an expert's tiles are taken in blocks of `rb` row tiles,
+// all column tiles of a block before the next block, row tiles fastest inside it.
+// rb is chosen so that a block's A rows (rb x 128 rows of the contraction) take about
+// this many bytes: they stay in L2 while every column tile of the block reads them,
+// so each A row comes from DRAM about once instead of once per column tile (the hot
+// experts of a skewed layer hold far more rows than L2), and the block's column
+// slices of B, read by its rb row tiles, stay in L2 as well.
+constexpr long long kRasterABytes = 32ll << 20;
+
 template <int kMode, int kEpi>
 struct Geo {
   int nt;       // column tiles per row tile (fwd/dgrad); dB row tiles (wgrad)
@@ -232,8 +245,10 @@ struct Geo {
   int bn_out;   // output columns per tile
   int kb_fixed; // contraction blocks (fwd/dgrad)
   int mn_rows;  // wgrad: contraction rows per stage
+  int rb;       // fwd/dgrad: row tiles per raster block
   __device__ Geo(const Params& p, int elem_bytes, int bn) {
     mn_rows = elem_bytes == 1 ? kMxWgRows : kMnRows;
+    rb = 1;
     if (kMode == kWgrad) {
       nt = (p.N + kBM - 1) / kBM;
       nt2 = (p.K + kBN - 1) / kBN;
@@ -247,6 +262,10 @@ struct Geo {
       nt2 = 1;
       kb_fixed = kMode == kFwd ? (p.K * elem_bytes + kBKBytes - 1) / kBKBytes
                                : (p.N + kMnRows - 1) / kMnRows;
+      const long long a_row = kMode == kFwd ? static_cast<long long>(p.K) * elem_bytes
+                                            : static_cast<long long>(p.N) * 2;   // dgrad: dC is bf16
+      const long long r = kRasterABytes / (static_cast<long long>(kBM) * (a_row > 0 ? a_row : 1));
+      rb = r < 1 ? 1 : (r > 1024 ? 1024 : static_cast<int>(r));
     }
   }
   __device__ int tiles_of(int cnt) const {
@@ -285,10 +304,13 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
     t.kblocks = (cnt + g.mn_rows - 1) / g.mn_rows;
   } else {
     const int mt = (cnt + kBM - 1) / kBM;   // >= 1: only non-empty groups own tiles
-    t.row0 = beg + (local % mt) * kBM;
+    const int blk = local / (g.rb * g.nt);   // raster block (see kRasterABytes)
+    const int rem = local - blk * g.rb * g.nt;
+    const int in_blk = mt - blk * g.rb < g.rb ? mt - blk * g.rb : g.rb;   // row tiles in this block
+    t.row0 = beg + (blk * g.rb + rem % in_blk) * kBM;
     const int left = beg + cnt - t.row0;
     t.rows = left < kBM ? left : kBM;
-    t.col0 = (local / mt) * g.bn_out;
+    t.col0 = (rem / in_blk) * g.bn_out;
     t.n0 = 0;
     t.kblocks = g.kb_fixed;
   }
@@ -296,40 +318,45 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
 }
 
 // Per-expert tile prefix in shared memory (all threads participate).  A group
-// whose offsets are out of range is flagged and treated as empty.
+// whose offsets are out of range is flagged and treated as empty.  `scratch` is
+// shared memory for E ints that nothing else uses yet (the first operand stage).
 template <int kMode, int kEpi>
-__device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p) {
+__device__ void build_tiles(Smem& s, const Geo<kMode, kEpi>& g, const Params& p, int* scratch) {
   const int32_t* offs = p.offsets;
   if (kMode == kWgrad) {
-    // expert list: groups with rows in id order, then empty (or invalid) ones
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      int nh = 0;
-      for (int base = 0; base < p.E; base += 32) {
-        const int e = base + lane;
-        bool rows = false;
-        if (e < p.E) {
-          const bool ok = group_ok(offs[e], offs[e + 1], p.M);
-          if (!ok && blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
-          rows = ok && offs[e + 1] > offs[e];
-        }
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, rows);
-        if (rows) s.prefix[nh + __popc(m & ((1u << lane) - 1u))] = e;
-        nh += __popc(m);
-      }
-      int nl = 0;
-      for (int base = 0; base < p.E; base += 32) {
-        const int e = base + lane;
-        const bool none = e < p.E && !(group_ok(offs[e], offs[e + 1], p.M) && offs[e + 1] > offs[e]);
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, none);
-        if (none) s.prefix[nh + nl + __popc(m & ((1u << lane) - 1u))] = e;
-        nl += __popc(m);
-      }
-      if (lane == 0) {
-        s.nnz = nh;
-        s.total_tiles = nh * g.nt * g.nt2;
-      }
+    // Expert list: the experts with rows by row count, largest first (ties: lower
+    // id), then the empty (or invalid) ones in id order.  Tiles are dealt to the
+    // CTAs round-robin, so the equal-cost tiles of one expert run side by side on
+    // every SM, in step through its rows, and share them in L2; the many short
+    // tiles of the small experts come last.
+    int* cnt = scratch;
+    if (threadIdx.x == 0) s.nnz = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+      const int beg = offs[e], end = offs[e + 1];
+      const bool ok = group_ok(beg, end, p.M);
+      if (!ok && blockIdx.x == 0) flag_error(p.status, MOE_DEV_BAD_INDEX);
+      cnt[e] = ok ? end - beg : 0;
+      if (ok && end > beg) atomicAdd(&s.nnz, 1);
     }
+    __syncthreads();
+    const int nh = s.nnz;
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+      const int c = cnt[e];
+      int rank = 0;
+      if (c > 0) {
+        for (int j = 0; j < p.E; ++j) {
+          const int cj = cnt[j];
+          rank += (cj > c || (cj == c && j < e)) ? 1 : 0;
+        }
+      } else {
+        rank = nh;
+        for (int j = 0; j < e; ++j) rank += cnt[j] == 0 ? 1 : 0;
+      }
+      s.prefix[rank] = e;
+    }
+    if (threadIdx.x == 0) s.total_tiles = nh * g.nt * g.nt2;
+    fence_proxy_async_smem();   // the scratch is the first stage, which TMA writes next
     __syncthreads();
     return;
   }
@@ -519,7 +546,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     tc_fence_before();
   }
   pdl_begin();             // the prologue above overlaps the preceding kernel
-  build_tiles(s, g, p);   // contains __syncthreads
+  build_tiles(s, g, p, reinterpret_cast<int*>(tiles));   // contains __syncthreads
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int total = s.total_tiles;
@@ -957,9 +984,17 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
                            reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         if (r < t.rows) {
           uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
+          if (g.n_out % 128 == 0 && t.col0 + 32 * NB <= g.n_out) {
+            // the NB scale bytes of this row are consecutive and 4-byte aligned
 #pragma unroll
-          for (int c = 0; c < NB; ++c)
-            if (t.col0 + 32 * c < g.n_out) srow[t.col0 / 32 + c] = static_cast<uint8_t>(sb[c]);
+            for (int c = 0; c < NB; c += 4)
+              *reinterpret_cast<uint32_t*>(srow + t.col0 / 32 + c) =
+                  sb[c] | (sb[c + 1] << 8) | (sb[c + 2] << 16) | (sb[c + 3] << 24);
+          } else {
+#pragma unroll
+            for (int c = 0; c < NB; ++c)
+              if (t.col0 + 32 * c < g.n_out) srow[t.col0 / 32 + c] = static_cast<uint8_t>(sb[c]);
+          }
         }
       } else if constexpr (kEpi == kEpiSwiglu) {
         const bool valid = r < t.rows;

@@ -208,6 +208,30 @@ def test_fwd_mxfp8_plain(counts, K, N):
     assert err < TOL_MXFP8 and err < 1e-2, err       # same quantised inputs: only fp32/bf16 rounding
 
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_fwd_mxfp8_plain_many_tiles_per_cta(out_dtype):
+    """Several tiles per persistent CTA (462 tiles of 128 x 256 for 152 SMs), so the
+    accumulator, the scale slots and the staging boxes are reused many times; a
+    partial last column tile; an empty and a one-row group."""
+    need_gpu()
+    cnt = [3000, 0, 1, 2900, 130, 2000]
+    E, K, N = len(cnt), 512, 1568 + 96
+    M = int(sum(cnt))
+    A, B = _mats(M, K, N, E, torch.bfloat16, seed=77)
+    Aq, As, A_deq = _quantize(A)
+    Bq, Bs, B_deq = _quantize(B)
+    off = ragged_offsets(cnt)
+    C = torch.empty((M, N), dtype=out_dtype, device="cuda")
+    moe_gpu.moe_grouped_gemm_fwd(Aq, Bq, off, A_scales=As, B_scales=Bs, out=C)
+    want = om.grouped_gemm(A_deq, B_deq.reshape(E, N, K), off.cpu().numpy())
+    err = rel_l2(f64(C), want)
+    assert err < 1e-2, err
+    for e in range(E):                                    # every group on its own
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            assert rel_l2(f64(C[lo:hi]), want[lo:hi]) < 1e-2, e
+
+
 @pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
 @pytest.mark.parametrize("K,f", [(512, 128), (1024, 256), (512, 96), (512, 288)])
 def test_fwd_mxfp8_swiglu(counts, K, f):
