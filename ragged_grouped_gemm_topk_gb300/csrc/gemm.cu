@@ -127,6 +127,28 @@ struct Cfg {
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
+// Wide tiles (bf16 operands, bf16 output, forward / plain data gradient / weight
+// gradient): 256 rows x 256 columns, computed as two M=128 MMAs that share each
+// stage's B slice, their accumulators in TMEM columns 0-255 and 256-511.  Per
+// FLOP each SM then takes in a third fewer operand bytes, and each 64 KB stage
+// carries twice the MMA work, so three stages cover more load latency than four
+// 48 KB stages of 128-row tiles.  Eight epilogue warps (two per TMEM lane
+// quarter, one set per 128-row half) drain the two accumulators side by side.
+// A group's last tile computes its second half only if it has rows there, so no
+// more rows are padded than with 128-row tiles.
+template <int kKind, int kMode, int kEpi, int kOutBytes>
+constexpr bool wide_tile() {
+  return kKind == 1 && kOutBytes == 2 && kEpi != kEpiTopk && kEpi != kEpiDswiglu;
+}
+constexpr int kWideM = 256;
+constexpr int kWideStages = 3;
+constexpr int kWideStage = kWideM * kBKBytes + kBStage;      // 64 KB
+constexpr int kWideEpiWarps = 8;
+// first epilogue warp: after the producer and the MMA warp, and for the weight
+// gradient the zero-fill warp (warp 2)
+template <int kMode>
+constexpr int wide_epi_warp0() { return kMode == kWgrad ? 3 : 2; }
+
 // wgrad: each epilogue warp stages its 32 dW rows in wg_bufs rotating 2 KB boxes of
 // 32 columns for the TMA store (so the 4-stage operand ring still fits), and a 7th
 // warp writes the dW of experts without rows.  MXFP8 wgrad keeps two boxes per warp
@@ -141,22 +163,28 @@ constexpr int wg_stage() { return 2048 * wg_bufs<kKind>(); }
 template <int kKind>
 constexpr int wg_atom_off() { return 4 * wg_stage<kKind>(); }
 constexpr int kMxWgRows = 128;                    // MXFP8 wgrad: contraction rows per stage (4 blocks)
-template <int kKind, int kMode>
-constexpr int stages_for() { return kStages; }
-template <int kKind, int kMode>
-constexpr int threads_for() { return (kKind >= 2 || kMode == kWgrad) ? 224 : 192; }
-template <int kKind, int kMode>
-constexpr size_t extra_smem() {
-  return kMode == kWgrad ? wg_atom_off<kKind>() + (kKind == 2 ? kStages * kAtomBytes : 0)
-                        : (kMode == kFwd ? (kKind == 3 ? kStages * kNvAtomBytes
-                                                       : kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
-                                                       : atom_off<kKind>())
-                                         : 0);
+template <int kKind, int kMode, bool kW = false>
+constexpr int stages_for() { return kW ? kWideStages : kStages; }
+template <int kKind, int kMode, bool kW = false>
+constexpr int threads_for() {
+  return kW ? 32 * (wide_epi_warp0<kMode>() + kWideEpiWarps) : ((kKind >= 2 || kMode == kWgrad) ? 224 : 192);
 }
-template <int kKind, int kMode>
+template <bool kW>
+constexpr int stage_bytes() { return kW ? kWideStage : kStageBytes; }
+// wide tiles: one 2 KB staging box per epilogue warp (forward and weight gradient)
+template <int kKind, int kMode, bool kW = false>
+constexpr size_t extra_smem() {
+  return kW ? (kMode == kDgrad ? 0 : kWideEpiWarps * kEpiBox)
+            : kMode == kWgrad ? wg_atom_off<kKind>() + (kKind == 2 ? kStages * kAtomBytes : 0)
+                              : (kMode == kFwd ? (kKind == 3 ? kStages * kNvAtomBytes
+                                                             : kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
+                                                             : atom_off<kKind>())
+                                               : 0);
+}
+template <int kKind, int kMode, bool kW = false>
 constexpr size_t smem_for() {
-  return 1024 + static_cast<size_t>(stages_for<kKind, kMode>()) * Cfg<kKind>::kStage +
-         extra_smem<kKind, kMode>() + sizeof(Smem);
+  return 1024 + static_cast<size_t>(stages_for<kKind, kMode, kW>()) * stage_bytes<kW>() +
+         extra_smem<kKind, kMode, kW>() + sizeof(Smem);
 }
 
 // Tile shape and TMEM layout per instantiation: 128 x 256 tiles everywhere.
@@ -220,7 +248,7 @@ __device__ __forceinline__ void group_range(const Params& p, int e, int& beg, in
 struct Tile {
   int e;
   int row0;    // fwd/dgrad: first row; wgrad: first row of the group
-  int rows;    // fwd/dgrad: valid rows (<= 128); wgrad: rows of the group
+  int rows;    // fwd/dgrad: valid rows (<= the tile rows); wgrad: rows of the group
   int col0;    // first output column (fwd/dgrad) / first dB column (wgrad)
   int n0;      // wgrad: first dB row
   int kblocks; // contraction blocks
@@ -246,11 +274,13 @@ struct Geo {
   int kb_fixed; // contraction blocks (fwd/dgrad)
   int mn_rows;  // wgrad: contraction rows per stage
   int rb;       // fwd/dgrad: row tiles per raster block
-  __device__ Geo(const Params& p, int elem_bytes, int bn) {
+  int tm;       // tile rows (fwd/dgrad: rows of the group; wgrad: dB rows): 128, or 256 for wide tiles
+  __device__ Geo(const Params& p, int elem_bytes, int bn, int tile_m = kBM) {
     mn_rows = elem_bytes == 1 ? kMxWgRows : kMnRows;
     rb = 1;
+    tm = tile_m;
     if (kMode == kWgrad) {
-      nt = (p.N + kBM - 1) / kBM;
+      nt = (p.N + tm - 1) / tm;
       nt2 = (p.K + kBN - 1) / kBN;
       n_out = p.K;
       bn_out = kBN;
@@ -264,13 +294,13 @@ struct Geo {
                                : (p.N + kMnRows - 1) / kMnRows;
       const long long a_row = kMode == kFwd ? static_cast<long long>(p.K) * elem_bytes
                                             : static_cast<long long>(p.N) * 2;   // dgrad: dC is bf16
-      const long long r = kRasterABytes / (static_cast<long long>(kBM) * (a_row > 0 ? a_row : 1));
+      const long long r = kRasterABytes / (static_cast<long long>(tm) * (a_row > 0 ? a_row : 1));
       rb = r < 1 ? 1 : (r > 1024 ? 1024 : static_cast<int>(r));
     }
   }
   __device__ int tiles_of(int cnt) const {
     if (kMode == kWgrad) return nt * nt2;
-    return ((cnt + kBM - 1) / kBM) * nt;
+    return ((cnt + tm - 1) / tm) * nt;
   }
 };
 
@@ -297,19 +327,19 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
   group_range(p, lo, beg, end);
   const int cnt = group_ok(beg, end, M) ? end - beg : 0;
   if (kMode == kWgrad) {
-    t.n0 = (local % g.nt) * kBM;
+    t.n0 = (local % g.nt) * g.tm;
     t.col0 = (local / g.nt) * kBN;
     t.row0 = cnt > 0 ? beg : 0;
     t.rows = cnt;
     t.kblocks = (cnt + g.mn_rows - 1) / g.mn_rows;
   } else {
-    const int mt = (cnt + kBM - 1) / kBM;   // >= 1: only non-empty groups own tiles
+    const int mt = (cnt + g.tm - 1) / g.tm;   // >= 1: only non-empty groups own tiles
     const int blk = local / (g.rb * g.nt);   // raster block (see kRasterABytes)
     const int rem = local - blk * g.rb * g.nt;
     const int in_blk = mt - blk * g.rb < g.rb ? mt - blk * g.rb : g.rb;   // row tiles in this block
-    t.row0 = beg + (blk * g.rb + rem % in_blk) * kBM;
+    t.row0 = beg + (blk * g.rb + rem % in_blk) * g.tm;
     const int left = beg + cnt - t.row0;
-    t.rows = left < kBM ? left : kBM;
+    t.rows = left < g.tm ? left : g.tm;
     t.col0 = (rem / in_blk) * g.bn_out;
     t.n0 = 0;
     t.kblocks = g.kb_fixed;
@@ -499,20 +529,26 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
 }
 
 template <int kKind, int kMode, int kEpi, typename OutT>
-__global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-    const __grid_constant__ CUtensorMap tmD, const Params p) {
+__global__ void __launch_bounds__(
+    (threads_for<kKind, kMode, wide_tile<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>()>()), 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                        const __grid_constant__ CUtensorMap tmD, const Params p) {
   using C = Cfg<kKind>;
-  constexpr int NS = stages_for<kKind, kMode>();
+  constexpr bool kW = wide_tile<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>();
+  constexpr int TM = kW ? kWideM : kBM;                 // tile rows
+  constexpr int NS = stages_for<kKind, kMode, kW>();
+  constexpr int kStageSz = stage_bytes<kW>();
+  constexpr int kASize = TM * kBKBytes;                 // A part of a stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& s = *reinterpret_cast<Smem*>(tiles + NS * C::kStage + extra_smem<kKind, kMode>());
+  Smem& s = *reinterpret_cast<Smem*>(tiles + NS * kStageSz + extra_smem<kKind, kMode, kW>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int eb = C::kEb;
   using TL = Tl<kKind, kMode, kEpi>;
   constexpr int BN = TL::BN;
-  const Geo<kMode, kEpi> g(p, eb, BN);
+  constexpr int kAccN = kW ? 1 : TL::kAcc;              // accumulator buffers (wide: one, in two halves)
+  const Geo<kMode, kEpi> g(p, eb, BN, TM);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -526,7 +562,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 128);
+      mbar_init(&s.tempty[i], kW ? 32 * kWideEpiWarps : 128);
     }
     s.abort = 0;
     fence_mbar_init();
@@ -562,7 +598,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (kKind == 2 && kMode == kFwd && kb % 4 == 0) {
             // raw E8M0 rows, 16 bytes per row = the scales of 4 K-blocks, into slot ss
             if (!mbar_wait(&s.sempty[ss], ss_phase ^ 1u, p.status, &s.abort)) break;
-            uint8_t* rsa = tiles + NS * C::kStage + raw_off<kKind>() + ss * kSfSlot;
+            uint8_t* rsa = tiles + NS * kStageSz + raw_off<kKind>() + ss * kSfSlot;
             uint8_t* rsb = rsa + kSfAStage;
             const int sx = 16 * (kb / 4);
             const int brow = t.e * p.N;
@@ -578,10 +614,10 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             if (++ss == raw_slots<kKind>()) { ss = 0; ss_phase ^= 1u; }
           }
           if (!mbar_wait(&s.empty[stage], phase ^ 1u, p.status, &s.abort)) break;
-          uint8_t* sa = tiles + stage * C::kStage;
-          uint8_t* sb = sa + kAStage;
+          uint8_t* sa = tiles + stage * kStageSz;
+          uint8_t* sb = sa + kASize;
           uint64_t* bar = &s.full[stage];
-          mbar_arrive_expect_tx(bar, (kEpi == kEpiTopk ? kAStage + p.n_mma * kBKBytes : kStageBytes) +
+          mbar_arrive_expect_tx(bar, (kEpi == kEpiTopk ? kAStage + p.n_mma * kBKBytes : kStageSz) +
                                          (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
                                          (kKind == 3 ? kNvAtomBytes : 0));
           if (kMode == kFwd) {
@@ -595,7 +631,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             }
             if constexpr (kKind == 3) {
               // raw scale rows of this stage: 16 bytes (= 256 elements) per row
-              uint8_t* at = tiles + NS * C::kStage + stage * kNvAtomBytes;
+              uint8_t* at = tiles + NS * kStageSz + stage * kNvAtomBytes;
               const int brow = t.e * p.N;
               tma_load_2d(at, &tmSA, bar, 16 * kb, t.row0);
               tma_load_2d(at + 2048, &tmSB, bar, 16 * kb, brow + t.col0);
@@ -614,13 +650,13 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
             tma_load_2d(sb, &tmB, bar, t.col0, r);
             tma_load_2d(sb + kBStage / 2, &tmB, bar, t.col0 + 128, r);
             const size_t quad = static_cast<size_t>(t.row0 / 128 + t.e + kb);
-            uint8_t* at = tiles + NS * C::kStage + wg_atom_off<kKind>() + stage * kAtomBytes;
+            uint8_t* at = tiles + NS * kStageSz + wg_atom_off<kKind>() + stage * kAtomBytes;
             bulk_load(at, p.sfa + (quad * (p.N / 128) + t.n0 / 128) * 512, 512, bar);
             bulk_load(at + 512, p.sfb + (quad * (p.K / 128) + t.col0 / 128) * 512, 1024, bar);
           } else {
             const int r = t.row0 + kb * kMnRows;          // contraction index (rows of the group)
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBox, &tmA, bar, t.n0 + 64 * j, r);
+            for (int j = 0; j < TM / 64; ++j) tma_load_2d(sa + j * kBox, &tmA, bar, t.n0 + 64 * j, r);
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kBox, &tmB, bar, t.col0 + 64 * j, r);
           }
@@ -649,7 +685,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           // 32-row steps wholly past the group (their scales are never read).
           if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
           tc_fence_after();
-          uint8_t* sa_ptr = tiles + stage * C::kStage;
+          uint8_t* sa_ptr = tiles + stage * kStageSz;
           const int valid = t.rows - kb * kMxWgRows;
           int steps = 4;
           if (valid < kMxWgRows) {
@@ -663,7 +699,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (lane == 0) {
             const uint32_t sa = smem_u32(sa_ptr);
             const uint32_t sb = sa + kAStage;
-            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + wg_atom_off<kKind>() + stage * kAtomBytes);
+            const uint32_t ssa = smem_u32(tiles + NS * kStageSz + wg_atom_off<kKind>() + stage * kAtomBytes);
             const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
             tc_cp_32x128b_warpx4(slot, make_sdesc(ssa, 0, 128, 0));
             tc_cp_32x128b_warpx4(slot + TL::kSfB, make_sdesc(ssa + 512, 0, 128, 0));
@@ -690,9 +726,9 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = smem_u32(tiles + stage * C::kStage);
+            const uint32_t sa = smem_u32(tiles + stage * kStageSz);
             const uint32_t sb = sa + kAStage;
-            const uint32_t at = smem_u32(tiles + NS * C::kStage + stage * kNvAtomBytes);
+            const uint32_t at = smem_u32(tiles + NS * kStageSz + stage * kNvAtomBytes);
             const uint32_t set = tmem + TL::kSfBase + 128u * static_cast<uint32_t>(stage & 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -714,9 +750,9 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (!mbar_wait(&s.sfready[stage], phase, p.status, &s.abort)) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = smem_u32(tiles + stage * C::kStage);
+            const uint32_t sa = smem_u32(tiles + stage * kStageSz);
             const uint32_t sb = sa + kAStage;
-            const uint32_t ssa = smem_u32(tiles + NS * C::kStage + atom_off<kKind>() + stage * kAtomBytes);  // atoms
+            const uint32_t ssa = smem_u32(tiles + NS * kStageSz + atom_off<kKind>() + stage * kAtomBytes);  // atoms
             const uint32_t ssb = ssa + 512;
             // scale slot of this stage: A atom at +0 (4 columns), B atoms at +kSfB, +kSfB+4
             const uint32_t slot = tmem + TL::kSfBase + TL::kSfStride * static_cast<uint32_t>(stage);
@@ -738,9 +774,9 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
         tc_fence_after();
-        uint8_t* sa_ptr = tiles + stage * C::kStage;
+        uint8_t* sa_ptr = tiles + stage * kStageSz;
         const uint32_t sa = smem_u32(sa_ptr);
-        const uint32_t sb = sa + kAStage;
+        const uint32_t sb = sa + kASize;
         int steps = 4;
         if (kMode == kWgrad) {
           // Last block of the group: zero rows [valid, 16*steps) of the A operand
@@ -750,7 +786,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (valid < kMnRows) {
             steps = (valid + 15) / 16;
             const int zrows = steps * 16 - valid;
-            for (int i = lane; i < zrows * 8 * (kBM / 64); i += 32) {
+            for (int i = lane; i < zrows * 8 * (TM / 64); i += 32) {
               const int box = i / (zrows * 8), rem = i % (zrows * 8);
               const int row = valid + rem / 8, chunk = rem % 8;
               *reinterpret_cast<uint4*>(sa_ptr + box * kBox + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
@@ -760,13 +796,19 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           __syncwarp();
         }
         if (lane == 0) {
+          // wide tiles: the second 128-row half (A rows / dB rows 128-255, accumulator
+          // columns 256-511) only where the tile has rows there
+          const int halves = kW ? ((kMode == kWgrad ? t.n0 + kBM < p.N : t.rows > kBM) ? 2 : 1) : 1;
           for (int kk = 0; kk < steps; ++kk) {
-            uint64_t ad, bd;
-            if (kMode == kWgrad) ad = make_sdesc(sa + kk * 2048, kBox, 1024, 2);
-            else ad = make_sdesc(sa + kk * 32, 16, 1024, 2);
+            uint64_t bd;
             if (kMode == kFwd) bd = make_sdesc(sb + kk * 32, 16, 1024, 2);
             else bd = make_sdesc(sb + kk * 2048, kBox, 1024, 2);
-            tc_mma<kKind>(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int h = 0; h < halves; ++h) {
+              // half h of A: 128 K-major rows further (16 KB), or two 64-column MN-major boxes
+              const uint64_t ad = kMode == kWgrad ? make_sdesc(sa + h * 2 * kBox + kk * 2048, kBox, 1024, 2)
+                                                  : make_sdesc(sa + h * kAStage + kk * 32, 16, 1024, 2);
+              tc_mma<kKind>(d_tmem + static_cast<uint32_t>(h) * 256u, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&s.empty[stage]);
         }
@@ -775,7 +817,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       }
       if (lane == 0) tc_commit(&s.tfull[acc]);
       __syncwarp();
-      if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == kAccN) { acc = 0; acc_phase ^= 1u; }
     }
   } else if (kKind == 3 && warp == 6) {
     // ------------------------------------------------------------------ NVFP4 scale layout
@@ -788,7 +830,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       const Tile t = tile_info(s, g, tile, p);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
-        uint8_t* at = tiles + NS * C::kStage + stage * kNvAtomBytes;
+        uint8_t* at = tiles + NS * kStageSz + stage * kNvAtomBytes;
         uint4 ra[4], rb[2][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) ra[i] = *reinterpret_cast<const uint4*>(at + (lane + 32 * i) * 16);
@@ -828,7 +870,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (kb % 4 == 0) {
           if (!mbar_wait(&s.sfull[ss], ss_phase, p.status, &s.abort)) break;
-          const uint8_t* rsa = tiles + NS * C::kStage + raw_off<kKind>() + ss * kSfSlot;
+          const uint8_t* rsa = tiles + NS * kStageSz + raw_off<kKind>() + ss * kSfSlot;
           const uint8_t* rsb = rsa + kSfAStage;
 #pragma unroll
           for (int j = 0; j < 4; ++j) ra[j] = *reinterpret_cast<const uint4*>(rsa + (lane + 32 * j) * 16);
@@ -839,7 +881,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           if (++ss == raw_slots<kKind>()) { ss = 0; ss_phase ^= 1u; }
         }
         if (!mbar_wait(&s.full[stage], phase, p.status, &s.abort)) break;
-        uint8_t* at = tiles + NS * C::kStage + atom_off<kKind>() + stage * kAtomBytes;
+        uint8_t* at = tiles + NS * kStageSz + atom_off<kKind>() + stage * kAtomBytes;
         const int w = kb % 4;
         auto word = [w](const uint4& v) { return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w)); };
         *reinterpret_cast<uint4*>(at + lane * 16) = make_uint4(word(ra[0]), word(ra[1]), word(ra[2]), word(ra[3]));
@@ -851,7 +893,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         if (++stage == NS) { stage = 0; phase ^= 1u; }
       }
     }
-  } else if (kMode == kWgrad && warp == 6) {
+  } else if (kMode == kWgrad && warp == (kW ? 2 : 6)) {
     // ------------------------------------------------------------------ wgrad zero fill
     // Experts without rows own no tiles; their dW (exact zeros) is written here,
     // alongside the MMA work, with plain 16-byte stores (not through the TMA unit,
@@ -869,12 +911,18 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
 #pragma unroll
       for (int i = lane; i < 128; i += 32) st_global_hint(dst + i, make_uint4(0, 0, 0, 0), pol);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2 && warp <= (kW ? wide_epi_warp0<kMode>() + kWideEpiWarps - 1 : 5)) {
     // ------------------------------------------------------------------ epilogue
     // The accumulator is released (tempty) as soon as its last TMEM read is done;
     // the global stores of the tile follow from registers (or, for wgrad, from a
     // shared-memory staging buffer by TMA), overlapping the next tile's MMAs.
+    // Wide tiles: the first four epilogue warps take the first 128-row half, the
+    // next four the second.
+    constexpr int kW0 = kW ? wide_epi_warp0<kMode>() : 2;
     const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int hh = kW ? (warp - kW0) >> 2 : 0;        // half of a wide tile
+    const int si = kW ? warp - kW0 : q;               // staging box set of this warp
+    constexpr int kEB = kW ? 1 : epi_bufs<kKind>();   // forward staging boxes per warp
     float alpha = 1.f;                      // NVFP4: undo the two tensor encode scales
     if constexpr (kKind == 3) alpha = __fdiv_rn(1.f, __fmul_rn(__ldg(p.ts_a), __ldg(p.ts_b)));
     const int r = q * 32 + lane;            // tile row owned by this thread
@@ -882,10 +930,26 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
-      const Tile t = tile_info(s, g, tile, p);
+      Tile t = tile_info(s, g, tile, p);
+      if (kW) {                              // this warp's half of the wide tile
+        if (kMode == kWgrad) {
+          t.n0 += hh * kBM;
+        } else {
+          t.row0 += hh * kBM;
+          t.rows -= hh * kBM;
+        }
+      }
       if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (kW && (kMode == kWgrad ? t.n0 >= p.N : t.rows <= 0)) {
+        // no rows in this half: nothing was computed for it
+        tc_fence_before();
+        mbar_arrive(&s.tempty[acc]);
+        if (++acc == kAccN) { acc = 0; acc_phase ^= 1u; }
+        continue;
+      }
+      const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN) +
+                          static_cast<uint32_t>(hh) * 256u;
       bool released = false;
       if constexpr (kMode == kWgrad) {
         // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns: the accumulator is read
@@ -908,8 +972,8 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
         released = true;
-        constexpr int kWgBufs = wg_bufs<kKind>();
-        uint8_t* stg = tiles + NS * C::kStage + q * wg_stage<kKind>();
+        constexpr int kWgBufs = kW ? 1 : wg_bufs<kKind>();
+        uint8_t* stg = tiles + NS * kStageSz + si * (kW ? 2048 : wg_stage<kKind>());
         const int sw = (lane >> 1) & 3;
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
@@ -980,7 +1044,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
                                                        bf16_to_f32(static_cast<uint16_t>(w1 >> 16)) * inv)) << 16);
           }
         }
-        epi_store_rows<64, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, cw, lane,
+        epi_store_rows<64, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, cw, lane,
                            reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         if (r < t.rows) {
           uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
@@ -1018,7 +1082,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          epi_store_rows<32, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, pk, lane,
+          epi_store_rows<32, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
                              reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
@@ -1196,7 +1260,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
           mbar_arrive(&s.tempty[acc]);
           released = true;
           if constexpr (kMode == kFwd) {
-            epi_store_rows<32, epi_bufs<kKind>()>(&tmD, tiles + NS * C::kStage + kEpiOff + q * epi_bufs<kKind>() * kEpiBox, pk, lane,
+            epi_store_rows<32, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
                                reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
 #pragma unroll
@@ -1232,7 +1296,7 @@ __global__ void __launch_bounds__(threads_for<kKind, kMode>(), 1) grouped_gemm_k
         tc_fence_before();
         mbar_arrive(&s.tempty[acc]);
       }
-      if (++acc == TL::kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == kAccN) { acc = 0; acc_phase ^= 1u; }
     }
     if constexpr (kMode == kWgrad || kMode == kFwd) {
       if (lane == 0) bulk_wait_all0();      // every TMA store has landed
@@ -1334,12 +1398,12 @@ template <int kKind, int kMode, int kEpi, typename OutT>
 moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t stream,
                     int sms, const char* what, const CUtensorMap* tsa = nullptr,
                     const CUtensorMap* tsb = nullptr, const CUtensorMap* td = nullptr) {
-  using C = Cfg<kKind>;
-  constexpr size_t smem = smem_for<kKind, kMode>();
+  constexpr bool kW = wide_tile<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>();
+  constexpr size_t smem = smem_for<kKind, kMode, kW>();
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  launch_pdl(kern, sms, threads_for<kKind, kMode>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
+  launch_pdl(kern, sms, threads_for<kKind, kMode, kW>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
              td ? *td : ta, p);
   return check_launch(what);
 }
@@ -1434,7 +1498,9 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   const uint32_t bk = kBKBytes / eb;
   CUtensorMap ta, tb;
   const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-  const uint32_t abox[2] = {bk, kBM};
+  // bf16 operands with bf16 output run the wide tile (256 A rows per stage)
+  const uint32_t a_rows = (A->dtype == MOE_BF16 && c_dtype == MOE_BF16) ? kWideM : kBM;
+  const uint32_t abox[2] = {bk, a_rows};
   const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint32_t bbox[3] = {bk, static_cast<uint32_t>(epi == MOE_EPI_SWIGLU ? kBN / 2 : kBN), 1};
   if (!make_map(&ta, map_type(A->dtype), eb, A->ptr, 2, adims, abox) ||
@@ -1545,7 +1611,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
   if (M == 0) return MOE_OK;
   CUtensorMap ta, tb;
   const uint64_t adims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
-  const uint32_t abox[2] = {64, kBM};
+  const uint32_t abox[2] = {64, static_cast<uint32_t>(epi == MOE_EPI_DSWIGLU ? kBM : kWideM)};   // plain: wide tile
   const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint32_t bbox[3] = {64, kMnRows, 1};
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC->ptr, 2, adims, abox) ||
