@@ -462,7 +462,8 @@ def run_ours(args, world, rank, local):
 
 def stage_fns(w, layer, x, nbuf):
     """The dispatch and the combine of a layer shape over nbuf rotating sets of their
-    input and output buffers (set 0 is the layer's own input): disp(i), comb(i)."""
+    input and output buffers (set 0 is the layer's own input): disp(i), comb(i).
+    comb(i) reads the dispatch map disp(i) wrote, so disp(i) runs first."""
     import torch
     import ragged_grouped_gemm_topk_gb300 as pkg
     dev = x.device
@@ -496,8 +497,8 @@ def stage_fns(w, layer, x, nbuf):
                             dev_status=layer.dev_status, **maps[i], **outs[i])
     yps = [layer.yp] + [layer.yp.clone() for _ in range(nbuf - 1)]
     ys = [torch.empty(w.T, d, dtype=layer.yp.dtype, device=dev) for _ in range(nbuf)]
-    def comb(i):
-        pkg.moe_unpermute_combine(yps[i], layer.dest_row, layer.topk_w, out=ys[i], dev_status=layer.dev_status)
+    def comb(i):   # the dispatch map that disp(i) wrote (run disp first)
+        pkg.moe_unpermute_combine(yps[i], maps[i]["dest_row"], layer.topk_w, out=ys[i], dev_status=layer.dev_status)
     return disp, comb, nbuf
 
 
