@@ -127,18 +127,21 @@ struct Cfg {
   static constexpr int kEb = kKind == 0 ? 4 : (kKind == 1 ? 2 : 1);
 };
 
-// Wide tiles (bf16 operands, bf16 output, forward / plain data gradient / weight
-// gradient): 256 rows x 256 columns, computed as two M=128 MMAs that share each
+// Wide tiles (bf16 operands, bf16 output, plain epilogue: GEMM2, the GEMM1 data
+// gradient, the weight gradients): 256 rows x 256 columns, computed as two M=128 MMAs that share each
 // stage's B slice, their accumulators in TMEM columns 0-255 and 256-511.  Per
 // FLOP each SM then takes in a third fewer operand bytes, and each 64 KB stage
 // carries twice the MMA work, so three stages cover more load latency than four
 // 48 KB stages of 128-row tiles.  Eight epilogue warps (two per TMEM lane
 // quarter, one set per 128-row half) drain the two accumulators side by side.
 // A group's last tile computes its second half only if it has rows there, so no
-// more rows are padded than with 128-row tiles.
+// more rows are padded than with 128-row tiles.  GEMM1 (SwiGLU, with the pre-
+// activation store that holds the accumulator while it writes) keeps 128-row tiles
+// and its double-buffered accumulator: measured no faster wide on the DeepSeek-V3
+// training layer and 6% slower on a smaller one.
 template <int kKind, int kMode, int kEpi, int kOutBytes>
 constexpr bool wide_tile() {
-  return kKind == 1 && kOutBytes == 2 && kEpi != kEpiTopk && kEpi != kEpiDswiglu;
+  return kKind == 1 && kOutBytes == 2 && kEpi == kEpiNone;
 }
 constexpr int kWideM = 256;
 constexpr int kWideStages = 3;
@@ -1498,8 +1501,8 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   const uint32_t bk = kBKBytes / eb;
   CUtensorMap ta, tb;
   const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-  // bf16 operands with bf16 output run the wide tile (256 A rows per stage)
-  const uint32_t a_rows = (A->dtype == MOE_BF16 && c_dtype == MOE_BF16) ? kWideM : kBM;
+  // bf16 operands, bf16 output, plain epilogue: the wide tile (256 A rows per stage)
+  const uint32_t a_rows = (A->dtype == MOE_BF16 && c_dtype == MOE_BF16 && epi == MOE_EPI_NONE) ? kWideM : kBM;
   const uint32_t abox[2] = {bk, a_rows};
   const uint64_t bdims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
   const uint32_t bbox[3] = {bk, static_cast<uint32_t>(epi == MOE_EPI_SWIGLU ? kBN / 2 : kBN), 1};
