@@ -482,30 +482,36 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 
 // Write one warp's 32 tile rows of output, held one row per lane as 32-bit words
 // (two bf16 or four E4M3 values each).  A warp whose 32 rows all belong to the
-// group sends 64-byte-wide boxes (16 words per row; kBoxElems elements) through its
-// kBufs rotating 2 KB staging buffers by TMA store; 16-byte chunk h of row r sits
-// at chunk h ^ ((r >> 1) & 3) (64-byte swizzle).  A warp whose rows cross the
-// group's end (the next group's rows follow) stores its valid rows directly.
-template <int kBoxElems, int kBufs, int kWords>
+// group sends boxes of kRowB-byte rows (kBoxElems elements) through its kBufs
+// rotating staging buffers of 32 x kRowB bytes by TMA store; 16-byte chunk h of row
+// r sits at chunk h ^ ((r >> 1) & 3) for 64-byte rows (64-byte swizzle) and h ^
+// ((r >> 2) & 1) for 32-byte rows (32-byte swizzle).  Two 1 KB boxes in place of one
+// 2 KB box let a box be staged while the previous one is still read by its store.
+// A warp whose rows cross the group's end (the next group's rows follow) stores its
+// valid rows directly.
+template <int kBoxElems, int kBufs, int kRowB, int kWords>
 __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
                                                int lane, uint8_t* out, int row0, int rows_valid, int col0,
                                                int n_out) {
-  constexpr int kElemBytes = kEpiRowBytes / kBoxElems;
+  static_assert(kRowB == 64 || kRowB == 32, "box rows of 64 or 32 bytes");
+  constexpr int kElemBytes = kRowB / kBoxElems;
+  constexpr int kRowWords = kRowB / 4;       // 32-bit words per box row
+  constexpr int kChunks = kRowB / 16;        // 16-byte chunks per box row
   const size_t row_bytes = static_cast<size_t>(n_out) * kElemBytes;
   if constexpr (kBufs == 0) {
     // no staging boxes (NVFP4): every row is stored directly below
   } else if (rows_valid >= 32) {
 #pragma unroll
-    for (int c = 0; c < kWords / 16; ++c) {
+    for (int c = 0; c < kWords / kRowWords; ++c) {
       if (col0 + c * kBoxElems >= n_out) break;
-      uint8_t* buf = stg + (c % (kBufs > 0 ? kBufs : 1)) * kEpiBox;
+      uint8_t* buf = stg + (c % (kBufs > 0 ? kBufs : 1)) * (32 * kRowB);
       if (lane == 0) bulk_wait_read<(kBufs > 0 ? kBufs - 1 : 0)>();   // the box that last used buf has been read
       __syncwarp();
-      const int sw = (lane >> 1) & 3;
+      const int sw = kRowB == 64 ? (lane >> 1) & 3 : (lane >> 2) & 1;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int w0 = c * 16 + 4 * h;
-        *reinterpret_cast<uint4*>(buf + lane * kEpiRowBytes + ((h ^ sw) * 16)) =
+      for (int h = 0; h < kChunks; ++h) {
+        const int w0 = c * kRowWords + 4 * h;
+        *reinterpret_cast<uint4*>(buf + lane * kRowB + ((h ^ sw) * 16)) =
             make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
       }
       fence_proxy_async_smem();
@@ -518,15 +524,15 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
   }
   if ((kBufs == 0 || rows_valid < 32) && lane < rows_valid) {
 #pragma unroll
-    for (int c = 0; c < kWords / 16; ++c) {
+    for (int c = 0; c < kWords / kRowWords; ++c) {
       const int col = col0 + c * kBoxElems;
       uint4* d4 = reinterpret_cast<uint4*>(out + static_cast<size_t>(row0 + lane) * row_bytes +
                                            static_cast<size_t>(col) * kElemBytes);
 #pragma unroll
-      for (int h = 0; h < 4; ++h)   // n_out is a multiple of 16 bytes' worth: check per chunk
+      for (int h = 0; h < kChunks; ++h)   // n_out is a multiple of 16 bytes' worth: check per chunk
         if (col + h * (16 / kElemBytes) < n_out)
-          d4[h] = make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2],
-                             pk[c * 16 + 4 * h + 3]);
+          d4[h] = make_uint4(pk[c * kRowWords + 4 * h], pk[c * kRowWords + 4 * h + 1], pk[c * kRowWords + 4 * h + 2],
+                             pk[c * kRowWords + 4 * h + 3]);
     }
   }
 }
@@ -925,7 +931,13 @@ __global__ void __launch_bounds__(
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int hh = kW ? (warp - kW0) >> 2 : 0;        // half of a wide tile
     const int si = kW ? warp - kW0 : q;               // staging box set of this warp
-    constexpr int kEB = kW ? 1 : epi_bufs<kKind>();   // forward staging boxes per warp
+    constexpr int kEB = kW ? 1 : epi_bufs<kKind>();   // forward staging: 2 KB units per warp
+    // MXFP8 has one 2 KB unit per warp: it holds two 1 KB boxes of 32-byte rows,
+    // double-buffered; the others use 2 KB boxes of 64-byte rows (on wide tiles 1 KB
+    // boxes measured slower: more, smaller stores)
+    constexpr bool kHalfBox = kKind == 2;
+    constexpr int kRB = kHalfBox ? 32 : kEpiRowBytes;    // box row bytes
+    constexpr int kNB = kHalfBox ? 2 * kEB : kEB;        // staging boxes per warp
     float alpha = 1.f;                      // NVFP4: undo the two tensor encode scales
     if constexpr (kKind == 3) alpha = __fdiv_rn(1.f, __fmul_rn(__ldg(p.ts_a), __ldg(p.ts_b)));
     const int r = q * 32 + lane;            // tile row owned by this thread
@@ -1047,7 +1059,7 @@ __global__ void __launch_bounds__(
                                                        bf16_to_f32(static_cast<uint16_t>(w1 >> 16)) * inv)) << 16);
           }
         }
-        epi_store_rows<64, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, cw, lane,
+        epi_store_rows<kRB, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, cw, lane,
                            reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         if (r < t.rows) {
           uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
@@ -1085,7 +1097,7 @@ __global__ void __launch_bounds__(
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          epi_store_rows<32, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
+          epi_store_rows<kRB / 2, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
                              reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
         } else {
 #pragma unroll 1
@@ -1263,7 +1275,7 @@ __global__ void __launch_bounds__(
           mbar_arrive(&s.tempty[acc]);
           released = true;
           if constexpr (kMode == kFwd) {
-            epi_store_rows<32, kEB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
+            epi_store_rows<kRB / 2, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
                                reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
 #pragma unroll
@@ -1516,9 +1528,12 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
   // (64-byte rows, 64-byte swizzle)
   CUtensorMap td = ta;
   if (!f32) {
+    // MXFP8 operands store 16-column boxes (32-byte rows, 32-byte swizzle), the others 32-column ones
+    const bool half_box = A->dtype == MOE_E4M3;
     const uint64_t cdims[2] = {static_cast<uint64_t>(sw ? N / 2 : N), static_cast<uint64_t>(M)};
-    const uint32_t cbox[2] = {kEpiRowBytes / 2, 32};
-    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint32_t cbox[2] = {static_cast<uint32_t>(half_box ? 16 : kEpiRowBytes / 2), 32};
+    if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, 2, cdims, cbox,
+                  half_box ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
       return MOE_ERR_INVALID_ARG;
   }
   if (A->dtype == MOE_E4M3) {
@@ -1579,14 +1594,14 @@ extern "C" moe_status_t moe_grouped_gemm_fwd_mxfp8_out(const moe_operand_t* A, c
   const uint64_t sadims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(M)};
   const uint64_t sbdims[2] = {static_cast<uint64_t>(K / 32), static_cast<uint64_t>(N) * static_cast<uint64_t>(E)};
   const uint32_t sbox[2] = {16, kBM};
-  // codes [M, n_out] are written by TMA from 32-row x 64-column staging boxes
+  // codes [M, n_out] are written by TMA from 32-row x 32-column staging boxes (32-byte swizzle)
   const uint64_t cdims[2] = {static_cast<uint64_t>(n_out), static_cast<uint64_t>(M)};
-  const uint32_t cbox[2] = {kEpiRowBytes, 32};
+  const uint32_t cbox[2] = {32, 32};
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->ptr, 2, adims, abox) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->ptr, 3, bdims, bbox) ||
       !make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, c_codes, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, c_codes, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_32B))
     return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, c_codes, nullptr, nullptr, c_scales, dev_status};
   if (sw) return launch<2, kFwd, kEpiSwiglu, uint8_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
@@ -1656,12 +1671,12 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, co
   const uint64_t sbdims[2] = {static_cast<uint64_t>(N / 32), static_cast<uint64_t>(K) * static_cast<uint64_t>(E)};
   const uint32_t sbox[2] = {16, kBM};
   const uint64_t cdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-  const uint32_t cbox[2] = {kEpiRowBytes / 2, 32};
+  const uint32_t cbox[2] = {16, 32};   // 32-byte rows, 32-byte swizzle
   if (!make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dC->ptr, 2, adims, abox) ||
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BT->ptr, 3, bdims, bbox) ||
       !make_map(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, dC->scales, 2, sadims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, BT->scales, 2, sbdims, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dA, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dA, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_32B))
     return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, K, N, E, dA, nullptr, preact, nullptr, dev_status};
   if (epi == MOE_EPI_DSWIGLU) return launch<2, kFwd, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn, &tsa, &tsb, &td);
