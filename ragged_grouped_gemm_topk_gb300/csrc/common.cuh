@@ -49,8 +49,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Two floats -> two bf16 (lo in bits 0..15), round-to-nearest-even, in one packed
+// conversion instruction: the same bits as two single conversions, at several times
+// their throughput (the GEMM epilogues that drain an accumulator are bound by it).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Two floats -> two E4M3 bytes (lo in bits 0..7), round-to-nearest-even with
