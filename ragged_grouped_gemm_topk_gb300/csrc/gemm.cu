@@ -14,10 +14,11 @@
 //              commits each stage back to the producer and each tile to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (TMEM lane = tile row, one
 //              row per thread), the fused epilogue, release of the accumulator,
-//              then the stores: forward bf16 output by TMA store from a per-warp
-//              shared staging box (a warp whose rows cross the group's end stores
-//              its valid rows directly), wgrad likewise per 64-column dW box, other
-//              outputs by 16-byte stores masked at the group's end and the edge.
+//              then the stores: forward bf16 output and the plain data gradient by
+//              TMA store from a per-warp shared staging box (a warp whose rows cross
+//              the group's end stores its valid rows directly), wgrad likewise per
+//              dW box, other outputs by 16-byte stores masked at the group's end and
+//              the edge.
 // Tiles are enumerated on the device from `offsets`, so the host never learns the
 // per-expert sizes:
 //   forward / dgrad  expert e owns ceil(count_e / 128) row tiles x the column
@@ -177,7 +178,7 @@ constexpr int stage_bytes() { return kW ? kWideStage : kStageBytes; }
 // wide tiles: one 2 KB staging box per epilogue warp (forward and weight gradient)
 template <int kKind, int kMode, bool kW = false>
 constexpr size_t extra_smem() {
-  return kW ? (kMode == kDgrad ? 0 : kWideEpiWarps * kEpiBox)
+  return kW ? kWideEpiWarps * kEpiBox
             : kMode == kWgrad ? wg_atom_off<kKind>() + (kKind == 2 ? kStages * kAtomBytes : 0)
                               : (kMode == kFwd ? (kKind == 3 ? kStages * kNvAtomBytes
                                                              : kKind == 2 ? raw_off<kKind>() + raw_slots<kKind>() * kSfSlot
@@ -583,7 +584,7 @@ __global__ void __launch_bounds__(
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
-    if (kMode == kWgrad || (kMode == kFwd && sizeof(OutT) <= 2)) tma_prefetch_desc(&tmD);
+    if (kMode == kWgrad || (kMode == kFwd && sizeof(OutT) <= 2) || kW) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
@@ -1274,7 +1275,7 @@ __global__ void __launch_bounds__(
           tc_fence_before();
           mbar_arrive(&s.tempty[acc]);
           released = true;
-          if constexpr (kMode == kFwd) {
+          if constexpr (kMode == kFwd || kW) {
             epi_store_rows<kRB / 2, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
                                reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
           } else if (valid) {
@@ -1313,7 +1314,7 @@ __global__ void __launch_bounds__(
       }
       if (++acc == kAccN) { acc = 0; acc_phase ^= 1u; }
     }
-    if constexpr (kMode == kWgrad || kMode == kFwd) {
+    if constexpr (kMode == kWgrad || kMode == kFwd || kW) {
       if (lane == 0) bulk_wait_all0();      // every TMA store has landed
       __syncwarp();
     }
@@ -1637,7 +1638,14 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
     return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dA, nullptr, preact, nullptr, dev_status};
   if (epi == MOE_EPI_DSWIGLU) return launch<1, kDgrad, kEpiDswiglu, uint16_t>(ta, tb, p, stream, sms, fn);
-  return launch<1, kDgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn);
+  // plain (wide tile): dA [M, K] is written by TMA from 32-row x 32-column staging boxes
+  // (64-byte rows, 64-byte swizzle), as the forward output is
+  CUtensorMap td;
+  const uint64_t cdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint32_t cbox[2] = {kEpiRowBytes / 2, 32};
+  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dA, 2, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_INVALID_ARG;
+  return launch<1, kDgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, const moe_operand_t* BT,
