@@ -707,12 +707,17 @@ def router_leg(w, x, lg, layer, pk):
                                             topk_w=layer.topk_w, counts=layer.counts, dev_status=layer.dev_status)
     t_f = _time_ms(fused)
     t_p = _time_ms(lambda: layer.route(lg))
+    # the unfused pair for comparison: the logits by a library GEMM (cuBLAS through
+    # torch, bf16 or tf32 out, cast to fp32), then the selection from logits
+    lg_out = torch.empty(w.T, w.E, dtype=torch.float32, device=x.device)
+    t_g = _time_ms(lambda: lg_out.copy_(torch.matmul(xr, Wr.t())))
     flops = 2.0 * w.T * w.d * w.E
     peak = pk["bf16"] * (0.5 if xr.dtype == torch.float32 else 1.0)
     return {"ms": round(t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
             "frac_of_peak": round(flops / (t_f * 1e-3) / 1e12 / peak, 4),
-            "route_from_logits_ms": round(t_p, 4), "logits_bytes_not_written": w.T * w.E * 4,
-            "timing": "eager, 20 calls; the tile is 128 tokens x E expert columns (E rounded up to 16)"}
+            "route_from_logits_ms": round(t_p, 4), "library_logits_gemm_ms": round(t_g, 4),
+            "unfused_ms": round(t_g + t_p, 4), "logits_bytes_not_written": w.T * w.E * 4,
+            "timing": "eager, 20 calls; one CTA per 128-token tile x E expert columns (E rounded up to 16)"}
 
 
 def capacity_leg(w, x, lg, layer, W1, W2, cf, dropless_ms):

@@ -115,6 +115,7 @@ struct Smem {
   int abort;
   int total_tiles;
   int nnz;                 // wgrad: experts with rows
+  int epi_ok;              // router: the accumulator is ready (else the pipeline gave up)
   int prefix[kMaxE + 1];   // fwd/dgrad: tile prefix; wgrad: expert ids, non-empty then empty
 };
 
@@ -172,6 +173,14 @@ constexpr int stages_for() { return kW ? kWideStages : kStages; }
 template <int kKind, int kMode, bool kW = false>
 constexpr int threads_for() {
   return kW ? 32 * (wide_epi_warp0<kMode>() + kWideEpiWarps) : ((kKind >= 2 || kMode == kWgrad) ? 224 : 192);
+}
+// Router (top-k epilogue): 16 warps, so that 14 epilogue warps share the selection
+// (the 4 of a 128-row tile's lane quarters stage the logits from TMEM).
+constexpr int kRouterWarps = 16;
+template <int kKind, int kMode, int kEpi, int kOutBytes>
+constexpr int block_threads() {
+  return kEpi == kEpiTopk ? 32 * kRouterWarps
+                          : threads_for<kKind, kMode, wide_tile<kKind, kMode, kEpi, kOutBytes>()>();
 }
 template <bool kW>
 constexpr int stage_bytes() { return kW ? kWideStage : kStageBytes; }
@@ -538,9 +547,12 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
   }
 }
 
+// Named barrier 1 over the epilogue warps (kThreads threads from warp 2 on).
+template <int kThreads>
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
 template <int kKind, int kMode, int kEpi, typename OutT>
-__global__ void __launch_bounds__(
-    (threads_for<kKind, kMode, wide_tile<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>()>()), 1)
+__global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>()), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         const __grid_constant__ CUtensorMap tmD, const Params p) {
@@ -921,7 +933,8 @@ __global__ void __launch_bounds__(
 #pragma unroll
       for (int i = lane; i < 128; i += 32) st_global_hint(dst + i, make_uint4(0, 0, 0, 0), pol);
     }
-  } else if (warp >= 2 && warp <= (kW ? wide_epi_warp0<kMode>() + kWideEpiWarps - 1 : 5)) {
+  } else if (warp >= 2 &&
+             warp <= (kW ? wide_epi_warp0<kMode>() + kWideEpiWarps - 1 : (kEpi == kEpiTopk ? kRouterWarps - 1 : 5))) {
     // ------------------------------------------------------------------ epilogue
     // The accumulator is released (tempty) as soon as its last TMEM read is done;
     // the global stores of the tile follow from registers (or, for wgrad, from a
@@ -945,7 +958,9 @@ __global__ void __launch_bounds__(
     OutT* out = static_cast<OutT*>(p.out);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+    // (the router's epilogue warps meet at named barriers, so they all enter the
+    // loop and all take the same decision to leave it: see below)
+    for (int tile = blockIdx.x; tile < total && (kEpi == kEpiTopk || !s.abort); tile += gridDim.x) {
       Tile t = tile_info(s, g, tile, p);
       if (kW) {                              // this warp's half of the wide tile
         if (kMode == kWgrad) {
@@ -955,7 +970,18 @@ __global__ void __launch_bounds__(
           t.rows -= hh * kBM;
         }
       }
-      if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
+      if constexpr (kEpi == kEpiTopk) {
+        // one bounded wait for all the router's epilogue warps; its outcome reaches
+        // them through a barrier that every one of them always reaches
+        if (warp == 2) {
+          const bool ok = mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort);
+          if (lane == 0) s.epi_ok = ok ? 1 : 0;
+        }
+        epi_bar_sync<32 * (kRouterWarps - 2)>();
+        if (!*reinterpret_cast<volatile int*>(&s.epi_ok)) break;
+      } else {
+        if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
+      }
       tc_fence_after();
       if (kW && (kMode == kWgrad ? t.n0 >= p.N : t.rows <= 0)) {
         // no rows in this half: nothing was computed for it
@@ -1156,106 +1182,167 @@ __global__ void __launch_bounds__(
           }
         }
       } else if constexpr (kEpi == kEpiTopk) {
-        // Router: this thread's row holds the token's E = p.N logits (fp32, columns
-        // past E are zero and ignored).  One pass keeps the top kTopkMax in
-        // registers, sorted by value descending; a value enters only if strictly
-        // larger, so among equal logits the lower expert id (seen first) stays
-        // ahead.  The same pass keeps a running max and sum of exp for the full
-        // softmax.  NaN logits are flagged and treated as -inf.
-        const bool valid = r < t.rows;
-        const size_t grow = static_cast<size_t>(t.row0 + r);
+        // Router: the tile's logits (128 tokens x E experts, fp32).  The selection runs
+        // one token at a time per warp with the experts spread over the lanes (lane l
+        // holds experts l, l + 32, ...): k rounds of a warp-wide max, the lowest expert
+        // id winning ties, so equal logits go to the lower id, -inf (masked) experts are
+        // taken last in id order, and NaN logits are flagged and treated as -inf.  (A
+        // thread-per-token insertion pass cost several times the whole contraction.)
+        // The launch gives every CTA exactly one tile, so the operand stages are free
+        // once the accumulator is ready: the logits are staged there (128 rows x 256
+        // floats; 16-byte chunk u of row j at chunk (u & ~7) | ((u ^ j) & 7)), and the
+        // tile's per-expert counts are summed in shared memory first.
         const int E = p.N;
-        float tv[kTopkMax];
-        int ti[kTopkMax];
-#pragma unroll
-        for (int j = 0; j < kTopkMax; ++j) {
-          tv[j] = -INFINITY;
-          ti[j] = -1;
-        }
-        float run_m = -INFINITY, run_s = 0.f;
-        const bool full_softmax = p.renorm == 0;
-        bool nan = false;
+        const int ew = ((E + 31) / 32) * 32;
         float* lout = static_cast<float*>(p.out);
+        fence_proxy_async_smem();            // the stages' TMA writes precede these stores
+        float* stg = reinterpret_cast<float*>(tiles);                       // [128][256]
+        int* tcnt = reinterpret_cast<int*>(tiles + kBM * kBN * sizeof(float));   // [256]
+        constexpr int kEpiThreads = 32 * (kRouterWarps - 2);
+        for (int i = threadIdx.x - 64; i < kBN; i += kEpiThreads) tcnt[i] = 0;
+        if (warp <= 5) {                     // one warp per TMEM lane quarter
 #pragma unroll 1
-        for (int c = 0; c < (E + 31) / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tb + c * 32, v);
-          tmem_ld_wait();
-          if (valid) {
-            float lg[32];
+          for (int c = 0; c < ew / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) lg[i] = __uint_as_float(v[i]);
-            const int col = c * 32;
-            if (lout != nullptr) {
-              if (col + 32 <= E && E % 4 == 0) {
-                float4* d4 = reinterpret_cast<float4*>(lout + grow * E + col);
+            for (int u = 0; u < 8; ++u) {
+              const int uu = c * 8 + u;
+              const int ph = (uu & ~7) | ((uu ^ r) & 7);
+              *reinterpret_cast<float4*>(stg + r * kBN + ph * 4) =
+                  make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                              __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&s.tempty[acc]);
+        }
+        released = true;
+        epi_bar_sync<kEpiThreads>();         // every row staged, the counts zeroed
+        {
+          const int ksel = p.k_sel;
+          const bool full_softmax = p.renorm == 0;
+          bool nan = false;
+          // kRb tokens at a time per warp (their rounds are independent), the warps
+          // taking the tile's rows in turn
+          constexpr int kRb = 2;
+#pragma unroll 1
+          for (int jb = (warp - 2) * kRb; jb < t.rows; jb += (kRouterWarps - 2) * kRb) {
+            float val[kRb][8];
+            uint32_t taken[kRb];                       // bit m: expert lane + 32 m is out
+            float run_m[kRb], run_s[kRb], top0[kRb], my_v[kRb];
+            int my_i[kRb];
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) d4[q4] = make_float4(lg[4 * q4], lg[4 * q4 + 1], lg[4 * q4 + 2], lg[4 * q4 + 3]);
-              } else {
+            for (int b = 0; b < kRb; ++b) {
+              const int row = jb + b;
+              const bool rok = row < t.rows;
+              taken[b] = rok ? 0u : 0xFFu;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (col + i < E) lout[grow * E + col + i] = lg[i];
+              for (int m = 0; m < 8; ++m) {
+                const int col = lane + 32 * m;
+                float x = -INFINITY;
+                if (rok && col < E) {
+                  const int uu = col >> 2;
+                  x = stg[row * kBN + (((uu & ~7) | ((uu ^ row) & 7)) << 2) + (col & 3)];
+                  if (lout != nullptr) lout[static_cast<size_t>(t.row0 + row) * E + col] = x;
+                  nan = nan || isnan(x);
+                  x = isnan(x) ? -INFINITY : x;
+                } else {
+                  taken[b] |= 1u << m;
+                }
+                val[b][m] = x;
+              }
+              run_m[b] = -INFINITY;
+              run_s[b] = 0.f;
+              top0[b] = -INFINITY;
+              my_v[b] = -INFINITY;
+              my_i[b] = -1;
+            }
+            // full softmax: max and sum of exp over the experts that are not masked
+            if (full_softmax) {
+#pragma unroll
+              for (int b = 0; b < kRb; ++b) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m) run_m[b] = fmaxf(run_m[b], val[b][m]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) run_m[b] = fmaxf(run_m[b], __shfl_xor_sync(0xFFFFFFFFu, run_m[b], o));
+              }
+#pragma unroll
+              for (int b = 0; b < kRb; ++b) {
+                if (run_m[b] != -INFINITY) {
+#pragma unroll
+                  for (int m = 0; m < 8; ++m) run_s[b] += val[b][m] == -INFINITY ? 0.f : expf(val[b][m] - run_m[b]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) run_s[b] += __shfl_xor_sync(0xFFFFFFFFu, run_s[b], o);
               }
             }
+            // k rounds: the largest value not yet taken, the lowest expert id among equals
+            for (int j = 0; j < ksel; ++j) {
+              uint32_t key[kRb];
+              int bm[kRb];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (col + i >= E) break;
-              float x = lg[i];
-              if (isnan(x)) {
-                nan = true;
-                x = -INFINITY;
-              }
-              if (full_softmax) {             // only the full-softmax weights need the sum
-                if (x == -INFINITY) {
-                  // masked expert: no softmax mass
-                } else if (x > run_m) {
-                  run_s = run_s * expf(run_m - x) + 1.f;
-                  run_m = x;
-                } else {
-                  run_s += expf(x - run_m);
-                }
-              }
-              if (x > tv[kTopkMax - 1] || ti[kTopkMax - 1] < 0) {
-                // insert (x, col + i) keeping the list sorted; strict compares keep
-                // earlier (lower-id) equal values ahead
+              for (int b = 0; b < kRb; ++b) {
+                bm[b] = -1;
+                float bv = -INFINITY;
 #pragma unroll
-                for (int j = kTopkMax - 1; j > 0; --j) {
-                  const bool up = x > tv[j - 1] || ti[j - 1] < 0;
-                  const bool here = x > tv[j] || ti[j] < 0;
-                  tv[j] = up ? tv[j - 1] : (here ? x : tv[j]);
-                  ti[j] = up ? ti[j - 1] : (here ? col + i : ti[j]);
+                for (int m = 0; m < 8; ++m) {
+                  const bool ok = !((taken[b] >> m) & 1u) && (bm[b] < 0 || val[b][m] > bv);
+                  bv = ok ? val[b][m] : bv;
+                  bm[b] = ok ? m : bm[b];
                 }
-                if (x > tv[0] || ti[0] < 0) {
-                  tv[0] = x;
-                  ti[0] = col + i;
+                // order-preserving key of the value (0: this lane has nothing left)
+                const uint32_t bu = __float_as_uint(bv);
+                key[b] = bm[b] < 0 ? 0u : ((bu & 0x80000000u) ? ~bu : (bu | 0x80000000u));
+              }
+              uint32_t wkey[kRb], mycol[kRb];
+#pragma unroll
+              for (int b = 0; b < kRb; ++b) wkey[b] = __reduce_max_sync(0xFFFFFFFFu, key[b]);
+#pragma unroll
+              for (int b = 0; b < kRb; ++b)
+                mycol[b] = bm[b] >= 0 && key[b] == wkey[b] ? static_cast<uint32_t>(lane + 32 * bm[b]) : 0xFFFFFFFFu;
+#pragma unroll
+              for (int b = 0; b < kRb; ++b) {
+                const uint32_t wkey_b = wkey[b];
+                const uint32_t wcol = __reduce_min_sync(0xFFFFFFFFu, mycol[b]);
+                if (mycol[b] == wcol) taken[b] |= 1u << bm[b];
+                const float wv = __uint_as_float((wkey_b & 0x80000000u) ? (wkey_b & 0x7FFFFFFFu) : ~wkey_b);
+                if (j == 0) top0[b] = wv;
+                if (lane == j) {
+                  my_v[b] = wv;
+                  my_i[b] = wkey_b == 0u ? -1 : static_cast<int>(wcol);
                 }
+              }
+            }
+            // weights: softmax over the k selected (renormalize) or the full softmax;
+            // every expert masked (-inf): no softmax mass, weight 0
+#pragma unroll
+            for (int b = 0; b < kRb; ++b) {
+              float w;
+              if (!full_softmax) {
+                const float e = lane < ksel && top0[b] != -INFINITY ? expf(my_v[b] - top0[b]) : 0.f;
+                float den = e;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+                w = top0[b] == -INFINITY ? 0.f : e / den;
+              } else {
+                w = top0[b] == -INFINITY || lane >= ksel ? 0.f : expf(my_v[b] - run_m[b]) / run_s[b];
+              }
+              const int row = jb + b;
+              if (lane < ksel && row < t.rows) {
+                const size_t grow = static_cast<size_t>(t.row0 + row);
+                p.topk_idx[grow * ksel + lane] = my_i[b];
+                p.topk_w[grow * ksel + lane] = w;
+                if (my_i[b] >= 0) atomicAdd(&tcnt[my_i[b]], 1);   // k <= E: always an expert
               }
             }
           }
-        }
-        tc_fence_before();
-        mbar_arrive(&s.tempty[acc]);
-        released = true;
-        if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_error(p.status, MOE_DEV_NAN_LOGIT);
-        const int ksel = p.k_sel;
-        float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < kTopkMax; ++j)
-          if (j < ksel) den += expf(tv[j] - tv[0]);
-#pragma unroll
-        for (int j = 0; j < kTopkMax; ++j) {
-          if (j < ksel) {
-            if (valid) {
-              // every expert masked (-inf): no softmax mass, weight 0
-              const float w = tv[0] == -INFINITY ? 0.f
-                              : p.renorm ? expf(tv[j] - tv[0]) / den : expf(tv[j] - run_m) / run_s;
-              p.topk_idx[grow * ksel + j] = ti[j];
-              p.topk_w[grow * ksel + j] = w;
-            }
-            // one atomic per distinct expert in the warp
-            const int id = valid ? ti[j] : -1;
-            const uint32_t same = __match_any_sync(0xFFFFFFFFu, id);
-            if (id >= 0 && lane == __ffs(same) - 1) atomicAdd(&p.counts[id], __popc(same));
+          if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) flag_error(p.status, MOE_DEV_NAN_LOGIT);
+          epi_bar_sync<kEpiThreads>();       // the tile's counts are complete
+          for (int i = threadIdx.x - 64; i < E; i += kEpiThreads) {
+            const int cnt = tcnt[i];
+            if (cnt > 0) atomicAdd(&p.counts[i], cnt);
           }
         }
       } else {
@@ -1419,7 +1506,7 @@ moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& 
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  launch_pdl(kern, sms, threads_for<kKind, kMode, kW>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
+  launch_pdl(kern, sms, block_threads<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
              td ? *td : ta, p);
   return check_launch(what);
 }
@@ -1730,8 +1817,10 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
     return MOE_ERR_INVALID_ARG;
   Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr, nullptr, nullptr,
            topk_idx, topk_w, counts, k, renormalize ? 1 : 0, n_mma};
-  if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
-  return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, sms, fn);
+  // one CTA per tile (the epilogue stages the tile's logits in the operand stages)
+  const int grid = (T + kBM - 1) / kBM;
+  if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn);
+  return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,

@@ -48,6 +48,15 @@ def test_route_topk_gemm_matches_oracle(T, d, E, k, dtype, renorm):
     assert torch.equal(idx, idx2) and torch.equal(w, w2) and torch.equal(counts, c2)
 
 
+@pytest.mark.parametrize("renorm", [True, False], ids=["renorm", "full"])
+def test_route_topk_gemm_deepseek_router_size(renorm):
+    """The DeepSeek-V3 router shape (8192 tokens, d = 7168, E = 256, k = 8): 64 tiles,
+    each selected by 14 warps sharing the tile's rows."""
+    need_gpu()
+    x, Wr = _inputs(8192, 7168, 256, torch.bfloat16, seed=71)
+    _check(x, Wr, 8, renorm, torch.bfloat16)
+
+
 def test_route_topk_gemm_ties_go_to_lower_expert():
     """Duplicate router rows give bit-equal logits; the lower expert id wins."""
     need_gpu()
