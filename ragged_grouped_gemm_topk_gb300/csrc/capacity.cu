@@ -93,6 +93,7 @@ extern "C" moe_status_t moe_permute_capacity(const void* x, moe_dtype_t x_dtype,
                                              int32_t* src_pair, void* xp, void* workspace,
                                              size_t workspace_bytes, int32_t* dev_status,
                                              cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_permute_capacity");
   const char* fn = "moe_permute_capacity";
   const int eb = x_dtype == MOE_F32 ? 4 : 2;
   if (T < 0 || d < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || capacity < 0 ||

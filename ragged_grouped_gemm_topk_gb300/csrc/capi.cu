@@ -100,6 +100,7 @@ __global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
 }  // namespace moe
 
 extern "C" moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_check_wait_timeout");
   using namespace moe;
   if (!dev_status || limit_us < 1 || limit_us > 2000000) {
     set_error("moe_check_wait_timeout: need a status word and 1 <= limit_us <= 2000000");

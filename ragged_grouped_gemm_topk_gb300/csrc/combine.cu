@@ -405,6 +405,7 @@ extern "C" moe_status_t moe_unpermute_combine(const void* yp, moe_dtype_t dtype,
                                               int k, const int32_t* dest_row,
                                               const float* topk_w, void* y, moe_dtype_t y_dtype,
                                               int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_unpermute_combine");
   if (static_cast<long long>(T) * k >= (1LL << 31)) {
     set_error("moe_unpermute_combine: T*k must fit in int32");
     return MOE_ERR_INVALID_ARG;
@@ -417,6 +418,7 @@ extern "C" moe_status_t moe_unpermute_combine_capacity(const void* yp, moe_dtype
                                                        int d, int k, const int32_t* dest_row,
                                                        const float* topk_w, void* y, moe_dtype_t y_dtype,
                                                        int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_unpermute_combine_capacity");
   return combine_impl("moe_unpermute_combine_capacity", yp, dtype, rows, T, d, k, dest_row, topk_w, y, y_dtype,
                       1, dev_status, stream);
 }
@@ -426,6 +428,7 @@ extern "C" moe_status_t moe_unpermute_combine_bwd(const void* dy, const void* yp
                                                   const int32_t* dest_row, const float* topk_w,
                                                   void* dyp, float* dw, int32_t* dev_status,
                                                   cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_unpermute_combine_bwd");
   if (T < 0 || d < 0 || k < 1 || k > 32 || d % 8 || (dtype != MOE_BF16 && dtype != MOE_F32)) {
     set_error("moe_unpermute_combine_bwd: need T, d >= 0, d %% 8 == 0, 1 <= k <= 32, BF16/F32");
     return MOE_ERR_INVALID_ARG;
@@ -458,6 +461,7 @@ extern "C" moe_status_t moe_unpermute_combine_bwd_mxfp8(const void* dy, const vo
                                                         const float* topk_w, uint8_t* dyp_codes,
                                                         uint8_t* dyp_scales, float* dw, int32_t* dev_status,
                                                         cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_unpermute_combine_bwd_mxfp8");
   const char* fn = "moe_unpermute_combine_bwd_mxfp8";
   if (T < 0 || d < 0 || k < 1 || k > 32 || d % 32 || dtype != MOE_BF16) {
     set_error("%s: need T, d >= 0, d %% 32 == 0, 1 <= k <= 32, BF16 dy and yp", fn);

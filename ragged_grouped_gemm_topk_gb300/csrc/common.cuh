@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/moe.h"
@@ -16,6 +17,17 @@ namespace moe {
 
 void set_error(const char* fmt, ...);
 moe_status_t check_launch(const char* what);
+
+// An NVTX range named after the C entry point, for the span of the call (the
+// host-side work and the launches it enqueues show up under that name in a
+// timeline tool; with no tool attached the push and pop do nothing).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // MOE_OK on an sm_103 device (and its SM count), MOE_ERR_UNSUPPORTED on another
 // architecture, MOE_ERR_CUDA when the runtime cannot be queried.
 moe_status_t device_check(int* sm_count);

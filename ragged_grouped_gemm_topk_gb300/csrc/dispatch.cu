@@ -795,6 +795,7 @@ extern "C" moe_status_t moe_permute(const void* x, moe_dtype_t x_dtype, int T, i
                                     void* xp, moe_dtype_t xp_dtype, uint8_t* xp_scales,
                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                     cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_permute");
   moe_status_t st = permute_validate(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row,
                                      src_pair, xp, xp_dtype, xp_scales);
   if (st != MOE_OK) return st;
@@ -840,6 +841,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_gathered(const void* x, moe_dtype_t x
                                                     const int32_t* offsets, int E,
                                                     int axis, uint8_t* codes, uint8_t* scales,
                                                     int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_quantize_mxfp8_gathered");
   const char* fn = "moe_quantize_mxfp8_gathered";
   if (axis != 1 && axis != 2) {
     set_error("%s: axis 1 (column-wise) or 2 (column-wise, tiled scales)", fn);
@@ -872,6 +874,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
                                                    int K, const int32_t* offsets, int E, int axis,
                                                    uint8_t* codes, uint8_t* scales,
                                                    cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_quantize_mxfp8_grouped");
   if (axis != 0 && axis != 1 && axis != 2) {
     set_error("moe_quantize_mxfp8_grouped: axis 0 (row-wise), 1 (column-wise) or 2 (column-wise, tiled scales)");
     return MOE_ERR_UNSUPPORTED;
@@ -913,6 +916,7 @@ extern "C" moe_status_t moe_quantize_mxfp8_grouped(const void* in, moe_dtype_t i
 extern "C" moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_t in_dtype, int G, int R,
                                                       int C, uint8_t* codes, uint8_t* scales,
                                                       cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_quantize_mxfp8_transposed");
   if (G < 0 || R < 0 || C < 0 || R % 32 || C % 8 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
     set_error("moe_quantize_mxfp8_transposed: need G, R, C >= 0, R %% 32 == 0, C %% 8 == 0, BF16/F32 input");
     return MOE_ERR_INVALID_ARG;
@@ -951,6 +955,7 @@ extern "C" moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, in
                                           uint8_t* xp_codes, uint8_t* xp_scales, float* tensor_scale,
                                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                           cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_permute_nvfp4");
   const char* fn = "moe_permute_nvfp4";
   if (T < 0 || d < 0 || d % 16 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E ||
       (x_dtype != MOE_BF16 && x_dtype != MOE_F32) || static_cast<long long>(T) * k >= (1LL << 31)) {

@@ -1553,6 +1553,7 @@ extern "C" moe_status_t moe_grouped_gemm_fwd(const moe_operand_t* A, const moe_o
                                              moe_epilogue_t epi, void* C, moe_dtype_t c_dtype,
                                              void* preact, int32_t* dev_status,
                                              cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_gemm_fwd");
   const char* fn = "moe_grouped_gemm_fwd";
   int sms = 0;
   moe_status_t st = common_checks(fn, A, B, offsets, M, N, K, E, C, &sms);
@@ -1654,6 +1655,7 @@ extern "C" moe_status_t moe_grouped_gemm_fwd_mxfp8_out(const moe_operand_t* A, c
                                                        const int32_t* offsets, int M, int N, int K, int E,
                                                        moe_epilogue_t epi, uint8_t* c_codes, uint8_t* c_scales,
                                                        int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_gemm_fwd_mxfp8_out");
   const char* fn = "moe_grouped_gemm_fwd_mxfp8_out";
   int sms = 0;
   moe_status_t st = common_checks(fn, A, B, offsets, M, N, K, E, c_codes, &sms);
@@ -1701,6 +1703,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad(const moe_operand_t* dC, const mo
                                                moe_epilogue_t epi, const void* preact, void* dA,
                                                moe_dtype_t dA_dtype, int32_t* dev_status,
                                                cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_gemm_dgrad");
   const char* fn = "moe_grouped_gemm_dgrad";
   int sms = 0;
   moe_status_t st = common_checks(fn, dC, B, offsets, M, N, K, E, dA, &sms);
@@ -1739,6 +1742,7 @@ extern "C" moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, co
                                                      const int32_t* offsets, int M, int N, int K, int E,
                                                      moe_epilogue_t epi, const void* preact, void* dA,
                                                      int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_gemm_dgrad_mxfp8");
   // dA[R_e] = dC[R_e] @ B[e] with both operands quantised along the contraction dim N:
   // dC codes [M, N] (scales [M, N/32]) and B^T codes [E, K, N] (scales [E*K, N/32]).
   // That is the forward problem with N and K swapped, so the forward MXFP8 kernel runs it.
@@ -1782,6 +1786,7 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
                                             int d, int E, int k, int renormalize, float* logits,
                                             int32_t* topk_idx, float* topk_w, int32_t* counts,
                                             int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_route_topk_gemm");
   // logits = x . W_r^T on the tensor cores, top-k selection and softmax weights in
   // the GEMM epilogue: the logits need not make a round trip through memory.
   const char* fn = "moe_route_topk_gemm";
@@ -1827,6 +1832,7 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
                                                const int32_t* offsets, int M, int N, int K, int E,
                                                void* dB, moe_dtype_t dB_dtype, int32_t* dev_status,
                                                cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_grouped_gemm_wgrad");
   const char* fn = "moe_grouped_gemm_wgrad";
   int sms = 0;
   moe_status_t st = common_checks(fn, A, dC, offsets, M, N, K, E, dB, &sms);

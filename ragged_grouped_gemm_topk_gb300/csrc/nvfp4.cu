@@ -115,6 +115,7 @@ using namespace moe;
 
 extern "C" moe_status_t moe_quantize_nvfp4(const void* in, moe_dtype_t in_dtype, int rows, int K, uint8_t* codes,
                                            uint8_t* scales, float* tensor_scale, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_quantize_nvfp4");
   const char* fn = "moe_quantize_nvfp4";
   if (rows < 0 || K < 0 || K % 16 || (in_dtype != MOE_BF16 && in_dtype != MOE_F32)) {
     set_error("%s: need rows >= 0, K %% 16 == 0, BF16/F32 input", fn);

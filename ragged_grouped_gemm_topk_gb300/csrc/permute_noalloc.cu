@@ -113,6 +113,7 @@ extern "C" moe_status_t moe_permute_noalloc(const void* x, moe_dtype_t x_dtype, 
                                             int32_t* dest_row, int32_t* src_pair, void* xp,
                                             moe_dtype_t xp_dtype, uint8_t* xp_scales,
                                             int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_permute_noalloc");
   moe_status_t st = permute_validate(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row,
                                      src_pair, xp, xp_dtype, xp_scales);
   if (st != MOE_OK) return st;

@@ -192,6 +192,7 @@ using namespace moe;
 extern "C" moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int renormalize,
                                        int32_t* topk_idx, float* topk_w, int32_t* counts,
                                        int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_route_topk");
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > E || k > 32) {
     set_error("moe_route_topk: need T >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32) (T=%d E=%d k=%d)",
               T, E, k);
@@ -220,6 +221,7 @@ extern "C" moe_status_t moe_route_topk_bwd(const float* dw, const float* topk_w,
                                            const int32_t* topk_idx, const float* logits, int T,
                                            int E, int k, int renormalize, float* dlogits,
                                            int32_t* dev_status, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_route_topk_bwd");
   if (T < 0 || E < 1 || k < 1 || k > E || k > 32) {
     set_error("moe_route_topk_bwd: need T >= 0, 1 <= k <= min(E, 32)");
     return MOE_ERR_INVALID_ARG;
