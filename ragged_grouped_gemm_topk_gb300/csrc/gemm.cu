@@ -921,17 +921,28 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     // alongside the MMA work, with plain 16-byte stores (not through the TMA unit,
     // which the operand loads need) marked evict-first in L2 (so the zeros do not
     // push the operands out).  An expert's dW is N*K*2 bytes, a multiple of 2048
-    // since N and K are multiples of 32; a warp writes one 2 KB chunk per pass.
+    // since N and K are multiples of 32.  The CTA's chunks are c = blockIdx.x +
+    // i * gridDim.x; a warp writes four of them (8 KB) per pass, which measured a few
+    // percent faster than one (the fill ends earlier, ahead of the store-bound tiles
+    // of the small experts at the end).
+    constexpr int kZfU = 4;
     const uint64_t pol = l2_evict_first_policy();
     const size_t per = static_cast<size_t>(p.N) * p.K * 2;
     const size_t cpe = per / 2048;
     const size_t chunks = static_cast<size_t>(p.E - s.nnz) * cpe;
     uint8_t* outb = static_cast<uint8_t*>(p.out);
-    for (size_t c = blockIdx.x; c < chunks && !s.abort; c += gridDim.x) {
-      const int e = s.prefix[s.nnz + static_cast<int>(c / cpe)];
-      uint4* dst = reinterpret_cast<uint4*>(outb + static_cast<size_t>(e) * per + (c % cpe) * 2048);
+    for (size_t c0 = blockIdx.x; c0 < chunks && !s.abort; c0 += kZfU * static_cast<size_t>(gridDim.x)) {
 #pragma unroll
-      for (int i = lane; i < 128; i += 32) st_global_hint(dst + i, make_uint4(0, 0, 0, 0), pol);
+      for (int u = 0; u < kZfU; ++u) {
+        const size_t c = c0 + static_cast<size_t>(u) * gridDim.x;
+        if (c < chunks) {
+          const size_t ci = c / cpe;
+          const int e = s.prefix[s.nnz + static_cast<int>(ci)];
+          uint4* dst = reinterpret_cast<uint4*>(outb + static_cast<size_t>(e) * per + (c - ci * cpe) * 2048);
+#pragma unroll
+          for (int i = lane; i < 128; i += 32) st_global_hint(dst + i, make_uint4(0, 0, 0, 0), pol);
+        }
+      }
     }
   } else if (warp >= 2 &&
              warp <= (kW ? wide_epi_warp0<kMode>() + kWideEpiWarps - 1 : (kEpi == kEpiTopk ? kRouterWarps - 1 : 5))) {
