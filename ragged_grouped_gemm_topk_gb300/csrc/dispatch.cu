@@ -380,14 +380,25 @@ __global__ void __launch_bounds__(kScatterThreads) quantize_rowwise_kernel(
 // gweight (per-pair weights, the routing weights) the rows are gweight[p] *
 // in[p / gk], the product taken in fp32 and rounded to Tin: the rows the combine
 // backward writes as dYp, quantised without being stored.
+//
+// slots (gathered form): every token row is read by k blocks, one per expert it routes
+// to.  Taken in group order, those reads are far apart and each comes from DRAM.  With
+// slots > 0 the blocks are taken slot by slot instead: block b of a group with nb blocks
+// goes to slot floor(b * slots / nb), i.e. by its position in its group, and so, since a
+// group's rows are in token order, roughly by the tokens it reads; inside a slot, group
+// by group.  The blocks of one slot read one token range, which stays in L2 for its k
+// readers.  The slot tables sit in dynamic shared memory: qtab[s][e] = sum over e' < e of
+// ceil(s * nb_e' / slots), for s = 0..slots and e = 0..E.  The output does not depend on
+// the order.
 constexpr int kColThreads = 128;
 
 template <typename Tin, bool kTiled>
 __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     const uint8_t* __restrict__ in, int rows, int K, const int32_t* __restrict__ offsets, int E,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const int32_t* __restrict__ gather,
-    const float* __restrict__ gweight, int gk, int gpairs, int32_t* status) {
+    const float* __restrict__ gweight, int gk, int gpairs, int32_t* status, int slots) {
   pdl_begin();
+  extern __shared__ int qtab[];                // slots > 0: [slots + 1][E + 1]
   constexpr int EB = sizeof(Tin);
   constexpr int CPT = 4;                       // columns per thread
   constexpr int NW = CPT * EB / 4;             // 32-bit words per chunk
@@ -438,16 +449,78 @@ __global__ void __launch_bounds__(kColThreads) quantize_colwise_kernel(
     if (threadIdx.x == kColThreads - 1) bpre[E] = run;   // every block row
   }
   __syncthreads();
+  if (slots > 0) {
+    // qtab[s][e]: exclusive scan over the groups of ceil(s * nb_e / slots)
+    for (int sl = 0; sl <= slots; ++sl) {
+      int* q = qtab + sl * (E + 1);
+      int own = 0;
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const int e = threadIdx.x * G + u;
+        const int nb = e < E ? bpre[e + 1] - bpre[e] : 0;
+        cnt[u] = (sl * nb + slots - 1) / slots;
+        own += cnt[u];
+      }
+      part[threadIdx.x] = own;
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        int carry = 0;
+        for (int base = 0; base < kColThreads; base += 32) {
+          int v = part[base + threadIdx.x];
+          const int mine = v;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int w = __shfl_up_sync(kFull, v, off);
+            if (static_cast<int>(threadIdx.x) >= off) v += w;
+          }
+          part[base + threadIdx.x] = carry + v - mine;   // exclusive
+          carry += __shfl_sync(kFull, v, 31);
+        }
+      }
+      __syncthreads();
+      int run = part[threadIdx.x];
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const int e = threadIdx.x * G + u;
+        if (e < E) q[e] = run;
+        run += cnt[u];
+      }
+      if (threadIdx.x == kColThreads - 1) q[E] = run;
+      __syncthreads();
+    }
+  }
   const int total = bpre[E];
   const int nstrip = (K + kStrip - 1) / kStrip;
   const size_t in_row = static_cast<size_t>(K) * EB;
   for (long long task = blockIdx.x; task < static_cast<long long>(total) * nstrip; task += gridDim.x) {
-    const int br = static_cast<int>(task / nstrip);
     const int strip = static_cast<int>(task % nstrip);
-    int lo_e = 0, hi_e = E - 1;                 // last group whose first block row <= br
-    while (lo_e < hi_e) {
-      const int mid = (lo_e + hi_e + 1) >> 1;
-      if (bpre[mid] <= br) lo_e = mid; else hi_e = mid - 1;
+    int br, lo_e = 0;
+    if (slots > 0) {
+      // block ordinal i -> slot sl (blocks of slots < sl: qtab[sl][E]) -> group (blocks of
+      // slot sl in groups < e: qtab[sl + 1][e] - qtab[sl][e]) -> block in the group
+      const int i = static_cast<int>(task / nstrip);
+      int sl = 0, hs = slots - 1;
+      while (sl < hs) {
+        const int mid = (sl + hs + 1) >> 1;
+        if (qtab[mid * (E + 1) + E] <= i) sl = mid; else hs = mid - 1;
+      }
+      const int* q0 = qtab + sl * (E + 1);
+      const int* q1 = q0 + (E + 1);
+      const int j = i - q0[E];
+      int hi_e = E - 1;
+      while (lo_e < hi_e) {
+        const int mid = (lo_e + hi_e + 1) >> 1;
+        if (q1[mid] - q0[mid] <= j) lo_e = mid; else hi_e = mid - 1;
+      }
+      const int b = (q0[lo_e + 1] - q0[lo_e]) + (j - (q1[lo_e] - q0[lo_e]));
+      br = bpre[lo_e] + b;
+    } else {
+      br = static_cast<int>(task / nstrip);
+      int hi_e = E - 1;                         // last group whose first block row <= br
+      while (lo_e < hi_e) {
+        const int mid = (lo_e + hi_e + 1) >> 1;
+        if (bpre[mid] <= br) lo_e = mid; else hi_e = mid - 1;
+      }
     }
     const int r0 = offsets[lo_e] + (br - bpre[lo_e]) * 32;
     const int n = min(32, offsets[lo_e + 1] - r0);
@@ -816,22 +889,28 @@ void colwise_launch(const void* in, moe_dtype_t in_dtype, int rows, int K, const
                     int gpairs, int32_t* status, cudaStream_t stream, int sms) {
   const int strip = kColThreads * 4;
   const long long items = (static_cast<long long>(rows) / 32 + E) * ((K + strip - 1) / strip);
-  const int grid = static_cast<int>(items < static_cast<long long>(sms) * 8 ? (items > 0 ? items : 1) : sms * 8);
+  // the gathered form takes its blocks slot by slot (see the kernel); its slot tables
+  // take (slots + 1) * (E + 1) ints of dynamic shared memory
+  const int slots = gather ? (E <= 512 ? 16 : 8) : 0;
+  const size_t dyn = slots > 0 ? static_cast<size_t>(slots + 1) * (E + 1) * sizeof(int) : 0;
   const uint8_t* src = static_cast<const uint8_t*>(in);
+  auto go = [&](auto kern) {
+    // as many CTAs as stay resident (they walk the work in a grid-stride loop)
+    int per_sm = 8;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kColThreads, dyn) != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    per_sm = per_sm < 8 ? per_sm : 8;
+    const long long cap = static_cast<long long>(sms) * per_sm;
+    const int grid = static_cast<int>(items < cap ? (items > 0 ? items : 1) : cap);
+    launch_pdl(kern, grid, kColThreads, dyn, stream, src, rows, K, offsets, E, codes, scales, gather, gweight, gk,
+               gpairs, status, slots);
+  };
   if (in_dtype == MOE_BF16) {
-    if (axis == 2)
-      launch_pdl(quantize_colwise_kernel<uint16_t, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gweight, gk, gpairs, status);
-    else
-      launch_pdl(quantize_colwise_kernel<uint16_t, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gweight, gk, gpairs, status);
+    if (axis == 2) go(quantize_colwise_kernel<uint16_t, true>);
+    else go(quantize_colwise_kernel<uint16_t, false>);
   } else {
-    if (axis == 2)
-      launch_pdl(quantize_colwise_kernel<float, true>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gweight, gk, gpairs, status);
-    else
-      launch_pdl(quantize_colwise_kernel<float, false>, grid, kColThreads, 0, stream, src, rows, K, offsets, E,
-                 codes, scales, gather, gweight, gk, gpairs, status);
+    if (axis == 2) go(quantize_colwise_kernel<float, true>);
+    else go(quantize_colwise_kernel<float, false>);
   }
 }
 }  // namespace
