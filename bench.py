@@ -717,7 +717,8 @@ def router_leg(w, x, lg, layer, pk):
             "frac_of_peak": round(flops / (t_f * 1e-3) / 1e12 / peak, 4),
             "route_from_logits_ms": round(t_p, 4), "library_logits_gemm_ms": round(t_g, 4),
             "unfused_ms": round(t_g + t_p, 4), "logits_bytes_not_written": w.T * w.E * 4,
-            "timing": "eager, 20 calls; one CTA per 128-token tile x E expert columns (E rounded up to 16)"}
+            "timing": "eager, 20 calls; one CTA per 128-token tile x E expert columns (E rounded up to 16), "
+                      "or a cluster of 2-4 CTAs per tile splitting the contraction when the tiles leave SMs idle"}
 
 
 def capacity_leg(w, x, lg, layer, W1, W2, cf, dropless_ms):

@@ -119,7 +119,10 @@ moe_status_t moe_route_topk(const float* logits, int T, int E, int k, int renorm
  *   logits    [T, E] float32 out, or NULL (the logits then never reach memory;
  *             the router backward with renormalize == 0 needs them).
  *   topk_idx, topk_w, counts: as moe_route_topk (counts zeroed inside).
- * The MMA is E (rounded up to 16) columns wide; one 128-token tile per CTA.
+ * The MMA is E (rounded up to 16) columns wide; one 128-token tile per CTA, or,
+ * when the tiles would leave SMs idle, per thread-block cluster of 2 or 4 CTAs that
+ * split the contraction: the partial logits are summed in slice order through
+ * distributed shared memory, so the logits are the same from call to call.
  * Limits: d % 32 == 0, 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 0. */
 moe_status_t moe_route_topk_gemm(const void* x, const void* w_router, moe_dtype_t dtype, int T, int d,
                                  int E, int k, int renormalize, float* logits, int32_t* topk_idx,

@@ -91,6 +91,8 @@ constexpr int kMaxE = 1024;
 enum { kFwd = 0, kDgrad = 1, kWgrad = 2 };
 enum { kEpiNone = 0, kEpiSwiglu = 1, kEpiDswiglu = 2, kEpiTopk = 3 };
 constexpr int kTopkMax = 8;                       // router epilogue: experts per token
+constexpr int kMaxSplit = 4;                      // router: CTAs of a cluster sharing one tile
+constexpr int kMinSliceBlocks = 8;                // router: K blocks of a contraction slice, at least
 
 // Instruction descriptor (kind::f16 / kind::tf32): D = f32 (bit 4), A/B format
 // (bits 7-9 / 10-12: 1 = bf16, 2 = tf32), A/B major (bits 15 / 16: 1 = MN-major),
@@ -111,11 +113,15 @@ struct Smem {
   uint64_t sempty[2];      // MXFP8 raw scale slots read into registers
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t xready;         // router split over a cluster: every peer's partial logits are staged
+  uint64_t xdone;          //   every peer has finished reading this CTA's partial logits
   uint32_t tmem_base;
   int abort;
   int total_tiles;
   int nnz;                 // wgrad: experts with rows
   int epi_ok;              // router: the accumulator is ready (else the pipeline gave up)
+  int x_ok;                // router split: every CTA of the cluster staged its partial
+  int peer_ok[kMaxSplit];  // router split: written by each peer before it arrives on xready
   int prefix[kMaxE + 1];   // fwd/dgrad: tile prefix; wgrad: expert ids, non-empty then empty
 };
 
@@ -245,6 +251,7 @@ struct Params {
   int k_sel;               //   experts per token (<= kTopkMax)
   int renorm;              //   softmax over the selected logits (1) or over all (0)
   int n_mma;               //   MMA width: E rounded up to 16 (the B tile holds that many rows)
+  int split;               //   CTAs (one cluster) sharing a tile's contraction: 1, 2 or 4
 };
 
 // Rows of group e.  Without an offsets array the problem is one dense group of M rows.
@@ -265,6 +272,7 @@ struct Tile {
   int col0;    // first output column (fwd/dgrad) / first dB column (wgrad)
   int n0;      // wgrad: first dB row
   int kblocks; // contraction blocks
+  int kb0;     // first contraction block (the router's slice of a split contraction)
 };
 
 __device__ __forceinline__ bool group_ok(int beg, int end, int M) { return beg >= 0 && end >= beg && end <= M; }
@@ -288,10 +296,17 @@ struct Geo {
   int mn_rows;  // wgrad: contraction rows per stage
   int rb;       // fwd/dgrad: row tiles per raster block
   int tm;       // tile rows (fwd/dgrad: rows of the group; wgrad: dB rows): 128, or 256 for wide tiles
+  int split;    // CTAs sharing a tile (router: a cluster, each a slice of the contraction); else 1
+  int crank;    // this CTA's rank in that cluster
+  int t0, ts;   // this CTA's first tile and its stride through the tile list
   __device__ Geo(const Params& p, int elem_bytes, int bn, int tile_m = kBM) {
     mn_rows = elem_bytes == 1 ? kMxWgRows : kMnRows;
     rb = 1;
     tm = tile_m;
+    split = kEpi == kEpiTopk && p.split > 1 ? p.split : 1;
+    crank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    t0 = static_cast<int>(blockIdx.x) / split;
+    ts = static_cast<int>(gridDim.x) / split;
     if (kMode == kWgrad) {
       nt = (p.N + tm - 1) / tm;
       nt2 = (p.K + kBN - 1) / kBN;
@@ -345,6 +360,7 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
     t.row0 = cnt > 0 ? beg : 0;
     t.rows = cnt;
     t.kblocks = (cnt + g.mn_rows - 1) / g.mn_rows;
+    t.kb0 = 0;
   } else {
     const int mt = (cnt + g.tm - 1) / g.tm;   // >= 1: only non-empty groups own tiles
     const int blk = local / (g.rb * g.nt);   // raster block (see kRasterABytes)
@@ -355,7 +371,9 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
     t.rows = left < g.tm ? left : g.tm;
     t.col0 = (rem / in_blk) * g.bn_out;
     t.n0 = 0;
-    t.kblocks = g.kb_fixed;
+    // a split contraction: slice crank of split near-equal runs of K blocks
+    t.kb0 = g.crank * g.kb_fixed / g.split;
+    t.kblocks = (g.crank + 1) * g.kb_fixed / g.split - t.kb0;
   }
   return t;
 }
@@ -586,6 +604,9 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
       mbar_init(&s.tfull[i], 1);
       mbar_init(&s.tempty[i], kW ? 32 * kWideEpiWarps : 128);
     }
+    // router split: one arrival from each peer of the cluster
+    mbar_init(&s.xready, g.split > 1 ? g.split - 1 : 1);
+    mbar_init(&s.xdone, g.split > 1 ? g.split - 1 : 1);
     s.abort = 0;
     fence_mbar_init();
   }
@@ -605,6 +626,9 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
   }
   pdl_begin();             // the prologue above overlaps the preceding kernel
   build_tiles(s, g, p, reinterpret_cast<int*>(tiles));   // contains __syncthreads
+  // a cluster's CTAs see each other's barriers initialised before any remote arrival
+  // (reached by every thread, before any other wait)
+  if (kEpi == kEpiTopk && g.split > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int total = s.total_tiles;
@@ -614,7 +638,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     if (lane == 0) {
       int stage = 0, ss = 0;
       uint32_t phase = 0, ss_phase = 0;
-      for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+      for (int tile = g.t0; tile < total && !s.abort; tile += g.ts) {
         const Tile t = tile_info(s, g, tile, p);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (kKind == 2 && kMode == kFwd && kb % 4 == 0) {
@@ -643,7 +667,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                                          (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
                                          (kKind == 3 ? kNvAtomBytes : 0));
           if (kMode == kFwd) {
-            const int kx = kb * (kBKBytes / eb);
+            const int kx = (t.kb0 + kb) * (kBKBytes / eb);
             tma_load_2d(sa, &tmA, bar, kx, t.row0);
             if (kEpi == kEpiSwiglu) {
               tma_load_3d(sb, &tmB, bar, kx, t.col0, t.e);
@@ -695,7 +719,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                                                         kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total && !s.abort; tile += gridDim.x) {
+    for (int tile = g.t0; tile < total && !s.abort; tile += g.ts) {
       const Tile t = tile_info(s, g, tile, p);
       if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.status, &s.abort)) break;
       tc_fence_after();
@@ -969,9 +993,10 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     OutT* out = static_cast<OutT*>(p.out);
     int acc = 0;
     uint32_t acc_phase = 0;
+    bool xchg = false;                      // router split: this CTA exchanged partials with its peers
     // (the router's epilogue warps meet at named barriers, so they all enter the
     // loop and all take the same decision to leave it: see below)
-    for (int tile = blockIdx.x; tile < total && (kEpi == kEpiTopk || !s.abort); tile += gridDim.x) {
+    for (int tile = g.t0; tile < total && (kEpi == kEpiTopk || !s.abort); tile += g.ts) {
       Tile t = tile_info(s, g, tile, p);
       if (kW) {                              // this warp's half of the wide tile
         if (kMode == kWgrad) {
@@ -981,6 +1006,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           t.rows -= hh * kBM;
         }
       }
+      [[maybe_unused]] bool acc_ok = true;
       if constexpr (kEpi == kEpiTopk) {
         // one bounded wait for all the router's epilogue warps; its outcome reaches
         // them through a barrier that every one of them always reaches
@@ -989,7 +1015,9 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           if (lane == 0) s.epi_ok = ok ? 1 : 0;
         }
         epi_bar_sync<32 * (kRouterWarps - 2)>();
-        if (!*reinterpret_cast<volatile int*>(&s.epi_ok)) break;
+        acc_ok = *reinterpret_cast<volatile int*>(&s.epi_ok) != 0;
+        // a CTA of a split cluster goes on to its exchanges with its peers either way
+        if (!acc_ok && g.split == 1) break;
       } else {
         if (!mbar_wait(&s.tfull[acc], acc_phase, p.status, &s.abort)) break;
       }
@@ -1211,7 +1239,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
         int* tcnt = reinterpret_cast<int*>(tiles + kBM * kBN * sizeof(float));   // [256]
         constexpr int kEpiThreads = 32 * (kRouterWarps - 2);
         for (int i = threadIdx.x - 64; i < kBN; i += kEpiThreads) tcnt[i] = 0;
-        if (warp <= 5) {                     // one warp per TMEM lane quarter
+        if (acc_ok && warp <= 5) {           // one warp per TMEM lane quarter
 #pragma unroll 1
           for (int c = 0; c < ew / 32; ++c) {
             uint32_t v[32];
@@ -1231,6 +1259,73 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
         }
         released = true;
         epi_bar_sync<kEpiThreads>();         // every row staged, the counts zeroed
+        // Rows this CTA selects: the whole tile, or with a split contraction (a
+        // cluster of g.split CTAs, each holding the partial logits of one run of K
+        // blocks) its 128 / g.split rows, the partials summed in slice order (so the
+        // logits do not depend on which CTA sums them) from the peers' staging
+        // through distributed shared memory.
+        const int rbeg = g.crank * (kBM / g.split);
+        const int rend = t.rows < rbeg + kBM / g.split ? t.rows : rbeg + kBM / g.split;
+        bool go = acc_ok;
+        if (g.split > 1) {
+          // (1) tell every peer whether this CTA's partial is staged, then wait for theirs
+          if (warp == 2 && lane == 0) {
+            fence_acq_rel_cluster();
+            for (int j = 1; j < g.split; ++j) {
+              const uint32_t pr = static_cast<uint32_t>((g.crank + j) % g.split);
+              st_cluster_u32(cluster_map(smem_u32(&s.peer_ok[g.crank]), pr), acc_ok ? 1u : 0u);
+              mbar_arrive_cluster(cluster_map(smem_u32(&s.xready), pr));
+            }
+          }
+          if (warp == 2) {
+            const bool ok = mbar_wait_cluster(&s.xready, 0, p.status);
+            fence_acq_rel_cluster();
+            if (lane == 0) {
+              bool all = ok && acc_ok;
+              for (int j = 0; j < g.split; ++j)
+                if (j != g.crank) all = all && *reinterpret_cast<volatile int*>(&s.peer_ok[j]) != 0;
+              s.x_ok = all ? 1 : 0;
+            }
+          }
+          epi_bar_sync<kEpiThreads>();
+          go = *reinterpret_cast<volatile int*>(&s.x_ok) != 0;
+          // (2) the sums of this CTA's rows, in place (the peers read only their own rows
+          // of this CTA's staging); the chunk swizzle stays within a row, so chunk c of a
+          // row is the same 4 experts in every CTA
+          if (go && rend > rbeg) {
+            const int nch = ew / 4;
+            const uint32_t lb = smem_u32(stg);
+            uint32_t pb[kMaxSplit];
+#pragma unroll
+            for (int j = 0; j < kMaxSplit; ++j) pb[j] = j < g.split ? cluster_map(lb, static_cast<uint32_t>(j)) : 0u;
+#pragma unroll 2
+            for (int i = threadIdx.x - 64; i < (rend - rbeg) * nch; i += kEpiThreads) {
+              const int row = rbeg + i / nch, ch = i % nch;
+              const uint32_t off = static_cast<uint32_t>(row * kBN + ch * 4) * 4u;
+              float4 a = ld_cluster_f4(pb[0] + off);
+#pragma unroll
+              for (int j = 1; j < kMaxSplit; ++j) {
+                if (j < g.split) {
+                  const float4 v = ld_cluster_f4(pb[j] + off);
+                  a.x += v.x;
+                  a.y += v.y;
+                  a.z += v.z;
+                  a.w += v.w;
+                }
+              }
+              *reinterpret_cast<float4*>(stg + row * kBN + ch * 4) = a;
+            }
+          }
+          epi_bar_sync<kEpiThreads>();
+          // (3) done with the peers' staging (each waits for this before it exits)
+          if (warp == 2 && lane == 0) {
+            fence_acq_rel_cluster();
+            for (int j = 1; j < g.split; ++j)
+              mbar_arrive_cluster(cluster_map(smem_u32(&s.xdone), static_cast<uint32_t>((g.crank + j) % g.split)));
+          }
+          xchg = true;
+        }
+        if (!go) break;
         {
           const int ksel = p.k_sel;
           const bool full_softmax = p.renorm == 0;
@@ -1239,7 +1334,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           // taking the tile's rows in turn
           constexpr int kRb = 2;
 #pragma unroll 1
-          for (int jb = (warp - 2) * kRb; jb < t.rows; jb += (kRouterWarps - 2) * kRb) {
+          for (int jb = rbeg + (warp - 2) * kRb; jb < rend; jb += (kRouterWarps - 2) * kRb) {
             float val[kRb][8];
             uint32_t taken[kRb];                       // bit m: expert lane + 32 m is out
             float run_m[kRb], run_s[kRb], top0[kRb], my_v[kRb];
@@ -1247,7 +1342,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
 #pragma unroll
             for (int b = 0; b < kRb; ++b) {
               const int row = jb + b;
-              const bool rok = row < t.rows;
+              const bool rok = row < rend;
               taken[b] = rok ? 0u : 0xFFu;
 #pragma unroll
               for (int m = 0; m < 8; ++m) {
@@ -1341,7 +1436,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                 w = top0[b] == -INFINITY || lane >= ksel ? 0.f : expf(my_v[b] - run_m[b]) / run_s[b];
               }
               const int row = jb + b;
-              if (lane < ksel && row < t.rows) {
+              if (lane < ksel && row < rend) {
                 const size_t grow = static_cast<size_t>(t.row0 + row);
                 p.topk_idx[grow * ksel + lane] = my_i[b];
                 p.topk_w[grow * ksel + lane] = w;
@@ -1412,6 +1507,8 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
       }
       if (++acc == kAccN) { acc = 0; acc_phase ^= 1u; }
     }
+    // a CTA of a split cluster exits only after its peers have read its staging
+    if (kEpi == kEpiTopk && xchg && warp == 2) (void)mbar_wait_cluster(&s.xdone, 0, p.status);
     if constexpr (kMode == kWgrad || kMode == kFwd || kW) {
       if (lane == 0) bulk_wait_all0();      // every TMA store has landed
       __syncwarp();
@@ -1511,14 +1608,14 @@ bool ensure_smem(Kern k, size_t bytes) {
 template <int kKind, int kMode, int kEpi, typename OutT>
 moe_status_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p, cudaStream_t stream,
                     int sms, const char* what, const CUtensorMap* tsa = nullptr,
-                    const CUtensorMap* tsb = nullptr, const CUtensorMap* td = nullptr) {
+                    const CUtensorMap* tsb = nullptr, const CUtensorMap* td = nullptr, int cluster = 1) {
   constexpr bool kW = wide_tile<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>();
   constexpr size_t smem = smem_for<kKind, kMode, kW>();
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = grouped_gemm_kernel<kKind, kMode, kEpi, OutT>;
   if (!ensure_smem(kern, smem)) return MOE_ERR_CUDA;
-  launch_pdl(kern, sms, block_threads<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>(), smem, stream, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb,
-             td ? *td : ta, p);
+  launch_pdl_cluster(kern, sms, block_threads<kKind, kMode, kEpi, static_cast<int>(sizeof(OutT))>(), smem, stream,
+                     cluster, ta, tb, tsa ? *tsa : ta, tsb ? *tsb : tb, td ? *td : ta, p);
   return check_launch(what);
 }
 
@@ -1831,12 +1928,23 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
   if (!make_map(&ta, map_type(dtype), eb, x, 2, adims, abox) ||
       !make_map(&tb, map_type(dtype), eb, w_router, 3, bdims, bbox))
     return MOE_ERR_INVALID_ARG;
+  // One CTA per tile (the epilogue stages the tile's logits in the operand stages),
+  // or, when the tiles leave SMs idle, a cluster of `split` CTAs per tile, each
+  // taking one run of the contraction (at least kMinSliceBlocks K blocks) and the
+  // selection of 128 / split of its rows; every cluster owns exactly one tile.
+  const int tiles = (T + kBM - 1) / kBM;
+  const int kblocks = (d * eb + kBKBytes - 1) / kBKBytes;
+  int split = 1;
+  for (int c = kMaxSplit; c > 1; c /= 2)
+    if (tiles * c <= sms && kblocks >= c * kMinSliceBlocks) {
+      split = c;
+      break;
+    }
   Params p{nullptr, T, E, d, 1, logits, nullptr, nullptr, nullptr, dev_status, nullptr, nullptr, nullptr, nullptr,
-           topk_idx, topk_w, counts, k, renormalize ? 1 : 0, n_mma};
-  // one CTA per tile (the epilogue stages the tile's logits in the operand stages)
-  const int grid = (T + kBM - 1) / kBM;
-  if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn);
-  return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn);
+           topk_idx, topk_w, counts, k, renormalize ? 1 : 0, n_mma, split};
+  const int grid = tiles * split;
+  if (dtype == MOE_F32) return launch<0, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn, nullptr, nullptr, nullptr, split);
+  return launch<1, kFwd, kEpiTopk, float>(ta, tb, p, stream, grid, fn, nullptr, nullptr, nullptr, split);
 }
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,

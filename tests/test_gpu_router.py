@@ -48,10 +48,53 @@ def test_route_topk_gemm_matches_oracle(T, d, E, k, dtype, renorm):
     assert torch.equal(idx, idx2) and torch.equal(w, w2) and torch.equal(counts, c2)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "tf32"])
+@pytest.mark.parametrize("renorm", [True, False], ids=["renorm", "full"])
+@pytest.mark.parametrize("T,d,E,k", [(777, 2048, 96, 6), (2500, 1024, 160, 8), (50, 2048, 256, 8),
+                                     (4100, 4096, 64, 4)])
+def test_route_topk_gemm_split_contraction(T, d, E, k, dtype, renorm):
+    """Tiles that leave SMs idle split their contraction over a cluster of 2 or 4 CTAs
+    (the partial logits summed through distributed shared memory, each CTA selecting
+    its share of the rows).  On 152 SMs: 777 x 2048 takes clusters of 4 (7 tiles, the
+    last with 9 rows, so three CTAs of its cluster select nothing); 2500 x 1024 clusters
+    of 2 in bf16 (16 K blocks) and of 4 in tf32 (68 rows in the last tile); 50 x 2048 one
+    cluster of 4 over a single partial tile; 4100 x 4096 clusters of 4 (33 tiles, 4 rows
+    in the last).  Clusters of 2 at the 8192-token DeepSeek-V3 size are tested below."""
+    need_gpu()
+    x, Wr = _inputs(T, d, E, dtype, seed=T + d + E + k + 1)
+    idx, w, counts = _check(x, Wr, k, renorm, dtype)
+    # the partials are summed in a fixed order: a second call is bit-identical
+    idx2, w2, c2, lg2 = moe_gpu.moe_route_topk_gemm(x, Wr, k, renorm, want_logits=True)
+    _, _, _, lg1 = moe_gpu.moe_route_topk_gemm(x, Wr, k, renorm, want_logits=True)
+    assert torch.equal(idx, idx2) and torch.equal(w, w2) and torch.equal(counts, c2)
+    assert torch.equal(lg1, lg2)
+
+
+def test_route_topk_gemm_split_ties_and_nan():
+    """Under a split contraction: bit-equal logits of duplicate router rows go to the
+    lower expert id, and a NaN in a token owned by the second CTA of a cluster is
+    flagged."""
+    need_gpu()
+    x, Wr = _inputs(200, 2048, 24, torch.bfloat16, seed=15)
+    Wr[9] = Wr[2]
+    Wr[17] = Wr[2]
+    idx, _, _ = _check(x, Wr, 4, True, torch.bfloat16)
+    i = i64(idx)
+    for t, j in zip(*np.where(i == 9)):
+        assert 2 in i[t, :j]
+    for t, j in zip(*np.where(i == 17)):
+        assert 2 in i[t, :j] and 9 in i[t, :j]
+    x[190, 7] = float("nan")                  # tile 1, row 62: the second CTA's share
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe_gpu.moe_route_topk_gemm(x, Wr, 4, True, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == moe_gpu.binding._lib.MOE_DEV_NAN_LOGIT
+
+
 @pytest.mark.parametrize("renorm", [True, False], ids=["renorm", "full"])
 def test_route_topk_gemm_deepseek_router_size(renorm):
     """The DeepSeek-V3 router shape (8192 tokens, d = 7168, E = 256, k = 8): 64 tiles,
-    each selected by 14 warps sharing the tile's rows."""
+    each contracted by a cluster of 2 CTAs whose 14 selecting warps share its rows."""
     need_gpu()
     x, Wr = _inputs(8192, 7168, 256, torch.bfloat16, seed=71)
     _check(x, Wr, 8, renorm, torch.bfloat16)
