@@ -106,11 +106,56 @@ __device__ __forceinline__ float ue4m3_value(uint32_t code) {
 // encode scale is g: the E4M3 scale byte s = E4M3_rn_sat((amax / 6) * g) and the
 // multiplier g / s (0 when s decodes to 0), every step one fp32 rounding.
 __device__ __forceinline__ float nvfp4_tensor_scale(float amax_t) { return amax_t == 0.f ? 1.f : 2688.f / amax_t; }
+__device__ __forceinline__ uint32_t nvfp4_block_code(float amax, float g) {
+  return f32x2_to_e4m3x2(__fmul_rn(__fdiv_rn(amax, 6.f), g), 0.f) & 0xFFu;
+}
+// The multiplier of a block whose scale byte is `code`: g / value(code), 0 for a zero scale.
+__device__ __forceinline__ float nvfp4_block_inv(uint32_t code, float g) {
+  const float sval = ue4m3_value(code);
+  return sval == 0.f ? 0.f : __fdiv_rn(g, sval);
+}
 __device__ __forceinline__ void nvfp4_block_scale(float amax, float g, uint32_t* scode, float* inv) {
-  const float sf = __fmul_rn(__fdiv_rn(amax, 6.f), g);
-  *scode = f32x2_to_e4m3x2(sf, 0.f) & 0xFFu;
-  const float sval = ue4m3_value(*scode);
-  *inv = sval == 0.f ? 0.f : __fdiv_rn(g, sval);
+  *scode = nvfp4_block_code(amax, g);
+  *inv = nvfp4_block_inv(*scode, g);
+}
+
+// Tensor amax of a bf16 (Tin = uint16_t) or fp32 array of n16 16-byte chunks, the part
+// of block blk of nblocks (blockDim.x threads each), merged into *amax_bits (the fp32
+// bits of a non-negative value, so an integer max orders them): four chunks in flight
+// per thread.  Every thread of the block calls it.
+template <typename Tin>
+__device__ __forceinline__ void nvfp4_amax_body(const uint8_t* __restrict__ in, long long n16, uint32_t* amax_bits,
+                                                long long blk, long long nblocks) {
+  float m = 0.f;
+  const uint4* v4 = reinterpret_cast<const uint4*>(in);
+  const long long stride = nblocks * blockDim.x;
+  for (long long i = blk * blockDim.x + threadIdx.x; i < n16; i += 4 * stride) {
+    uint4 u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) u[q] = i + q * stride < n16 ? v4[i + q * stride] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if constexpr (sizeof(Tin) == 2) {
+          m = fmaxf(m, fabsf(bf16_to_f32(static_cast<uint16_t>(w[j] & 0xFFFFu))));
+          m = fmaxf(m, fabsf(bf16_to_f32(static_cast<uint16_t>(w[j] >> 16))));
+        } else {
+          m = fmaxf(m, fabsf(__uint_as_float(w[j])));
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  __shared__ float part[32];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) m = fmaxf(m, part[i]);
+    atomicMax(amax_bits, __float_as_uint(m));
+  }
 }
 
 // MXFP8 shared-exponent rule (OCP Microscaling Formats v1.0): X = floor(log2 amax)

@@ -31,10 +31,9 @@ constexpr int kRankThreads = 256;                    // 8 warps x 32 tokens per 
 constexpr int kTokensPerRankBlock = kRankThreads;
 constexpr int kScatterThreads = 256;
 
-__global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
-    const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ local_rank,
-    int32_t* __restrict__ block_hist, int32_t* status) {
-  pdl_begin();
+__device__ __forceinline__ void permute_rank_body(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                  int32_t* __restrict__ local_rank, int32_t* __restrict__ block_hist,
+                                                  int32_t* status) {
   extern __shared__ uint32_t sm[];
   uint32_t* mask = sm;                                      // [8][E]
   int32_t* wbase = reinterpret_cast<int32_t*>(sm + 8 * E);  // [8][E]
@@ -72,6 +71,27 @@ __global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
       local_rank[static_cast<size_t>(t) * k + j] = r;
     }
   }
+}
+
+__global__ void __launch_bounds__(kRankThreads) permute_rank_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ local_rank,
+    int32_t* __restrict__ block_hist, int32_t* status) {
+  pdl_begin();
+  permute_rank_body(idx, T, k, E, local_rank, block_hist, status);
+}
+
+// NVFP4 dispatch, first pass: the rank blocks (the first nblk) and the tensor amax of
+// x (the other blocks) in one launch, as the two are independent.
+template <typename Tin>
+__global__ void __launch_bounds__(kRankThreads) permute_rank_amax_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ local_rank,
+    int32_t* __restrict__ block_hist, int32_t* status, int nblk, const uint8_t* __restrict__ x, long long n16,
+    uint32_t* amax_bits) {
+  pdl_begin();
+  if (static_cast<int>(blockIdx.x) < nblk)
+    permute_rank_body(idx, T, k, E, local_rank, block_hist, status);
+  else
+    nvfp4_amax_body<Tin>(x, n16, amax_bits, blockIdx.x - nblk, gridDim.x - nblk);
 }
 
 struct alignas(16) Vec16 {
@@ -131,12 +151,41 @@ __device__ __forceinline__ void mx_chunk(const Vec16& v, uint32_t (&codes)[2], u
 // flight (8 KB per warp), and the first batch is requested before the token's
 // destinations are resolved so that the two latencies overlap.
 constexpr int kScatterU = 8;
+// Quantising scatter: each warp quantises a segment of 32 * kScatterU chunks of its
+// token once, into a shared-memory buffer (codes, then scales), and copies the segment
+// out to the token's k rows with wide stores.
+constexpr int kSegCodes = 32 * kScatterU * 8;       // MXFP8 from bf16: 8 code bytes a chunk
+constexpr int kSegBytes = kSegCodes + 32 * kScatterU * 8 / 16;   // + NVFP4 scales from bf16 (the most)
+
+// Warp-cooperative copy of n bytes from shared memory (16-byte aligned) to global
+// memory: 16-byte stores where the destination and the length allow, else 4- or 1-byte.
+__device__ __forceinline__ void warp_copy_out(uint8_t* dst, const uint8_t* src, int n, int lane) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | static_cast<uintptr_t>(n);
+  if ((a & 15) == 0) {
+    for (int o = lane * 16; o < n; o += 512)
+      *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(src + o);
+  } else if ((a & 3) == 0) {
+    for (int o = lane * 4; o < n; o += 128)
+      *reinterpret_cast<uint32_t*>(dst + o) = *reinterpret_cast<const uint32_t*>(src + o);
+  } else {
+    for (int o = lane; o < n; o += 32) dst[o] = src[o];
+  }
+}
 
 // kQuant: 0 = copy rows, 1 = MXFP8 rows, 2 = NVFP4 rows (packed E2M1 codes [.., d/2],
 // E4M3 scales per 16 [.., d/16], tensor scale from the amax of x in *amax_bits, which
 // is the amax of the permuted rows: every token is routed).
+// Chunk of a segment held in a lane's slot i: chunks i*32 + lane (coalesced), or, for
+// bf16 rows quantised to NVFP4, each lane two adjacent chunks (one whole 16-element
+// block) per pair of slots.
+template <bool kBlockLane>
+__device__ __forceinline__ int chunk_of(int i, int lane) {
+  return kBlockLane ? 64 * (i / 2) + 2 * lane + (i & 1) : 32 * i + lane;
+}
+
+// (four CTAs per SM: 64 registers, no spill, for every row type)
 template <typename Tin, int kQuant>
-__global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
+__global__ void __launch_bounds__(kScatterThreads, 4) permute_scatter_kernel(
     const uint8_t* __restrict__ x, int T, int d, const int32_t* __restrict__ idx, int k, int E,
     const int32_t* __restrict__ counts, const int32_t* local_rank, const int32_t* __restrict__ block_hist,
     int nblk, int32_t* __restrict__ offsets, int32_t* dest_row, int32_t* __restrict__ src_pair,
@@ -144,9 +193,14 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     int32_t* status) {
   pdl_begin();
   float g4 = 1.f;
+  // NVFP4: the multiplier of every scale byte (g / its value), computed once per CTA
+  __shared__ float s_inv[kQuant == 2 ? 256 : 1];
+  // quantising scatter: one staging segment per warp
+  __shared__ __align__(16) uint8_t s_seg[kQuant ? kScatterThreads / 32 : 1][kQuant ? kSegBytes : 16];
   if constexpr (kQuant == 2) {
     g4 = nvfp4_tensor_scale(__uint_as_float(*amax_bits));
     if (blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale = g4;
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_inv[c] = nvfp4_block_inv(static_cast<uint32_t>(c), g4);
   }
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -198,13 +252,14 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
   const size_t in_row = static_cast<size_t>(d) * sizeof(Tin);
   const size_t out_row = kQuant == 2 ? static_cast<size_t>(d) / 2 : (kQuant ? static_cast<size_t>(d) : in_row);
   const int n16 = static_cast<int>(in_row / 16);
+  constexpr bool kBlockLane = kQuant == 2 && Mx<Tin>::kEpl == 8;
   for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
     const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
     Vec16 v[kScatterU];
     auto load = [&](int base) {
 #pragma unroll
       for (int i = 0; i < kScatterU; ++i) {
-        const int c = base + 32 * i + lane;
+        const int c = base + chunk_of<kBlockLane>(i, lane);
         if (c < n16) {
           v[i] = src[c];
         } else {
@@ -245,60 +300,102 @@ __global__ void __launch_bounds__(kScatterThreads) permute_scatter_kernel(
     }
     if (xp == nullptr) continue;
     for (int base = 0; base < n16; base += 32 * kScatterU) {
-      if (base > 0) load(base);
+      if (kQuant == 0 && base > 0) load(base);
+      if constexpr (kQuant != 0) {
+        // quantise the segment once into this warp's staging buffer: codes at
+        // [0, kSegCodes), the scale bytes after them
+        constexpr int EPL = Mx<Tin>::kEpl;
+        constexpr int CB = kQuant == 2 ? EPL / 2 : EPL;      // code bytes per chunk
+        constexpr int BLK = kQuant == 2 ? 16 : 32;           // elements per scale byte
+        uint8_t* seg = s_seg[threadIdx.x >> 5];
+        if constexpr (kBlockLane) {
+          // bf16 to NVFP4: each lane one whole 16-element block per pair of slots (no
+          // shuffle for the block amax, one scale per lane); n16 is even (d % 16 == 0)
 #pragma unroll
-      for (int i = 0; i < kScatterU; ++i) {
-        const int c = base + 32 * i + lane;
-        const bool active = c < n16;
-        if constexpr (kQuant == 2) {
-          if (base + 32 * i >= n16) break;     // warp-uniform
-          // a 16-element block spans 16 / EPL lanes
-          constexpr int EPL = Mx<Tin>::kEpl;
-          constexpr int LPB = 16 / EPL;
-          float f[EPL];
-          Mx<Tin>::values(v[i], f);
-          float amax = 0.f;
+          for (int m = 0; m < kScatterU / 2; ++m) {
+            if (base + 64 * m >= n16) break;   // warp-uniform
+            const int cl = 64 * m + 2 * lane;  // the block's first chunk within the segment
+            float f0[8], f1[8];
+            Mx<Tin>::values(v[2 * m], f0);
+            Mx<Tin>::values(v[2 * m + 1], f1);
+            float amax = 0.f;
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(f0[e]), fabsf(f1[e])));
+            const uint32_t scode = nvfp4_block_code(amax, g4);
+            const float inv = s_inv[scode];
+            float y0[8], y1[8];
 #pragma unroll
-          for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-          uint32_t scode;
-          float inv;
-          nvfp4_block_scale(amax, g4, &scode, &inv);
-          float y[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = e < EPL ? __fmul_rn(f[e < EPL ? e : 0], inv) : 0.f;
-          const uint32_t packed = f32x8_to_e2m1x8(y);   // EPL codes in the low EPL nibbles
-          for (int j = 0; j < k; ++j) {
-            const int dj = __shfl_sync(kFull, dest, j);
-            if (active && dj >= 0) {
-              uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * (EPL / 2);
-              if (EPL == 8)
-                *reinterpret_cast<uint32_t*>(orow) = packed;
-              else
-                *reinterpret_cast<uint16_t*>(orow) = static_cast<uint16_t>(packed);
-              if ((lane % LPB) == 0)
-                xp_scales[static_cast<size_t>(dj) * (d / 16) + (c * EPL) / 16] = static_cast<uint8_t>(scode);
+            for (int e = 0; e < 8; ++e) {
+              y0[e] = __fmul_rn(f0[e], inv);
+              y1[e] = __fmul_rn(f1[e], inv);
             }
-          }
-        } else if constexpr (kQuant == 1) {
-          if (base + 32 * i >= n16) break;     // warp-uniform: no lane of this chunk row is active
-          uint32_t codes[2], sbyte;
-          mx_chunk<Tin>(v[i], codes, &sbyte);
-          constexpr int EPL = Mx<Tin>::kEpl;
-          for (int j = 0; j < k; ++j) {
-            const int dj = __shfl_sync(kFull, dest, j);
-            if (active && dj >= 0) {
-              uint8_t* orow = xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(c) * EPL;
-              if (EPL == 8)
-                *reinterpret_cast<uint2*>(orow) = make_uint2(codes[0], codes[1]);
-              else
-                *reinterpret_cast<uint32_t*>(orow) = codes[0];
-              if ((lane % Mx<Tin>::kLpb) == 0)
-                xp_scales[static_cast<size_t>(dj) * (d / 32) + (c * EPL) / 32] = static_cast<uint8_t>(sbyte);
+            if (base + cl < n16) {
+              *reinterpret_cast<uint2*>(seg + cl * 4) = make_uint2(f32x8_to_e2m1x8(y0), f32x8_to_e2m1x8(y1));
+              seg[kSegCodes + cl / 2] = static_cast<uint8_t>(scode);
             }
           }
         } else {
+#pragma unroll
+        for (int i = 0; i < kScatterU; ++i) {
+          if (base + 32 * i >= n16) break;     // warp-uniform: no lane of this chunk row is active
+          const int cl = 32 * i + lane;        // chunk within the segment
+          const bool active = base + cl < n16;
+          if constexpr (kQuant == 2) {
+            // a 16-element block spans 16 / EPL lanes
+            constexpr int LPB = 16 / EPL;
+            float f[EPL];
+            Mx<Tin>::values(v[i], f);
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+            for (int off = 1; off < LPB; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+            const uint32_t scode = nvfp4_block_code(amax, g4);
+            const float inv = s_inv[scode];
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = e < EPL ? __fmul_rn(f[e < EPL ? e : 0], inv) : 0.f;
+            const uint32_t packed = f32x8_to_e2m1x8(y);   // EPL codes in the low EPL nibbles
+            if (active) {
+              if (EPL == 8)
+                *reinterpret_cast<uint32_t*>(seg + cl * CB) = packed;
+              else
+                *reinterpret_cast<uint16_t*>(seg + cl * CB) = static_cast<uint16_t>(packed);
+              if ((lane % LPB) == 0) seg[kSegCodes + (cl * EPL) / BLK] = static_cast<uint8_t>(scode);
+            }
+          } else {
+            uint32_t codes[2], sbyte;
+            mx_chunk<Tin>(v[i], codes, &sbyte);
+            if (active) {
+              if (EPL == 8)
+                *reinterpret_cast<uint2*>(seg + cl * CB) = make_uint2(codes[0], codes[1]);
+              else
+                *reinterpret_cast<uint32_t*>(seg + cl * CB) = codes[0];
+              if ((lane % Mx<Tin>::kLpb) == 0) seg[kSegCodes + (cl * EPL) / BLK] = static_cast<uint8_t>(sbyte);
+            }
+          }
+        }
+        }
+        __syncwarp();
+        // the next segment's loads (the registers are free now) overlap this one's stores
+        if (base + 32 * kScatterU < n16) load(base + 32 * kScatterU);
+        // then copy it out to each of the token's rows
+        const int nvalid = n16 - base < 32 * kScatterU ? n16 - base : 32 * kScatterU;
+        const size_t srow = static_cast<size_t>(d) / BLK;
+        for (int j = 0; j < k; ++j) {
+          const int dj = __shfl_sync(kFull, dest, j);
+          if (dj < 0) continue;                // warp-uniform
+          warp_copy_out(xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(base) * CB, seg, nvalid * CB,
+                        lane);
+          warp_copy_out(xp_scales + static_cast<size_t>(dj) * srow + static_cast<size_t>(base) * EPL / BLK,
+                        seg + kSegCodes, nvalid * EPL / BLK, lane);
+        }
+        __syncwarp();                          // the segment is read before the next one is written
+      } else {
+#pragma unroll
+        for (int i = 0; i < kScatterU; ++i) {
+          const int c = base + 32 * i + lane;
+          const bool active = c < n16;
           for (int j = 0; j < k; ++j) {
             const int dj = __shfl_sync(kFull, dest, j);
             if (active && dj >= 0)
@@ -749,28 +846,44 @@ int scatter_grid(int T, int sms) {
 
 }  // namespace
 
-// Launches the three permute kernels; shared by the workspace and the
-// fixed-scratch entry points.
-// xp_dtype MOE_E2M1: NVFP4 rows, with the tensor amax already in *amax_bits and the
-// tensor scale written to *tensor_scale.
+// Launches the permute kernels (the rank pass, then the scatter); shared by the
+// workspace and the fixed-scratch entry points.
+// xp_dtype MOE_E2M1 (x not null): NVFP4 rows; the first launch also takes the tensor
+// amax of x into *amax_bits (zeroed by the caller), and the scatter writes the tensor
+// scale to *tensor_scale.
 moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
                             const int32_t* topk_idx, int k, int E, const int32_t* counts,
                             int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
                             moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
                             int32_t* dev_status, cudaStream_t stream, int sms,
-                            const uint32_t* amax_bits, float* tensor_scale) {
+                            uint32_t* amax_bits, float* tensor_scale) {
   const int nblk = (T + kTokensPerRankBlock - 1) / kTokensPerRankBlock;
   const size_t rank_smem = static_cast<size_t>(2) * 8 * E * sizeof(uint32_t);  // mask + base, [8][E] each
+  // NVFP4 rows: the rank pass and the tensor amax of x (zeroed by the caller) share a launch
+  const bool with_amax = xp_dtype == MOE_E2M1;
+  const void* first = with_amax ? (x_dtype == MOE_BF16 ? reinterpret_cast<const void*>(permute_rank_amax_kernel<uint16_t>)
+                                                        : reinterpret_cast<const void*>(permute_rank_amax_kernel<float>))
+                                : reinterpret_cast<const void*>(permute_rank_kernel);
   if (rank_smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(permute_rank_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(first, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(rank_smem));
     if (e != cudaSuccess) {
       set_error("moe_permute: cudaFuncSetAttribute: %s", cudaGetErrorString(e));
       return MOE_ERR_CUDA;
     }
   }
-  if (nblk > 0) {
+  if (with_amax) {
+    const long long n16 = static_cast<long long>(T) * d * (x_dtype == MOE_BF16 ? 2 : 4) / 16;
+    const long long g1 = (n16 + kRankThreads - 1) / kRankThreads;
+    const int agrid = static_cast<int>(g1 < 1 ? 1 : (g1 < sms * 8 ? g1 : sms * 8));
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    if (x_dtype == MOE_BF16)
+      launch_pdl(permute_rank_amax_kernel<uint16_t>, nblk + agrid, kRankThreads, rank_smem, stream, topk_idx, T, k,
+                 E, dest_row, hist, dev_status, nblk, xb, n16, amax_bits);
+    else
+      launch_pdl(permute_rank_amax_kernel<float>, nblk + agrid, kRankThreads, rank_smem, stream, topk_idx, T, k, E,
+                 dest_row, hist, dev_status, nblk, xb, n16, amax_bits);
+  } else if (nblk > 0) {
     launch_pdl(permute_rank_kernel, nblk, kRankThreads, rank_smem, stream, topk_idx, T, k, E, dest_row,
                                                                    hist, dev_status);
   }
@@ -1023,11 +1136,6 @@ extern "C" moe_status_t moe_quantize_mxfp8_transposed(const void* in, moe_dtype_
   return check_launch("moe_quantize_mxfp8_transposed");
 }
 
-namespace moe {
-void nvfp4_amax_launch(const void* in, moe_dtype_t dtype, long long elems, uint32_t* amax_bits,
-                       cudaStream_t stream, int sms);
-}  // namespace moe
-
 extern "C" moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, int T, int d,
                                           const int32_t* topk_idx, int k, int E, const int32_t* counts,
                                           int32_t* offsets, int32_t* dest_row, int32_t* src_pair,
@@ -1059,8 +1167,8 @@ extern "C" moe_status_t moe_permute_nvfp4(const void* x, moe_dtype_t x_dtype, in
     set_error("%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
     return MOE_ERR_CUDA;
   }
-  // the amax of x is the amax of the permuted rows (every token is routed)
-  nvfp4_amax_launch(x, x_dtype, static_cast<long long>(T) * d, amax_bits, stream, sms);
+  // the amax of x is the amax of the permuted rows (every token is routed); the
+  // first of the dispatch's two launches takes it beside the rank pass
   return permute_launch(x, x_dtype, T, d, topk_idx, k, E, counts, offsets, dest_row, src_pair, xp_codes,
                         MOE_E2M1, xp_scales, static_cast<int32_t*>(workspace), dev_status, stream, sms,
                         amax_bits, tensor_scale);

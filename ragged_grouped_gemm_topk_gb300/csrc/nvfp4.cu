@@ -20,31 +20,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kQThreads) nvfp4_amax_kernel(const uint8_t* __restrict__ in, long long n16,
                                                                uint32_t* amax_bits) {
   pdl_begin();
-  float m = 0.f;
-  const uint4* v4 = reinterpret_cast<const uint4*>(in);
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const uint4 u = v4[i];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if constexpr (sizeof(Tin) == 2) {
-        m = fmaxf(m, fabsf(bf16_to_f32(static_cast<uint16_t>(w[j] & 0xFFFFu))));
-        m = fmaxf(m, fabsf(bf16_to_f32(static_cast<uint16_t>(w[j] >> 16))));
-      } else {
-        m = fmaxf(m, fabsf(__uint_as_float(w[j])));
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-  __shared__ float part[kQThreads / 32];
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < kQThreads / 32; ++i) m = fmaxf(m, part[i]);
-    atomicMax(amax_bits, __float_as_uint(m));
-  }
+  nvfp4_amax_body<Tin>(in, n16, amax_bits, blockIdx.x, gridDim.x);
 }
 
 template <typename Tin>

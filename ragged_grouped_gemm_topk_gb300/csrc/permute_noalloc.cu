@@ -38,7 +38,7 @@ moe_status_t permute_launch(const void* x, moe_dtype_t x_dtype, int T, int d,
                             int32_t* offsets, int32_t* dest_row, int32_t* src_pair, void* xp,
                             moe_dtype_t xp_dtype, uint8_t* xp_scales, int32_t* hist,
                             int32_t* dev_status, cudaStream_t stream, int sms,
-                            const uint32_t* amax_bits, float* tensor_scale);
+                            uint32_t* amax_bits, float* tensor_scale);
 size_t permute_hist_bytes(int T, int E);
 
 namespace {
