@@ -121,6 +121,21 @@ def test_permute_fused_mxfp8_bit_exact(w):
     assert (out["xp_scales"].cpu().numpy() == scales).all()
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("d", [4192, 6144])
+def test_permute_fused_mxfp8_segments(d, dtype):
+    """Rows longer than one staging segment of the quantising scatter (2048 bf16 or 1024
+    fp32 elements): d = 4192 ends in a partial segment and has 131-byte scale rows (copied
+    out byte by byte), d = 6144 is whole segments with 16-byte copies throughout."""
+    need_gpu()
+    w = W.WORKLOADS[3].scaled(T=200, E=32, k=4, d=d, name="mx-seg")
+    x = W.make_x(w, "cuda").to(dtype)
+    out, (o_off, o_dest, o_src), _, _ = _dispatch_check(w, x, quant=True)
+    codes, scales = omx.quantize_rowwise(f64(x)[o_src // w.k])
+    assert (out["xp"].cpu().numpy() == codes).all()
+    assert (out["xp_scales"].cpu().numpy() == scales).all()
+
+
 def test_permute_mxfp8_rejects_width_not_multiple_of_32():
     need_gpu()
     w = SMALL[1]                                     # d = 40

@@ -155,10 +155,15 @@ def test_nvfp4_layer_scaled():
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
-@pytest.mark.parametrize("T,d,E,k", [(300, 256, 8, 2), (1000, 512, 64, 8), (77, 48, 4, 3)])
+@pytest.mark.parametrize("T,d,E,k", [(300, 256, 8, 2), (1000, 512, 64, 8), (77, 48, 4, 3), (300, 4368, 16, 4),
+                                     (200, 6144, 32, 8), (600, 256, 1024, 4)])
 def test_permute_nvfp4_equals_permute_then_quantize(dtype, T, d, E, k):
     """The fused NVFP4 dispatch writes, bit for bit, the NVFP4 of the rows moe_permute
-    writes (and the same maps), which the quantiser tests pin to the oracle."""
+    writes (and the same maps), which the quantiser tests pin to the oracle.  Beside
+    the small rows: rows over several staging segments of the scatter, the last partial
+    with 273-byte scale rows (d = 4368) or all whole (d = 6144), and E = 1024 (the rank
+    pass, which shares its launch with the tensor amax, then needs 64 KB of shared
+    memory)."""
     need_gpu()
     w = W.BY_NAME["qwen3-235b-bf16"].scaled(T=T, E=E, k=k, d=d, name="fp4-perm")
     x = W.make_x(w, "cuda").to(dtype)
