@@ -253,7 +253,10 @@ __global__ void __launch_bounds__(kScatterThreads, 4) permute_scatter_kernel(
   const size_t out_row = kQuant == 2 ? static_cast<size_t>(d) / 2 : (kQuant ? static_cast<size_t>(d) : in_row);
   const int n16 = static_cast<int>(in_row / 16);
   constexpr bool kBlockLane = kQuant == 2 && Mx<Tin>::kEpl == 8;
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+  for (int tw = blockIdx.x * wpb + (threadIdx.x >> 5); tw < T; tw += gridDim.x * wpb) {
+    // NVFP4: the tensor-amax pass has just streamed x, last rows last, so the scatter
+    // takes the tokens from the end and finds the most recent of them still in L2
+    const int t = kQuant == 2 ? T - 1 - tw : tw;
     const Vec16* src = reinterpret_cast<const Vec16*>(x + static_cast<size_t>(t) * in_row);
     Vec16 v[kScatterU];
     auto load = [&](int base) {
