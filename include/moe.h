@@ -348,15 +348,21 @@ moe_status_t moe_grouped_gemm_dgrad_mxfp8(const moe_operand_t* dC, const moe_ope
 
 /* Weight gradient: dB[e] = dC[R_e]^T . A[R_e], a contraction over the ragged rows
  * R_e of each expert; an expert with no rows gets an exact zero gradient.
- *   A [M, K], dC [M, N], both MOE_BF16 -> dB [E, N, K] in dB_dtype (MOE_BF16).
+ *   A [M, K], dC [M, N], both MOE_BF16 -> dB [E, N, K] in dB_dtype (MOE_BF16 or
+ *   MOE_F32, the fp32 accumulator as it is).
  *   Or both MOE_E4M3 ([1] "grouped quantisation": the blocks of 32 run down the
  *   contraction, restarting at each group): codes and tiled scales from
  *   moe_quantize_mxfp8_grouped axis 2 of A and of dC (scales required);
  *   N % 128 == 0 and K % 128 == 0.
+ *   accumulate != 0 (dB_dtype MOE_F32 only, else MOE_ERR_INVALID_ARG): dB[e] +=
+ *   the product instead, each element with one fp32 rounding of (dB + product), for
+ *   gradients summed over several batches; an expert with no rows keeps its dB
+ *   unchanged.  Each element belongs to one output tile, so a call adds to it once:
+ *   the result does not depend on the order the tiles run in.
  * Limits as the forward. */
 moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
                                     const int32_t* offsets, int M, int N, int K, int E,
-                                    void* dB, moe_dtype_t dB_dtype,
+                                    int accumulate, void* dB, moe_dtype_t dB_dtype,
                                     int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- combine ---

@@ -47,7 +47,7 @@ SIGNATURES = {
     "moe_quantize_nvfp4": (st, [vp, i32, i32, i32, vp, vp, vp, vp]),
     "moe_permute_nvfp4": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]),
     "moe_grouped_gemm_dgrad_mxfp8": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]),
-    "moe_grouped_gemm_wgrad": (st, [OP, OP, vp, i32, i32, i32, i32, vp, i32, vp, vp]),
+    "moe_grouped_gemm_wgrad": (st, [OP, OP, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp]),
     "moe_unpermute_combine": (st, [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]),
     "moe_permute_capacity_workspace_size": (sz, [i32, i32, i32]),
     "moe_permute_capacity": (st, [vp, i32, i32, i32, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]),

@@ -418,9 +418,12 @@ def moe_grouped_gemm_dgrad_mxfp8(dC, BT, offsets, *, dC_scales, BT_scales, epi="
 
 
 def moe_grouped_gemm_wgrad(A, dC, offsets, E, *, A_scales=None, dC_scales=None, out_dtype=torch.bfloat16,
-                           out=None, dev_status=None):
-    """dB[e] = dC[R_e]^T . A[R_e] -> [E, N, K].  MXFP8: A and dC are codes from the
-    tiled column-wise quantiser (axis 2), with their scale buffers."""
+                           out=None, accumulate=False, dev_status=None):
+    """dB[e] = dC[R_e]^T . A[R_e] -> [E, N, K] (bf16 or fp32).  MXFP8: A and dC are
+    codes from the tiled column-wise quantiser (axis 2), with their scale buffers.
+    accumulate: dB[e] += the product, into the given fp32 ``out``."""
+    if accumulate and (out is None or out.dtype != torch.float32):
+        raise ValueError("accumulate needs an fp32 out tensor to add to")
     M, K = A.shape
     M2, N = dC.shape
     if M2 != M:
@@ -436,7 +439,7 @@ def moe_grouped_gemm_wgrad(A, dC, offsets, E, *, A_scales=None, dC_scales=None, 
         out = torch.empty(E, N, K, dtype=out_dtype, device=A.device)
     a, b = _operand(A, A_scales), _operand(dC, dC_scales)
     _lib.call("moe_grouped_gemm_wgrad", C.byref(a), C.byref(b), _ptr(offsets), M, N, K, E,
-              _ptr(out), _dt(out), _ptr(dev_status), _stream())
+              1 if accumulate else 0, _ptr(out), _dt(out), _ptr(dev_status), _stream())
     return out
 
 

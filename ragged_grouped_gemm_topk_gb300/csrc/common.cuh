@@ -398,6 +398,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+// Shared -> global tiled reduction: each element of the box is added to the one in
+// global memory (in the tensor map's element type), out-of-range parts untouched.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // L2 policy for data written once and not read again by this kernel: its lines are
 // the first to be evicted, so streaming output does not push operands out of L2.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

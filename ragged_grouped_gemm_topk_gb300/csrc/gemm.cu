@@ -252,6 +252,7 @@ struct Params {
   int renorm;              //   softmax over the selected logits (1) or over all (0)
   int n_mma;               //   MMA width: E rounded up to 16 (the B tile holds that many rows)
   int split;               //   CTAs (one cluster) sharing a tile's contraction: 1, 2 or 4
+  int accumulate;          // wgrad, fp32 dB: add to dB (TMA reductions) instead of writing it
 };
 
 // Rows of group e.  Without an offsets array the problem is one dense group of M rows.
@@ -949,11 +950,12 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     // i * gridDim.x; a warp writes four of them (8 KB) per pass, which measured a few
     // percent faster than one (the fill ends earlier, ahead of the store-bound tiles
     // of the small experts at the end).
+    // Accumulating into dW, the experts without rows keep theirs: nothing to write.
     constexpr int kZfU = 4;
     const uint64_t pol = l2_evict_first_policy();
-    const size_t per = static_cast<size_t>(p.N) * p.K * 2;
+    const size_t per = static_cast<size_t>(p.N) * p.K * sizeof(OutT);
     const size_t cpe = per / 2048;
-    const size_t chunks = static_cast<size_t>(p.E - s.nnz) * cpe;
+    const size_t chunks = p.accumulate ? 0 : static_cast<size_t>(p.E - s.nnz) * cpe;
     uint8_t* outb = static_cast<uint8_t*>(p.out);
     for (size_t c0 = blockIdx.x; c0 < chunks && !s.abort; c0 += kZfU * static_cast<size_t>(gridDim.x)) {
 #pragma unroll
@@ -1032,7 +1034,47 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
       const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN) +
                           static_cast<uint32_t>(hh) * 256u;
       bool released = false;
-      if constexpr (kMode == kWgrad) {
+      if constexpr (kMode == kWgrad && sizeof(OutT) == 4) {
+        // fp32 dW rows n0 + 32q .. +31 (this warp): each 32-column chunk read from TMEM
+        // leaves as two 16-column boxes (64-byte rows, 64-byte swizzle) through the
+        // warp's rotating 2 KB staging buffers, written by TMA (clipped at N and K) or,
+        // accumulating, added to dW by a TMA reduction (one fp32 rounding an element).
+        // The accumulator is released once its last chunk is read.
+        constexpr int kWgBufs = wg_bufs<kKind>();
+        uint8_t* stg = tiles + NS * kStageSz + si * wg_stage<kKind>();
+        const int sw = (lane >> 1) & 3;
+        const int nch = (p.K - t.col0) / 32 < kBN / 32 ? (p.K - t.col0) / 32 : kBN / 32;   // K % 32 == 0
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tmem_ld_wait();
+          if (c == nch - 1) {
+            tc_fence_before();
+            mbar_arrive(&s.tempty[acc]);
+            released = true;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint8_t* buf = stg + ((2 * c + h) % kWgBufs) * 2048;
+            if (lane == 0) bulk_wait_read<kWgBufs - 1>();   // the box that last used buf is read
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ sw) * 16)) =
+                  make_uint4(v[16 * h + 4 * j], v[16 * h + 4 * j + 1], v[16 * h + 4 * j + 2], v[16 * h + 4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (p.accumulate)
+                tma_reduce_add_3d(&tmD, buf, t.col0 + 32 * c + 16 * h, t.n0 + 32 * q, t.e);
+              else
+                tma_store_3d(&tmD, buf, t.col0 + 32 * c + 16 * h, t.n0 + 32 * q, t.e);
+              bulk_commit();
+            }
+          }
+        }
+      } else if constexpr (kMode == kWgrad) {
         // bf16 dW rows n0 + 32q .. +31 (this warp) x 256 columns: the accumulator is read
         // whole into registers and released, then written by TMA (clipped at N and K) in
         // 32-column boxes (64-byte swizzle) through the warp's wg_bufs rotating 2 KB
@@ -1949,22 +1991,29 @@ extern "C" moe_status_t moe_route_topk_gemm(const void* x, const void* w_router,
 
 extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe_operand_t* dC,
                                                const int32_t* offsets, int M, int N, int K, int E,
-                                               void* dB, moe_dtype_t dB_dtype, int32_t* dev_status,
-                                               cudaStream_t stream) {
+                                               int accumulate, void* dB, moe_dtype_t dB_dtype,
+                                               int32_t* dev_status, cudaStream_t stream) {
   const moe::NvtxRange nvtx_range("moe_grouped_gemm_wgrad");
   const char* fn = "moe_grouped_gemm_wgrad";
   int sms = 0;
   moe_status_t st = common_checks(fn, A, dC, offsets, M, N, K, E, dB, &sms);
   if (st != MOE_OK) return st;
-  if ((A->dtype != MOE_BF16 && A->dtype != MOE_E4M3) || dB_dtype != MOE_BF16) {
-    set_error("%s: BF16 or MXFP8 (E4M3) operands, BF16 output", fn);
+  if ((A->dtype != MOE_BF16 && A->dtype != MOE_E4M3) || (dB_dtype != MOE_BF16 && dB_dtype != MOE_F32)) {
+    set_error("%s: BF16 or MXFP8 (E4M3) operands, BF16 or F32 output", fn);
     return MOE_ERR_UNSUPPORTED;
   }
-  // dB [E, N, K] is written by TMA from 32-column x 32-row staging boxes (64-byte swizzle)
+  if (accumulate && dB_dtype != MOE_F32) {
+    set_error("%s: accumulating needs an F32 dB (one rounding per element)", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  // dB [E, N, K] is written by TMA from 32-row staging boxes of 64-byte rows (64-byte
+  // swizzle): 32 bf16 or 16 fp32 columns
+  const bool f32 = dB_dtype == MOE_F32;
   CUtensorMap td;
   const uint64_t ddims[3] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(E)};
-  const uint32_t dbox[3] = {32, 32, 1};
-  if (!make_map(&td, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dB, 3, ddims, dbox, CU_TENSOR_MAP_SWIZZLE_64B))
+  const uint32_t dbox[3] = {f32 ? 16u : 32u, 32, 1};
+  if (!make_map(&td, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2, dB, 3,
+                ddims, dbox, CU_TENSOR_MAP_SWIZZLE_64B))
     return MOE_ERR_INVALID_ARG;
   if (A->dtype == MOE_E4M3) {
     // Both operands quantised column-wise (group-aware, along the rows), scales in
@@ -1985,6 +2034,8 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
       return MOE_ERR_INVALID_ARG;
     Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status,
              static_cast<const uint8_t*>(dC->scales), static_cast<const uint8_t*>(A->scales)};
+    p.accumulate = accumulate ? 1 : 0;
+    if (f32) return launch<2, kWgrad, kEpiNone, float>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
     return launch<2, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   }
   CUtensorMap ta, tb;
@@ -1999,5 +2050,7 @@ extern "C" moe_status_t moe_grouped_gemm_wgrad(const moe_operand_t* A, const moe
       !make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aptr, 2, adims, box))
     return MOE_ERR_INVALID_ARG;
   Params p{offsets, M, N, K, E, dB, nullptr, nullptr, nullptr, dev_status};
+  p.accumulate = accumulate ? 1 : 0;
+  if (f32) return launch<1, kWgrad, kEpiNone, float>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
   return launch<1, kWgrad, kEpiNone, uint16_t>(ta, tb, p, stream, sms, fn, nullptr, nullptr, &td);
 }

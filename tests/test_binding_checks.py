@@ -82,6 +82,11 @@ def test_wgrad_and_dgrad_check_their_buffers():
     with pytest.raises(ValueError, match="out"):
         B.moe_grouped_gemm_wgrad(A, dC, off, E, A_scales=sA, dC_scales=sC,
                                  out=torch.empty(E, N, K - 1, dtype=bf16))
+    with pytest.raises(ValueError, match="accumulate"):                 # adds only into fp32
+        B.moe_grouped_gemm_wgrad(A, dC, off, E, A_scales=sA, dC_scales=sC,
+                                 out=torch.zeros(E, N, K, dtype=bf16), accumulate=True)
+    with pytest.raises(ValueError, match="accumulate"):                 # and only into a given buffer
+        B.moe_grouped_gemm_wgrad(A, dC, off, E, A_scales=sA, dC_scales=sC, accumulate=True)
     dCb, Wb = torch.zeros(M, N, dtype=bf16), torch.zeros(E, N, K, dtype=bf16)
     with pytest.raises(ValueError, match="preact"):
         B.moe_grouped_gemm_dgrad(dCb, Wb, off, epi="dswiglu", preact=torch.zeros(M, K, dtype=bf16))

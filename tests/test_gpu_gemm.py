@@ -171,6 +171,62 @@ def test_wgrad(counts, N, K):
     assert rel_l2(got, want) < TOL_BF16
 
 
+def _check_fp32_and_accumulate(call, want, cnt, E, N, K, tol):
+    """fp32 dB: the fp32 accumulator as it is, empty groups exact +0.  Accumulating:
+    dB + the product with one fp32 rounding (bit for bit the fp32 sum of the old dB and
+    the fp32 result), empty groups keep their values; a second call adds it again."""
+    dB = torch.full((E, N, K), float("nan"), dtype=torch.float32, device="cuda")
+    call(dB, False)
+    got = f64(dB)
+    for e in range(E):
+        if cnt[e] == 0:
+            assert (got[e] == 0).all() and not np.signbit(got[e]).any(), f"expert {e} not exactly zero"
+    assert not np.isnan(got).any()
+    assert rel_l2(got, want) < tol
+    old = W.make_matrix(E * N, K, seed=N + K + 77, dtype=torch.float32, device="cuda").view(E, N, K)
+    acc = old.clone()
+    call(acc, True)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, old + dB)
+    for e in range(E):
+        if cnt[e] == 0:
+            assert torch.equal(acc[e], old[e]), f"expert {e} changed"
+    call(acc, True)
+    assert rel_l2(f64(acc), f64(old) + 2 * want) < tol
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles", "one-expert"], ids=str)
+@pytest.mark.parametrize("N,K", [(256, 512), (160, 96)])
+def test_wgrad_fp32_and_accumulate(counts, N, K):
+    """The weight gradient into an fp32 dB, written or added to (gradients summed over
+    several batches), bf16 operands; rows no group owns are poisoned."""
+    need_gpu()
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    M = int(sum(cnt)) + 7
+    A = W.make_matrix(M, K, seed=N + K + 5, dtype=torch.bfloat16, device="cuda")
+    dC = W.make_matrix(M, N, seed=N + K + 6, dtype=torch.bfloat16, device="cuda")
+    A[int(sum(cnt)):] = 1e4
+    off = ragged_offsets(cnt)
+    want = om.grouped_gemm_wgrad(f64(A), f64(dC), off.cpu().numpy(), E)
+    # bf16 products are exact in fp32: only the fp32 accumulation rounds
+    _check_fp32_and_accumulate(lambda out, a: moe_gpu.moe_grouped_gemm_wgrad(A, dC, off, E, out=out, accumulate=a),
+                               want, cnt, E, N, K, 2e-5)
+
+
+def test_wgrad_accumulate_rejects_bf16_output():
+    need_gpu()
+    off = ragged_offsets([32, 32])
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    dB = torch.zeros(2, 64, 64, dtype=torch.bfloat16, device="cuda")
+    lib = moe_gpu.binding._lib
+    a, b = moe_gpu.binding._operand(A), moe_gpu.binding._operand(A)
+    import ctypes
+    st = lib.load().moe_grouped_gemm_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(off.data_ptr()), 64, 64,
+                                           64, 2, 1, ctypes.c_void_p(dB.data_ptr()), lib.MOE_BF16, None, None)
+    assert st == lib.MOE_ERR_INVALID_ARG
+
+
 # ----------------------------------------------------------------------------- MXFP8 forward
 
 from oracle import mxfp8 as omx  # noqa: E402
@@ -445,6 +501,26 @@ def test_wgrad_mxfp8(counts, N, K):
     assert not np.isnan(got).any()
     err = rel_l2(got, want)
     assert err < TOL_MXFP8 and err < 1e-2, err       # same quantised inputs: only fp32/bf16 rounding
+
+
+@pytest.mark.parametrize("counts", ["mixed", "singles"], ids=str)
+def test_wgrad_mxfp8_fp32_and_accumulate(counts):
+    """The MXFP8 weight gradient into an fp32 dB, written or added to."""
+    need_gpu()
+    N, K = 256, 384
+    cnt = COUNTS[counts]
+    E = len(cnt)
+    rows = int(sum(cnt))
+    A = W.make_matrix(rows + 7, K, seed=N + K + 41, dtype=torch.bfloat16, device="cuda")
+    dC = W.make_matrix(rows + 7, N, seed=N + K + 43, dtype=torch.bfloat16, device="cuda")
+    off = ragged_offsets(cnt)
+    Aq, As, A_deq = _colwise_tiled(A, off, E)
+    Cq, Cs, C_deq = _colwise_tiled(dC, off, E)
+    Aq[rows:] = 0x7E
+    want = om.grouped_gemm_wgrad(A_deq, C_deq, off.cpu().numpy(), E)
+    _check_fp32_and_accumulate(lambda out, a: moe_gpu.moe_grouped_gemm_wgrad(Aq, Cq, off, E, A_scales=As,
+                                                                             dC_scales=Cs, out=out, accumulate=a),
+                               want, cnt, E, N, K, 1e-4)
 
 
 def test_wgrad_mxfp8_rejects_bad_shapes_and_missing_scales():
