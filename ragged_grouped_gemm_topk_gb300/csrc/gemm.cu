@@ -299,15 +299,12 @@ struct Geo {
   int tm;       // tile rows (fwd/dgrad: rows of the group; wgrad: dB rows): 128, or 256 for wide tiles
   int split;    // CTAs sharing a tile (router: a cluster, each a slice of the contraction); else 1
   int crank;    // this CTA's rank in that cluster
-  int t0, ts;   // this CTA's first tile and its stride through the tile list
   __device__ Geo(const Params& p, int elem_bytes, int bn, int tile_m = kBM) {
     mn_rows = elem_bytes == 1 ? kMxWgRows : kMnRows;
     rb = 1;
     tm = tile_m;
     split = kEpi == kEpiTopk && p.split > 1 ? p.split : 1;
-    crank = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    t0 = static_cast<int>(blockIdx.x) / split;
-    ts = static_cast<int>(gridDim.x) / split;
+    crank = kEpi == kEpiTopk && split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     if (kMode == kWgrad) {
       nt = (p.N + tm - 1) / tm;
       nt2 = (p.K + kBN - 1) / kBN;
@@ -330,6 +327,14 @@ struct Geo {
   __device__ int tiles_of(int cnt) const {
     if (kMode == kWgrad) return nt * nt2;
     return ((cnt + tm - 1) / tm) * nt;
+  }
+  // this CTA's first tile and its stride through the tile list (a router cluster
+  // shares one tile)
+  __device__ int first_tile() const {
+    return kEpi == kEpiTopk ? static_cast<int>(blockIdx.x) / split : static_cast<int>(blockIdx.x);
+  }
+  __device__ int tile_stride() const {
+    return kEpi == kEpiTopk ? static_cast<int>(gridDim.x) / split : static_cast<int>(gridDim.x);
   }
 };
 
@@ -372,9 +377,14 @@ __device__ __forceinline__ Tile tile_info(const Smem& s, const Geo<kMode, kEpi>&
     t.rows = left < g.tm ? left : g.tm;
     t.col0 = (rem / in_blk) * g.bn_out;
     t.n0 = 0;
-    // a split contraction: slice crank of split near-equal runs of K blocks
-    t.kb0 = g.crank * g.kb_fixed / g.split;
-    t.kblocks = (g.crank + 1) * g.kb_fixed / g.split - t.kb0;
+    if constexpr (kEpi == kEpiTopk) {
+      // a split contraction: slice crank of split near-equal runs of K blocks
+      t.kb0 = g.crank * g.kb_fixed / g.split;
+      t.kblocks = (g.crank + 1) * g.kb_fixed / g.split - t.kb0;
+    } else {
+      t.kb0 = 0;
+      t.kblocks = g.kb_fixed;
+    }
   }
   return t;
 }
@@ -639,7 +649,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     if (lane == 0) {
       int stage = 0, ss = 0;
       uint32_t phase = 0, ss_phase = 0;
-      for (int tile = g.t0; tile < total && !s.abort; tile += g.ts) {
+      for (int tile = g.first_tile(); tile < total && !s.abort; tile += g.tile_stride()) {
         const Tile t = tile_info(s, g, tile, p);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (kKind == 2 && kMode == kFwd && kb % 4 == 0) {
@@ -720,7 +730,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                                                         kMode != kFwd);
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
-    for (int tile = g.t0; tile < total && !s.abort; tile += g.ts) {
+    for (int tile = g.first_tile(); tile < total && !s.abort; tile += g.tile_stride()) {
       const Tile t = tile_info(s, g, tile, p);
       if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, p.status, &s.abort)) break;
       tc_fence_after();
@@ -995,10 +1005,13 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
     OutT* out = static_cast<OutT*>(p.out);
     int acc = 0;
     uint32_t acc_phase = 0;
+    // wgrad: boxes this warp has staged so far; the staging buffers rotate over all of
+    // them, across tiles, so the buffer a box takes was last used kWgBufs boxes before
+    int wbox = 0;
     bool xchg = false;                      // router split: this CTA exchanged partials with its peers
     // (the router's epilogue warps meet at named barriers, so they all enter the
     // loop and all take the same decision to leave it: see below)
-    for (int tile = g.t0; tile < total && (kEpi == kEpiTopk || !s.abort); tile += g.ts) {
+    for (int tile = g.first_tile(); tile < total && (kEpi == kEpiTopk || !s.abort); tile += g.tile_stride()) {
       Tile t = tile_info(s, g, tile, p);
       if (kW) {                              // this warp's half of the wide tile
         if (kMode == kWgrad) {
@@ -1056,7 +1069,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint8_t* buf = stg + ((2 * c + h) % kWgBufs) * 2048;
+            uint8_t* buf = stg + (wbox++ % kWgBufs) * 2048;
             if (lane == 0) bulk_wait_read<kWgBufs - 1>();   // the box that last used buf is read
             __syncwarp();
 #pragma unroll
@@ -1101,7 +1114,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
           if (t.col0 + 32 * c >= p.K) break;      // warp-uniform: past the last dW column
-          uint8_t* buf = stg + (c % kWgBufs) * 2048;
+          uint8_t* buf = stg + (wbox++ % kWgBufs) * 2048;
           if (lane == 0) bulk_wait_read<kWgBufs - 1>();   // the box that last used buf is read
           __syncwarp();
 #pragma unroll

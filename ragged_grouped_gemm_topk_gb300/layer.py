@@ -36,12 +36,15 @@ class MoELayer:
     """
 
     def __init__(self, T, d, E, k, f, W1, W2, *, dtype="bf16", renormalize=True, training=False,
-                 w_router=None, keep_logits=False):
+                 w_router=None, keep_logits=False, accumulate_grads=False):
         """``w_router`` [E, d] (bf16, or fp32 for the fp32 layer) makes the layer score
         the tokens itself: ``forward(x)`` then runs the router GEMM fused with the
         top-k selection instead of taking logits.  With ``keep_logits`` (or when
         training without renormalisation, whose router backward needs them) the
-        fused router also writes its fp32 logits to ``self.logits``."""
+        fused router also writes its fp32 logits to ``self.logits``.
+        ``accumulate_grads`` (training): dW1 and dW2 are fp32 sums over the backward
+        calls since construction or ``zero_grads()`` (gradients summed over several
+        batches), each call's weight gradients added in by the GEMM itself."""
         self.T, self.d, self.E, self.k, self.f = T, d, E, k, f
         self.w_router = w_router
         keep = w_router is not None and (keep_logits or (training and not renormalize))
@@ -116,8 +119,13 @@ class MoELayer:
             self.dxp = torch.empty(M, d, dtype=store, device=dev)
             self.dx = torch.empty(T, d, dtype=store, device=dev)
             self.dlogits = torch.empty(T, E, dtype=torch.float32, device=dev)
-            self.dW1 = torch.empty_like(W1)
-            self.dW2 = torch.empty_like(W2)
+            self.accumulate_grads = accumulate_grads
+            if accumulate_grads:
+                self.dW1 = torch.zeros(W1.shape, dtype=torch.float32, device=dev)
+                self.dW2 = torch.zeros(W2.shape, dtype=torch.float32, device=dev)
+            else:
+                self.dW1 = torch.empty_like(W1)
+                self.dW2 = torch.empty_like(W2)
 
     # ------------------------------------------------------------------ forward
     def route(self, logits, x=None):
@@ -219,6 +227,11 @@ class MoELayer:
         return 7 + (3 if self.dtype == "mxfp8" else 0)
 
     # ------------------------------------------------------------------ backward
+    def zero_grads(self):
+        """Reset the summed weight gradients (``accumulate_grads``) to zero."""
+        self.dW1.zero_()
+        self.dW2.zero_()
+
     def backward(self, dy, logits=None, dx_out=None, mark=None):
         """Gradients of sum(y * dy) with respect to x, logits, W1 and W2 (after forward);
         dx goes to ``dx_out`` when given.  ``mark(name)``, when given, is called after
@@ -241,7 +254,7 @@ class MoELayer:
                                            epi="dswiglu", preact=self.gu, out=self.dgu, dev_status=st)
             mark("dgrad2")
             B.moe_grouped_gemm_wgrad(self.hcq, self.dycq, off, E, A_scales=self.hcs, dC_scales=self.dycs,
-                                     out=self.dW2, dev_status=st)
+                                     out=self.dW2, accumulate=self.accumulate_grads, dev_status=st)
             mark("wgrad2")
             B.moe_quantize_mxfp8_grouped(self.dgu, codes=self.dgq, scales=self.dgs)
             B.moe_quantize_mxfp8_grouped(self.dgu, off, E, codes=self.dgcq, scales=self.dgcs, axis=2)
@@ -250,7 +263,7 @@ class MoELayer:
                                            out=self.dxp, dev_status=st)
             mark("dgrad1")
             B.moe_grouped_gemm_wgrad(self.xcq, self.dgcq, off, E, A_scales=self.xcs, dC_scales=self.dgcs,
-                                     out=self.dW1, dev_status=st)
+                                     out=self.dW1, accumulate=self.accumulate_grads, dev_status=st)
             mark("wgrad1")
         else:
             B.moe_unpermute_combine_bwd(dy, self.yp, self.dest_row, self.topk_w, dyp=self.dyp, dw=self.dw,
@@ -259,11 +272,13 @@ class MoELayer:
             B.moe_grouped_gemm_dgrad(self.dyp, self.W2, self.offsets, epi="dswiglu", preact=self.gu,
                                      out=self.dgu, dev_status=st)
             mark("dgrad2")
-            B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.h, self.dyp, self.offsets, self.E, out=self.dW2,
+                                     accumulate=self.accumulate_grads, dev_status=st)
             mark("wgrad2")
             B.moe_grouped_gemm_dgrad(self.dgu, self.W1, self.offsets, out=self.dxp, dev_status=st)
             mark("dgrad1")
-            B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1, dev_status=st)
+            B.moe_grouped_gemm_wgrad(self.xp, self.dgu, self.offsets, self.E, out=self.dW1,
+                                     accumulate=self.accumulate_grads, dev_status=st)
             mark("wgrad1")
         dx = self.dx if dx_out is None else dx_out
         B.moe_unpermute_combine(self.dxp, self.dest_row, None, out=dx, dev_status=st)

@@ -227,6 +227,40 @@ def test_graph_replay_training_step(dtype):
     assert len(seen) == 3                     # the counts changed between replays
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_accumulated_weight_gradients(dtype):
+    """accumulate_grads: dW1 and dW2 are the fp32 sums of the weight gradients of every
+    backward since construction (three batches with different routing, so different
+    experts are empty in each) and start again from zero after zero_grads()."""
+    import dataclasses
+    need_gpu()
+    base = W.BY_NAME["dsv3-mxfp8-train" if dtype == "mxfp8" else "dsv3-bf16-train"]
+    w = base.scaled(T=384, E=32, d=512, f=512, name=f"acc-grads-{dtype}")   # MXFP8: K % 512 == 0
+    W1, W2 = W.make_w1(w, "cuda"), W.make_w2(w, "cuda")
+    layer = moe_gpu.MoELayer(w.T, w.d, w.E, w.k, w.f, W1, W2, dtype=w.dtype, renormalize=w.renormalize,
+                             training=True, accumulate_grads=True)
+    assert layer.dW1.dtype == torch.float32 and layer.dW2.dtype == torch.float32
+    tol = TOL_MXFP8 if dtype == "mxfp8" else TOL_BF16
+    mx = dtype == "mxfp8"
+    sums = [0.0, 0.0]
+    for b in range(4):
+        if b == 3:
+            layer.zero_grads()
+            sums = [0.0, 0.0]
+        wr = dataclasses.replace(w, seed=w.seed + 11 * (b + 1))
+        x, lg, dy = W.make_x(wr, "cuda"), logits_dev(wr), W.make_dy(wr, "cuda")
+        layer.forward(x, lg)
+        layer.backward(dy, lg)
+        torch.cuda.synchronize()
+        assert int(layer.dev_status.item()) == 0
+        lg_h = lg.cpu().numpy()
+        ref = om.layer_forward(f64(x), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=mx)
+        bwd = om.layer_backward(ref, f64(dy), f64(x), lg_h, f64(W1), f64(W2), w.k, mxfp8_operands=mx)
+        sums = [sums[0] + bwd["dW1"], sums[1] + bwd["dW2"]]
+        assert rel_l2(f64(layer.dW1), sums[0]) < tol, (b, "dW1")
+        assert rel_l2(f64(layer.dW2), sums[1]) < tol, (b, "dW2")
+
+
 @pytest.mark.parametrize("w", [W.BY_NAME["dsv3-bf16-train"].scaled(T=256, d=256, f=128, name="dsv3-train-small"),
                                W.BY_NAME["dsv3-bf16-train"].scaled(T=700, E=16, d=192, f=320, name="train-E16"),
                                W.BY_NAME["mixtral-bf16"].scaled(T=300, d=128, f=448, name="mixtral-train-small")],
