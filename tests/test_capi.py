@@ -45,6 +45,30 @@ def test_binding_declares_every_symbol():
     assert sorted(_lib.SIGNATURES) == _declared()
 
 
+def _declared_arity():
+    """Parameter count of every moe_* function declared in include/*.h."""
+    arity = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            src = re.sub(r"//[^\n]*", "", src)
+            for name, params in re.findall(r"\b(moe_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+                params = params.strip()
+                arity[name] = 0 if params in ("", "void") else len(params.split(","))
+    return arity
+
+
+def test_binding_prototypes_match_the_header():
+    """The ctypes prototype of every entry point takes as many arguments as the
+    header declares (a signature changed on one side only fails here, not at a call)."""
+    from ragged_grouped_gemm_topk_gb300 import _lib
+    arity = _declared_arity()
+    assert sorted(arity) == _declared()
+    wrong = {n: (len(_lib.SIGNATURES[n][1]), arity[n]) for n in arity if len(_lib.SIGNATURES[n][1]) != arity[n]}
+    assert not wrong, wrong
+
+
 def test_python_binding_has_every_entry_point_by_name():
     """One Python function per C entry point, same name (the error-string accessor
     is internal: failures surface as MoeError carrying its text)."""
