@@ -66,6 +66,8 @@ typedef enum {
 #define MOE_DEV_BAD_INDEX 2 /* an expert id / row index outside its range, or counts
                                inconsistent with topk_idx                        */
 #define MOE_DEV_TIMEOUT 4   /* a bounded pipeline wait gave up; outputs are garbage */
+#define MOE_DEV_ASSERT 8    /* a MOE_DEBUG build's device-side check failed; the
+                               access it guards was skipped, outputs are garbage */
 
 /* One GEMM operand.  For MOE_E4M3, `scales` points at the E8M0 bytes, one per 32
  * consecutive elements along the contraction dimension ([rows, K/32] row-major).
@@ -88,6 +90,15 @@ const char* moe_last_error_string(void);  /* message of this thread's last error
  * ORs MOE_DEV_TIMEOUT into *dev_status and the kernel returns, leaving the CUDA
  * context usable.  Asynchronous on `stream`. */
 moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us, cudaStream_t stream);
+
+/* Diagnostic: whether this library is a MOE_DEBUG build (compiled with -DMOE_DEBUG).
+ * Such a build adds device-side checks of the kernels' invariants (TMA coordinate
+ * alignment and ranges, tile bounds, staging offsets) that OR MOE_DEV_ASSERT into
+ * dev_status and skip the access they guard instead of trapping.  This call launches
+ * one check that always fails: a debug build sets MOE_DEV_ASSERT in *dev_status, a
+ * release build (whose checks compile to nothing) leaves it unchanged.  Asynchronous
+ * on `stream`; *is_debug (host) receives 1 for a debug build, else 0. */
+moe_status_t moe_debug_selftest(int32_t* dev_status, int* is_debug, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- route ----
  * Top-k expert selection with softmax routing weights ([1] opening section: a

@@ -11,7 +11,7 @@ the same name, ``layer`` chains them into a layer, ``workloads`` draws seeded
 synthetic inputs.
 """
 
-from .binding import (moe_check_wait_timeout, moe_grouped_gemm_dgrad, moe_grouped_gemm_dgrad_mxfp8,  # noqa: F401
+from .binding import (moe_check_wait_timeout, moe_debug_selftest, moe_grouped_gemm_dgrad, moe_grouped_gemm_dgrad_mxfp8,  # noqa: F401
                       moe_grouped_gemm_fwd, moe_grouped_gemm_fwd_mxfp8_out, moe_grouped_gemm_wgrad,
                       moe_permute, moe_permute_capacity, moe_permute_capacity_workspace_size,
                       moe_permute_noalloc, moe_permute_nvfp4, moe_permute_workspace_size,

@@ -14,7 +14,7 @@ from . import build as _build
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = range(5)
 MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1 = 0, 1, 2, 3
 MOE_EPI_NONE, MOE_EPI_SWIGLU, MOE_EPI_DSWIGLU = 0, 1, 2
-MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_INDEX, MOE_DEV_TIMEOUT = 1, 2, 4
+MOE_DEV_NAN_LOGIT, MOE_DEV_BAD_INDEX, MOE_DEV_TIMEOUT, MOE_DEV_ASSERT = 1, 2, 4, 8
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE"}
@@ -32,6 +32,7 @@ SIGNATURES = {
     "moe_version": (C.c_int, []),
     "moe_last_error_string": (C.c_char_p, []),
     "moe_check_wait_timeout": (st, [vp, i32, vp]),
+    "moe_debug_selftest": (st, [vp, C.POINTER(C.c_int), vp]),
     "moe_route_topk": (st, [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
     "moe_permute_workspace_size": (sz, [i32, i32, i32]),
     "moe_permute": (st, [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, sz,
@@ -61,7 +62,9 @@ _lib = None
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The library this process uses: the MOE_DEBUG build when the environment sets
+    MOE_DEBUG=1 (device-side invariant checks into the status word), else the release one."""
+    return _build.lib_for(debug=os.environ.get("MOE_DEBUG") == "1")
 
 
 def load(path: str | None = None) -> C.CDLL:

@@ -199,6 +199,18 @@ def moe_check_wait_timeout(limit_us, dev_status=None):
     return dev_status
 
 
+def moe_debug_selftest(dev_status=None):
+    """(is_debug, status word): whether the loaded library is a MOE_DEBUG build, and
+    the device status word after a device-side check that always fails (a debug
+    build ORs MOE_DEV_ASSERT into it, a release build leaves it unchanged)."""
+    _need(dev_status, "dev_status", _I32, 1)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=_I32, device=torch.cuda.current_device())
+    flag = C.c_int(-1)
+    _lib.call("moe_debug_selftest", _ptr(dev_status), C.byref(flag), _stream())
+    return bool(flag.value), dev_status
+
+
 def _colwise_scale_shape(rows, K, E, axis):
     return {0: (rows, K // 32), 1: ((rows + 31) // 32 + E, K),
             2: (((rows + 127) // 128 + E) * (K // 128), 512)}[axis]

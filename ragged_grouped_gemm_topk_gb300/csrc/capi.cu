@@ -96,8 +96,33 @@ __global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
   if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status, &abort_flag, limit_ns);
 }
 
+// One thread runs a device-side check that always fails.
+__global__ void debug_selftest_kernel(int32_t* status) {
+  pdl_begin();
+  if (threadIdx.x == 0) (void)dbg_check(status == nullptr, status);
+}
+
 }  // namespace
 }  // namespace moe
+
+extern "C" moe_status_t moe_debug_selftest(int32_t* dev_status, int* is_debug, cudaStream_t stream) {
+  const moe::NvtxRange nvtx_range("moe_debug_selftest");
+  using namespace moe;
+#ifdef MOE_DEBUG
+  const int dbg = 1;
+#else
+  const int dbg = 0;
+#endif
+  if (is_debug) *is_debug = dbg;
+  if (!dev_status) {
+    set_error("moe_debug_selftest: need a status word");
+    return MOE_ERR_INVALID_ARG;
+  }
+  int sms = 0;
+  if (const moe_status_t dst = device_check(&sms); dst != MOE_OK) return dst;
+  launch_pdl(debug_selftest_kernel, 1, 32, 0, stream, dev_status);
+  return check_launch("moe_debug_selftest");
+}
 
 extern "C" moe_status_t moe_check_wait_timeout(int32_t* dev_status, int limit_us, cudaStream_t stream) {
   const moe::NvtxRange nvtx_range("moe_check_wait_timeout");

@@ -39,6 +39,18 @@ __device__ __forceinline__ void flag_error(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Device-side invariant check of a MOE_DEBUG build: a failed condition ORs
+// MOE_DEV_ASSERT into the status word (never a trap) and the result lets the caller
+// skip the access it guards.  In a release build it is `true` and costs nothing.
+#ifdef MOE_DEBUG
+__device__ __forceinline__ bool dbg_check(bool cond, int32_t* status) {
+  if (!cond) flag_error(status, MOE_DEV_ASSERT);
+  return cond;
+}
+#else
+__device__ __forceinline__ constexpr bool dbg_check(bool, int32_t*) { return true; }
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

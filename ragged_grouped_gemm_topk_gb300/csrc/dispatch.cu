@@ -385,7 +385,9 @@ __global__ void __launch_bounds__(kScatterThreads, 4) permute_scatter_kernel(
         // then copy it out to each of the token's rows
         const int nvalid = n16 - base < 32 * kScatterU ? n16 - base : 32 * kScatterU;
         const size_t srow = static_cast<size_t>(d) / BLK;
-        for (int j = 0; j < k; ++j) {
+        // MOE_DEBUG: the segment's codes and scales lie inside the warp's buffer
+        const bool seg_ok = dbg_check(nvalid * CB <= kSegCodes && nvalid * EPL / BLK <= kSegBytes - kSegCodes, status);
+        for (int j = 0; j < k && seg_ok; ++j) {
           const int dj = __shfl_sync(kFull, dest, j);
           if (dj < 0) continue;                // warp-uniform
           warp_copy_out(xp + static_cast<size_t>(dj) * out_row + static_cast<size_t>(base) * CB, seg, nvalid * CB,

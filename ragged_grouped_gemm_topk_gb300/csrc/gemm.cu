@@ -519,6 +519,12 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
   }
 }
 
+// MOE_DEBUG: a TMA copy's x coordinate starts on a 16-byte boundary and no coordinate
+// is negative (a copy that breaks either faults); a release build takes it as true.
+__device__ __forceinline__ bool tma_x_ok(long long x, int elem_bytes, long long y, int32_t* status) {
+  return dbg_check(x >= 0 && y >= 0 && (x * elem_bytes) % 16 == 0, status);
+}
+
 // Write one warp's 32 tile rows of output, held one row per lane as 32-bit words
 // (two bf16 or four E4M3 values each).  A warp whose 32 rows all belong to the
 // group sends boxes of kRowB-byte rows (kBoxElems elements) through its kBufs
@@ -527,11 +533,13 @@ __device__ __forceinline__ void load32(const T* src, float (&v)[32]) {
 // ((r >> 2) & 1) for 32-byte rows (32-byte swizzle).  Two 1 KB boxes in place of one
 // 2 KB box let a box be staged while the previous one is still read by its store.
 // A warp whose rows cross the group's end (the next group's rows follow) stores its
-// valid rows directly.
+// valid rows directly.  `box` counts the warp's staged boxes across its tiles: the
+// buffers rotate over that count, so the buffer a box takes was last used kBufs boxes
+// before whatever the number of boxes of a tile.
 template <int kBoxElems, int kBufs, int kRowB, int kWords>
 __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* stg, const uint32_t (&pk)[kWords],
                                                int lane, uint8_t* out, int row0, int rows_valid, int col0,
-                                               int n_out) {
+                                               int n_out, int& box, int32_t* status) {
   static_assert(kRowB == 64 || kRowB == 32, "box rows of 64 or 32 bytes");
   constexpr int kElemBytes = kRowB / kBoxElems;
   constexpr int kRowWords = kRowB / 4;       // 32-bit words per box row
@@ -543,7 +551,7 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
 #pragma unroll
     for (int c = 0; c < kWords / kRowWords; ++c) {
       if (col0 + c * kBoxElems >= n_out) break;
-      uint8_t* buf = stg + (c % (kBufs > 0 ? kBufs : 1)) * (32 * kRowB);
+      uint8_t* buf = stg + (box++ % (kBufs > 0 ? kBufs : 1)) * (32 * kRowB);
       if (lane == 0) bulk_wait_read<(kBufs > 0 ? kBufs - 1 : 0)>();   // the box that last used buf has been read
       __syncwarp();
       const int sw = kRowB == 64 ? (lane >> 1) & 3 : (lane >> 2) & 1;
@@ -555,7 +563,7 @@ __device__ __forceinline__ void epi_store_rows(const CUtensorMap* tmD, uint8_t* 
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && tma_x_ok(col0 + c * kBoxElems, kElemBytes, row0, status)) {
         tma_store_2d(tmD, buf, col0 + c * kBoxElems, row0);
         bulk_commit();
       }
@@ -674,6 +682,21 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           uint8_t* sa = tiles + stage * kStageSz;
           uint8_t* sb = sa + kASize;
           uint64_t* bar = &s.full[stage];
+          {
+            // MOE_DEBUG: the stage's TMA x coordinates (a misaligned copy faults); a
+            // failed check completes the stage without copies (garbage, flagged)
+            bool xok;
+            if constexpr (kMode == kFwd) xok = tma_x_ok((t.kb0 + kb) * (kBKBytes / eb), eb, t.row0, p.status);
+            else if constexpr (kMode == kDgrad) xok = tma_x_ok(kb * kMnRows, 2, t.row0, p.status) &&
+                                                      tma_x_ok(t.col0, 2, 0, p.status);
+            else if constexpr (C::kMx) xok = tma_x_ok(t.n0, 1, t.row0, p.status) && tma_x_ok(t.col0, 1, 0, p.status);
+            else xok = tma_x_ok(t.n0, 2, t.row0, p.status) && tma_x_ok(t.col0, 2, 0, p.status);
+            if (!xok) {
+              mbar_arrive(bar);
+              if (++stage == NS) { stage = 0; phase ^= 1u; }
+              continue;
+            }
+          }
           mbar_arrive_expect_tx(bar, (kEpi == kEpiTopk ? kAStage + p.n_mma * kBKBytes : kStageSz) +
                                          (C::kMx && kMode == kWgrad ? kAtomBytes : 0) +
                                          (kKind == 3 ? kNvAtomBytes : 0));
@@ -1078,7 +1101,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                   make_uint4(v[16 * h + 4 * j], v[16 * h + 4 * j + 1], v[16 * h + 4 * j + 2], v[16 * h + 4 * j + 3]);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0 && tma_x_ok(t.col0 + 32 * c + 16 * h, 4, t.n0 + 32 * q, p.status)) {
               if (p.accumulate)
                 tma_reduce_add_3d(&tmD, buf, t.col0 + 32 * c + 16 * h, t.n0 + 32 * q, t.e);
               else
@@ -1123,7 +1146,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
                 make_uint4(pk[c * 16 + 4 * h], pk[c * 16 + 4 * h + 1], pk[c * 16 + 4 * h + 2], pk[c * 16 + 4 * h + 3]);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
+          if (lane == 0 && tma_x_ok(t.col0 + 32 * c, 2, t.n0 + 32 * q, p.status)) {
             tma_store_3d(&tmD, buf, t.col0 + 32 * c, t.n0 + 32 * q, t.e);
             bulk_commit();
           }
@@ -1181,7 +1204,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           }
         }
         epi_store_rows<kRB, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, cw, lane,
-                           reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+                           reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out, wbox, p.status);
         if (r < t.rows) {
           uint8_t* srow = p.out_scales + static_cast<size_t>(t.row0 + r) * (g.n_out / 32);
           if (g.n_out % 128 == 0 && t.col0 + 32 * NB <= g.n_out) {
@@ -1219,7 +1242,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           mbar_arrive(&s.tempty[acc]);
           released = true;
           epi_store_rows<kRB / 2, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
-                             reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+                             reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out, wbox, p.status);
         } else {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -1357,6 +1380,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
             for (int i = threadIdx.x - 64; i < (rend - rbeg) * nch; i += kEpiThreads) {
               const int row = rbeg + i / nch, ch = i % nch;
               const uint32_t off = static_cast<uint32_t>(row * kBN + ch * 4) * 4u;
+              if (!dbg_check(row < kBM && off + 16u <= static_cast<uint32_t>(kBM * kBN * 4), p.status)) break;
               float4 a = ld_cluster_f4(pb[0] + off);
 #pragma unroll
               for (int j = 1; j < kMaxSplit; ++j) {
@@ -1525,7 +1549,7 @@ __global__ void __launch_bounds__((block_threads<kKind, kMode, kEpi, static_cast
           released = true;
           if constexpr (kMode == kFwd || kW) {
             epi_store_rows<kRB / 2, kNB, kRB>(&tmD, tiles + NS * kStageSz + kEpiOff + si * kEB * kEpiBox, pk, lane,
-                               reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out);
+                               reinterpret_cast<uint8_t*>(out), t.row0 + q * 32, t.rows - q * 32, t.col0, g.n_out, wbox, p.status);
           } else if (valid) {
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
