@@ -62,11 +62,15 @@ print("RESULT " + json.dumps(out))
 """
 
 
-def test_release_build_selftest_sets_nothing():
+def test_selftest_matches_the_loaded_build():
+    """The release build's check compiles to nothing; the MOE_DEBUG build's (loaded
+    when the environment sets MOE_DEBUG=1) sets MOE_DEV_ASSERT."""
     need_gpu()
+    want = os.environ.get("MOE_DEBUG") == "1"
     dbg, st = moe_gpu.binding.moe_debug_selftest()
     torch.cuda.synchronize()
-    assert not dbg and int(st.item()) == 0
+    assert dbg == want
+    assert int(st.item()) == (moe_gpu.binding._lib.MOE_DEV_ASSERT if want else 0)
 
 
 def test_debug_build_runs_the_path_clean():
