@@ -229,6 +229,8 @@ class MoELayer:
     # ------------------------------------------------------------------ backward
     def zero_grads(self):
         """Reset the summed weight gradients (``accumulate_grads``) to zero."""
+        if not self.training:
+            raise RuntimeError("construct the layer with training=True")
         self.dW1.zero_()
         self.dW2.zero_()
 
