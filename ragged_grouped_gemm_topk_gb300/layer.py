@@ -212,11 +212,12 @@ class MoELayer:
 
     def launches_per_forward(self) -> int:
         """Kernels one forward enqueues: route (zero counts + top-k), dispatch (rank,
-        scatter), GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine;
-        MXFP8 training adds the gathered column-wise quantisation of Xp and the row-
-        and column-wise quantisation of H."""
+        scatter; NVFP4: the rank pass takes the tensor amax of x in the same launch),
+        GEMM1 (MXFP8: with H quantised in its epilogue), GEMM2, combine; NVFP4 adds the
+        amax and the quantisation of H; MXFP8 training adds the gathered column-wise
+        quantisation of Xp and the row- and column-wise quantisation of H."""
         route = 1 if self.w_router is not None else 2     # fused router GEMM (counts zeroed by a memset)
-        nv = 3 if self.dtype == "nvfp4" else 0            # amax of x; amax + quantise of H
+        nv = 2 if self.dtype == "nvfp4" else 0            # amax + quantise of H
         return route + 2 + 2 + 1 + nv + (3 if self.dtype == "mxfp8" and self.training else 0)
 
     def launches_per_backward(self) -> int:
